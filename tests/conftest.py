@@ -1,0 +1,26 @@
+"""Shared pytest configuration.
+
+``-m gpu`` tests need a CUDA device and the built ``libopam.so``; everything
+else runs on the CPU (oracle pins, host-side argument checks, symbol exports,
+multi-process host logic over gloo).
+"""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA device (B300, sm_103a)")
+    config.addinivalue_line("markers", "slow: full-size workload checks")
+
+
+@pytest.fixture(scope="session")
+def oracle_mod():
+    from oracle import oracle
+    oracle.build()
+    return oracle
