@@ -1,0 +1,549 @@
+#!/usr/bin/env python3
+"""Benchmark of the outer-product associative-memory layers on one GPU per rank.
+
+Default run (N=1): the Tensor Cache bf16 prefill workload (B=4, H=8, T=4096,
+d=64, W=512) as the headline step -- one tc_layer_forward over the batch --
+timed with CUDA events after warm-up, an L2 flush (256 MiB write) between
+timed steps, plus:
+  * roofline of the dominant kernel, timed live through the library's
+    profiling events, against MEASURED_PEAKS.json;
+  * e2e: the same step through the public binding from pinned host buffers,
+    host<->device copies inside the timed region;
+  * cpu_baseline: the float64 oracle on the host cores;
+  * the other workloads (long-context prefill, 64-sequence decode, DeltaNet,
+    BDH sparse) under "workloads", each with its own roofline;
+  * SM clocks / throttle reasons sampled with nvidia-smi during timing.
+``--impl reference`` times the oracle instead (the reference arm).
+Multi-GPU (torchrun): each rank runs an independent batch (weak scaling, no
+collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "memory-layer tokens/s (prefill, decode) and % of HBM/tensor-core roofline"
+HEADLINE = "tc_bf16_B4_H8_T4096_d64_W512"
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ----------------------------------------------------------------- peaks
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------- algorithmic work
+def tc_pairs(T, W):
+    """Number of (query, key) pairs inside the causal window of W, per head."""
+    if T <= W:
+        return T * (T + 1) // 2
+    return W * (W + 1) // 2 + (T - W) * W
+
+
+def tc_prefill_work(B, H, T, d_k, d_v, W, elem):
+    """Algorithmic flops / bytes of the fused prefill kernel: QK^T and PV over
+    the window, the L2 read q A (2 d_k d_v per token with evictions) and the
+    intra-chunk L2 term it replaces; q, k, v read once, y written once."""
+    BH = B * H
+    soft = 2 * (d_k + d_v) * tc_pairs(T, W) * BH
+    l2_read = 2 * d_k * d_v * max(0, T - W) * BH
+    flops = soft + l2_read
+    bytes_ = BH * T * (2 * d_k + 2 * d_v) * elem
+    return flops, bytes_
+
+
+def tc_decode_work(S, H, d_k, d_v, W, elem):
+    """Per decode step: the ring (W keys + W values) streamed once, A read and
+    written once (fp32), q/k/v in and y out."""
+    SH = S * H
+    flops = SH * (2 * W * (d_k + d_v) + 4 * d_k * d_v)
+    bytes_ = SH * (W * (d_k + d_v) * elem + 2 * d_k * d_v * 4 + (2 * d_k + 2 * d_v) * elem)
+    return flops, bytes_
+
+
+def delta_work(B, H, T, d_k, d_v, elem, C=64):
+    """Chunked form: per token 2C(d_k + d_v) (intra-chunk products) plus
+    6 d_k d_v (state read, correction, write); q, k, v, beta read, y written."""
+    BH = B * H
+    flops = BH * T * (4 * C * (d_k + d_v) // 2 + 6 * d_k * d_v)
+    bytes_ = BH * T * ((2 * d_k + 2 * d_v) * elem + 4)
+    return flops, bytes_
+
+
+def sparse_work(B, H, T, N, d_v, density):
+    """Sparse write + read: 4 nnz d_v flops per token; dense q, k, v read, y written."""
+    BH = B * H
+    nnz = density * N
+    flops = BH * T * 4 * nnz * d_v
+    bytes_ = BH * T * (2 * N + 2 * d_v) * 4
+    return flops, bytes_
+
+
+def roofline(flops, bytes_, seconds, peaks, peak_kind, traffic=None, scope="kernel"):
+    tf_key = "bf16_tflops" if peak_kind == "burst" else "bf16_tflops_sustained"
+    t_mem = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks[tf_key] * 1e12)
+    if t_mem >= t_tc:
+        ach = bytes_ / seconds / 1e9
+        out = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    else:
+        ach = flops / seconds / 1e12
+        out = {"bound": "tensor", "achieved": ach, "peak": peaks[tf_key], "unit": "TFLOP/s"}
+    out["frac"] = out["achieved"] / out["peak"]
+    out["traffic"] = traffic
+    out["algorithmic_bytes"] = bytes_
+    out["algorithmic_flops"] = flops
+    out["scope"] = scope
+    return out
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = [r for t, r in self.rows if t0 - 0.25 <= t <= t1 + 0.25] or [r for _, r in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[4 + i].lower() == "active"})
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- distributed
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    """Max of a float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(units_per_rank, seconds_per_rank, world):
+    """Whole-job throughput: units all ranks processed / slowest rank's time."""
+    return units_per_rank * world / max_over_ranks(seconds_per_rank, world)
+
+
+# ----------------------------------------------------------------- timing helpers
+def timed_steps(step, K, flush, torch, prof=True, binding=None):
+    """K steps, each bracketed by events; L2 flushed before each (untimed).
+    Returns (per-step ms list, dominant-kernel ms list or None)."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    kd = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev + kd:   # torch creates the CUDA event on first record
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        if prof and binding is not None:
+            binding.profile_events(kd[i][0], kd[i][1])
+        ev[i][0].record()
+        step()
+        ev[i][1].record()
+    if binding is not None:
+        binding.profile_events(None, None)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    dom_ms = [a.elapsed_time(b) for a, b in kd] if prof and binding is not None else None
+    return step_ms, dom_ms
+
+
+def load_traffic(kernel):
+    """ncu DRAM bytes per launch recorded for `kernel`, if the kernel source is
+    unchanged since the capture (else None)."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    import hashlib
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, "outer_product_associative_chunked_b300", "csrc", d["source"])
+    if not os.path.exists(src):
+        return None
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return d["dram_bytes_per_launch"] if h == d["source_sha256_16"] else None
+
+
+# ----------------------------------------------------------------- our arm
+def tc_prefill_setup(name, rank, torch, binding, synth):
+    w = synth.WORKLOADS[name]
+    d = w.dims
+    inp = synth.tc_inputs(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], dtype=d["dtype"],
+                          seed=w.seed + 1000 * rank, lam=d.get("lam"), eta=d.get("eta"), gate=d.get("gate"))
+    return w, d, inp
+
+
+def bench_headline(args, rank, world, torch, binding, synth, peaks, peak_src, flush):
+    w, d, inp = tc_prefill_setup(args.workload, rank, torch, binding, synth)
+    q, k, v, lam, eta, gate = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate)]
+    y = torch.empty(d["B"], d["H"], d["T"], d["d_v"], dtype=q.dtype, device="cuda")
+    ws = torch.empty(binding.tc_layer_forward_workspace_size(d["B"], d["H"], d["T"], d["d_k"], d["d_v"],
+                                                             d["W"], q.dtype), dtype=torch.uint8, device="cuda")
+
+    def step():
+        binding.tc_layer_forward(q, k, v, lam, eta, gate, d["W"], out=y, workspace=ws)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    l0 = binding.kernel_launches()
+    t0 = time.time()
+    step_ms, dom_ms = timed_steps(step, args.steps, flush, torch, prof=True, binding=binding)
+    t1 = time.time()
+    launches = binding.kernel_launches() - l0
+    barrier(world)
+    if sampler:
+        time.sleep(0.3)
+        sampler.stop()
+    tokens = d["B"] * d["T"]
+    total_s = sum(step_ms) / 1e3
+    value = aggregate_throughput(tokens * args.steps, total_s, world)
+    ms_per_step = max_over_ranks(total_s, world) * 1e3 / args.steps
+    elem = 2 if d["dtype"] == "bf16" else 4
+    fl, by = tc_prefill_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], elem)
+    dom_s = statistics.mean(dom_ms) / 1e3
+    roof = roofline(fl, by, dom_s, peaks, "burst", traffic=load_traffic("tc_fwd"), scope="kernel")
+    roof["kernel"] = "tc_fwd (fused window softmax + L2 read + gate)"
+    roof["kernel_ms"] = dom_s * 1e3
+    roof["peak_source"] = f"of {peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "of fallback"
+    clocks = sampler.summary(t0, t1) if sampler else None
+
+    # e2e through the public binding from pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (x.pin_memory() for x in (inp.q, inp.k, inp.v))
+        hl, he, hg = (x.pin_memory() for x in (inp.lam, inp.eta, inp.gate))
+        hy = torch.empty(tuple(y.shape), dtype=y.dtype).pin_memory()
+        dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dl, de, dg = torch.empty_like(lam), torch.empty_like(eta), torch.empty_like(gate)
+
+        def e2e_step():
+            for dst, src in ((dq, hq), (dk_, hk), (dv_, hv), (dl, hl), (de, he), (dg, hg)):
+                dst.copy_(src, non_blocking=True)
+            binding.tc_layer_forward(dq, dk_, dv_, dl, de, dg, d["W"], out=y, workspace=ws)
+            hy.copy_(y, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        barrier(world)
+        e_ms, _ = timed_steps(e2e_step, args.steps, None, torch, prof=False)
+        h2d = sum(x.numel() * x.element_size() for x in (hq, hk, hv, hl, he, hg))
+        d2h = hy.numel() * hy.element_size()
+        e2e = {"value": aggregate_throughput(tokens * args.steps, sum(e_ms) / 1e3, world), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": statistics.mean(e_ms)}
+    del ws
+    return {"value": value, "ms_per_step": ms_per_step, "roofline": roof, "clocks": clocks,
+            "e2e": e2e, "gpu_launches": launches, "tokens_per_step": tokens, "dims": d, "inp": inp}
+
+
+def bench_extras(args, torch, binding, synth, peaks, flush):
+    """The other workloads, each timed with CUDA events (L2 flushed between
+    steps); roofline on the whole step's algorithmic work."""
+    out = {}
+    K, Wm = args.extra_steps, 2
+
+    def summarize(name, tokens, ms, fl, by, peak_kind, kernel, dom):
+        r = roofline(fl, by, statistics.mean(ms) / 1e3, peaks, peak_kind, scope="step")
+        entry = {"value": tokens / (statistics.mean(ms) / 1e3), "unit": "tokens/s",
+                 "ms_per_step": statistics.mean(ms), "roofline": r, "dominant_kernel": kernel}
+        if dom:
+            entry["dominant_kernel_ms"] = statistics.mean(dom)
+        out[name] = entry
+
+    # Long-context prefill, then the 64-sequence decode continuing from it.
+    name = "tc_bf16_B1_H16_T32768_d128_W2048"
+    w, d, inp = tc_prefill_setup(name, 0, torch, binding, synth)
+    q, k, v, lam, eta, gate = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate)]
+    y = torch.empty(d["B"], d["H"], d["T"], d["d_v"], dtype=q.dtype, device="cuda")
+    ws = torch.empty(binding.tc_layer_forward_workspace_size(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"],
+                                                             q.dtype), dtype=torch.uint8, device="cuda")
+    st1 = binding.TCState(d["B"], d["H"], d["W"], d["d_k"], d["d_v"], dtype=q.dtype)
+    step = lambda: binding.tc_layer_forward(q, k, v, lam, eta, gate, d["W"], out=y, workspace=ws)  # noqa: E731
+    for _ in range(Wm):
+        step()
+    ms, dom = timed_steps(step, K, flush, torch, prof=True, binding=binding)
+    fl, by = tc_prefill_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], 2)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "sustained", "tc_fwd", dom)
+    binding.tc_layer_forward(q, k, v, lam, eta, gate, d["W"], out=y, workspace=ws, state=st1)
+    del ws, y, q, k, v
+
+    dname = "tc_decode_bf16_S64_H16_d128_W2048_steps256"
+    dd = synth.WORKLOADS[dname].dims
+    S, steps = dd["S"], dd["steps"]
+    dec = synth.tc_decode_inputs(steps, S, dd["H"], dd["d_k"], dd["d_v"], dtype="bf16",
+                                 seed=synth.WORKLOADS[dname].seed)
+    dq, dk_, dv_ = dec.q.cuda(), dec.k.cuda(), dec.v.cuda()
+    st = binding.TCState(S, dd["H"], dd["W"], dd["d_k"], dd["d_v"], dtype=torch.bfloat16)
+    st.ring_k.copy_(st1.ring_k.expand(S, -1, -1, -1))
+    st.ring_v.copy_(st1.ring_v.expand(S, -1, -1, -1))
+    st.A.copy_(st1.A.expand(S, -1, -1, -1))
+    st.pos.fill_(d["T"])
+    yd = torch.empty(S, dd["H"], dd["d_v"], dtype=torch.bfloat16, device="cuda")
+    wsd = torch.empty(binding.tc_decode_step_workspace_size(st), dtype=torch.uint8, device="cuda")
+    counter = [0]
+
+    def dstep():
+        i = counter[0] % steps
+        binding.tc_decode_step(st, dq[i], dk_[i], dv_[i], lam, eta, gate, out=yd, workspace=wsd)
+        counter[0] += 1
+
+    for _ in range(Wm):
+        dstep()
+    # One timed "step" of this workload = 256 decode steps; the working set
+    # (ring 1 GiB + A 64 MiB) is far above L2, so no flush is needed.
+    ms, dom = timed_steps(dstep, steps, None, torch, prof=True, binding=binding)
+    fl, by = tc_decode_work(S, dd["H"], dd["d_k"], dd["d_v"], dd["W"], 2)
+    summarize(dname, S, ms, fl, by, "sustained", "tc_decode_partial", dom)
+    out[dname]["note"] = "value = decoded tokens/s (64 sequences x 1 token per step, averaged over 256 steps)"
+    del st, st1, dq, dk_, dv_, wsd
+
+    name = "delta_bf16_B8_H16_T8192_d128_C64"
+    d = synth.WORKLOADS[name].dims
+    inp = synth.delta_inputs(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], dtype="bf16",
+                             seed=synth.WORKLOADS[name].seed)
+    q, k, v, beta = inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), inp.beta.cuda()
+    y = torch.empty_like(v)
+    ws = torch.empty(binding.delta_rule_forward_workspace_size(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], 64,
+                                                               torch.bfloat16), dtype=torch.uint8, device="cuda")
+    step = lambda: binding.delta_rule_forward(q, k, v, beta, chunk=64, out=y, workspace=ws)  # noqa: E731
+    for _ in range(Wm):
+        step()
+    ms, dom = timed_steps(step, K, flush, torch, prof=True, binding=binding)
+    fl, by = delta_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], 2)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "sustained", "delta_state", dom)
+    del q, k, v, beta, y, ws
+
+    name = "bdh_fp32_B2_H4_T2048_N16384_dv256"
+    d = synth.WORKLOADS[name].dims
+    inp = synth.sparse_inputs(d["B"], d["H"], d["T"], d["N"], d["d_v"], seed=synth.WORKLOADS[name].seed)
+    dens = float((inp.k > 0).float().mean())
+    q, k, v = inp.q.cuda(), inp.k.cuda(), inp.v.cuda()
+    y = torch.empty_like(v)
+    ws = torch.empty(binding.sparse_linattn_forward_workspace_size(d["B"], d["H"], d["T"], d["N"], d["d_v"]),
+                     dtype=torch.uint8, device="cuda")
+    step = lambda: binding.sparse_linattn_forward(q, k, v, out=y, workspace=ws)  # noqa: E731
+    for _ in range(Wm):
+        step()
+    ms, dom = timed_steps(step, K, flush, torch, prof=True, binding=binding)
+    fl, by = sparse_work(d["B"], d["H"], d["T"], d["N"], d["d_v"], dens)
+    # fp32 path: bound by HBM (its flops are far below any fp32 peak as well)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "sustained", "sparse_read (chunked)", dom)
+    out[name]["density"] = dens
+    del q, k, v, y, ws
+    return out
+
+
+def cpu_baseline_headline(inp, d, budget_s=20.0):
+    """The float64 oracle on the host cores, on the headline workload's units
+    (all of them when they fit the time budget, else a prefix of units)."""
+    from oracle import oracle
+    oracle.build()
+    threads = oracle.get_threads()
+    B, H, T = d["B"], d["H"], d["T"]
+    units = B * H
+    # time one unit first to size the sample
+    t0 = time.perf_counter()
+    oracle.tc_prefill(inp.q[:1, :1], inp.k[:1, :1], inp.v[:1, :1], inp.lam[:1], inp.eta[:1], inp.gate[:1], d["W"])
+    one = time.perf_counter() - t0
+    n_units = max(1, min(units, int(budget_s * threads / max(one, 1e-6))))
+    nb = max(1, n_units // H)   # whole batch rows of H heads
+    t0 = time.perf_counter()
+    oracle.tc_prefill(inp.q[:nb], inp.k[:nb], inp.v[:nb], inp.lam, inp.eta, inp.gate, d["W"])
+    dt = time.perf_counter() - t0
+    return {"value": nb * T / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{nb} of {B} sequences x {H} heads x {T} tokens (float64, OpenMP over heads), {dt:.1f} s"}
+
+
+# ----------------------------------------------------------------- reference arm
+def bench_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import torch  # noqa: F401
+    from outer_product_associative_chunked_b300 import synth
+    from oracle import oracle
+    oracle.build()
+    w = synth.WORKLOADS[args.workload]
+    d = w.dims
+    inp = synth.tc_inputs(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], dtype=d["dtype"], seed=w.seed,
+                          lam=d.get("lam"), eta=d.get("eta"), gate=d.get("gate"))
+    threads = oracle.get_threads()
+    # one step = one sequence of the batch (H heads x T tokens)
+    sample = lambda: oracle.tc_prefill(inp.q[:1], inp.k[:1], inp.v[:1], inp.lam, inp.eta, inp.gate, d["W"])  # noqa: E731
+    for _ in range(args.warmup):
+        sample()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sample()
+    dt = time.perf_counter() - t0
+    value = d["T"] * args.steps / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generator)",
+            "config": {"workload": args.workload, **{k: v for k, v in d.items() if k != "dtype"},
+                       "input_dtype": d["dtype"]},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": f"each step: 1 of {d['B']} sequences ({d['H']} heads x {d['T']} tokens)"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    return line
+
+
+# ----------------------------------------------------------------- main
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--extra-steps", type=int, default=5)
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = dist_setup()
+
+    if args.impl == "reference":
+        line = bench_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    from outer_product_associative_chunked_b300 import binding, build, synth
+    build.build()
+    peaks, peak_src = load_peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    res = bench_headline(args, rank, world, torch, binding, synth, peaks, peak_src, flush)
+    extras = None
+    if rank == 0 and world == 1 and not args.no_extras:
+        extras = bench_extras(args, torch, binding, synth, peaks, flush)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_headline(res["inp"], res["dims"])
+    if rank == 0:
+        d = res["dims"]
+        line = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic (seeded generator, page workload shapes)",
+                "config": {"workload": args.workload, **{k: v for k, v in d.items() if k != "dtype"},
+                           "input_dtype": d["dtype"], "tokens_per_step": res["tokens_per_step"],
+                           "l2": "256 MiB buffer written between timed steps (untimed)",
+                           "parallelism": f"replicas x{world} (independent batch per GPU)"},
+                "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
+                "gpu_launches": res["gpu_launches"], "clocks": res["clocks"]}
+        if extras is not None:
+            line["workloads"] = extras
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

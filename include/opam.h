@@ -1,0 +1,197 @@
+/*
+ * opam.h -- C ABI of libopam: outer-product associative-memory layers on one
+ * NVIDIA B300 (sm_103a).
+ *
+ * A layer keeps a fixed-size state written with outer products k (x) v and
+ * read with a query, using q (k (x) v) = <q, k> v (gist.science 2605.22884
+ * "Tensor Cache", Methodology 1, read mechanism; molayo1419.me "DeltaNet-family
+ * linear attention variants", opening identity).  Three write rules are
+ * exported:
+ *   - Tensor Cache: exact softmax over a ring of the W most recent tokens; a
+ *     token evicted from the ring is written A <- lambda A + eta k v^T and read
+ *     as m_t = q_t A; y_t = y_local,t + sigmoid(g) m_t  (tc_layer_forward,
+ *     tc_decode_step);
+ *   - DeltaNet delta rule e_t = beta_t (v_t - S_{t-1} k_t), S_t = S_{t-1} +
+ *     e_t k_t^T, o_t = S_t q_t  (delta_rule_forward);
+ *   - BDH-style additive linear attention over wide, sparse, non-negative keys,
+ *     S_t = S_{t-1} + v_t k_t^T, o_t = S_t q_t  (sparse_linattn_forward).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers are DEVICE pointers unless stated otherwise, owned by the
+ *     caller, 16-byte aligned, and every tensor is dense row-major
+ *     ("contiguous") in the shape given.  The library allocates nothing and
+ *     keeps no state between calls except a per-thread error string.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and runs asynchronously.  The return value reports argument
+ *     errors and launch failures synchronously; device-side faults surface at
+ *     the caller's next synchronisation like any CUDA error.
+ *   - Every state is stored key-major: element (a, b) of a d_k x d_v matrix at
+ *     [a * d_v + b].  For Tensor Cache that is A = sum eta lambda^.. k v^T.
+ *     DeltaNet and BDH write their state as S in R^{d_v x d_k} with read S q;
+ *     the stored matrix is S^T, so S_{i,j} sits at [j * d_v + i].
+ *   - Scratch memory ("workspace") is caller-provided device memory of at
+ *     least the size the matching *_workspace_size() returns for the same
+ *     arguments; its contents on entry do not matter.  Calls that share a
+ *     workspace must not overlap on the GPU.
+ *   - Return value: OPAM_OK, or a negative opam_status; opam_last_error()
+ *     then holds a one-line message (per calling thread).
+ */
+#ifndef OPAM_H
+#define OPAM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of q, k, v and y.  Scalars (lambda, eta, gate, beta) and every
+ * state matrix are always float32. */
+typedef enum { OPAM_F32 = 0, OPAM_BF16 = 1 } opam_dtype;
+
+typedef enum {
+    OPAM_OK = 0,
+    OPAM_ERR_INVALID_ARG = -1,  /* null/misaligned pointer, bad extent        */
+    OPAM_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. d = 96)    */
+    OPAM_ERR_CUDA = -3,         /* a CUDA launch or API call failed           */
+    OPAM_ERR_WORKSPACE = -4     /* workspace missing or smaller than required */
+} opam_status;
+
+/* ------------------------------------------------------------------------
+ * Tensor Cache streaming state (Methodology 1: L1 ring buffer of the W most
+ * recent tokens plus the L2 outer-product matrix A; Main contributions:
+ * bounded state, O(W d + d_k d_v) per head).  All buffers caller-owned:
+ *   ring_k  [B][H][W][d_k]  element type `dtype`; slot j holds the newest
+ *           token position p < pos[b] with p mod W == j (zero when
+ *           pos[b] <= j)
+ *   ring_v  [B][H][W][d_v]  same slots
+ *   A       [B][H][d_k][d_v] float32
+ *   pos     [B] int64        tokens seen so far by sequence b (all heads)
+ * ---------------------------------------------------------------------- */
+typedef struct {
+    void *ring_k;
+    void *ring_v;
+    float *A;
+    int64_t *pos;
+    int32_t B, H, W, d_k, d_v;
+    int32_t dtype; /* opam_dtype */
+} opam_tc_state;
+
+/* Tensor Cache layer forward over a whole sequence from an empty state
+ * ("Tensor Cache", Methodology 1 for the layer; Methodology 2 for the
+ * parallel weighted-sum scan that makes the prefill equal to the per-token
+ * writes, with no chunk averaging).
+ *
+ *   q, k      [B][H][T][d_k]   dtype
+ *   v         [B][H][T][d_v]   dtype
+ *   lambda, eta, gate  [H] float32 per-head decay, write rate, gate logit g
+ *   softmax_scale      tau in softmax(tau q.k); <= 0 selects 1/sqrt(d_k)
+ *   y         [B][H][T][d_v]   dtype, output:
+ *       y_t = sum_{s=max(0,t-W+1)}^{t} softmax_s(tau q_t.k_s) v_s
+ *           + sigmoid(g) sum_{s<=t-W} eta lambda^(t-W-s) <q_t,k_s> v_s
+ *   state_out  NULL, or a state with matching B, H, W, d_k, d_v, dtype that
+ *              receives the ring, A and pos = T so decoding can continue.
+ *
+ * Supported: d_k, d_v in {32, 64, 128}; 1 <= W; 1 <= T; B*H >= 1.
+ * Errors: OPAM_ERR_INVALID_ARG for null or misaligned pointers or
+ * non-positive extents, OPAM_ERR_UNSUPPORTED for other head sizes,
+ * OPAM_ERR_WORKSPACE if workspace_bytes is below the required size. */
+size_t tc_layer_forward_workspace_size(int B, int H, int T, int d_k, int d_v, int W,
+                                       int dtype);
+int tc_layer_forward(const void *q, const void *k, const void *v, int dtype,
+                     int B, int H, int T, int d_k, int d_v, int W,
+                     const float *lambda, const float *eta, const float *gate,
+                     float softmax_scale, void *y, opam_tc_state *state_out,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* One Tensor Cache decode step for a batch of independent sequences
+ * ("Tensor Cache", Methodology 1: when the ring overwrites an entry the
+ * displaced (k, v) is written into A; the new token is then read through the
+ * ring softmax and q A).  For every sequence b and head h, with p = pos[b]:
+ *   1. slot = p mod W; if p >= W: A <- lambda A + eta k_e v_e^T with
+ *      (k_e, v_e) = ring[slot] (the token p - W);
+ *   2. ring[slot] <- (k, v);
+ *   3. y = softmax over the min(p+1, W) occupied slots + sigmoid(g) q A;
+ * then pos[b] += 1.
+ *   st          state (updated in place); st->B is the number of sequences
+ *   q, k        [B][H][d_k] dtype (one token per sequence and head)
+ *   v           [B][H][d_v] dtype
+ *   lambda, eta, gate [H] float32; softmax_scale as above
+ *   y           [B][H][d_v] dtype, output
+ * Same support and errors as tc_layer_forward. */
+size_t tc_decode_step_workspace_size(const opam_tc_state *st);
+int tc_decode_step(opam_tc_state *st, const void *q, const void *k, const void *v,
+                   const float *lambda, const float *eta, const float *gate,
+                   float softmax_scale, void *y, void *workspace,
+                   size_t workspace_bytes, void *stream);
+
+/* DeltaNet delta-rule forward (molayo1419.me, "DeltaNet-family linear
+ * attention variants", section "DeltaNet: write the prediction error instead
+ * of the value"), evaluated chunk by chunk in an exact closed form of the
+ * same recurrence:
+ *   e_t = beta_t (v_t - S_{t-1} k_t),  S_t = S_{t-1} + e_t k_t^T,
+ *   o_t = S_t q_t (read after the write).
+ *   q, k   [B][H][T][d_k] dtype;  v [B][H][T][d_v] dtype
+ *   beta   [B][H][T] float32 in [0, 1]
+ *   chunk  tokens per chunk: 0 (default 64), 16, 32 or 64; results do not
+ *          depend on it beyond rounding
+ *   S0     NULL (zero state) or [B][H][d_k][d_v] float32 key-major start state
+ *   S_out  NULL or [B][H][d_k][d_v] float32 key-major final state (may equal S0)
+ *   y      [B][H][T][d_v] dtype, output o_t
+ * Supported: d_k, d_v in {32, 64, 128}. Errors as above. */
+size_t delta_rule_forward_workspace_size(int B, int H, int T, int d_k, int d_v,
+                                         int chunk, int dtype);
+int delta_rule_forward(const void *q, const void *k, const void *v,
+                       const float *beta, int dtype, int B, int H, int T,
+                       int d_k, int d_v, int chunk, const float *S0,
+                       float *S_out, void *y, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/* BDH-style linear attention over wide, sparse, non-negative keys
+ * (ainews.random.gg BDH memory-architecture post: keys/queries are neuron
+ * activations in a very high-dimensional space, the state is the accumulated
+ * connectivity and a read is propagation; mo.ai.kr "Hebbian memory MLP",
+ * simple construction W = sum_i v_i k_i^T):
+ *   S_t = S_{t-1} + v_t k_t^T,  o_t = S_t q_t  (read after the write).
+ * q and k are passed dense (the ReLU output a model produces); their supports
+ * are found inside the library.  Any real values are handled exactly; the
+ * speed relies on most entries being zero.
+ *   q, k   [B][H][T][N] float32
+ *   v      [B][H][T][d_v] float32
+ *   S0     NULL or [B][H][N][d_v] float32 key-major start state
+ *   S_out  NULL or [B][H][N][d_v] float32 key-major final state (may equal S0)
+ *   y      [B][H][T][d_v] float32, output
+ * Supported: 1 <= N <= 49152, d_v in {32, 64, 128, 256}. Errors as above. */
+size_t sparse_linattn_forward_workspace_size(int B, int H, int T, int N, int d_v);
+int sparse_linattn_forward(const float *q, const float *k, const float *v,
+                           int B, int H, int T, int N, int d_v,
+                           const float *S0, float *S_out, float *y,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/* Message for the last non-OK status returned on the calling thread. */
+const char *opam_last_error(void);
+
+/* ------------------------------------------------------------------------
+ * Instrumentation (no counterpart on the pages; used by benchmarks).
+ *
+ * opam_profile_events: on the calling thread, every later entry-point call
+ * records `start` (a cudaEvent_t) on its stream immediately before launching
+ * its dominant kernel and `stop` immediately after it, so the caller can time
+ * that kernel alone with cudaEventElapsedTime.  The dominant kernel is the
+ * fused window-softmax kernel of tc_layer_forward, the split-ring kernel of
+ * tc_decode_step, the sequential state pass of delta_rule_forward and the
+ * chunked read of sparse_linattn_forward (summed over its launches: `start`
+ * goes before the first, `stop` after the last).  Pass NULL, NULL to stop.
+ * Events stay owned by the caller.  Returns OPAM_OK.
+ *
+ * opam_kernel_launches: number of kernels this library has launched in the
+ * process so far (all threads). */
+int opam_profile_events(void *start, void *stop);
+uint64_t opam_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OPAM_H */

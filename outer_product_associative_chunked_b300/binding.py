@@ -1,0 +1,227 @@
+"""ctypes binding for libopam.so: argument marshalling only.
+
+Every function here checks tensor placement, passes raw device pointers,
+sizes and the current CUDA stream to the C entry point of the same name, and
+turns a non-OK status into an exception.  All arithmetic happens in the CUDA
+kernels behind the C ABI; there is no fallback path.  PyTorch only allocates
+device memory (outputs, state, workspace) and supplies the stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libopam.so")
+
+OPAM_F32, OPAM_BF16 = 0, 1
+_STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "CUDA", -4: "WORKSPACE"}
+
+# Every symbol the C header declares (checked by the CPU test-suite).
+EXPORTS = (
+    "tc_layer_forward_workspace_size", "tc_layer_forward",
+    "tc_decode_step_workspace_size", "tc_decode_step",
+    "delta_rule_forward_workspace_size", "delta_rule_forward",
+    "sparse_linattn_forward_workspace_size", "sparse_linattn_forward",
+    "opam_last_error", "opam_profile_events", "opam_kernel_launches",
+)
+
+
+class OpamError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class TCStateStruct(ctypes.Structure):
+    _fields_ = [("ring_k", ctypes.c_void_p), ("ring_v", ctypes.c_void_p),
+                ("A", ctypes.c_void_p), ("pos", ctypes.c_void_p),
+                ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("W", ctypes.c_int32),
+                ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libopam.so; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m outer_product_associative_chunked_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        sp = ctypes.POINTER(TCStateStruct)
+        L.opam_last_error.restype = ctypes.c_char_p
+        L.opam_last_error.argtypes = []
+        L.tc_layer_forward_workspace_size.restype = sz
+        L.tc_layer_forward_workspace_size.argtypes = [i, i, i, i, i, i, i]
+        L.tc_layer_forward.restype = i
+        L.tc_layer_forward.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, f, vp, sp, vp, sz, vp]
+        L.tc_decode_step_workspace_size.restype = sz
+        L.tc_decode_step_workspace_size.argtypes = [sp]
+        L.tc_decode_step.restype = i
+        L.tc_decode_step.argtypes = [sp, vp, vp, vp, vp, vp, vp, f, vp, vp, sz, vp]
+        L.delta_rule_forward_workspace_size.restype = sz
+        L.delta_rule_forward_workspace_size.argtypes = [i, i, i, i, i, i, i]
+        L.delta_rule_forward.restype = i
+        L.delta_rule_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
+        L.sparse_linattn_forward_workspace_size.restype = sz
+        L.sparse_linattn_forward_workspace_size.argtypes = [i, i, i, i, i]
+        L.sparse_linattn_forward.restype = i
+        L.sparse_linattn_forward.argtypes = [vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
+        L.opam_profile_events.restype = i
+        L.opam_profile_events.argtypes = [vp, vp]
+        L.opam_kernel_launches.restype = ctypes.c_uint64
+        L.opam_kernel_launches.argtypes = []
+        _lib = L
+    return _lib
+
+
+def last_error() -> str:
+    return lib().opam_last_error().decode()
+
+
+def profile_events(start=None, stop=None) -> None:
+    """Have later calls on this thread record two torch.cuda.Events around
+    their dominant kernel (None, None switches it off)."""
+    lib().opam_profile_events(None if start is None else ctypes.c_void_p(start.cuda_event),
+                              None if stop is None else ctypes.c_void_p(stop.cuda_event))
+
+
+def kernel_launches() -> int:
+    """Kernels libopam has launched in this process so far."""
+    return int(lib().opam_kernel_launches())
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise OpamError(rc, last_error())
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return OPAM_F32
+    if dt == torch.bfloat16:
+        return OPAM_BF16
+    raise TypeError(f"unsupported element type {dt}; use float32 or bfloat16")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _workspace(nbytes: int, workspace, device):
+    if nbytes == 0:
+        raise OpamError(-1, last_error() or "invalid arguments")
+    if workspace is None:
+        return torch.empty(nbytes, dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise OpamError(-4, f"workspace holds {workspace.numel()} bytes, {nbytes} required")
+    return workspace
+
+
+# ------------------------------------------------------------------ Tensor Cache
+class TCState:
+    """Caller-owned Tensor Cache streaming state (ring, A, pos) on the GPU."""
+
+    def __init__(self, B, H, W, d_k, d_v, dtype=torch.bfloat16, device="cuda"):
+        self.B, self.H, self.W, self.d_k, self.d_v, self.dtype = B, H, W, d_k, d_v, dtype
+        self.ring_k = torch.zeros(B, H, W, d_k, dtype=dtype, device=device)
+        self.ring_v = torch.zeros(B, H, W, d_v, dtype=dtype, device=device)
+        self.A = torch.zeros(B, H, d_k, d_v, dtype=torch.float32, device=device)
+        self.pos = torch.zeros(B, dtype=torch.int64, device=device)
+
+    def struct(self) -> TCStateStruct:
+        return TCStateStruct(self.ring_k.data_ptr(), self.ring_v.data_ptr(), self.A.data_ptr(),
+                             self.pos.data_ptr(), self.B, self.H, self.W, self.d_k, self.d_v,
+                             dtype_code(self.dtype))
+
+
+def tc_layer_forward_workspace_size(B, H, T, d_k, d_v, W, dtype) -> int:
+    return int(lib().tc_layer_forward_workspace_size(B, H, T, d_k, d_v, W, dtype_code(dtype)))
+
+
+def tc_layer_forward(q, k, v, lam, eta, gate, W, softmax_scale=0.0, out=None, state=None,
+                     workspace=None, stream=None):
+    """Tensor Cache prefill; q,k [B,H,T,d_k], v [B,H,T,d_v]; returns y [B,H,T,d_v]."""
+    _dev(q, k, v, lam, eta, gate, out, workspace)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dt = dtype_code(q.dtype)
+    y = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device) if out is None else out
+    ws = _workspace(tc_layer_forward_workspace_size(B, H, T, dk, dv, W, q.dtype), workspace, q.device)
+    st = ctypes.byref(state.struct()) if state is not None else None
+    _check(lib().tc_layer_forward(_ptr(q), _ptr(k), _ptr(v), dt, B, H, T, dk, dv, int(W), _ptr(lam),
+                                  _ptr(eta), _ptr(gate), float(softmax_scale), _ptr(y), st, _ptr(ws),
+                                  ws.numel(), _stream(stream)))
+    return y
+
+
+def tc_decode_step_workspace_size(state: TCState) -> int:
+    return int(lib().tc_decode_step_workspace_size(ctypes.byref(state.struct())))
+
+
+def tc_decode_step(state: TCState, q, k, v, lam, eta, gate, softmax_scale=0.0, out=None,
+                   workspace=None, stream=None):
+    """One decode step; q,k [B,H,d_k], v [B,H,d_v]; returns y [B,H,d_v]; updates state."""
+    _dev(q, k, v, lam, eta, gate, out, workspace)
+    y = torch.empty(state.B, state.H, state.d_v, dtype=state.dtype, device=q.device) if out is None else out
+    st = state.struct()
+    ws = _workspace(int(lib().tc_decode_step_workspace_size(ctypes.byref(st))), workspace, q.device)
+    _check(lib().tc_decode_step(ctypes.byref(st), _ptr(q), _ptr(k), _ptr(v), _ptr(lam), _ptr(eta),
+                                _ptr(gate), float(softmax_scale), _ptr(y), _ptr(ws), ws.numel(),
+                                _stream(stream)))
+    return y
+
+
+# ------------------------------------------------------------------ DeltaNet
+def delta_rule_forward_workspace_size(B, H, T, d_k, d_v, chunk, dtype) -> int:
+    return int(lib().delta_rule_forward_workspace_size(B, H, T, d_k, d_v, chunk, dtype_code(dtype)))
+
+
+def delta_rule_forward(q, k, v, beta, chunk=0, S0=None, S_out=None, out=None, workspace=None,
+                       stream=None):
+    """DeltaNet delta rule; q,k [B,H,T,d_k], v [B,H,T,d_v], beta [B,H,T] fp32."""
+    _dev(q, k, v, beta, S0, S_out, out, workspace)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    y = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device) if out is None else out
+    ws = _workspace(delta_rule_forward_workspace_size(B, H, T, dk, dv, chunk, q.dtype), workspace,
+                    q.device)
+    _check(lib().delta_rule_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), dtype_code(q.dtype), B, H,
+                                    T, dk, dv, int(chunk), _ptr(S0), _ptr(S_out), _ptr(y), _ptr(ws),
+                                    ws.numel(), _stream(stream)))
+    return y
+
+
+# ------------------------------------------------------------------ BDH
+def sparse_linattn_forward_workspace_size(B, H, T, N, d_v) -> int:
+    return int(lib().sparse_linattn_forward_workspace_size(B, H, T, N, d_v))
+
+
+def sparse_linattn_forward(q, k, v, S0=None, S_out=None, out=None, workspace=None, stream=None):
+    """BDH-style additive linear attention; q,k [B,H,T,N] fp32, v [B,H,T,d_v] fp32."""
+    _dev(q, k, v, S0, S_out, out, workspace)
+    B, H, T, N = q.shape
+    dv = v.shape[-1]
+    y = torch.empty(B, H, T, dv, dtype=torch.float32, device=q.device) if out is None else out
+    ws = _workspace(sparse_linattn_forward_workspace_size(B, H, T, N, dv), workspace, q.device)
+    _check(lib().sparse_linattn_forward(_ptr(q), _ptr(k), _ptr(v), B, H, T, N, dv, _ptr(S0),
+                                        _ptr(S_out), _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
+    return y

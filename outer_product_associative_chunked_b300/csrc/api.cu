@@ -1,0 +1,274 @@
+// libopam C ABI: argument validation, workspace sizing and launch sequencing.
+// Every check runs on the host before anything is enqueued, so a rejected
+// call leaves the device untouched.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+
+#include "opam_internal.cuh"
+
+namespace opam {
+
+static thread_local char g_err[512] = "";
+
+void set_error(const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+}
+
+int cuda_fail(cudaError_t e, const char *where) {
+    if (e == cudaSuccess) return OPAM_OK;
+    set_error("%s: %s", where, cudaGetErrorString(e));
+    return OPAM_ERR_CUDA;
+}
+
+static std::atomic<uint64_t> g_launches{0};
+static thread_local cudaEvent_t g_prof_start = nullptr;
+static thread_local cudaEvent_t g_prof_stop = nullptr;
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+void prof_begin(cudaStream_t s) {
+    if (g_prof_start) cudaEventRecord(g_prof_start, s);
+}
+void prof_end(cudaStream_t s) {
+    if (g_prof_stop) cudaEventRecord(g_prof_stop, s);
+}
+
+namespace {
+
+constexpr int kMaxGridY = 65535;
+constexpr int kSparseMaxN = 49152;   // dense copy of one query row must fit shared memory
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+bool head_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+#define OPAM_CHECK_PTR(p)                                                      \
+    do {                                                                       \
+        if (!(p)) {                                                            \
+            set_error("%s: %s is NULL", fn, #p);                               \
+            return OPAM_ERR_INVALID_ARG;                                       \
+        }                                                                      \
+        if (!aligned16(p)) {                                                   \
+            set_error("%s: %s is not 16-byte aligned", fn, #p);                \
+            return OPAM_ERR_INVALID_ARG;                                       \
+        }                                                                      \
+    } while (0)
+
+#define OPAM_CHECK_OPT_PTR(p)                                                  \
+    do {                                                                       \
+        if ((p) && !aligned16(p)) {                                            \
+            set_error("%s: %s is not 16-byte aligned", fn, #p);                \
+            return OPAM_ERR_INVALID_ARG;                                       \
+        }                                                                      \
+    } while (0)
+
+int check_tc_dims(const char *fn, int dtype, int B, int H, int T, int dk, int dv, int W) {
+    if (dtype != OPAM_F32 && dtype != OPAM_BF16) {
+        set_error("%s: dtype %d is not OPAM_F32 or OPAM_BF16", fn, dtype);
+        return OPAM_ERR_INVALID_ARG;
+    }
+    if (B < 1 || H < 1 || T < 1 || W < 1 || dk < 1 || dv < 1) {
+        set_error("%s: extents must be positive (B=%d H=%d T=%d W=%d d_k=%d d_v=%d)", fn, B, H, T, W,
+                  dk, dv);
+        return OPAM_ERR_INVALID_ARG;
+    }
+    if (!head_ok(dk) || !head_ok(dv)) {
+        set_error("%s: head sizes d_k=%d d_v=%d not in {32, 64, 128}", fn, dk, dv);
+        return OPAM_ERR_UNSUPPORTED;
+    }
+    if ((long long)B * H > kMaxGridY) {
+        set_error("%s: B*H=%lld above %d", fn, (long long)B * H, kMaxGridY);
+        return OPAM_ERR_UNSUPPORTED;
+    }
+    return OPAM_OK;
+}
+
+float resolve_scale(float s, int dk) { return s > 0.f ? s : 1.0f / std::sqrt((float)dk); }
+
+int delta_chunk(int chunk) { return chunk == 0 ? 64 : chunk; }
+
+}  // namespace
+}  // namespace opam
+
+using namespace opam;
+
+extern "C" {
+
+const char *opam_last_error(void) { return g_err; }
+
+int opam_profile_events(void *start, void *stop) {
+    g_prof_start = (cudaEvent_t)start;
+    g_prof_stop = (cudaEvent_t)stop;
+    return OPAM_OK;
+}
+
+uint64_t opam_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t tc_layer_forward_workspace_size(int B, int H, int T, int d_k, int d_v, int W, int dtype) {
+    const char *fn = "tc_layer_forward_workspace_size";
+    if (check_tc_dims(fn, dtype, B, H, T, d_k, d_v, W) != OPAM_OK) return 0;
+    return tc_prefill_simt_workspace(B * H, T, d_k, d_v, W);
+}
+
+int tc_layer_forward(const void *q, const void *k, const void *v, int dtype, int B, int H, int T,
+                     int d_k, int d_v, int W, const float *lambda, const float *eta,
+                     const float *gate, float softmax_scale, void *y, opam_tc_state *state_out,
+                     void *workspace, size_t workspace_bytes, void *stream) {
+    const char *fn = "tc_layer_forward";
+    if (int rc = check_tc_dims(fn, dtype, B, H, T, d_k, d_v, W)) return rc;
+    OPAM_CHECK_PTR(q);
+    OPAM_CHECK_PTR(k);
+    OPAM_CHECK_PTR(v);
+    OPAM_CHECK_PTR(lambda);
+    OPAM_CHECK_PTR(eta);
+    OPAM_CHECK_PTR(gate);
+    OPAM_CHECK_PTR(y);
+    if (state_out) {
+        if (state_out->B != B || state_out->H != H || state_out->W != W || state_out->d_k != d_k ||
+            state_out->d_v != d_v || state_out->dtype != dtype) {
+            set_error("%s: state_out shape/dtype does not match the call", fn);
+            return OPAM_ERR_INVALID_ARG;
+        }
+        OPAM_CHECK_PTR(state_out->ring_k);
+        OPAM_CHECK_PTR(state_out->ring_v);
+        OPAM_CHECK_PTR(state_out->A);
+        OPAM_CHECK_PTR(state_out->pos);
+        if ((long long)W > kMaxGridY * 1024LL) {
+            set_error("%s: W=%d too large for the ring export", fn, W);
+            return OPAM_ERR_UNSUPPORTED;
+        }
+    }
+    const size_t need = tc_prefill_simt_workspace(B * H, T, d_k, d_v, W);
+    if (!workspace || workspace_bytes < need) {
+        set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
+        return OPAM_ERR_WORKSPACE;
+    }
+    OPAM_CHECK_PTR(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+    const float scale = resolve_scale(softmax_scale, d_k);
+    if (int rc = tc_prefill_simt(q, k, v, dtype, B, H, T, d_k, d_v, W, lambda, eta, gate, scale, y,
+                                 state_out ? state_out->A : nullptr, workspace, s))
+        return rc;
+    if (state_out)
+        return tc_export_ring(k, v, dtype, B, H, T, d_k, d_v, W, state_out->ring_k, state_out->ring_v,
+                              state_out->pos, s);
+    return OPAM_OK;
+}
+
+size_t tc_decode_step_workspace_size(const opam_tc_state *st) {
+    if (!st) return 0;
+    if (check_tc_dims("tc_decode_step_workspace_size", st->dtype, st->B, st->H, 1, st->d_k, st->d_v,
+                      st->W) != OPAM_OK)
+        return 0;
+    return tc_decode_workspace(st->B, st->H, st->d_k, st->d_v, st->W);
+}
+
+int tc_decode_step(opam_tc_state *st, const void *q, const void *k, const void *v,
+                   const float *lambda, const float *eta, const float *gate, float softmax_scale,
+                   void *y, void *workspace, size_t workspace_bytes, void *stream) {
+    const char *fn = "tc_decode_step";
+    if (!st) {
+        set_error("%s: state is NULL", fn);
+        return OPAM_ERR_INVALID_ARG;
+    }
+    if (int rc = check_tc_dims(fn, st->dtype, st->B, st->H, 1, st->d_k, st->d_v, st->W)) return rc;
+    OPAM_CHECK_PTR(st->ring_k);
+    OPAM_CHECK_PTR(st->ring_v);
+    OPAM_CHECK_PTR(st->A);
+    OPAM_CHECK_PTR(st->pos);
+    OPAM_CHECK_PTR(q);
+    OPAM_CHECK_PTR(k);
+    OPAM_CHECK_PTR(v);
+    OPAM_CHECK_PTR(lambda);
+    OPAM_CHECK_PTR(eta);
+    OPAM_CHECK_PTR(gate);
+    OPAM_CHECK_PTR(y);
+    const size_t need = tc_decode_workspace(st->B, st->H, st->d_k, st->d_v, st->W);
+    if (!workspace || workspace_bytes < need) {
+        set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
+        return OPAM_ERR_WORKSPACE;
+    }
+    OPAM_CHECK_PTR(workspace);
+    return tc_decode(st, q, k, v, lambda, eta, gate, resolve_scale(softmax_scale, st->d_k), y,
+                     workspace, (cudaStream_t)stream);
+}
+
+size_t delta_rule_forward_workspace_size(int B, int H, int T, int d_k, int d_v, int chunk, int dtype) {
+    const char *fn = "delta_rule_forward_workspace_size";
+    if (check_tc_dims(fn, dtype, B, H, T, d_k, d_v, 1) != OPAM_OK) return 0;
+    const int C = delta_chunk(chunk);
+    if (C != 16 && C != 32 && C != 64) return 0;
+    return delta_simt_workspace(B * H, T, d_k, d_v, C);
+}
+
+int delta_rule_forward(const void *q, const void *k, const void *v, const float *beta, int dtype,
+                       int B, int H, int T, int d_k, int d_v, int chunk, const float *S0,
+                       float *S_out, void *y, void *workspace, size_t workspace_bytes,
+                       void *stream) {
+    const char *fn = "delta_rule_forward";
+    if (int rc = check_tc_dims(fn, dtype, B, H, T, d_k, d_v, 1)) return rc;
+    const int C = delta_chunk(chunk);
+    if (C != 16 && C != 32 && C != 64) {
+        set_error("%s: chunk=%d not in {0, 16, 32, 64}", fn, chunk);
+        return OPAM_ERR_UNSUPPORTED;
+    }
+    OPAM_CHECK_PTR(q);
+    OPAM_CHECK_PTR(k);
+    OPAM_CHECK_PTR(v);
+    OPAM_CHECK_PTR(beta);
+    OPAM_CHECK_PTR(y);
+    OPAM_CHECK_OPT_PTR(S0);
+    OPAM_CHECK_OPT_PTR(S_out);
+    const size_t need = delta_simt_workspace(B * H, T, d_k, d_v, C);
+    if (!workspace || workspace_bytes < need) {
+        set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
+        return OPAM_ERR_WORKSPACE;
+    }
+    OPAM_CHECK_PTR(workspace);
+    return delta_simt(q, k, v, beta, dtype, B, H, T, d_k, d_v, C, S0, S_out, y, workspace,
+                      (cudaStream_t)stream);
+}
+
+size_t sparse_linattn_forward_workspace_size(int B, int H, int T, int N, int d_v) {
+    if (B < 1 || H < 1 || T < 1 || N < 1 || N > kSparseMaxN) return 0;
+    if (d_v != 32 && d_v != 64 && d_v != 128 && d_v != 256) return 0;
+    // The state lives in S_out when the caller supplies it; size for the
+    // worst case (no S_out) so one query serves both.
+    return sparse_workspace(B * H, T, N, d_v, true);
+}
+
+int sparse_linattn_forward(const float *q, const float *k, const float *v, int B, int H, int T, int N,
+                           int d_v, const float *S0, float *S_out, float *y, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    const char *fn = "sparse_linattn_forward";
+    if (B < 1 || H < 1 || T < 1 || N < 1) {
+        set_error("%s: extents must be positive (B=%d H=%d T=%d N=%d)", fn, B, H, T, N);
+        return OPAM_ERR_INVALID_ARG;
+    }
+    if (N > kSparseMaxN || (d_v != 32 && d_v != 64 && d_v != 128 && d_v != 256)) {
+        set_error("%s: N=%d (max %d) or d_v=%d (32/64/128/256) unsupported", fn, N, kSparseMaxN, d_v);
+        return OPAM_ERR_UNSUPPORTED;
+    }
+    if ((long long)B * H > kMaxGridY) {
+        set_error("%s: B*H above %d", fn, kMaxGridY);
+        return OPAM_ERR_UNSUPPORTED;
+    }
+    OPAM_CHECK_PTR(q);
+    OPAM_CHECK_PTR(k);
+    OPAM_CHECK_PTR(v);
+    OPAM_CHECK_PTR(y);
+    OPAM_CHECK_OPT_PTR(S0);
+    OPAM_CHECK_OPT_PTR(S_out);
+    const size_t need = sparse_workspace(B * H, T, N, d_v, S_out == nullptr);
+    if (!workspace || workspace_bytes < need) {
+        set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
+        return OPAM_ERR_WORKSPACE;
+    }
+    OPAM_CHECK_PTR(workspace);
+    return sparse_forward(q, k, v, B, H, T, N, d_v, S0, S_out, y, workspace, (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+// Internal declarations shared by the libopam translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "opam.h"
+
+namespace opam {
+
+// ---------------------------------------------------------------- errors
+void set_error(const char *fmt, ...);
+int cuda_fail(cudaError_t e, const char *where);
+
+// ---------------------------------------------------------------- instrumentation
+// count_launch(): one kernel enqueued.  prof_begin / prof_end bracket the
+// dominant kernel of an entry point with the caller's events, if any.
+void count_launch(int n = 1);
+void prof_begin(cudaStream_t s);
+void prof_end(cudaStream_t s);
+// After a kernel launch: count it and turn a launch error into OPAM_ERR_CUDA.
+inline int launched(const char *what) {
+    count_launch();
+    return cuda_fail(cudaGetLastError(), what);
+}
+
+// ---------------------------------------------------------------- element I/O
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float load(const float *p) { return *p; }
+    static __device__ __forceinline__ void store(float *p, float x) { *p = x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
+        return __bfloat162float(*p);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, float x) {
+        *p = __float2bfloat16_rn(x);
+    }
+};
+
+__device__ __forceinline__ float logistic(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+// Finite stand-in for -infinity in running maxima (keeps exp() finite).
+constexpr float kNegBig = -1.0e30f;
+
+inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------- launchers
+// Tensor Cache prefill, CUDA-core path (any supported head size / dtype).
+size_t tc_prefill_simt_workspace(int BH, int T, int dk, int dv, int W);
+int tc_prefill_simt(const void *q, const void *k, const void *v, int dtype, int B, int H,
+                    int T, int dk, int dv, int W, const float *lam, const float *eta,
+                    const float *gate, float scale, void *y, float *A_final,
+                    void *ws, cudaStream_t s);
+// Ring / pos export after a prefill (A is written by the prefill itself).
+int tc_export_ring(const void *k, const void *v, int dtype, int B, int H, int T, int dk,
+                   int dv, int W, void *ring_k, void *ring_v, int64_t *pos, cudaStream_t s);
+
+size_t tc_decode_workspace(int S, int H, int dk, int dv, int W);
+int tc_decode(const opam_tc_state *st, const void *q, const void *k, const void *v,
+              const float *lam, const float *eta, const float *gate, float scale, void *y,
+              void *ws, cudaStream_t s);
+
+size_t delta_simt_workspace(int BH, int T, int dk, int dv, int C);
+int delta_simt(const void *q, const void *k, const void *v, const float *beta, int dtype,
+               int B, int H, int T, int dk, int dv, int C, const float *S0, float *S_out,
+               void *y, void *ws, cudaStream_t s);
+
+size_t sparse_workspace(int BH, int T, int N, int dv, bool need_state);
+int sparse_forward(const float *q, const float *k, const float *v, int B, int H, int T, int N,
+                   int dv, const float *S0, float *S_out, float *y, void *ws, cudaStream_t s);
+
+}  // namespace opam

@@ -1,0 +1,269 @@
+// Tensor Cache single-token decode for a batch of independent sequences.
+//
+// "Tensor Cache: Eviction-conditioned Associative Memory for Transformers"
+// (gist.science 2605.22884), Methodology 1: the L1 ring holds the W most
+// recent tokens; when the ring overwrites an entry the displaced (k, v) is
+// written A <- lambda A + eta k v^T; the new token reads the ring with exact
+// softmax and the compressed past as q A; y = y_local + sigmoid(g) q A.
+//
+// Work per (sequence, head) is one pass over the ring (2 W d elements) and
+// one read-modify-write of A (d_k d_v floats): memory bound.  The ring is
+// split over `nsplit` CTAs per (sequence, head); each CTA also owns a slice
+// of A's rows, so A is streamed exactly once.  Kernel 1 writes per-split
+// partials (softmax max / sum / weighted values, and the partial q A of its
+// rows); kernel 2 merges them flash-decoding style, applies the gate and
+// stores the new token into its ring slot (after every reader of the evicted
+// entry has finished); kernel 3 advances pos.
+#include "opam_internal.cuh"
+
+namespace opam {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kMaxKeysPerSplit = 8192;
+
+struct DecodeGeom {
+    int nsplit, keys_per_split;
+};
+
+DecodeGeom geom(int W) {
+    int ns = ceil_div(W, 256);
+    if (ns > 64) ns = 64;
+    if (ns < ceil_div(W, kMaxKeysPerSplit)) ns = ceil_div(W, kMaxKeysPerSplit);
+    return {ns, ceil_div(W, ns)};
+}
+
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(kThreads)
+tc_decode_partial_kernel(const T *__restrict__ ring_k, const T *__restrict__ ring_v,
+                         float *__restrict__ A, const int64_t *__restrict__ pos,
+                         const T *__restrict__ q, const T *__restrict__ k,
+                         const T *__restrict__ v, int H, int W, int keys_per_split,
+                         const float *__restrict__ lam, const float *__restrict__ eta,
+                         float scale, float *__restrict__ part_m, float *__restrict__ part_o,
+                         float *__restrict__ part_ml) {
+    extern __shared__ float sm[];
+    float *qs = sm;             // [DK]
+    float *kes = qs + DK;       // [DK] evicted key
+    float *ves = kes + DK;      // [DV] evicted value
+    float *red = ves + DV;      // [kThreads] reduction scratch
+    float *sc = red + kThreads; // [keys_per_split] scores, then weights
+
+    const int sh = blockIdx.x, sp = blockIdx.y, nsplit = gridDim.y;
+    const int b = sh / H, h = sh - b * H;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t p = pos[b];
+    const int slot = (int)(p % W);
+    const bool evict = p >= W;
+    const size_t ring_row = (size_t)sh * W;
+
+    for (int a = tid; a < DK; a += kThreads) {
+        qs[a] = Elem<T>::load(q + (size_t)sh * DK + a);
+        kes[a] = evict ? Elem<T>::load(ring_k + (ring_row + slot) * DK + a) : 0.f;
+    }
+    for (int c = tid; c < DV; c += kThreads)
+        ves[c] = evict ? Elem<T>::load(ring_v + (ring_row + slot) * DV + c) : 0.f;
+    __syncthreads();
+
+    // ---- A rows owned by this split: eviction write, then partial q A.
+    {
+        constexpr int G = kThreads / DV;  // row groups
+        const int col = tid % DV, g = tid / DV;
+        const int rows = (DK + nsplit - 1) / nsplit;
+        const int r0 = sp * rows, r1 = min(DK, r0 + rows);
+        const float lm = lam[h], et = eta[h];
+        float *Ab = A + (size_t)sh * DK * DV;
+        float pm = 0.f;
+        for (int a = r0 + g; a < r1; a += G) {
+            float x = Ab[(size_t)a * DV + col];
+            if (evict) {
+                x = fmaf(lm, x, et * kes[a] * ves[col]);
+                Ab[(size_t)a * DV + col] = x;
+            }
+            pm = fmaf(qs[a], x, pm);
+        }
+        red[tid] = pm;
+        __syncthreads();
+        if (tid < DV) {
+            float s = 0.f;
+            for (int gg = 0; gg < G; ++gg) s += red[gg * DV + tid];
+            part_m[((size_t)sh * nsplit + sp) * DV + tid] = s;
+        }
+        __syncthreads();
+    }
+
+    // ---- ring softmax over this split's occupied slots (new token at `slot`).
+    const int occ = (p + 1 < (int64_t)W) ? (int)(p + 1) : W;
+    const int s0 = sp * keys_per_split, s1 = min(occ, s0 + keys_per_split);
+    const int nk = max(0, s1 - s0);
+    for (int jj = warp; jj < nk; jj += kThreads / 32) {
+        const int j = s0 + jj;
+        const T *kr = (j == slot) ? k + (size_t)sh * DK : ring_k + (ring_row + j) * DK;
+        float d = 0.f;
+        for (int a = lane; a < DK; a += 32) d = fmaf(qs[a], Elem<T>::load(kr + a), d);
+        d = warp_sum(d);
+        if (lane == 0) sc[jj] = d * scale;
+    }
+    __syncthreads();
+    float mx = kNegBig;
+    for (int jj = tid; jj < nk; jj += kThreads) mx = fmaxf(mx, sc[jj]);
+    mx = warp_max(mx);
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = kNegBig;
+    for (int w = 0; w < kThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+    __syncthreads();
+    float ssum = 0.f;
+    for (int jj = tid; jj < nk; jj += kThreads) {
+        const float e = expf(sc[jj] - mx);
+        sc[jj] = e;
+        ssum += e;
+    }
+    ssum = warp_sum(ssum);
+    if (lane == 0) red[warp] = ssum;
+    __syncthreads();
+    if (tid == 0) {
+        float s = 0.f;
+        for (int w = 0; w < kThreads / 32; ++w) s += red[w];
+        part_ml[((size_t)sh * nsplit + sp) * 2 + 0] = mx;
+        part_ml[((size_t)sh * nsplit + sp) * 2 + 1] = s;
+    }
+    __syncthreads();
+    {
+        constexpr int G = kThreads / DV;
+        const int col = tid % DV, g = tid / DV;
+        float o = 0.f;
+        for (int jj = g; jj < nk; jj += G) {
+            const int j = s0 + jj;
+            const T *vr = (j == slot) ? v + (size_t)sh * DV : ring_v + (ring_row + j) * DV;
+            o = fmaf(sc[jj], Elem<T>::load(vr + col), o);
+        }
+        red[tid] = o;
+        __syncthreads();
+        if (tid < DV) {
+            float s = 0.f;
+            for (int gg = 0; gg < G; ++gg) s += red[gg * DV + tid];
+            part_o[((size_t)sh * nsplit + sp) * DV + tid] = s;
+        }
+    }
+}
+
+template <typename T, int DK, int DV>
+__global__ void tc_decode_combine_kernel(T *__restrict__ ring_k, T *__restrict__ ring_v,
+                                         const int64_t *__restrict__ pos,
+                                         const T *__restrict__ k, const T *__restrict__ v,
+                                         int H, int W, int nsplit,
+                                         const float *__restrict__ gate,
+                                         const float *__restrict__ part_m,
+                                         const float *__restrict__ part_o,
+                                         const float *__restrict__ part_ml, T *__restrict__ y) {
+    const int sh = blockIdx.x, b = sh / H, h = sh - b * H;
+    const int tid = threadIdx.x;
+    const float *ml = part_ml + (size_t)sh * nsplit * 2;
+    float M = kNegBig;
+    for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[2 * s]);
+    if (tid < DV) {
+        float L = 0.f, o = 0.f, m = 0.f;
+        for (int s = 0; s < nsplit; ++s) {
+            const float f = expf(ml[2 * s] - M);
+            L = fmaf(ml[2 * s + 1], f, L);
+            o = fmaf(part_o[((size_t)sh * nsplit + s) * DV + tid], f, o);
+            m += part_m[((size_t)sh * nsplit + s) * DV + tid];
+        }
+        const float sg = 1.0f / (1.0f + expf(-gate[h]));
+        Elem<T>::store(y + (size_t)sh * DV + tid, o / L + sg * m);
+    }
+    const int slot = (int)(pos[b] % W);
+    for (int a = tid; a < DK; a += blockDim.x)
+        ring_k[((size_t)sh * W + slot) * DK + a] = k[(size_t)sh * DK + a];
+    for (int c = tid; c < DV; c += blockDim.x)
+        ring_v[((size_t)sh * W + slot) * DV + c] = v[(size_t)sh * DV + c];
+}
+
+__global__ void advance_pos_kernel(int64_t *pos, int B) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B) pos[b] += 1;
+}
+
+struct Parts {
+    float *m, *o, *ml;
+};
+
+Parts carve(void *ws, int SH, int nsplit, int dv) {
+    char *p = (char *)ws;
+    Parts r;
+    r.m = (float *)p;
+    p += align_up(sizeof(float) * (size_t)SH * nsplit * dv, 256);
+    r.o = (float *)p;
+    p += align_up(sizeof(float) * (size_t)SH * nsplit * dv, 256);
+    r.ml = (float *)p;
+    return r;
+}
+
+template <typename T, int DK, int DV>
+int launch(const opam_tc_state *st, const void *q, const void *k, const void *v, const float *lam,
+           const float *eta, const float *gate, float scale, void *y, void *ws, cudaStream_t s) {
+    const int SH = st->B * st->H;
+    const DecodeGeom g = geom(st->W);
+    const Parts pr = carve(ws, SH, g.nsplit, DV);
+    const size_t smem = sizeof(float) * (DK + DK + DV + kThreads + g.keys_per_split);
+    auto k1 = tc_decode_partial_kernel<T, DK, DV>;
+    cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "tc_decode smem attribute");
+    prof_begin(s);
+    k1<<<dim3(SH, g.nsplit), kThreads, smem, s>>>(
+        (const T *)st->ring_k, (const T *)st->ring_v, st->A, st->pos, (const T *)q, (const T *)k,
+        (const T *)v, st->H, st->W, g.keys_per_split, lam, eta, scale, pr.m, pr.o, pr.ml);
+    if (int rc = launched("tc_decode_partial")) return rc;
+    prof_end(s);
+    tc_decode_combine_kernel<T, DK, DV><<<SH, 128, 0, s>>>(
+        (T *)st->ring_k, (T *)st->ring_v, st->pos, (const T *)k, (const T *)v, st->H, st->W,
+        g.nsplit, gate, pr.m, pr.o, pr.ml, (T *)y);
+    if (int rc = launched("tc_decode_combine")) return rc;
+    advance_pos_kernel<<<ceil_div(st->B, 128), 128, 0, s>>>(st->pos, st->B);
+    return launched("advance_pos");
+}
+
+template <typename T, int DK>
+int by_dv(const opam_tc_state *st, const void *q, const void *k, const void *v, const float *lam,
+          const float *eta, const float *gate, float scale, void *y, void *ws, cudaStream_t s) {
+    switch (st->d_v) {
+        case 32: return launch<T, DK, 32>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
+        case 64: return launch<T, DK, 64>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
+        case 128: return launch<T, DK, 128>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
+    }
+    set_error("d_v=%d unsupported", st->d_v);
+    return OPAM_ERR_UNSUPPORTED;
+}
+
+template <typename T>
+int by_dk(const opam_tc_state *st, const void *q, const void *k, const void *v, const float *lam,
+          const float *eta, const float *gate, float scale, void *y, void *ws, cudaStream_t s) {
+    switch (st->d_k) {
+        case 32: return by_dv<T, 32>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
+        case 64: return by_dv<T, 64>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
+        case 128: return by_dv<T, 128>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
+    }
+    set_error("d_k=%d unsupported", st->d_k);
+    return OPAM_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+size_t tc_decode_workspace(int S, int H, int dk, int dv, int W) {
+    (void)dk;
+    const DecodeGeom g = geom(W);
+    const size_t SH = (size_t)S * H;
+    return 2 * align_up(sizeof(float) * SH * g.nsplit * dv, 256) +
+           align_up(sizeof(float) * SH * g.nsplit * 2, 256);
+}
+
+int tc_decode(const opam_tc_state *st, const void *q, const void *k, const void *v,
+              const float *lam, const float *eta, const float *gate, float scale, void *y,
+              void *ws, cudaStream_t s) {
+    if (st->dtype == OPAM_BF16)
+        return by_dk<__nv_bfloat16>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
+    return by_dk<float>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
+}
+
+}  // namespace opam

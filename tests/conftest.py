@@ -24,3 +24,14 @@ def oracle_mod():
     from oracle import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def cuda_lib():
+    """Build (if stale) and load libopam.so; skip when no CUDA device exists."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from outer_product_associative_chunked_b300 import binding, build
+    build.build()
+    return binding

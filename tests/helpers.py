@@ -39,3 +39,37 @@ def rms_rel(x, ref):
 # Parity bars for the CUDA path against the float64 oracle.
 TOL_F32_REL_L2 = 1e-5      # fp32 inputs / fp32 state
 TOL_BF16_RMS = 2e-2        # bf16 inputs / fp32 state, relative to output RMS
+
+
+def to_np(t):
+    """float64 numpy copy of a (device) tensor."""
+    return t.detach().to("cpu").double().numpy()
+
+
+def check_parity(y, ref, dtype, what=""):
+    """Apply the parity bar of the given input dtype; return the measured error."""
+    if dtype in ("f32", "float32"):
+        err = rel_l2(y, ref)
+        assert err <= TOL_F32_REL_L2, f"{what}: rel L2 {err:.3e} > {TOL_F32_REL_L2}"
+    else:
+        err = rms_rel(y, ref)
+        assert err <= TOL_BF16_RMS, f"{what}: RMS err {err:.3e} > {TOL_BF16_RMS} of output RMS"
+    return err
+
+
+def guarded(shape, dtype, device="cuda", pad=4096):
+    """Output tensor followed by a canary tail; returns (view, full buffer)."""
+    import torch
+    n = 1
+    for s in shape:
+        n *= s
+    buf = torch.full((n + pad,), 1234.5, dtype=dtype, device=device)
+    return buf[:n].view(*shape), buf
+
+
+def canary_intact(buf, shape):
+    import torch
+    n = 1
+    for s in shape:
+        n *= s
+    return bool(torch.all(buf[n:] == 1234.5))

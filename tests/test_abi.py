@@ -1,0 +1,108 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+the header declares, sizes workspaces, and rejects bad arguments on the host
+before anything is enqueued (each call below fails validation, so no kernel
+launches and no pointer is dereferenced)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from outer_product_associative_chunked_b300 import binding, build
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "opam.h")
+FAKE = 0x10000  # 16-byte aligned, never dereferenced: every call here fails validation first
+
+
+@pytest.fixture(scope="module")
+def L():
+    build.build()
+    return binding.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_binding_exports():
+    assert sorted(binding.EXPORTS) == _declared_functions()
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_workspace_sizes(L):
+    assert binding.tc_layer_forward_workspace_size(4, 8, 4096, 64, 64, 512, __import__("torch").bfloat16) > 0
+    assert L.tc_layer_forward_workspace_size(1, 1, 16, 96, 96, 4, 0) == 0       # unsupported head
+    assert L.tc_layer_forward_workspace_size(1, 1, 0, 64, 64, 4, 0) == 0        # empty sequence
+    assert L.delta_rule_forward_workspace_size(8, 16, 8192, 128, 128, 64, 1) > 0
+    assert L.delta_rule_forward_workspace_size(1, 1, 8, 64, 64, 48, 1) == 0     # bad chunk
+    assert L.sparse_linattn_forward_workspace_size(2, 4, 2048, 16384, 256) > 0
+    assert L.sparse_linattn_forward_workspace_size(1, 1, 8, 100000, 64) == 0    # N too wide
+    st = binding.TCStateStruct(FAKE, FAKE, FAKE, FAKE, 64, 16, 2048, 128, 128, 1)
+    assert L.tc_decode_step_workspace_size(ctypes.byref(st)) > 0
+
+
+def _tc(L, **kw):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, dtype=1, B=1, H=1, T=16, dk=64, dv=64, W=4, lam=FAKE, eta=FAKE,
+             gate=FAKE, scale=0.0, y=FAKE, state=None, ws=FAKE, wsb=0, stream=None)
+    a.update(kw)
+    a["wsb"] = kw.get("wsb", L.tc_layer_forward_workspace_size(a["B"], a["H"], a["T"], a["dk"], a["dv"],
+                                                               a["W"], a["dtype"]))
+    rc = L.tc_layer_forward(a["q"], a["k"], a["v"], a["dtype"], a["B"], a["H"], a["T"], a["dk"], a["dv"],
+                            a["W"], a["lam"], a["eta"], a["gate"], a["scale"], a["y"], a["state"],
+                            a["ws"], a["wsb"], a["stream"])
+    return rc, binding.last_error()
+
+
+def test_tc_forward_rejects_bad_arguments(L):
+    assert _tc(L, q=None)[0] == -1
+    assert _tc(L, y=FAKE + 4)[0] == -1            # misaligned
+    assert _tc(L, T=0)[0] == -1
+    assert _tc(L, W=0)[0] == -1
+    assert _tc(L, dtype=7)[0] == -1
+    assert _tc(L, dk=96, dv=96)[0] == -2
+    rc, msg = _tc(L, wsb=16)
+    assert rc == -4 and "workspace" in msg
+    assert _tc(L, ws=None)[0] == -4
+    bad_state = binding.TCStateStruct(FAKE, FAKE, FAKE, FAKE, 1, 1, 8, 64, 64, 1)  # W mismatch
+    assert _tc(L, state=ctypes.byref(bad_state))[0] == -1
+
+
+def test_decode_rejects_bad_arguments(L):
+    st = binding.TCStateStruct(FAKE, FAKE, FAKE, FAKE, 2, 2, 16, 64, 64, 1)
+    need = L.tc_decode_step_workspace_size(ctypes.byref(st))
+    call = lambda st, ws=need, q=FAKE: L.tc_decode_step(  # noqa: E731
+        ctypes.byref(st), q, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, FAKE, FAKE, ws, None)
+    assert call(st, q=None) == -1
+    assert call(st, ws=need - 1) == -4
+    st2 = binding.TCStateStruct(None, FAKE, FAKE, FAKE, 2, 2, 16, 64, 64, 1)
+    assert call(st2) == -1
+    st3 = binding.TCStateStruct(FAKE, FAKE, FAKE, FAKE, 2, 2, 16, 48, 48, 1)
+    assert call(st3) == -2
+    assert L.tc_decode_step(None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0.0, FAKE, FAKE, need, None) == -1
+
+
+def test_delta_and_sparse_reject_bad_arguments(L):
+    ws = L.delta_rule_forward_workspace_size(1, 1, 16, 64, 64, 0, 1)
+    d = lambda **kw: L.delta_rule_forward(  # noqa: E731
+        kw.get("q", FAKE), FAKE, FAKE, kw.get("beta", FAKE), 1, 1, 1, 16, 64, 64, kw.get("chunk", 0),
+        kw.get("S0", None), None, FAKE, FAKE, kw.get("ws", ws), None)
+    assert d(q=None) == -1
+    assert d(beta=None) == -1
+    assert d(chunk=48) == -2
+    assert d(S0=FAKE + 8) == -1
+    assert d(ws=ws - 1) == -4
+    wss = L.sparse_linattn_forward_workspace_size(1, 1, 16, 512, 64)
+    s = lambda **kw: L.sparse_linattn_forward(  # noqa: E731
+        FAKE, kw.get("k", FAKE), FAKE, 1, 1, 16, kw.get("N", 512), kw.get("dv", 64), None, None, FAKE,
+        FAKE, kw.get("ws", wss), None)
+    assert s(k=None) == -1
+    assert s(dv=48) == -2
+    assert s(N=0) == -1
+    assert s(ws=wss - 1) == -4

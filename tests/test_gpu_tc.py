@@ -1,0 +1,112 @@
+"""Tensor Cache prefill on the GPU vs the float64 oracle.
+
+Bars: fp32 inputs -> relative L2 <= 1e-5 over the whole output; bf16 inputs /
+fp32 state -> RMS(error) <= 2e-2 of the output RMS.  Small cases cover ragged
+tails, windows around the chunk length, head sizes 32/64/128, unequal d_k /
+d_v and odd B*H; the two page-sized workloads run at full size on the GPU and
+are checked on sampled heads and positions the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+from helpers import canary_intact, check_parity, guarded, to_np
+from outer_product_associative_chunked_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu(inp):
+    return [x.cuda() for x in (inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate)]
+
+
+SMALL = [
+    # dtype, B, H, T, d_k, d_v, W
+    ("f32", 1, 1, 1, 32, 32, 1),
+    ("f32", 1, 3, 2, 64, 64, 1),
+    ("f32", 3, 1, 3, 32, 64, 2),
+    ("f32", 1, 1, 15, 128, 128, 4),
+    ("f32", 2, 1, 16, 64, 32, 16),
+    ("f32", 1, 3, 17, 32, 32, 63),
+    ("f32", 1, 1, 63, 64, 64, 64),
+    ("f32", 1, 2, 64, 128, 64, 65),
+    ("f32", 1, 1, 65, 32, 32, 64),
+    ("f32", 1, 1, 200, 64, 64, 63),
+    ("f32", 1, 1, 200, 128, 128, 65),
+    ("f32", 2, 3, 200, 32, 32, 300),
+    ("f32", 1, 1, 257, 64, 64, 1),
+    ("bf16", 1, 1, 1, 64, 64, 1),
+    ("bf16", 3, 1, 17, 64, 64, 2),
+    ("bf16", 1, 3, 65, 128, 128, 64),
+    ("bf16", 1, 1, 200, 64, 64, 63),
+    ("bf16", 2, 1, 333, 128, 128, 129),
+    ("bf16", 1, 2, 640, 64, 64, 128),
+    ("bf16", 1, 1, 700, 128, 128, 256),
+    ("bf16", 1, 1, 150, 32, 128, 50),
+]
+
+
+@pytest.mark.parametrize("dtype,B,H,T,dk,dv,W", SMALL)
+def test_small_parity(cuda_lib, oracle_mod, dtype, B, H, T, dk, dv, W):
+    inp = synth.tc_inputs(B, H, T, dk, dv, W, dtype=dtype, seed=T * 7 + W)
+    q, k, v, lam, eta, gate = _gpu(inp)
+    y, buf = guarded((B, H, T, dv), q.dtype)
+    cuda_lib.tc_layer_forward(q, k, v, lam, eta, gate, W, out=y)
+    torch.cuda.synchronize()
+    assert canary_intact(buf, (B, H, T, dv))
+    ref = oracle_mod.tc_prefill(inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate, W)["y"]
+    check_parity(to_np(y), ref, dtype, f"T={T} W={W} d={dk}/{dv}")
+
+
+@pytest.mark.parametrize("dtype,T,W,d", [("f32", 100, 7, 32), ("f32", 20, 50, 64),
+                                         ("bf16", 300, 64, 128), ("bf16", 130, 129, 64)])
+def test_state_export(cuda_lib, oracle_mod, dtype, T, W, d):
+    B, H = 2, 2
+    inp = synth.tc_inputs(B, H, T, d, d, W, dtype=dtype, seed=11)
+    q, k, v, lam, eta, gate = _gpu(inp)
+    st = cuda_lib.TCState(B, H, W, d, d, dtype=q.dtype)
+    st.pos.fill_(-5)
+    cuda_lib.tc_layer_forward(q, k, v, lam, eta, gate, W, state=st)
+    torch.cuda.synchronize()
+    ref = oracle_mod.tc_prefill(inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate, W, want_state=True)
+    np.testing.assert_array_equal(to_np(st.ring_k), ref["ring_k"])   # copies are exact
+    np.testing.assert_array_equal(to_np(st.ring_v), ref["ring_v"])
+    assert torch.all(st.pos.cpu() == T)
+    check_parity(to_np(st.A), ref["A"], "f32" if dtype == "f32" else "bf16", "A")
+
+
+def test_fp32_workload_T256_d32_W32(cuda_lib, oracle_mod):
+    w = synth.WORKLOADS["tc_fp32_T256_d32_W32"]
+    inp = synth.tc_inputs(**{k: w.dims[k] for k in ("B", "H", "T", "d_k", "d_v", "W", "dtype", "lam",
+                                                    "eta", "gate")}, seed=w.seed)
+    q, k, v, lam, eta, gate = _gpu(inp)
+    y = cuda_lib.tc_layer_forward(q, k, v, lam, eta, gate, inp.W)
+    torch.cuda.synchronize()
+    ref = oracle_mod.tc_prefill(inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate, inp.W)["y"]
+    err = check_parity(to_np(y), ref, "f32", "fp32 workload")
+    assert err < 1e-5
+
+
+def _sampled_positions(T, W):
+    ts = {0, 1, W - 1, W, W + 1, T // 2, T - 2, T - 1}
+    ts |= set(np.random.default_rng(T).integers(0, T, 8).tolist())
+    return sorted(t for t in ts if 0 <= t < T)
+
+
+@pytest.mark.parametrize("name,units", [("tc_bf16_B4_H8_T4096_d64_W512", [(0, 0), (3, 7), (1, 4)]),
+                                        ("tc_bf16_B1_H16_T32768_d128_W2048", [(0, 0), (0, 9), (0, 15)])])
+def test_full_size_workload_sampled(cuda_lib, oracle_mod, name, units):
+    w = synth.WORKLOADS[name]
+    d = w.dims
+    inp = synth.tc_inputs(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], dtype=d["dtype"], seed=w.seed)
+    q, k, v, lam, eta, gate = _gpu(inp)
+    y = cuda_lib.tc_layer_forward(q, k, v, lam, eta, gate, inp.W)
+    torch.cuda.synchronize()
+    assert torch.isfinite(y.float()).all()
+    ts = _sampled_positions(d["T"], d["W"])
+    got, ref = [], []
+    for b, h in units:
+        got.append(to_np(y[b, h, ts]))
+        ref.append(oracle_mod.tc_output_at(inp.q[b, h], inp.k[b, h], inp.v[b, h], float(inp.lam[h]),
+                                           float(inp.eta[h]), float(inp.gate[h]), inp.W, ts))
+    check_parity(np.stack(got), np.stack(ref), "bf16", name)
