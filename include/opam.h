@@ -105,6 +105,35 @@ int tc_layer_forward(const void *q, const void *k, const void *v, int dtype,
                      float softmax_scale, void *y, opam_tc_state *state_out,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* Bytes of scratch built into the library for tc_layer_forward_noalloc. */
+#define OPAM_STATIC_SCRATCH_BYTES (64u << 20)
+
+/* tc_layer_forward without a workspace argument, for callers that cannot
+ * allocate device memory.  The pages have no counterpart to this: it exists
+ * for host software, not for the method.
+ *
+ * Who needs it: plugins living inside an application that owns all device
+ * memory through its own allocator, and services that forbid allocation after
+ * start-up (cudaMalloc can block, synchronise the device, or fail once the
+ * pool is reserved).  Such callers can pass inputs and outputs but cannot
+ * provide the scratch tc_layer_forward requires.
+ *
+ * Behaviour: identical arguments and results to tc_layer_forward, with the
+ * scratch taken from a fixed OPAM_STATIC_SCRATCH_BYTES array inside the
+ * library (present on every GPU that loads the library until the process
+ * exits).  Nothing is allocated.  A problem whose
+ * tc_layer_forward_workspace_size() exceeds OPAM_STATIC_SCRATCH_BYTES returns
+ * OPAM_ERR_WORKSPACE with both sizes in opam_last_error().  The first call on
+ * each device looks up the array's device address with that device current;
+ * make that first call before any stream capture.  All calls on a device share
+ * the array: calls that overlap on the GPU (other streams, other threads) race
+ * and must be serialised by the caller. */
+int tc_layer_forward_noalloc(const void *q, const void *k, const void *v, int dtype,
+                             int B, int H, int T, int d_k, int d_v, int W,
+                             const float *lambda, const float *eta, const float *gate,
+                             float softmax_scale, void *y, opam_tc_state *state_out,
+                             void *stream);
+
 /* One Tensor Cache decode step for a batch of independent sequences
  * ("Tensor Cache", Methodology 1: when the ring overwrites an entry the
  * displaced (k, v) is written into A; the new token is then read through the

@@ -21,7 +21,7 @@ _STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "CUDA", -4: "WORKS
 
 # Every symbol the C header declares (checked by the CPU test-suite).
 EXPORTS = (
-    "tc_layer_forward_workspace_size", "tc_layer_forward",
+    "tc_layer_forward_workspace_size", "tc_layer_forward", "tc_layer_forward_noalloc",
     "tc_decode_step_workspace_size", "tc_decode_step",
     "delta_rule_forward_workspace_size", "delta_rule_forward",
     "sparse_linattn_forward_workspace_size", "sparse_linattn_forward",
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
         L.tc_layer_forward_workspace_size.argtypes = [i, i, i, i, i, i, i]
         L.tc_layer_forward.restype = i
         L.tc_layer_forward.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, f, vp, sp, vp, sz, vp]
+        L.tc_layer_forward_noalloc.restype = i
+        L.tc_layer_forward_noalloc.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, f, vp, sp, vp]
         L.tc_decode_step_workspace_size.restype = sz
         L.tc_decode_step_workspace_size.argtypes = [sp]
         L.tc_decode_step.restype = i
@@ -171,6 +173,31 @@ def tc_layer_forward(q, k, v, lam, eta, gate, W, softmax_scale=0.0, out=None, st
                                   _ptr(eta), _ptr(gate), float(softmax_scale), _ptr(y), st, _ptr(ws),
                                   ws.numel(), _stream(stream)))
     return y
+
+
+STATIC_SCRATCH_BYTES = 64 << 20  # OPAM_STATIC_SCRATCH_BYTES in include/opam.h
+
+
+def tc_layer_forward_noalloc(q, k, v, lam, eta, gate, W, out, softmax_scale=0.0, state=None,
+                             stream=None):
+    """tc_layer_forward for callers that cannot allocate device memory.
+
+    For hosts that hand the library only input and output buffers (plugins
+    inside an application that owns all device memory, services that forbid
+    allocation after start-up).  ``out`` must be given; no workspace is taken:
+    the library uses its built-in scratch of STATIC_SCRATCH_BYTES, and rejects
+    larger problems with OpamError(WORKSPACE).  Calls sharing a device must
+    not overlap on the GPU; make the first call on a device before any stream
+    capture.
+    """
+    _dev(q, k, v, lam, eta, gate, out)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    st = ctypes.byref(state.struct()) if state is not None else None
+    _check(lib().tc_layer_forward_noalloc(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), B, H, T, dk, dv,
+                                          int(W), _ptr(lam), _ptr(eta), _ptr(gate), float(softmax_scale),
+                                          _ptr(out), st, _stream(stream)))
+    return out
 
 
 def tc_decode_step_workspace_size(state: TCState) -> int:
