@@ -55,7 +55,8 @@ typedef enum {
     OPAM_ERR_INVALID_ARG = -1,  /* null/misaligned pointer, bad extent        */
     OPAM_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. d = 96)    */
     OPAM_ERR_CUDA = -3,         /* a CUDA launch or API call failed           */
-    OPAM_ERR_WORKSPACE = -4     /* workspace missing or smaller than required */
+    OPAM_ERR_WORKSPACE = -4,    /* workspace missing or smaller than required */
+    OPAM_ERR_TIMEOUT = -5       /* a kernel's bounded wait ran out (see below) */
 } opam_status;
 
 /* ------------------------------------------------------------------------
@@ -200,6 +201,14 @@ int sparse_linattn_forward(const float *q, const float *k, const float *v,
 
 /* Message for the last non-OK status returned on the calling thread. */
 const char *opam_last_error(void);
+
+/* Device-side status of the tensor-core kernels.  Their pipeline waits are
+ * bounded (about one second each); a wait that runs out abandons the CTA's
+ * work, leaves the outputs undefined and records a status bit instead of
+ * hanging the GPU.  This call synchronises the device, returns OPAM_OK when
+ * no bit is set and OPAM_ERR_TIMEOUT otherwise (with a message), and clears
+ * the bits when `clear` is non-zero. */
+int opam_device_status(int clear);
 
 /* ------------------------------------------------------------------------
  * Instrumentation (no counterpart on the pages; used by benchmarks).

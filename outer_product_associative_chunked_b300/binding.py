@@ -17,7 +17,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libopam.so")
 
 OPAM_F32, OPAM_BF16 = 0, 1
-_STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "CUDA", -4: "WORKSPACE"}
+_STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "CUDA", -4: "WORKSPACE", -5: "TIMEOUT"}
 
 # Every symbol the C header declares (checked by the CPU test-suite).
 EXPORTS = (
@@ -25,7 +25,7 @@ EXPORTS = (
     "tc_decode_step_workspace_size", "tc_decode_step",
     "delta_rule_forward_workspace_size", "delta_rule_forward",
     "sparse_linattn_forward_workspace_size", "sparse_linattn_forward",
-    "opam_last_error", "opam_profile_events", "opam_kernel_launches",
+    "opam_last_error", "opam_profile_events", "opam_kernel_launches", "opam_device_status",
 )
 
 
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.opam_profile_events.argtypes = [vp, vp]
         L.opam_kernel_launches.restype = ctypes.c_uint64
         L.opam_kernel_launches.argtypes = []
+        L.opam_device_status.restype = i
+        L.opam_device_status.argtypes = [i]
         _lib = L
     return _lib
 
@@ -98,6 +100,12 @@ def profile_events(start=None, stop=None) -> None:
 def kernel_launches() -> int:
     """Kernels libopam has launched in this process so far."""
     return int(lib().opam_kernel_launches())
+
+
+def device_status(clear: bool = True) -> None:
+    """Raise OpamError(TIMEOUT) if a bounded wait inside a tensor-core kernel
+    ran out since the last check (synchronises the device)."""
+    _check(lib().opam_device_status(1 if clear else 0))
 
 
 def _check(rc: int) -> None:

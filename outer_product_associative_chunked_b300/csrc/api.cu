@@ -90,6 +90,12 @@ float resolve_scale(float s, int dk) { return s > 0.f ? s : 1.0f / std::sqrt((fl
 
 int delta_chunk(int chunk) { return chunk == 0 ? 64 : chunk; }
 
+// Scratch of the Tensor Cache prefill on the path the call takes.
+size_t tc_prefill_workspace(int B, int H, int T, int dk, int dv, int W, int dtype) {
+    if (tc_prefill_tcgen05_supported(dtype, dk, dv)) return tc_prefill_tcgen05_workspace(B * H, T, dk, dv);
+    return tc_prefill_simt_workspace(B * H, T, dk, dv, W);
+}
+
 }  // namespace
 }  // namespace opam
 
@@ -107,10 +113,18 @@ int opam_profile_events(void *start, void *stop) {
 
 uint64_t opam_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
+int opam_device_status(int clear) {
+    const unsigned int st = tc_prefill_tcgen05_status(clear != 0);
+    if (st == 0) return OPAM_OK;
+    set_error("opam_device_status: a bounded wait ran out in the tensor-core Tensor Cache prefill "
+              "(status bits 0x%x); its outputs are not valid", st);
+    return OPAM_ERR_TIMEOUT;
+}
+
 size_t tc_layer_forward_workspace_size(int B, int H, int T, int d_k, int d_v, int W, int dtype) {
     const char *fn = "tc_layer_forward_workspace_size";
     if (check_tc_dims(fn, dtype, B, H, T, d_k, d_v, W) != OPAM_OK) return 0;
-    return tc_prefill_simt_workspace(B * H, T, d_k, d_v, W);
+    return tc_prefill_workspace(B, H, T, d_k, d_v, W, dtype);
 }
 
 int tc_layer_forward(const void *q, const void *k, const void *v, int dtype, int B, int H, int T,
@@ -141,7 +155,7 @@ int tc_layer_forward(const void *q, const void *k, const void *v, int dtype, int
             return OPAM_ERR_UNSUPPORTED;
         }
     }
-    const size_t need = tc_prefill_simt_workspace(B * H, T, d_k, d_v, W);
+    const size_t need = tc_prefill_workspace(B, H, T, d_k, d_v, W, dtype);
     if (!workspace || workspace_bytes < need) {
         set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
         return OPAM_ERR_WORKSPACE;
@@ -149,9 +163,13 @@ int tc_layer_forward(const void *q, const void *k, const void *v, int dtype, int
     OPAM_CHECK_PTR(workspace);
     cudaStream_t s = (cudaStream_t)stream;
     const float scale = resolve_scale(softmax_scale, d_k);
-    if (int rc = tc_prefill_simt(q, k, v, dtype, B, H, T, d_k, d_v, W, lambda, eta, gate, scale, y,
-                                 state_out ? state_out->A : nullptr, workspace, s))
-        return rc;
+    float *A_final = state_out ? state_out->A : nullptr;
+    const int rc = tc_prefill_tcgen05_supported(dtype, d_k, d_v)
+                       ? tc_prefill_tcgen05(q, k, v, B, H, T, d_k, d_v, W, lambda, eta, gate, scale, y,
+                                            A_final, workspace, s)
+                       : tc_prefill_simt(q, k, v, dtype, B, H, T, d_k, d_v, W, lambda, eta, gate, scale,
+                                         y, A_final, workspace, s);
+    if (rc) return rc;
     if (state_out)
         return tc_export_ring(k, v, dtype, B, H, T, d_k, d_v, W, state_out->ring_k, state_out->ring_v,
                               state_out->pos, s);

@@ -70,6 +70,16 @@ int tc_prefill_simt(const void *q, const void *k, const void *v, int dtype, int 
 int tc_export_ring(const void *k, const void *v, int dtype, int B, int H, int T, int dk,
                    int dv, int W, void *ring_k, void *ring_v, int64_t *pos, cudaStream_t s);
 
+// Tensor Cache prefill, tensor-core path (bf16 inputs, d_k, d_v in {64, 128}).
+bool tc_prefill_tcgen05_supported(int dtype, int dk, int dv);
+size_t tc_prefill_tcgen05_workspace(int BH, int T, int dk, int dv);
+int tc_prefill_tcgen05(const void *q, const void *k, const void *v, int B, int H, int T, int dk,
+                       int dv, int W, const float *lam, const float *eta, const float *gate,
+                       float scale, void *y, float *A_final, void *ws, cudaStream_t s);
+// Status bits recorded by bounded waits that ran out (0 = none); reads the
+// device word synchronously and optionally clears it.
+unsigned int tc_prefill_tcgen05_status(bool clear);
+
 size_t tc_decode_workspace(int S, int H, int dk, int dv, int W);
 int tc_decode(const opam_tc_state *st, const void *q, const void *k, const void *v,
               const float *lam, const float *eta, const float *gate, float scale, void *y,

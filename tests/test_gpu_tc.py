@@ -16,6 +16,14 @@ from outer_product_associative_chunked_b300 import synth
 pytestmark = pytest.mark.gpu
 
 
+@pytest.fixture(autouse=True)
+def _no_device_timeouts(cuda_lib):
+    """Every case must leave the tensor-core kernels' wait status clean."""
+    cuda_lib.device_status(clear=True)
+    yield
+    cuda_lib.device_status(clear=True)
+
+
 def _gpu(inp):
     return [x.cuda() for x in (inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate)]
 
