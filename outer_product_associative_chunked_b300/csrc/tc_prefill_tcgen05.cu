@@ -8,7 +8,7 @@
 // parallel weighted-sum scan equal to the per-token writes.  Token s is
 // written at step s + W, so m_t = sum_{s <= t-W} eta lambda^(t-W-s) <q_t,k_s> v_s.
 //
-// Blocks of C = 128 positions.  Query block j covers [jC, jC+C); the tokens
+// Chunks of C = 128 positions.  Query block j covers [jC, jC+C); the tokens
 // evicted during its steps are the shifted chunk [jC-W, jC-W+C).  With A_j the
 // state before the block (every token s < jC-W) and row i of the block:
 //   m_{jC+i} = lambda^(i+1) q A_j + sum_{l<=i} eta lambda^(i-l) <q, k'_l> v'_l
@@ -17,22 +17,24 @@
 // (keys [jC-W, jC+C) in tiles of 128), so one Q K^T product serves both the
 // L2 term (key l <= row i) and the softmax (l > i).
 //
-// Three kernels:
-//   tc_l2_delta_kernel  dA_j = K'^T diag(w) V' per (head, chunk) on tcgen05;
-//   tc_l2_scan_kernel   A_j from the dA_j (a first-order linear recurrence per
-//                       element), written as bf16 for the next kernel, and the
-//                       final fp32 state;
+// The chunk recurrence is split into segments of L chunks so that many CTAs
+// share it: within segment g (chunks [gL, gL+L)) the state is
+//   A_j = A_j^loc + lambda^(C (j - gL)) A_{gL},
+// where A_j^loc starts from zero at the segment.  Three kernels:
+//   tc_l2_state_kernel  per (head, segment, 64 columns of d_v), chunk after
+//                       chunk: dA_j = K'^T diag(w) V' on tcgen05 and the local
+//                       recurrence in fp32; writes A_j^loc (bf16) and the
+//                       segment's local final state (fp32);
+//   tc_l2_carry_kernel  per head: the segment start states A_{gL} (bf16) and
+//                       the final state after the whole sequence (fp32);
 //   tc_fwd_kernel       per (head, query block): flash-style online softmax
 //                       over the window tiles (S = Q K^T and O += P V on
-//                       tcgen05), the L2 term P2 V' and q A_j, and the gate.
+//                       tcgen05), the L2 term P2 V' and q (A_j^loc +
+//                       lambda^(C (j - gL)) A_{gL}), and the gate.
 //
-// tc_fwd_kernel warp roles (192 threads): warps 0-3 own one query row per
-// thread (softmax, P, epilogue); warp 4 issues TMA loads; warp 5 issues the
-// MMAs and owns the TMEM allocation.  TMEM columns: S double buffer [0,256),
-// O [256, 256+DV), O2 (the L2 term) [256+DV, 256+2DV); q A_j lands in the S
-// buffer that is free after the last tile.  Every wait is bounded; a wait that
-// runs out records a status bit (tc_prefill_tcgen05_status) and the CTA winds
-// down without hanging.
+// Every wait inside these kernels is bounded; a wait that runs out records a
+// status bit (tc_prefill_tcgen05_status) and the CTA winds down without
+// hanging.
 #include <math.h>
 
 #include "opam_internal.cuh"
@@ -50,156 +52,240 @@ constexpr float kRescale = 8.0f;   // lazy-rescale threshold (log2 units)
 
 __device__ unsigned int g_status = 0;
 enum : unsigned int {
-    kStDeltaWait = 1u,
-    kStFwdProducer = 2u,
-    kStFwdMma = 4u,
-    kStFwdSoftmax = 8u,
+    kStStateProducer = 1u,
+    kStStateMma = 2u,
+    kStStateScan = 4u,
+    kStFwdProducer = 8u,
+    kStFwdMma = 16u,
+    kStFwdSoftmax = 32u,
+    kStFwdAlign = 64u,
 };
 
-// --------------------------------------------------------------------- dA_j
-// One CTA per (chunk j, head).  A = K'^T is read MN-major from the K' tile
-// (tokens x d_k); M is fixed at 128, so for d_k = 64 the two 64-wide M blocks
-// alias the same data (lanes 64..127 hold a copy and are ignored).
-template <int DK, int DV>
-__global__ void __launch_bounds__(128)
-tc_l2_delta_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
-                   int T, int W, int H, const float *__restrict__ lam,
-                   const float *__restrict__ eta, int nch, float *__restrict__ dA) {
-    constexpr uint32_t KBYTES = kBlk * DK * 2, VBYTES = kBlk * DV * 2;
-    constexpr uint32_t TCOLS = DV < 32 ? 32 : DV;
-    extern __shared__ unsigned char smraw[];
-    unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
-    unsigned char *Ks = sm, *Vs = sm + KBYTES;
-    __shared__ uint64_t bars[2];
-    __shared__ uint32_t tbase;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int j = blockIdx.x, bh = blockIdx.y, h = bh % H;
-    const int kt = j * kBlk - W;
-    const int n = min(kBlk, T - j * kBlk);
-    float *out = dA + ((size_t)bh * nch + j) * (size_t)(DK * DV);
-    if (kt + n <= 0) {  // nothing evicted during this chunk
-        for (int e = tid; e < DK * DV / 4; e += 128)
-            reinterpret_cast<float4 *>(out)[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-        return;
-    }
-    if (warp == 0) tmem_alloc(&tbase, TCOLS);
-    if (tid == 0) {
-        mbar_init(&bars[0], 1);
-        mbar_init(&bars[1], 1);
-        mbar_fence_init();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tm = tbase;
-    if (tid == 0) {
-        mbar_expect_tx(&bars[0], KBYTES + VBYTES);
-#pragma unroll
-        for (int b = 0; b < DK / 64; ++b) tma_load_3d(Ks + b * 16384, &mk, &bars[0], 64 * b, kt, bh);
-#pragma unroll
-        for (int b = 0; b < DV / 64; ++b) tma_load_3d(Vs + b * 16384, &mv, &bars[0], 64 * b, kt, bh);
-    }
-    bool ok = mbar_wait(&bars[0], 0);
-    // Row l of V' times w_l = eta lambda^(n-1-l) (zero for rows outside the
-    // chunk or before position 0); a row keeps its 16-byte chunks in place.
-    {
-        const int l = tid;
-        const float w = (l < n && kt + l >= 0) ? eta[h] * powf(lam[h], (float)(n - 1 - l)) : 0.f;
-#pragma unroll
-        for (int b = 0; b < DV / 64; ++b) {
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t a = smem_u32(Vs) + b * 16384 + l * 128 + c * 16;
-                uint32_t x[4];
-                ld_shared_v4(a, x[0], x[1], x[2], x[3]);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    __nv_bfloat162 hv = *reinterpret_cast<__nv_bfloat162 *>(&x[u]);
-                    float2 f = __bfloat1622float2(hv);
-                    x[u] = pack_bf16(f.x * w, f.y * w);
-                }
-                st_shared_v4(a, x[0], x[1], x[2], x[3]);
-            }
-        }
-        fence_async_smem();
-    }
-    __syncthreads();
-    if (tid == 0 && ok) {
-        tc_fence_after();
-        constexpr uint32_t idesc = idesc_bf16_f32(128, DV, true, true);
-        const uint32_t ka = smem_u32(Ks), va = smem_u32(Vs);
-#pragma unroll
-        for (int k = 0; k < kBlk / 16; ++k)
-            mma_ss(tm, sdesc_sw128(ka + k * 2048, DK == 128 ? 16384 : 0, 1024),
-                   sdesc_sw128(va + k * 2048, 16384, 1024), idesc, k > 0 ? 1u : 0u);
-        mma_commit(&bars[1]);
-    }
-    ok = __syncthreads_and(ok);
-    if (ok) ok = mbar_wait(&bars[1], 0);
-    __syncwarp();
-    tc_fence_after();
-    if (!ok) {
-        if (tid == 0) atomicOr(&g_status, kStDeltaWait);
-    } else if (warp < DK / 32) {
-        const int a = tid;  // row of dA = key coordinate
-#pragma unroll
-        for (int c0 = 0; c0 < DV; c0 += 32) {
-            float v[32];
-            tmem_ld32(tm + ((uint32_t)(warp * 32) << 16) + c0, v);
-            tmem_wait_ld();
-            float4 *dst = reinterpret_cast<float4 *>(out + (size_t)a * DV + c0);
-#pragma unroll
-            for (int u = 0; u < 8; ++u) dst[u] = make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, TCOLS);
+// Chunks per segment of the state recurrence: enough segments that the state
+// kernel fills the GPU (two CTAs per SM), at most one segment per chunk.
+struct Segments {
+    int nch, nseg, L;
+};
+Segments segments(int BH, int T, int dv, int num_sms) {
+    const int nch = ceil_div(T, kBlk);
+    const int units = BH * (dv / 64);
+    int want = (2 * num_sms) / units;
+    if (want < 1) want = 1;
+    if (want > nch) want = nch;
+    const int L = ceil_div(nch, want);
+    return {nch, ceil_div(nch, L), L};
 }
 
-// --------------------------------------------------------------------- scan
-// A_0 = 0, A_{j+1} = lambda^{n_j} A_j + dA_j.  Each thread owns 4 adjacent
-// elements of one head's d_k x d_v state; Abf[bh][j] receives A_j (bf16) and
-// A_final the state after the last chunk (fp32).
+// --------------------------------------------------------------------- chunk states
+// One CTA per (64-column slice, segment, head) walks the segment's chunks:
+//   dA_j = K'^T diag(w) V' on tcgen05 (A = K'^T read MN-major from the K'
+//          tile; M is fixed at 128, so for d_k = 64 both 64-wide M blocks
+//          alias the same rows and TMEM lanes 64..127 hold an unused copy),
+//   A_j^loc -> bf16 for the forward kernel, then A^loc <- lambda^n A^loc + dA_j
+//          in fp32 registers (one state row per thread).
+// Warps 0-3 weight V' rows by w_l = eta lambda^(n-1-l) (thread = token row)
+// and run the recurrence (thread = state row a < d_k); warp 4 loads K'/V' by
+// TMA; warp 5 issues the MMAs.  Loads, weighting and MMAs of later chunks
+// overlap the recurrence of the current one.
+template <int DK>
+struct StateCfg {
+    static constexpr uint32_t KBYTES = kBlk * DK * 2;
+    static constexpr uint32_t VBYTES = kBlk * 64 * 2;
+    static constexpr int NS = DK == 64 ? 3 : 2;
+    static constexpr uint32_t SMEM = NS * (KBYTES + VBYTES) + 1024;
+};
+
+struct StateBars {
+    uint64_t kv_full[4], scaled[4], kv_empty[4], mma_done[2], tm_free[2], drain;
+    uint32_t tbase;
+    float pw[kBlk];  // eta lambda^d
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(192, 2)
+tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
+                   int T, int W, int H, const float *__restrict__ lam, const float *__restrict__ eta,
+                   int nch, int L, __nv_bfloat16 *__restrict__ Aloc, float *__restrict__ Lfin) {
+    using C = StateCfg<DK>;
+    constexpr int NS = C::NS;
+    extern __shared__ unsigned char smraw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    __shared__ StateBars B;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int slice = blockIdx.x, seg = blockIdx.y, bh = blockIdx.z, h = bh % H;
+    const int nseg = gridDim.y;
+    const int j0 = seg * L, j1 = min(nch, j0 + L), nj = j1 - j0;
+    const uint32_t s0 = smem_u32(sm);
+    if (warp == 5) tmem_alloc(&B.tbase, 128);
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&B.kv_full[s], 1);
+            mbar_init(&B.scaled[s], 4);
+            mbar_init(&B.kv_empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&B.mma_done[b], 1);
+            mbar_init(&B.tm_free[b], DK / 32);
+        }
+        mbar_init(&B.drain, 1);
+        mbar_fence_init();
+    }
+    if (tid < kBlk) B.pw[tid] = eta[h] * powf(lam[h], (float)tid);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = B.tbase;
+    auto stage_k = [&](int s) { return s0 + s * (C::KBYTES + C::VBYTES); };
+
+    if (warp == 4) {
+        if (lane == 0) {
+            bool ok = true;
+            int issued = 0;
+            for (int i = 0; i < nj && ok; ++i) {
+                const int s = i % NS;
+                if (i >= NS) ok = mbar_wait(&B.kv_empty[s], ((i / NS) - 1) & 1);
+                if (!ok) break;
+                unsigned char *kd = sm + (stage_k(s) - s0);
+                const int kt = (j0 + i) * kBlk - W;
+                mbar_expect_tx(&B.kv_full[s], C::KBYTES + C::VBYTES);
+#pragma unroll
+                for (int b = 0; b < DK / 64; ++b) tma_load_3d(kd + b * 16384, &mk, &B.kv_full[s], 64 * b, kt, bh);
+                tma_load_3d(kd + C::KBYTES, &mv, &B.kv_full[s], 64 * slice, kt, bh);
+                ++issued;
+            }
+            if (!ok) atomicOr(&g_status, kStStateProducer);
+            bool dok = true;
+            for (int i = max(0, issued - NS); i < issued && dok; ++i)
+                dok = mbar_wait(&B.kv_full[i % NS], (i / NS) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        if (lane == 0) {
+            bool ok = true;
+            constexpr uint32_t idesc = idesc_bf16_f32(128, 64, true, true);
+            for (int i = 0; i < nj && ok; ++i) {
+                const int s = i % NS, b = i & 1;
+                ok = mbar_wait(&B.scaled[s], (i / NS) & 1);
+                if (ok && i >= 2) ok = mbar_wait(&B.tm_free[b], ((i - 2) >> 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t ka = stage_k(s), va = ka + C::KBYTES;
+#pragma unroll
+                for (int k = 0; k < kBlk / 16; ++k)
+                    mma_ss(tm + b * 64, sdesc_sw128(ka + k * 2048, DK == 128 ? 16384 : 0, 1024),
+                           sdesc_sw128(va + k * 2048, 16384, 1024), idesc, k > 0 ? 1u : 0u);
+                mma_commit(&B.mma_done[b]);
+                mma_commit(&B.kv_empty[s]);
+            }
+            if (!ok) atomicOr(&g_status, kStStateMma);
+            mma_commit(&B.drain);
+            mbar_wait(&B.drain, 0);
+        }
+        __syncwarp();
+    } else {
+        const int r = tid;  // token row when weighting, state row when scanning
+        const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+        const bool scan_row = r < DK;
+        const float lm = lam[h];
+        const float lamC = powf(lm, (float)kBlk);
+        float A[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) A[i] = 0.f;
+        __nv_bfloat16 *arow = Aloc + ((size_t)bh * nch * DK + r) * DV + slice * 64;
+        bool ok = true;
+        // A^loc <- lambda^n A^loc + dA of local chunk i (TMEM buffer i & 1).
+        auto absorb = [&](int i) -> bool {
+            const int b = i & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(&B.mma_done[b], (i >> 1) & 1))) return false;
+            tc_fence_after();
+            float d0[32], d1[32];
+            tmem_ld32(tm + lrow + b * 64, d0);
+            tmem_ld32(tm + lrow + b * 64 + 32, d1);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.tm_free[b]);
+            const int n = min(kBlk, T - (j0 + i) * kBlk);
+            const float f = n == kBlk ? lamC : powf(lm, (float)n);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                A[e] = fmaf(f, A[e], d0[e]);
+                A[32 + e] = fmaf(f, A[32 + e], d1[e]);
+            }
+            return true;
+        };
+        auto emit = [&](int j) {  // A_j^loc as bf16, 128 contiguous bytes per row
+            uint4 *dst = reinterpret_cast<uint4 *>(arow + (size_t)j * DK * DV);
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                dst[u] = make_uint4(pack_bf16(A[8 * u], A[8 * u + 1]), pack_bf16(A[8 * u + 2], A[8 * u + 3]),
+                                    pack_bf16(A[8 * u + 4], A[8 * u + 5]), pack_bf16(A[8 * u + 6], A[8 * u + 7]));
+        };
+        for (int i = 0; i < nj && ok; ++i) {
+            const int s = i % NS, j = j0 + i;
+            ok = __all_sync(0xffffffffu, mbar_wait(&B.kv_full[s], (i / NS) & 1));
+            if (!ok) break;
+            {   // weight row r of V' in place; chunk order rotated by row (no bank conflicts)
+                const int kt = j * kBlk - W, n = min(kBlk, T - j * kBlk);
+                const float w = (r < n && kt + r >= 0) ? B.pw[(n - 1 - r) & (kBlk - 1)] : 0.f;
+                const __nv_bfloat162 w2 = __floats2bfloat162_rn(w, w);
+                const uint32_t va = stage_k(s) + C::KBYTES + r * 128;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t a = va + (((c + r) & 7) << 4);
+                    uint32_t x[4];
+                    ld_shared_v4(a, x[0], x[1], x[2], x[3]);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        __nv_bfloat162 hv = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&x[u]), w2);
+                        x[u] = *reinterpret_cast<uint32_t *>(&hv);
+                    }
+                    st_shared_v4(a, x[0], x[1], x[2], x[3]);
+                }
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&B.scaled[s]);
+            }
+            if (scan_row) {
+                if (i >= 1) ok = absorb(i - 1);
+                if (ok) emit(j);
+            }
+        }
+        if (ok && scan_row) {
+            ok = absorb(nj - 1);
+            if (ok) {
+                float4 *dst = reinterpret_cast<float4 *>(Lfin + (((size_t)bh * nseg + seg) * DK + r) * DV + slice * 64);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) dst[u] = make_float4(A[4 * u], A[4 * u + 1], A[4 * u + 2], A[4 * u + 3]);
+            }
+        }
+        if (!ok && lane == 0) atomicOr(&g_status, kStStateScan);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) tmem_dealloc(tm, 128);
+}
+
+// --------------------------------------------------------------------- segment carries
+// A_{0} = 0, A_{(g+1)L} = lambda^{tokens of segment g} A_{gL} + local final of g.
+// Each thread owns 4 adjacent state elements of one head.
 __global__ void __launch_bounds__(128)
-tc_l2_scan_kernel(const float *__restrict__ dA, int nch, int T, int dkdv, int H,
-                  const float *__restrict__ lam, __nv_bfloat16 *__restrict__ Abf,
-                  float *__restrict__ A_final) {
+tc_l2_carry_kernel(const float *__restrict__ Lfin, int nseg, int L, int T, int dkdv, int H,
+                   const float *__restrict__ lam, __nv_bfloat16 *__restrict__ Cbf,
+                   float *__restrict__ A_final) {
     const int bh = blockIdx.y;
     const int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (e >= dkdv) return;
     const float lm = lam[bh % H];
-    const float lamC = powf(lm, (float)kBlk);
-    const float *src = dA + (size_t)bh * nch * dkdv + e;
-    __nv_bfloat16 *dst = Abf + (size_t)bh * nch * dkdv + e;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    int j = 0;
-    for (; j + 8 <= nch; j += 8) {
-        float4 d[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) d[u] = *reinterpret_cast<const float4 *>(src + (size_t)(j + u) * dkdv);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            uint2 o;
-            o.x = pack_bf16(A.x, A.y);
-            o.y = pack_bf16(A.z, A.w);
-            *reinterpret_cast<uint2 *>(dst + (size_t)(j + u) * dkdv) = o;
-            const int n = min(kBlk, T - (j + u) * kBlk);
-            const float f = n == kBlk ? lamC : powf(lm, (float)n);
-            A.x = fmaf(f, A.x, d[u].x);
-            A.y = fmaf(f, A.y, d[u].y);
-            A.z = fmaf(f, A.z, d[u].z);
-            A.w = fmaf(f, A.w, d[u].w);
-        }
-    }
-    for (; j < nch; ++j) {
-        const float4 d = *reinterpret_cast<const float4 *>(src + (size_t)j * dkdv);
+    for (int g = 0; g < nseg; ++g) {
         uint2 o;
         o.x = pack_bf16(A.x, A.y);
         o.y = pack_bf16(A.z, A.w);
-        *reinterpret_cast<uint2 *>(dst + (size_t)j * dkdv) = o;
-        const int n = min(kBlk, T - j * kBlk);
-        const float f = n == kBlk ? lamC : powf(lm, (float)n);
+        *reinterpret_cast<uint2 *>(Cbf + ((size_t)bh * nseg + g) * dkdv + e) = o;
+        const float4 d = *reinterpret_cast<const float4 *>(Lfin + ((size_t)bh * nseg + g) * dkdv + e);
+        const int ntok = min(T, (g + 1) * L * kBlk) - g * L * kBlk;
+        const float f = powf(lm, (float)ntok);
         A.x = fmaf(f, A.x, d.x);
         A.y = fmaf(f, A.y, d.y);
         A.z = fmaf(f, A.z, d.z);
@@ -212,18 +298,20 @@ tc_l2_scan_kernel(const float *__restrict__ dA, int nch, int T, int dkdv, int H,
 template <int DK, int DV>
 struct Fwd {
     static constexpr uint32_t QBYTES = kBlk * DK * 2;
-    static constexpr uint32_t KBYTES = kBlk * DK * 2;  // also holds A_j (DK x DV bf16)
-    static constexpr uint32_t VBYTES = kBlk * DV * 2;
-    static constexpr uint32_t PBYTES = kBlk * kBlk * 2;
-    static constexpr uint32_t kBudget = 226 * 1024;
-    static constexpr int kStagesFit = (int)((kBudget - 1024 - QBYTES - 2 * PBYTES) / (KBYTES + VBYTES));
+    static constexpr uint32_t KBYTES = kBlk * DK * 2;  // also holds A_j^loc (DK x DV bf16)
+    static constexpr uint32_t VBYTES = kBlk * DV * 2;  // also holds the segment carry
+    static constexpr uint32_t PHALF = kBlk * 64 * 2;   // P of one key half: 128 rows x 64 keys
+    static constexpr uint32_t kBudget = 227 * 1024 - 3072;  // 3 KB kept for the barriers block
+    static constexpr int kStagesFit = (int)((kBudget - QBYTES - 4 * PHALF) / (KBYTES + VBYTES));
     static constexpr int NST = kStagesFit > 4 ? 4 : kStagesFit;
     static_assert(NST >= 2, "need two K/V stages");
     static constexpr uint32_t OFF_K = QBYTES;
     static constexpr uint32_t OFF_P = QBYTES + NST * (KBYTES + VBYTES);
-    static constexpr uint32_t SMEM = OFF_P + 2 * PBYTES + 1024;  // +1024: alignment slack
-    static constexpr uint32_t COL_O = 256, COL_O2 = 256 + DV;
-    static_assert(256 + 2 * DV <= 512, "TMEM columns");
+    static constexpr uint32_t OFF_BARS = OFF_P + 4 * PHALF;
+    // TMEM columns: S [0,128); O of key half 0 / 1; O2 (the L2 term).  q A_j
+    // lands in the S columns after the last tile.
+    static constexpr uint32_t COL_O0 = 128, COL_O1 = 128 + DV, COL_O2 = 128 + 2 * DV;
+    static_assert(128 + 3 * DV <= 512, "TMEM columns");
     static constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);
     static constexpr uint32_t ID_PV = idesc_bf16_f32(128, DV, false, true);
 };
@@ -231,26 +319,42 @@ struct Fwd {
 struct FwdBars {
     uint64_t q_full;
     uint64_t k_full[4], v_full[4], kv_empty[4];
-    uint64_t s_full[2], s_empty[2], p_full[2], p_empty[2];
-    uint64_t o_done, drain;
+    uint64_t s_full, s_empty;
+    uint64_t p_full[2][2], p_empty[2][2];  // [key half][slot]
+    uint64_t c_ready, xe, o_done, drain;
     uint32_t tbase;
-    float pw[kBlk];  // eta lambda^d, d = 0..127
+    float pw[kBlk];      // eta lambda^d, d = 0..127
+    float xm[2][kBlk];   // [key half][row] running maxima, exchanged once at the end
+    float xl[2][kBlk];   // [key half][row] running sums
 };
 
+// 320 threads.  Warps 0-7 run the softmax: warp w owns rows 32 (w % 4) .. +31
+// (its TMEM lane quarter) and keys 64 (w / 4) .. +63 of every tile.  The two
+// key halves of a row keep separate running maxima, sums and P V accumulators
+// (O0, O1) and are merged once in the epilogue, so the softmax warps never
+// wait for each other inside the tile loop.  Warp 8 issues TMA loads and
+// scales the segment carry; warp 9 issues the MMAs and owns the TMEM
+// allocation.
 template <int DK, int DV>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ma,
-              int T, int W, int H, int nch, const float *__restrict__ lam,
-              const float *__restrict__ eta, const float *__restrict__ gate, float scale,
-              __nv_bfloat16 *__restrict__ y) {
+              const __grid_constant__ CUtensorMap mc, int T, int W, int H, int nch, int nseg, int L,
+              const float *__restrict__ lam, const float *__restrict__ eta,
+              const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y) {
     using C = Fwd<DK, DV>;
     constexpr int NST = C::NST;
-    extern __shared__ unsigned char smraw[];
-    unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
-    __shared__ FwdBars B;
+    // All shared memory is dynamic: with no static shared memory its base is
+    // 1024-byte aligned, as the 128-byte-swizzle tiles require (checked).
+    extern __shared__ __align__(1024) unsigned char sm[];
+    FwdBars &B = *reinterpret_cast<FwdBars *>(sm + C::OFF_BARS);
+    if ((smem_u32(sm) & 1023u) != 0) {
+        if (threadIdx.x == 0) atomicOr(&g_status, kStFwdAlign);
+        return;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int jq = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int seg = jq / L;
     const int t0 = jq * kBlk;
     const int kt0 = t0 - W;  // first key of tile 0 (the shifted chunk)
     const int nt_total = (W + kBlk - 1) / kBlk + 1;
@@ -258,7 +362,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const int ntiles = nt_total - j_first;
     const bool has_l2 = (j_first == 0);
 
-    if (warp == 5) tmem_alloc(&B.tbase, 512);
+    if (warp == 9) tmem_alloc(&B.tbase, 512);
     if (tid == 0) {
         mbar_init(&B.q_full, 1);
         for (int s = 0; s < NST; ++s) {
@@ -266,12 +370,15 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             mbar_init(&B.v_full[s], 1);
             mbar_init(&B.kv_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&B.s_full[s], 1);
-            mbar_init(&B.s_empty[s], 4);
-            mbar_init(&B.p_full[s], 4);
-            mbar_init(&B.p_empty[s], 1);
-        }
+        mbar_init(&B.s_full, 1);
+        mbar_init(&B.s_empty, 8);
+        for (int hh = 0; hh < 2; ++hh)
+            for (int s = 0; s < 2; ++s) {
+                mbar_init(&B.p_full[hh][s], 4);
+                mbar_init(&B.p_empty[hh][s], 1);
+            }
+        mbar_init(&B.c_ready, 1);
+        mbar_init(&B.xe, 8);
         mbar_init(&B.o_done, 1);
         mbar_init(&B.drain, 1);
         mbar_fence_init();
@@ -285,17 +392,17 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const uint32_t sK0 = sQ + C::OFF_K;
     const uint32_t sP0 = sQ + C::OFF_P;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------ TMA producer
+        bool ok = true;
+        const int sA = ntiles % NST;  // stage of A_j^loc (K slot) and the carry (V slot)
         if (lane == 0) {
-            bool ok = true;
             tma_prefetch_desc(&mq);
             tma_prefetch_desc(&mk);
             tma_prefetch_desc(&mv);
             mbar_expect_tx(&B.q_full, C::QBYTES);
 #pragma unroll
             for (int b = 0; b < DK / 64; ++b) tma_load_3d(sm + b * 16384, &mq, &B.q_full, 64 * b, t0, bh);
-            int issued = 0;
             for (int n = 0; n <= ntiles && ok; ++n) {
                 const int s = n % NST;
                 if (n >= NST) ok = mbar_wait(&B.kv_empty[s], ((n / NST) - 1) & 1);
@@ -310,84 +417,112 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
                     for (int b = 0; b < DV / 64; ++b)
                         tma_load_3d(kd + C::KBYTES + b * 16384, &mv, &B.v_full[s], 64 * b, kt, bh);
-                } else {  // the carried state A_j (bf16, d_k rows x d_v) into the K slot
-                    mbar_expect_tx(&B.k_full[s], DK * DV * 2);
+                } else {  // A_j^loc into the K slot, the segment carry into the V slot
+                    mbar_expect_tx(&B.k_full[s], 2 * DK * DV * 2);
 #pragma unroll
-                    for (int b = 0; b < DV / 64; ++b)
+                    for (int b = 0; b < DV / 64; ++b) {
                         tma_load_3d(kd + b * (DK * 128), &ma, &B.k_full[s], 64 * b, 0, bh * nch + jq);
+                        tma_load_3d(kd + C::KBYTES + b * (DK * 128), &mc, &B.k_full[s], 64 * b, 0, bh * nseg + seg);
+                    }
                 }
-                ++issued;
             }
-            if (!ok) atomicOr(&g_status, kStFwdProducer);
-            // Drain: the newest load of each stage has landed before the CTA exits.
-            bool dok = mbar_wait(&B.q_full, 0);
-            for (int n = max(0, issued - NST); n < issued && dok; ++n) {
-                const int s = n % NST;
-                dok = mbar_wait(&B.k_full[s], (n / NST) & 1);
-                if (dok && n < ntiles) dok = mbar_wait(&B.v_full[s], (n / NST) & 1);
+            if (ok) ok = mbar_wait(&B.k_full[sA], (ntiles / NST) & 1);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) {
+            // Carry times lambda^(C (j - gL)), in place, so q A_j^loc and the
+            // carry share one accumulator.
+            const float c = powf(lam[h], (float)(kBlk * (jq - seg * L)));
+            const __nv_bfloat162 c2 = __floats2bfloat162_rn(c, c);
+            const uint32_t base = sK0 + sA * (C::KBYTES + C::VBYTES) + C::KBYTES;
+            for (int e = lane; e < DK * DV / 8; e += 32) {
+                uint32_t x[4];
+                ld_shared_v4(base + e * 16, x[0], x[1], x[2], x[3]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    __nv_bfloat162 hv = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&x[u]), c2);
+                    x[u] = *reinterpret_cast<uint32_t *>(&hv);
+                }
+                st_shared_v4(base + e * 16, x[0], x[1], x[2], x[3]);
             }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.c_ready);
+        } else if (lane == 0) {
+            atomicOr(&g_status, kStFwdProducer);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             bool ok = mbar_wait(&B.q_full, 0);
-            uint32_t use = 0;  // P-slot uses so far
+            uint32_t use[2] = {0, 0};  // P-slot uses so far, per key half
             auto kdesc = [&](int s, int k) {
                 return sdesc_sw128(sK0 + s * (C::KBYTES + C::VBYTES) + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
             };
             auto qdesc = [&](int k) { return sdesc_sw128(sQ + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); };
-            auto vdesc = [&](int s, int k) {
-                return sdesc_sw128(sK0 + s * (C::KBYTES + C::VBYTES) + C::KBYTES + k * 2048, 16384, 1024);
+            // V rows 64 hh + 16 k .. of stage s (MN-major B).
+            auto vdesc = [&](int s, int hh, int k) {
+                return sdesc_sw128(sK0 + s * (C::KBYTES + C::VBYTES) + C::KBYTES + hh * 8192 + k * 2048, 16384,
+                                   1024);
             };
-            auto pdesc = [&](int slot, int k) {
-                return sdesc_sw128(sP0 + slot * C::PBYTES + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+            auto pdesc = [&](int hh, int slot, int k) {
+                return sdesc_sw128(sP0 + (slot * 2 + hh) * C::PHALF + k * 32, 16, 1024);
             };
-            // O += P V (and O2 = P2 V' for tile 0) for processed tile n.
+            // P V products of processed tile n: per key half, O2 += P2 V' (tile 0)
+            // then O_half += P V.
             auto pv = [&](int n) -> bool {
                 const int s = n % NST;
                 if (!mbar_wait(&B.v_full[s], (n / NST) & 1)) return false;
                 const int uses = (n == 0 && has_l2) ? 2 : 1;
-                for (int u = 0; u < uses; ++u) {
-                    const int slot = use & 1;
-                    if (!mbar_wait(&B.p_full[slot], (use >> 1) & 1)) return false;
-                    tc_fence_after();
-                    const bool l2 = (uses == 2 && u == 0);
-                    const uint32_t dcol = l2 ? C::COL_O2 : C::COL_O;
+                for (int hh = 0; hh < 2; ++hh) {
+                    for (int u = 0; u < uses; ++u) {
+                        const int slot = use[hh] & 1;
+                        if (!mbar_wait(&B.p_full[hh][slot], (use[hh] >> 1) & 1)) return false;
+                        tc_fence_after();
+                        const bool l2 = (uses == 2 && u == 0);
+                        const uint32_t dcol = l2 ? C::COL_O2 : (hh ? C::COL_O1 : C::COL_O0);
 #pragma unroll
-                    for (int k = 0; k < kBlk / 16; ++k)
-                        mma_ss(tm + dcol, pdesc(slot, k), vdesc(s, k), C::ID_PV,
-                               (l2 ? k > 0 : (n > 0 || k > 0)) ? 1u : 0u);
-                    mma_commit(&B.p_empty[slot]);
-                    ++use;
+                        for (int k = 0; k < 4; ++k) {
+                            const bool acc = l2 ? (hh > 0 || k > 0) : (n > 0 || k > 0);
+                            mma_ss(tm + dcol, pdesc(hh, slot, k), vdesc(s, hh, k), C::ID_PV, acc ? 1u : 0u);
+                        }
+                        mma_commit(&B.p_empty[hh][slot]);
+                        ++use[hh];
+                    }
                 }
                 mma_commit(&B.kv_empty[s]);
                 return true;
             };
             for (int n = 0; n < ntiles && ok; ++n) {
-                const int s = n % NST, sb = n & 1;
+                const int s = n % NST;
                 ok = mbar_wait(&B.k_full[s], (n / NST) & 1);
-                if (ok && n >= 2) ok = mbar_wait(&B.s_empty[sb], ((n - 2) >> 1) & 1);
+                if (ok && n >= 1) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
                 for (int k = 0; k < DK / 16; ++k)
-                    mma_ss(tm + sb * 128, qdesc(k), kdesc(s, k), C::ID_S, k > 0 ? 1u : 0u);
-                mma_commit(&B.s_full[sb]);
+                    mma_ss(tm, qdesc(k), kdesc(s, k), C::ID_S, k > 0 ? 1u : 0u);
+                mma_commit(&B.s_full);
                 if (n >= 1) ok = pv(n - 1);
             }
             if (ok) ok = pv(ntiles - 1);
-            if (ok) {  // q A_j into the S buffer that follows the last tile
-                const int n = ntiles, s = n % NST, sb = n & 1;
+            if (ok) {  // q (A_j^loc + c A_{gL}) into the S columns
+                const int n = ntiles, s = n % NST;
                 ok = mbar_wait(&B.k_full[s], (n / NST) & 1);
-                if (ok && n >= 2) ok = mbar_wait(&B.s_empty[sb], ((n - 2) >> 1) & 1);
+                if (ok) ok = mbar_wait(&B.c_ready, 0);
+                if (ok) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
                 if (ok) {
                     tc_fence_after();
                     const uint32_t aslot = sK0 + s * (C::KBYTES + C::VBYTES);
 #pragma unroll
                     for (int k = 0; k < DK / 16; ++k)
-                        mma_ss(tm + sb * 128, qdesc(k), sdesc_sw128(aslot + k * 2048, DK * 128, 1024),
-                               C::ID_PV, k > 0 ? 1u : 0u);
+                        mma_ss(tm, qdesc(k), sdesc_sw128(aslot + k * 2048, DK * 128, 1024), C::ID_PV,
+                               k > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < DK / 16; ++k)
+                        mma_ss(tm, qdesc(k), sdesc_sw128(aslot + C::KBYTES + k * 2048, DK * 128, 1024),
+                               C::ID_PV, 1u);
                     mma_commit(&B.o_done);
                 }
             }
@@ -398,96 +533,122 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ softmax / epilogue (row r)
-        const int r = tid;
+        // ------------------------------------------------ softmax / epilogue
+        const int half = warp >> 2;            // keys 64 half .. +63 of every tile
+        const int r = (warp & 3) * 32 + lane;  // query row
         const int t = t0 + r;
-        const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+        const int c0 = half * 64;
+        const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
+        const uint32_t col_o = half ? C::COL_O1 : C::COL_O0;
         const float sc = scale * kLog2e;
         float m = kNegBig, l = 0.f;
         uint32_t use = 0;
         int last_o_use = -1;
         bool ok = true;
         auto wait_slot = [&](uint32_t u) -> bool {  // slot of use u is free again
-            return u < 2 || mbar_wait(&B.p_empty[u & 1], ((u - 2) >> 1) & 1);
+            return u < 2 || mbar_wait(&B.p_empty[half][u & 1], ((u - 2) >> 1) & 1);
         };
-        // Row r of a P slot: 16 chunks of 8 bf16 in the 128-byte-swizzle K-major layout.
+        // 8 keys of row r into this half's P slot (128-byte-swizzle K-major).
         auto store8 = [&](uint32_t slot, int c, const float *p) {
-            st_shared_v4(sP0 + slot * C::PBYTES + (c >> 3) * 16384 + sw128_off(r, c & 7),
-                         pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]),
-                         pack_bf16(p[6], p[7]));
+            st_shared_v4(sP0 + (slot * 2 + half) * C::PHALF + sw128_off(r, c), pack_bf16(p[0], p[1]),
+                         pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
         };
+        auto publish = [&](uint32_t slot) {
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.p_full[half][slot]);
+        };
+        const int wrow_hi = (warp & 3) * 32 + 31;
         for (int n = 0; n < ntiles && ok; ++n) {
             const int j = j_first + n;
             const int kt = kt0 + kBlk * j;
-            const int sb = n & 1;
-            ok = mbar_wait(&B.s_full[sb], (n >> 1) & 1);
-            ok = __all_sync(0xffffffffu, ok);
+            ok = __all_sync(0xffffffffu, mbar_wait(&B.s_full, n & 1));
             if (!ok) break;
             tc_fence_after();
-            float s[kBlk];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            float s[64];
+            {
                 float v[32];
-                tmem_ld32(tm + lrow + sb * 128 + c * 32, v);
+                tmem_ld32(tm + lrow + c0, v);
 #pragma unroll
-                for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
+                for (int i = 0; i < 32; ++i) s[i] = v[i];
+                tmem_ld32(tm + lrow + c0 + 32, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[32 + i] = v[i];
             }
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&B.s_empty[sb]);
+            if (lane == 0) mbar_arrive(&B.s_empty);
 
             if (j == 0) {  // L2 part of the shifted chunk: keys l <= r at positions >= 0
                 const int lo = max(0, -kt);
                 ok = __all_sync(0xffffffffu, wait_slot(use));
                 if (!ok) break;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    float p2[8];
+                for (int g = 0; g < 2; ++g) {
+                    // 32-key groups with no L2 key for any row of this warp are zeros.
+                    const int gk = c0 + 32 * g;
+                    const bool act = (gk <= wrow_hi) && (gk + 31 >= lo);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int i = 8 * c + e;
-                        p2[e] = (i >= lo && i <= r) ? B.pw[(r - i) & (kBlk - 1)] * s[i] : 0.f;
+                    for (int q = 0; q < 4; ++q) {
+                        float p2[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int i = gk + 8 * q + e;
+                            p2[e] = (act && i >= lo && i <= r) ? B.pw[(r - i) & (kBlk - 1)] * s[32 * g + 8 * q + e]
+                                                               : 0.f;
+                        }
+                        store8(use & 1, 4 * g + q, p2);
                     }
-                    store8(use & 1, c, p2);
                 }
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&B.p_full[use & 1]);
+                publish(use & 1);
                 ++use;
             }
-            // Softmax part: keys max(0, t-W+1) <= p <= t.
+            // Softmax part: keys max(0, t-W+1) <= p <= t.  On edge tiles, 32-key
+            // groups masked for every row of the warp skip the exponentials.
             const bool interior = (j >= 1) && (kt >= 0) && (kt <= t0 - (kBlk - 1));
-            float mx = -INFINITY;
+            unsigned act = 0x3u;
+            float pm[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
             if (interior) {
 #pragma unroll
-                for (int i = 0; i < kBlk; ++i) mx = fmaxf(mx, s[i]);
+                for (int i = 0; i < 64; ++i) pm[i & 7] = fmaxf(pm[i & 7], s[i]);
             } else {
-                const int lo = max(0, t - W + 1) - kt, hi = t - kt;
+                const int lo = max(0, t - W + 1) - kt - c0, hi = t - kt - c0;
+                const int wlo = __reduce_min_sync(0xffffffffu, lo), whi = __reduce_max_sync(0xffffffffu, hi);
+                act = 0;
 #pragma unroll
-                for (int i = 0; i < kBlk; ++i) {
-                    s[i] = (i >= lo && i <= hi) ? s[i] : -INFINITY;
-                    mx = fmaxf(mx, s[i]);
+                for (int g = 0; g < 2; ++g) {
+                    if (32 * g <= whi && 32 * g + 31 >= wlo) {
+                        act |= 1u << g;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int i = 32 * g + e;
+                            s[i] = (i >= lo && i <= hi) ? s[i] : -INFINITY;
+                            pm[e & 7] = fmaxf(pm[e & 7], s[i]);
+                        }
+                    }
                 }
             }
-            mx *= sc;
+            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * sc;
             const bool grow = mx > m + kRescale;
-            const bool rescale_o = grow && l > 0.f;
-            if (__any_sync(0xffffffffu, rescale_o)) {
-                // O must hold every earlier P V product before it is rescaled.
+            if (__any_sync(0xffffffffu, grow) && last_o_use >= 0) {
+                // This half's O must hold every earlier P V product before it is rescaled.
                 const uint32_t u = (uint32_t)last_o_use;
-                ok = __all_sync(0xffffffffu, mbar_wait(&B.p_empty[u & 1], (u >> 1) & 1));
+                ok = __all_sync(0xffffffffu, mbar_wait(&B.p_empty[half][u & 1], (u >> 1) & 1));
                 if (!ok) break;
                 tc_fence_after();
-                const float f = rescale_o ? ex2(m - mx) : 1.f;
-#pragma unroll
-                for (int c0 = 0; c0 < DV; c0 += 32) {
+                const float f = grow ? ex2(m - mx) : 1.f;
+#pragma unroll 1
+                for (int cc = 0; cc < DV; cc += 32) {
                     float v[32];
-                    tmem_ld32(tm + lrow + C::COL_O + c0, v);
+                    tmem_ld32(tm + lrow + col_o + cc, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) v[i] *= f;
-                    tmem_st32(tm + lrow + C::COL_O + c0, v);
+                    tmem_st32(tm + lrow + col_o + cc, v);
                 }
                 tmem_wait_st();
             }
@@ -495,51 +656,83 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 l *= ex2(m - mx);
                 m = mx;
             }
-            float rs = 0.f;
+            const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m, -m);
+            float2 ps[4];
 #pragma unroll
-            for (int i = 0; i < kBlk; ++i) {
-                s[i] = ex2(fmaf(s[i], sc, -m));
-                rs += s[i];
+            for (int u = 0; u < 4; ++u) ps[u] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int g = 0; g < 2; ++g) {
+                if (act & (1u << g)) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int i = 32 * g + e;
+                        float2 x = fma2(make_float2(s[i], s[i + 1]), sc2, nm2);
+                        x.x = ex2(x.x);
+                        x.y = ex2(x.y);
+                        s[i] = x.x;
+                        s[i + 1] = x.y;
+                        ps[(e >> 1) & 3] = add2(ps[(e >> 1) & 3], x);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[32 * g + e] = 0.f;
+                }
             }
-            l += rs;
+            l += ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
             ok = __all_sync(0xffffffffu, wait_slot(use));
             if (!ok) break;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) store8(use & 1, c, &s[8 * c]);
-            fence_async_smem();
+            for (int c = 0; c < 8; ++c) store8(use & 1, c, &s[8 * c]);
             tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.p_full[use & 1]);
+            publish(use & 1);
             last_o_use = (int)use;
             ++use;
         }
-        // ------------------------------------------------ epilogue
+        // ------------------------------------------------ epilogue (DV/2 columns per half)
+        if (ok) {
+            B.xm[half][r] = m;
+            B.xl[half][r] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.xe);
+            ok = __all_sync(0xffffffffu, mbar_wait(&B.xe, 0));
+        }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&B.o_done, 0));
         if (ok) {
             tc_fence_after();
-            const uint32_t col_qa = (uint32_t)(ntiles & 1) * 128;
+            const float m0 = B.xm[0][r], m1 = B.xm[1][r];
+            const float M = fmaxf(m0, m1);
+            const float f0 = ex2(m0 - M), f1 = ex2(m1 - M);
+            const float lsum = B.xl[0][r] * f0 + B.xl[1][r] * f1;
+            const float inv_l = lsum > 0.f ? 1.0f / lsum : 0.f;
+            const float w0 = f0 * inv_l, w1 = f1 * inv_l;
             const float sg = 1.0f / (1.0f + expf(-gate[h]));
             const float decay = powf(lam[h], (float)(r + 1));
-            const float inv_l = l > 0.f ? 1.0f / l : 0.f;
             __nv_bfloat16 *yr = y + ((size_t)bh * T + t) * DV;
-#pragma unroll
-            for (int c0 = 0; c0 < DV; c0 += 32) {
-                float o[32], qa[32], o2[32];
-                tmem_ld32(tm + lrow + C::COL_O + c0, o);
-                tmem_ld32(tm + lrow + col_qa + c0, qa);
-                if (has_l2) tmem_ld32(tm + lrow + C::COL_O2 + c0, o2);
+#pragma unroll 1
+            for (int cc = 0; cc < DV / 2; cc += 16) {
+                const int col = half * (DV / 2) + cc;
+                float o0[16], o1[16], qa[16], o2[16];
+                tmem_ld16(tm + lrow + C::COL_O0 + col, o0);
+                tmem_ld16(tm + lrow + C::COL_O1 + col, o1);
+                tmem_ld16(tm + lrow + col, qa);
+                if (has_l2) tmem_ld16(tm + lrow + C::COL_O2 + col, o2);
                 tmem_wait_ld();
                 if (t < T) {
-                    uint32_t pk[16];
+                    uint32_t pk[8];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        float a0 = fmaf(decay, qa[2 * i], has_l2 ? o2[2 * i] : 0.f);
-                        float a1 = fmaf(decay, qa[2 * i + 1], has_l2 ? o2[2 * i + 1] : 0.f);
-                        pk[i] = pack_bf16(fmaf(o[2 * i], inv_l, sg * a0), fmaf(o[2 * i + 1], inv_l, sg * a1));
+                    for (int i = 0; i < 8; ++i) {
+                        float v2[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int e = 2 * i + u;
+                            const float mem = fmaf(decay, qa[e], has_l2 ? o2[e] : 0.f);
+                            v2[u] = fmaf(o0[e], w0, fmaf(o1[e], w1, sg * mem));
+                        }
+                        pk[i] = pack_bf16(v2[0], v2[1]);
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(yr + c0);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                    uint4 *dst = reinterpret_cast<uint4 *>(yr + col);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
                 }
             }
         }
@@ -547,46 +740,72 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) tmem_dealloc(tm, 512);
+    if (warp == 9) tmem_dealloc(tm, 512);
+}
+
+struct Ws {
+    __nv_bfloat16 *Aloc, *Cbf;
+    float *Lfin;
+};
+
+Ws carve(void *ws, int BH, const Segments &g, int dk, int dv) {
+    char *p = (char *)ws;
+    Ws w;
+    w.Aloc = (__nv_bfloat16 *)p;
+    p += align_up(2 * (size_t)BH * g.nch * dk * dv, 1024);
+    w.Cbf = (__nv_bfloat16 *)p;
+    p += align_up(2 * (size_t)BH * g.nseg * dk * dv, 1024);
+    w.Lfin = (float *)p;
+    return w;
+}
+
+size_t ws_bytes(int BH, const Segments &g, int dk, int dv) {
+    return align_up(2 * (size_t)BH * g.nch * dk * dv, 1024) + align_up(2 * (size_t)BH * g.nseg * dk * dv, 1024) +
+           align_up(4 * (size_t)BH * g.nseg * dk * dv, 1024);
+}
+
+int num_sms() {
+    int dev = 0, n = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    return n > 0 ? n : 148;
 }
 
 template <int DK, int DV>
 int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W, const float *lam,
         const float *eta, const float *gate, float scale, void *y, float *A_final, void *ws,
         cudaStream_t st) {
-    const int BH = B_ * H, nch = ceil_div(T, kBlk);
-    float *dA = (float *)ws;
-    __nv_bfloat16 *Abf = (__nv_bfloat16 *)((char *)ws + align_up(sizeof(float) * (size_t)BH * nch * DK * DV, 1024));
-    CUtensorMap mq, mk, mv, mk_d, mv_d, ma;
+    const int BH = B_ * H;
+    const Segments g = segments(BH, T, DV, num_sms());
+    const Ws w = carve(ws, BH, g, DK, DV);
+    CUtensorMap mq, mk, mv, ma, mc;
     int rc;
     if ((rc = make_tmap_bf16_3d(&mq, q, DK, T, BH, kBlk))) return rc;
     if ((rc = make_tmap_bf16_3d(&mk, k, DK, T, BH, kBlk))) return rc;
     if ((rc = make_tmap_bf16_3d(&mv, v, DV, T, BH, kBlk))) return rc;
-    if ((rc = make_tmap_bf16_3d(&ma, Abf, DV, DK, (uint64_t)BH * nch, DK))) return rc;
-    mk_d = mk;
-    mv_d = mv;
+    if ((rc = make_tmap_bf16_3d(&ma, w.Aloc, DV, DK, (uint64_t)BH * g.nch, DK))) return rc;
+    if ((rc = make_tmap_bf16_3d(&mc, w.Cbf, DV, DK, (uint64_t)BH * g.nseg, DK))) return rc;
     {
-        const int smem = kBlk * (DK + DV) * 2 + 1024;
-        auto kern = tc_l2_delta_kernel<DK, DV>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return cuda_fail(e, "tc_l2_delta smem attribute");
-        kern<<<dim3(nch, BH), 128, smem, st>>>(mk_d, mv_d, T, W, H, lam, eta, nch, dA);
-        if ((rc = launched("tc_l2_delta"))) return rc;
+        using SC = StateCfg<DK>;
+        auto kern = tc_l2_state_kernel<DK, DV>;
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC::SMEM);
+        if (e != cudaSuccess) return cuda_fail(e, "tc_l2_state smem attribute");
+        kern<<<dim3(DV / 64, g.nseg, BH), 192, SC::SMEM, st>>>(mk, mv, T, W, H, lam, eta, g.nch, g.L, w.Aloc,
+                                                              w.Lfin);
+        if ((rc = launched("tc_l2_state"))) return rc;
     }
-    {
-        const int per = DK * DV / 4;
-        tc_l2_scan_kernel<<<dim3(ceil_div(per, 128), BH), 128, 0, st>>>(dA, nch, T, DK * DV, H, lam, Abf,
-                                                                       A_final);
-        if ((rc = launched("tc_l2_scan"))) return rc;
-    }
+    tc_l2_carry_kernel<<<dim3(ceil_div(DK * DV / 4, 128), BH), 128, 0, st>>>(w.Lfin, g.nseg, g.L, T, DK * DV, H,
+                                                                            lam, w.Cbf, A_final);
+    if ((rc = launched("tc_l2_carry"))) return rc;
     {
         using Cfg = Fwd<DK, DV>;
         auto kern = tc_fwd_kernel<DK, DV>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg::SMEM);
+        static_assert(sizeof(FwdBars) <= 3072, "barriers block");
+        const int smem = (int)(Cfg::OFF_BARS + sizeof(FwdBars));
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return cuda_fail(e, "tc_fwd smem attribute");
         prof_begin(st);
-        kern<<<dim3(nch, BH), 192, Cfg::SMEM, st>>>(mq, mk, mv, ma, T, W, H, nch, lam, eta, gate, scale,
-                                                    (__nv_bfloat16 *)y);
+        kern<<<dim3(g.nch, BH), 320, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, lam, eta,
+                                                       gate, scale, (__nv_bfloat16 *)y);
         rc = launched("tc_fwd");
         prof_end(st);
         return rc;
@@ -600,8 +819,7 @@ bool tc_prefill_tcgen05_supported(int dtype, int dk, int dv) {
 }
 
 size_t tc_prefill_tcgen05_workspace(int BH, int T, int dk, int dv) {
-    const size_t nch = (size_t)ceil_div(T, kBlk);
-    return align_up(sizeof(float) * BH * nch * dk * dv, 1024) + align_up(2 * BH * nch * dk * dv, 1024);
+    return ws_bytes(BH, segments(BH, T, dv, num_sms()), dk, dv);
 }
 
 int tc_prefill_tcgen05(const void *q, const void *k, const void *v, int B, int H, int T, int dk,
