@@ -9,7 +9,8 @@
 // Work per (sequence, head) is one pass over the ring (2 W d elements) and
 // one read-modify-write of A (d_k d_v floats): memory bound.  The ring is
 // split over `nsplit` CTAs per (sequence, head); each CTA also owns a slice
-// of A's rows, so A is streamed exactly once.  Kernel 1 writes per-split
+// of A's rows, so A is streamed exactly once.  Every stream is read with
+// coalesced 16-byte loads that bypass L1 (each byte is used once).  Kernel 1 writes per-split
 // partials (softmax max / sum / weighted values, and the partial q A of its
 // rows); kernel 2 merges them flash-decoding style, applies the gate and
 // stores the new token into its ring slot (after every reader of the evicted
@@ -33,6 +34,40 @@ DecodeGeom geom(int W) {
     return {ns, ceil_div(W, ns)};
 }
 
+// 16-byte vector of T: EPV elements.
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+    static constexpr int EPV = 4;
+    static __device__ __forceinline__ void unpack(const uint4 &u, float *f) {
+        f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+    }
+};
+template <> struct Vec<__nv_bfloat16> {
+    static constexpr int EPV = 8;
+    static __device__ __forceinline__ void unpack(const uint4 &u, float *f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+__device__ __forceinline__ uint4 ldg_stream(const void *p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+// Per (sequence, head, split): the A rows of this split (eviction write and
+// the partial q A), then the softmax over this split's ring slots.
+// Ring rows are read as 16-byte vectors, LPK lanes per key row (a warp load
+// covers KPW consecutive rows), with q held in registers; scores go to
+// shared memory, then P V reads the value rows the same way.
 template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThreads)
 tc_decode_partial_kernel(const T *__restrict__ ring_k, const T *__restrict__ ring_v,
@@ -42,12 +77,19 @@ tc_decode_partial_kernel(const T *__restrict__ ring_k, const T *__restrict__ rin
                          const float *__restrict__ lam, const float *__restrict__ eta,
                          float scale, float *__restrict__ part_m, float *__restrict__ part_o,
                          float *__restrict__ part_ml) {
+    constexpr int EPV = Vec<T>::EPV;
+    constexpr int LPK = DK / EPV, KPW = 32 / LPK;  // lanes per key row, rows per warp load
+    constexpr int LPV = DV / EPV, VPW = 32 / LPV;
+    constexpr int LPA = DV / 4, RPW = 32 / LPA;    // A rows: float4 per lane
+    constexpr int NW = kThreads / 32;
+    constexpr int U = 4;                           // loads in flight per lane
     extern __shared__ float sm[];
-    float *qs = sm;             // [DK]
-    float *kes = qs + DK;       // [DK] evicted key
-    float *ves = kes + DK;      // [DV] evicted value
-    float *red = ves + DV;      // [kThreads] reduction scratch
-    float *sc = red + kThreads; // [keys_per_split] scores, then weights
+    float *qs = sm;              // [DK]
+    float *kes = qs + DK;        // [DK] evicted key
+    float *ves = kes + DK;       // [DV] evicted value
+    float *red = ves + DV;       // [NW][DV] cross-warp reduction
+    float *wred = red + NW * DV; // [2 * NW]
+    float *sc = wred + 2 * NW;   // [keys_per_split] scores, then weights
 
     const int sh = blockIdx.x, sp = blockIdx.y, nsplit = gridDim.y;
     const int b = sh / H, h = sh - b * H;
@@ -65,85 +107,143 @@ tc_decode_partial_kernel(const T *__restrict__ ring_k, const T *__restrict__ rin
         ves[c] = evict ? Elem<T>::load(ring_v + (ring_row + slot) * DV + c) : 0.f;
     __syncthreads();
 
-    // ---- A rows owned by this split: eviction write, then partial q A.
+    // ---- A rows of this split: eviction write, then partial q A.
     {
-        constexpr int G = kThreads / DV;  // row groups
-        const int col = tid % DV, g = tid / DV;
         const int rows = (DK + nsplit - 1) / nsplit;
         const int r0 = sp * rows, r1 = min(DK, r0 + rows);
         const float lm = lam[h], et = eta[h];
+        const int c4 = (lane % LPA) * 4;
         float *Ab = A + (size_t)sh * DK * DV;
-        float pm = 0.f;
-        for (int a = r0 + g; a < r1; a += G) {
-            float x = Ab[(size_t)a * DV + col];
+        float pm[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int a = r0 + warp * RPW + lane / LPA; a < r1; a += NW * RPW) {
+            float4 x = *reinterpret_cast<const float4 *>(Ab + (size_t)a * DV + c4);
             if (evict) {
-                x = fmaf(lm, x, et * kes[a] * ves[col]);
-                Ab[(size_t)a * DV + col] = x;
+                const float ek = et * kes[a];
+                x.x = fmaf(lm, x.x, ek * ves[c4]);
+                x.y = fmaf(lm, x.y, ek * ves[c4 + 1]);
+                x.z = fmaf(lm, x.z, ek * ves[c4 + 2]);
+                x.w = fmaf(lm, x.w, ek * ves[c4 + 3]);
+                *reinterpret_cast<float4 *>(Ab + (size_t)a * DV + c4) = x;
             }
-            pm = fmaf(qs[a], x, pm);
+            const float qa = qs[a];
+            pm[0] = fmaf(qa, x.x, pm[0]);
+            pm[1] = fmaf(qa, x.y, pm[1]);
+            pm[2] = fmaf(qa, x.z, pm[2]);
+            pm[3] = fmaf(qa, x.w, pm[3]);
         }
-        red[tid] = pm;
+#pragma unroll
+        for (int o = LPA; o < 32; o <<= 1)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pm[i] += __shfl_xor_sync(0xffffffffu, pm[i], o);
+        if (lane < LPA)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) red[warp * DV + c4 + i] = pm[i];
         __syncthreads();
-        if (tid < DV) {
+        for (int c = tid; c < DV; c += kThreads) {
             float s = 0.f;
-            for (int gg = 0; gg < G; ++gg) s += red[gg * DV + tid];
-            part_m[((size_t)sh * nsplit + sp) * DV + tid] = s;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) s += red[w * DV + c];
+            part_m[((size_t)sh * nsplit + sp) * DV + c] = s;
         }
         __syncthreads();
     }
 
-    // ---- ring softmax over this split's occupied slots (new token at `slot`).
+    // ---- scores of this split's occupied slots (the new token sits at `slot`).
     const int occ = (p + 1 < (int64_t)W) ? (int)(p + 1) : W;
     const int s0 = sp * keys_per_split, s1 = min(occ, s0 + keys_per_split);
     const int nk = max(0, s1 - s0);
-    for (int jj = warp; jj < nk; jj += kThreads / 32) {
-        const int j = s0 + jj;
-        const T *kr = (j == slot) ? k + (size_t)sh * DK : ring_k + (ring_row + j) * DK;
-        float d = 0.f;
-        for (int a = lane; a < DK; a += 32) d = fmaf(qs[a], Elem<T>::load(kr + a), d);
-        d = warp_sum(d);
-        if (lane == 0) sc[jj] = d * scale;
+    {
+        const int ks = lane / LPK, kc = (lane % LPK) * EPV;
+        float qv[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) qv[e] = qs[kc + e];
+        for (int g0 = warp; g0 * KPW < nk; g0 += NW * U) {
+            uint4 raw[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int key = (g0 + NW * u) * KPW + ks, idx = s0 + key;
+                const T *src = (idx == slot) ? k + (size_t)sh * DK : ring_k + (ring_row + idx) * DK;
+                raw[u] = key < nk ? ldg_stream(src + kc) : make_uint4(0u, 0u, 0u, 0u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float f[EPV];
+                Vec<T>::unpack(raw[u], f);
+                float d = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) d = fmaf(qv[e], f[e], d);
+#pragma unroll
+                for (int o = LPK / 2; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                const int key = (g0 + NW * u) * KPW + ks;
+                if (lane % LPK == 0 && key < nk) sc[key] = d * scale;
+            }
+        }
     }
     __syncthreads();
     float mx = kNegBig;
-    for (int jj = tid; jj < nk; jj += kThreads) mx = fmaxf(mx, sc[jj]);
+    for (int i = tid; i < nk; i += kThreads) mx = fmaxf(mx, sc[i]);
     mx = warp_max(mx);
-    if (lane == 0) red[warp] = mx;
+    if (lane == 0) wred[warp] = mx;
     __syncthreads();
     mx = kNegBig;
-    for (int w = 0; w < kThreads / 32; ++w) mx = fmaxf(mx, red[w]);
-    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < NW; ++w) mx = fmaxf(mx, wred[w]);
     float ssum = 0.f;
-    for (int jj = tid; jj < nk; jj += kThreads) {
-        const float e = expf(sc[jj] - mx);
-        sc[jj] = e;
+    for (int i = tid; i < nk; i += kThreads) {
+        const float e = __expf(sc[i] - mx);
+        sc[i] = e;
         ssum += e;
     }
     ssum = warp_sum(ssum);
-    if (lane == 0) red[warp] = ssum;
+    if (lane == 0) wred[NW + warp] = ssum;
     __syncthreads();
     if (tid == 0) {
         float s = 0.f;
-        for (int w = 0; w < kThreads / 32; ++w) s += red[w];
+#pragma unroll
+        for (int w = 0; w < NW; ++w) s += wred[NW + w];
         part_ml[((size_t)sh * nsplit + sp) * 2 + 0] = mx;
         part_ml[((size_t)sh * nsplit + sp) * 2 + 1] = s;
     }
-    __syncthreads();
+
+    // ---- P V over this split's slots.
     {
-        constexpr int G = kThreads / DV;
-        const int col = tid % DV, g = tid / DV;
-        float o = 0.f;
-        for (int jj = g; jj < nk; jj += G) {
-            const int j = s0 + jj;
-            const T *vr = (j == slot) ? v + (size_t)sh * DV : ring_v + (ring_row + j) * DV;
-            o = fmaf(sc[jj], Elem<T>::load(vr + col), o);
+        const int vs = lane / LPV, vc = (lane % LPV) * EPV;
+        float acc[EPV];
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) acc[e] = 0.f;
+        for (int g0 = warp; g0 * VPW < nk; g0 += NW * U) {
+            uint4 raw[U];
+            float pw[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int key = (g0 + NW * u) * VPW + vs, idx = s0 + key;
+                const T *src = (idx == slot) ? v + (size_t)sh * DV : ring_v + (ring_row + idx) * DV;
+                const bool ok = key < nk;
+                raw[u] = ok ? ldg_stream(src + vc) : make_uint4(0u, 0u, 0u, 0u);
+                pw[u] = ok ? sc[key] : 0.f;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                float f[EPV];
+                Vec<T>::unpack(raw[u], f);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) acc[e] = fmaf(pw[u], f[e], acc[e]);
+            }
         }
-        red[tid] = o;
+#pragma unroll
+        for (int o = LPV; o < 32; o <<= 1)
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+        __syncthreads();  // red reused
+        if (lane < LPV)
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) red[warp * DV + vc + e] = acc[e];
         __syncthreads();
-        if (tid < DV) {
+        for (int c = tid; c < DV; c += kThreads) {
             float s = 0.f;
-            for (int gg = 0; gg < G; ++gg) s += red[gg * DV + tid];
-            part_o[((size_t)sh * nsplit + sp) * DV + tid] = s;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) s += red[w * DV + c];
+            part_o[((size_t)sh * nsplit + sp) * DV + c] = s;
         }
     }
 }
@@ -206,7 +306,7 @@ int launch(const opam_tc_state *st, const void *q, const void *k, const void *v,
     const int SH = st->B * st->H;
     const DecodeGeom g = geom(st->W);
     const Parts pr = carve(ws, SH, g.nsplit, DV);
-    const size_t smem = sizeof(float) * (DK + DK + DV + kThreads + g.keys_per_split);
+    const size_t smem = sizeof(float) * (DK + DK + DV + (kThreads / 32) * DV + 2 * (kThreads / 32) + g.keys_per_split);
     auto k1 = tc_decode_partial_kernel<T, DK, DV>;
     cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "tc_decode smem attribute");
