@@ -114,10 +114,11 @@ int opam_profile_events(void *start, void *stop) {
 uint64_t opam_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int opam_device_status(int clear) {
-    const unsigned int st = tc_prefill_tcgen05_status(clear != 0);
-    if (st == 0) return OPAM_OK;
-    set_error("opam_device_status: a bounded wait ran out in the tensor-core Tensor Cache prefill "
-              "(status bits 0x%x); its outputs are not valid", st);
+    const unsigned int tc = tc_prefill_tcgen05_status(clear != 0);
+    const unsigned int dn = delta_tcgen05_status(clear != 0);
+    if (tc == 0 && dn == 0) return OPAM_OK;
+    set_error("opam_device_status: a bounded wait ran out in a tensor-core kernel (Tensor Cache "
+              "prefill bits 0x%x, delta rule bits 0x%x); the affected outputs are not valid", tc, dn);
     return OPAM_ERR_TIMEOUT;
 }
 
@@ -219,6 +220,7 @@ size_t delta_rule_forward_workspace_size(int B, int H, int T, int d_k, int d_v, 
     if (check_tc_dims(fn, dtype, B, H, T, d_k, d_v, 1) != OPAM_OK) return 0;
     const int C = delta_chunk(chunk);
     if (C != 16 && C != 32 && C != 64) return 0;
+    if (delta_tcgen05_supported(dtype, d_k, d_v, C)) return delta_tcgen05_workspace(B * H, T, d_k);
     return delta_simt_workspace(B * H, T, d_k, d_v, C);
 }
 
@@ -240,12 +242,15 @@ int delta_rule_forward(const void *q, const void *k, const void *v, const float 
     OPAM_CHECK_PTR(y);
     OPAM_CHECK_OPT_PTR(S0);
     OPAM_CHECK_OPT_PTR(S_out);
-    const size_t need = delta_simt_workspace(B * H, T, d_k, d_v, C);
+    const bool tc = delta_tcgen05_supported(dtype, d_k, d_v, C);
+    const size_t need = tc ? delta_tcgen05_workspace(B * H, T, d_k) : delta_simt_workspace(B * H, T, d_k, d_v, C);
     if (!workspace || workspace_bytes < need) {
         set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
         return OPAM_ERR_WORKSPACE;
     }
     OPAM_CHECK_PTR(workspace);
+    if (tc)
+        return delta_tcgen05(q, k, v, beta, B, H, T, d_k, S0, S_out, y, workspace, (cudaStream_t)stream);
     return delta_simt(q, k, v, beta, dtype, B, H, T, d_k, d_v, C, S0, S_out, y, workspace,
                       (cudaStream_t)stream);
 }

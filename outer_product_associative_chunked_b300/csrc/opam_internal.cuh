@@ -90,6 +90,13 @@ int delta_simt(const void *q, const void *k, const void *v, const float *beta, i
                int B, int H, int T, int dk, int dv, int C, const float *S0, float *S_out,
                void *y, void *ws, cudaStream_t s);
 
+// DeltaNet, tensor-core path (bf16, d_k in {64, 128}, d_v = 128, chunk 64).
+bool delta_tcgen05_supported(int dtype, int dk, int dv, int chunk);
+size_t delta_tcgen05_workspace(int BH, int T, int dk);
+int delta_tcgen05(const void *q, const void *k, const void *v, const float *beta, int B, int H, int T,
+                  int dk, const float *S0, float *S_out, void *y, void *ws, cudaStream_t s);
+unsigned int delta_tcgen05_status(bool clear);
+
 size_t sparse_workspace(int BH, int T, int N, int dv, bool need_state);
 int sparse_forward(const float *q, const float *k, const float *v, int B, int H, int T, int N,
                    int dv, const float *S0, float *S_out, float *y, void *ws, cudaStream_t s);

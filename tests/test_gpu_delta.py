@@ -44,6 +44,31 @@ def test_small_parity(cuda_lib, oracle_mod, dtype, B, H, T, dk, dv, chunk, with_
     check_parity(to_np(S_out), ref["S"], dtype, "delta S")
 
 
+# Shapes served by the tensor-core path (bf16, d_v = 128, chunk 64): ragged
+# tails, a single token, exact chunk multiples, both key widths, start states.
+@pytest.mark.parametrize("B,H,T,dk,with_S0", [
+    (1, 1, 1, 128, False),
+    (1, 2, 63, 128, True),
+    (2, 1, 64, 128, False),
+    (1, 1, 65, 64, True),
+    (1, 3, 200, 128, True),
+    (2, 2, 333, 64, False),
+    (1, 1, 1024, 128, True),
+])
+def test_tensor_core_shapes(cuda_lib, oracle_mod, B, H, T, dk, with_S0):
+    inp = synth.delta_inputs(B, H, T, dk, 128, dtype="bf16", seed=T + 7 * dk)
+    q, k, v, beta = _gpu(inp)
+    S0 = (torch.randn(B, H, dk, 128, generator=torch.Generator().manual_seed(9)) * 0.1) if with_S0 else None
+    S = None if S0 is None else S0.clone().cuda()
+    S_out = S if S is not None else torch.empty(B, H, dk, 128, device="cuda")  # in place when given
+    y = cuda_lib.delta_rule_forward(q, k, v, beta, chunk=64, S0=S, S_out=S_out)
+    torch.cuda.synchronize()
+    cuda_lib.device_status(clear=True)
+    ref = oracle_mod.delta(inp.q, inp.k, inp.v, inp.beta, S0=S0, want_state=True)
+    check_parity(to_np(y), ref["y"], "bf16", "delta y (tensor cores)")
+    check_parity(to_np(S_out), ref["S"], "bf16", "delta S (tensor cores)")
+
+
 def test_in_place_state_and_chunk_independence(cuda_lib, oracle_mod):
     inp = synth.delta_inputs(2, 2, 150, 64, 64, dtype="f32", seed=5)
     q, k, v, beta = _gpu(inp)
