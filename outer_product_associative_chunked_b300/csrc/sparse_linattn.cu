@@ -47,29 +47,54 @@ __global__ void compact_rows_kernel(const float *__restrict__ x, int rows, int N
     if (lane == 0) cnt[row] = c;
 }
 
+// One CTA per (token t of the chunk, head).  o_t = q_t S (gathered over the
+// support of q_t, float4 columns, LOOK loads in flight per thread) +
+// sum_{s in chunk, s <= t} <k_s, q_t> v_s (keys' supports against a dense copy
+// of q_t in shared memory).
 template <int DV>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 3)
 sparse_read_kernel(int c0, int T_, int N, const int *__restrict__ kidx,
                    const float *__restrict__ kval, const int *__restrict__ kcnt,
                    const int *__restrict__ qidx, const float *__restrict__ qval,
                    const int *__restrict__ qcnt, const float *__restrict__ v,
                    const float *__restrict__ ST, float *__restrict__ y) {
-    extern __shared__ float qd[];  // [N] dense copy of q_t
+    constexpr int CG = DV / 4;           // float4 column groups
+    constexpr int RGN = kThreads / CG;   // support entries processed side by side
+    constexpr int LOOK = 8;              // gathers in flight per thread
+    extern __shared__ float qd[];        // [N] dense copy of q_t
     __shared__ float zs[kC];
-    __shared__ float red[kThreads];
-    constexpr int G = kThreads / DV;
+    __shared__ float4 red[kThreads];
     const int ti = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const size_t row = (size_t)bh * T_ + c0 + ti;
     for (int j = tid; j < N; j += kThreads) qd[j] = 0.f;
     __syncthreads();
     const int nq = qcnt[row];
-    for (int e = tid; e < nq; e += kThreads) qd[qidx[row * N + e]] = qval[row * N + e];
-    __syncthreads();
-    const int col = tid % DV, g = tid / DV;
-    float o = 0.f;
-    const float *Sb = ST + (size_t)bh * N * DV;
-    for (int e = g; e < nq; e += G) o = fmaf(qval[row * N + e], Sb[(size_t)qidx[row * N + e] * DV + col], o);
+    const int *qi = qidx + row * N;
+    const float *qv = qval + row * N;
+    for (int e = tid; e < nq; e += kThreads) qd[qi[e]] = qv[e];
+    const int cg = tid % CG, rg = tid / CG;
+    const float4 *Sb = reinterpret_cast<const float4 *>(ST + (size_t)bh * N * DV);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int e0 = rg; e0 < nq; e0 += RGN * LOOK) {
+        float4 x[LOOK];
+        float w[LOOK];
+#pragma unroll
+        for (int u = 0; u < LOOK; ++u) {
+            const int e = e0 + u * RGN;
+            const bool ok = e < nq;
+            w[u] = ok ? qv[e] : 0.f;
+            x[u] = ok ? Sb[(size_t)qi[e] * CG + cg] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < LOOK; ++u) {
+            o.x = fmaf(w[u], x[u].x, o.x);
+            o.y = fmaf(w[u], x[u].y, o.y);
+            o.z = fmaf(w[u], x[u].z, o.z);
+            o.w = fmaf(w[u], x[u].w, o.w);
+        }
+    }
+    __syncthreads();  // qd complete
     for (int si = warp; si <= ti; si += kThreads / 32) {
         const size_t srow = (size_t)bh * T_ + c0 + si;
         const int nk = kcnt[srow];
@@ -79,31 +104,48 @@ sparse_read_kernel(int c0, int T_, int N, const int *__restrict__ kidx,
         if (lane == 0) zs[si] = z;
     }
     __syncthreads();
-    for (int si = g; si <= ti; si += G)
-        o = fmaf(zs[si], v[((size_t)bh * T_ + c0 + si) * DV + col], o);
+    const float4 *vb = reinterpret_cast<const float4 *>(v + ((size_t)bh * T_ + c0) * DV);
+    for (int si = rg; si <= ti; si += RGN) {
+        const float z = zs[si];
+        const float4 vv = vb[(size_t)si * CG + cg];
+        o.x = fmaf(z, vv.x, o.x);
+        o.y = fmaf(z, vv.y, o.y);
+        o.z = fmaf(z, vv.z, o.z);
+        o.w = fmaf(z, vv.w, o.w);
+    }
     red[tid] = o;
     __syncthreads();
-    if (tid < DV) {
-        float s = 0.f;
-        for (int gg = 0; gg < G; ++gg) s += red[gg * DV + tid];
-        y[row * DV + tid] = s;
+    if (tid < CG) {
+        float4 s = red[tid];
+        for (int g = 1; g < RGN; ++g) {
+            const float4 a = red[g * CG + tid];
+            s.x += a.x; s.y += a.y; s.z += a.z; s.w += a.w;
+        }
+        reinterpret_cast<float4 *>(y + row * DV)[tid] = s;
     }
 }
 
+// One CTA per (token s of the chunk, head): S[j, :] += k_s[j] v_s for every j
+// in the support of k_s, as float4 vector reductions.
 template <int DV>
 __global__ void __launch_bounds__(kThreads)
 sparse_write_kernel(int c0, int T_, int N, const int *__restrict__ kidx,
                     const float *__restrict__ kval, const int *__restrict__ kcnt,
                     const float *__restrict__ v, float *__restrict__ ST) {
-    constexpr int G = kThreads / DV;
+    constexpr int CG = DV / 4, RGN = kThreads / CG;
     const int bh = blockIdx.y, tid = threadIdx.x;
     const size_t row = (size_t)bh * T_ + c0 + blockIdx.x;
-    const int col = tid % DV, g = tid / DV;
-    const float vv = v[row * DV + col];
-    float *Sb = ST + (size_t)bh * N * DV;
+    const int cg = tid % CG, rg = tid / CG;
+    const float4 vv = reinterpret_cast<const float4 *>(v + row * DV)[cg];
+    float4 *Sb = reinterpret_cast<float4 *>(ST + (size_t)bh * N * DV);
     const int nk = kcnt[row];
-    for (int e = g; e < nk; e += G)
-        atomicAdd(&Sb[(size_t)kidx[row * N + e] * DV + col], kval[row * N + e] * vv);
+    const int *ki = kidx + row * N;
+    const float *kv = kval + row * N;
+#pragma unroll 4
+    for (int e = rg; e < nk; e += RGN) {
+        const float a = kv[e];
+        atomicAdd(Sb + (size_t)ki[e] * CG + cg, make_float4(a * vv.x, a * vv.y, a * vv.z, a * vv.w));
+    }
 }
 
 struct WsLayout {
