@@ -743,6 +743,387 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     if (warp == 9) tmem_dealloc(tm, 512);
 }
 
+// --------------------------------------------------------------------- fused forward, one row per thread
+// Variant for d_k = d_v = 64 sized so that two CTAs share an SM (256 TMEM
+// columns, ~113 KB of shared memory): while one CTA waits on its loads, MMAs
+// or prologue/epilogue, the other runs its softmax.  192 threads: warps 0-3
+// own one query row each (softmax over all 128 keys of a tile, epilogue),
+// warp 4 issues TMA loads and scales the segment carry, warp 5 issues the
+// MMAs.  TMEM: S [0,128) (q A_j lands there after the last tile), O [128,
+// 128+DV), O2 [128+DV, 128+2DV).  One P slot, two K/V stages.
+template <int DK, int DV>
+struct FwdRow {
+    static constexpr uint32_t QBYTES = kBlk * DK * 2;
+    static constexpr uint32_t KBYTES = kBlk * DK * 2;  // also holds A_j^loc
+    static constexpr uint32_t VBYTES = kBlk * DV * 2;  // also holds the segment carry
+    static constexpr uint32_t PBYTES = kBlk * kBlk * 2;
+    static constexpr int NST = 2;
+    static constexpr uint32_t OFF_K = QBYTES;
+    static constexpr uint32_t OFF_P = QBYTES + NST * (KBYTES + VBYTES);
+    static constexpr uint32_t OFF_BARS = OFF_P + PBYTES;
+    static constexpr uint32_t COL_O = 128, COL_O2 = 128 + DV;
+    static constexpr uint32_t TCOLS = 128 + 2 * DV <= 256 ? 256 : 512;
+    static constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);
+    static constexpr uint32_t ID_PV = idesc_bf16_f32(128, DV, false, true);
+};
+
+struct FwdRowBars {
+    uint64_t q_full, k_full[2], v_full[2], kv_empty[2];
+    uint64_t s_full, s_empty, p_full, p_empty, c_ready, o_done, drain;
+    uint32_t tbase;
+    float pw[kBlk];  // eta lambda^d
+};
+
+template <int DK, int DV>
+__global__ void __launch_bounds__(192, 2)
+tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                  const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ma,
+                  const __grid_constant__ CUtensorMap mc, int T, int W, int H, int nch, int nseg, int L,
+                  const float *__restrict__ lam, const float *__restrict__ eta,
+                  const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y) {
+    using C = FwdRow<DK, DV>;
+    constexpr int NST = C::NST;
+    extern __shared__ __align__(1024) unsigned char sm[];
+    FwdRowBars &B = *reinterpret_cast<FwdRowBars *>(sm + C::OFF_BARS);
+    if ((smem_u32(sm) & 1023u) != 0) {
+        if (threadIdx.x == 0) atomicOr(&g_status, kStFwdAlign);
+        return;
+    }
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int jq = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const int seg = jq / L;
+    const int t0 = jq * kBlk;
+    const int kt0 = t0 - W;
+    const int nt_total = (W + kBlk - 1) / kBlk + 1;
+    const int j_first = (-kt0 - (kBlk - 1) > 0) ? (-kt0) / kBlk : 0;
+    const int ntiles = nt_total - j_first;
+    const bool has_l2 = (j_first == 0);
+
+    if (warp == 5) tmem_alloc(&B.tbase, C::TCOLS);
+    if (tid == 0) {
+        mbar_init(&B.q_full, 1);
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&B.k_full[s], 1);
+            mbar_init(&B.v_full[s], 1);
+            mbar_init(&B.kv_empty[s], 1);
+        }
+        mbar_init(&B.s_full, 1);
+        mbar_init(&B.s_empty, 4);
+        mbar_init(&B.p_full, 4);
+        mbar_init(&B.p_empty, 1);
+        mbar_init(&B.c_ready, 1);
+        mbar_init(&B.o_done, 1);
+        mbar_init(&B.drain, 1);
+        mbar_fence_init();
+    }
+    if (tid < kBlk) B.pw[tid] = eta[h] * powf(lam[h], (float)tid);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = B.tbase;
+    const uint32_t sQ = smem_u32(sm);
+    const uint32_t sK0 = sQ + C::OFF_K;
+    const uint32_t sP = sQ + C::OFF_P;
+
+    if (warp == 4) {
+        // ------------------------------------------------ TMA producer
+        bool ok = true;
+        const int sA = ntiles % NST;
+        if (lane == 0) {
+            tma_prefetch_desc(&mq);
+            tma_prefetch_desc(&mk);
+            tma_prefetch_desc(&mv);
+            mbar_expect_tx(&B.q_full, C::QBYTES);
+#pragma unroll
+            for (int b = 0; b < DK / 64; ++b) tma_load_3d(sm + b * 16384, &mq, &B.q_full, 64 * b, t0, bh);
+            for (int n = 0; n <= ntiles && ok; ++n) {
+                const int s = n % NST;
+                if (n >= NST) ok = mbar_wait(&B.kv_empty[s], ((n / NST) - 1) & 1);
+                if (!ok) break;
+                unsigned char *kd = sm + C::OFF_K + s * (C::KBYTES + C::VBYTES);
+                if (n < ntiles) {
+                    const int kt = kt0 + kBlk * (j_first + n);
+                    mbar_expect_tx(&B.k_full[s], C::KBYTES);
+#pragma unroll
+                    for (int b = 0; b < DK / 64; ++b) tma_load_3d(kd + b * 16384, &mk, &B.k_full[s], 64 * b, kt, bh);
+                    mbar_expect_tx(&B.v_full[s], C::VBYTES);
+#pragma unroll
+                    for (int b = 0; b < DV / 64; ++b)
+                        tma_load_3d(kd + C::KBYTES + b * 16384, &mv, &B.v_full[s], 64 * b, kt, bh);
+                } else {
+                    mbar_expect_tx(&B.k_full[s], 2 * DK * DV * 2);
+#pragma unroll
+                    for (int b = 0; b < DV / 64; ++b) {
+                        tma_load_3d(kd + b * (DK * 128), &ma, &B.k_full[s], 64 * b, 0, bh * nch + jq);
+                        tma_load_3d(kd + C::KBYTES + b * (DK * 128), &mc, &B.k_full[s], 64 * b, 0, bh * nseg + seg);
+                    }
+                }
+            }
+            if (ok) ok = mbar_wait(&B.k_full[sA], (ntiles / NST) & 1);
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok) {
+            const float c = powf(lam[h], (float)(kBlk * (jq - seg * L)));
+            const __nv_bfloat162 c2 = __floats2bfloat162_rn(c, c);
+            const uint32_t base = sK0 + sA * (C::KBYTES + C::VBYTES) + C::KBYTES;
+            for (int e = lane; e < DK * DV / 8; e += 32) {
+                uint32_t x[4];
+                ld_shared_v4(base + e * 16, x[0], x[1], x[2], x[3]);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    __nv_bfloat162 hv = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&x[u]), c2);
+                    x[u] = *reinterpret_cast<uint32_t *>(&hv);
+                }
+                st_shared_v4(base + e * 16, x[0], x[1], x[2], x[3]);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.c_ready);
+        } else if (lane == 0) {
+            atomicOr(&g_status, kStFwdProducer);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            bool ok = mbar_wait(&B.q_full, 0);
+            uint32_t use = 0;
+            auto stage = [&](int s) { return sK0 + s * (C::KBYTES + C::VBYTES); };
+            auto qdesc = [&](int k) { return sdesc_sw128(sQ + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); };
+            auto pv = [&](int n) -> bool {
+                const int s = n % NST;
+                if (!mbar_wait(&B.v_full[s], (n / NST) & 1)) return false;
+                const int uses = (n == 0 && has_l2) ? 2 : 1;
+                for (int u = 0; u < uses; ++u) {
+                    if (!mbar_wait(&B.p_full, use & 1)) return false;
+                    tc_fence_after();
+                    const bool l2 = (uses == 2 && u == 0);
+                    const uint32_t dcol = l2 ? C::COL_O2 : C::COL_O;
+#pragma unroll
+                    for (int k = 0; k < kBlk / 16; ++k)
+                        mma_ss(tm + dcol, sdesc_sw128(sP + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
+                               sdesc_sw128(stage(s) + C::KBYTES + k * 2048, 16384, 1024), C::ID_PV,
+                               (l2 ? k > 0 : (n > 0 || k > 0)) ? 1u : 0u);
+                    mma_commit(&B.p_empty);
+                    ++use;
+                }
+                mma_commit(&B.kv_empty[s]);
+                return true;
+            };
+            for (int n = 0; n < ntiles && ok; ++n) {
+                const int s = n % NST;
+                ok = mbar_wait(&B.k_full[s], (n / NST) & 1);
+                if (ok && n >= 1) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < DK / 16; ++k)
+                    mma_ss(tm, qdesc(k),
+                           sdesc_sw128(stage(s) + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024), C::ID_S,
+                           k > 0 ? 1u : 0u);
+                mma_commit(&B.s_full);
+                if (n >= 1) ok = pv(n - 1);
+            }
+            if (ok) ok = pv(ntiles - 1);
+            if (ok) {  // q (A_j^loc + c A_{gL}) into the S columns
+                const int n = ntiles, s = n % NST;
+                ok = mbar_wait(&B.k_full[s], (n / NST) & 1);
+                if (ok) ok = mbar_wait(&B.c_ready, 0);
+                if (ok) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
+                if (ok) {
+                    tc_fence_after();
+                    const uint32_t aslot = stage(s);
+#pragma unroll
+                    for (int k = 0; k < DK / 16; ++k)
+                        mma_ss(tm, qdesc(k), sdesc_sw128(aslot + k * 2048, DK * 128, 1024), C::ID_PV,
+                               k > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < DK / 16; ++k)
+                        mma_ss(tm, qdesc(k), sdesc_sw128(aslot + C::KBYTES + k * 2048, DK * 128, 1024),
+                               C::ID_PV, 1u);
+                    mma_commit(&B.o_done);
+                }
+            }
+            if (!ok) atomicOr(&g_status, kStFwdMma);
+            mma_commit(&B.drain);
+            mbar_wait(&B.drain, 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------ softmax / epilogue (row r)
+        const int r = tid;
+        const int t = t0 + r;
+        const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+        const float sc = scale * kLog2e;
+        float m = kNegBig, l = 0.f;
+        uint32_t use = 0;
+        bool ok = true;
+        auto slot_free = [&]() -> bool {  // the P slot is free once the previous use's MMAs are done
+            return use == 0 || mbar_wait(&B.p_empty, (use - 1) & 1);
+        };
+        auto store8 = [&](int c, const float *p) {
+            st_shared_v4(sP + (c >> 3) * 16384 + sw128_off(r, c & 7), pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
+                         pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
+        };
+        auto publish = [&]() {
+            fence_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.p_full);
+            ++use;
+        };
+        const int wrow_hi = warp * 32 + 31;
+        for (int n = 0; n < ntiles && ok; ++n) {
+            const int j = j_first + n;
+            const int kt = kt0 + kBlk * j;
+            ok = __all_sync(0xffffffffu, mbar_wait(&B.s_full, n & 1));
+            if (!ok) break;
+            tc_fence_after();
+            float s[kBlk];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(tm + lrow + 32 * c, *reinterpret_cast<float(*)[32]>(&s[32 * c]));
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.s_empty);
+
+            if (j == 0) {  // L2 part of the shifted chunk: keys l <= r at positions >= 0
+                const int lo = max(0, -kt);
+                ok = __all_sync(0xffffffffu, slot_free());
+                if (!ok) break;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    const bool act = (32 * g <= wrow_hi) && (32 * g + 31 >= lo);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float p2[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int i = 32 * g + 8 * q + e;
+                            p2[e] = (act && i >= lo && i <= r) ? B.pw[(r - i) & (kBlk - 1)] * s[i] : 0.f;
+                        }
+                        store8(4 * g + q, p2);
+                    }
+                }
+                publish();
+            }
+            const bool interior = (j >= 1) && (kt >= 0) && (kt <= t0 - (kBlk - 1));
+            unsigned act = 0xFu;
+            float pm[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
+            if (interior) {
+#pragma unroll
+                for (int i = 0; i < kBlk; ++i) pm[i & 7] = fmaxf(pm[i & 7], s[i]);
+            } else {
+                const int lo = max(0, t - W + 1) - kt, hi = t - kt;
+                const int wlo = __reduce_min_sync(0xffffffffu, lo), whi = __reduce_max_sync(0xffffffffu, hi);
+                act = 0;
+#pragma unroll
+                for (int g = 0; g < 4; ++g) {
+                    if (32 * g <= whi && 32 * g + 31 >= wlo) {
+                        act |= 1u << g;
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int i = 32 * g + e;
+                            s[i] = (i >= lo && i <= hi) ? s[i] : -INFINITY;
+                            pm[e & 7] = fmaxf(pm[e & 7], s[i]);
+                        }
+                    }
+                }
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * sc;
+            const bool grow = mx > m + kRescale;
+            // The P slot must be free before it is written; that also means every
+            // earlier P V product is in O, so O may be rescaled now.
+            ok = __all_sync(0xffffffffu, slot_free());
+            if (!ok) break;
+            if (__any_sync(0xffffffffu, grow) && use > (has_l2 && n == 0 ? 1u : 0u)) {
+                tc_fence_after();
+                const float f = grow ? ex2(m - mx) : 1.f;
+#pragma unroll 1
+                for (int cc = 0; cc < DV; cc += 32) {
+                    float v[32];
+                    tmem_ld32(tm + lrow + C::COL_O + cc, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= f;
+                    tmem_st32(tm + lrow + C::COL_O + cc, v);
+                }
+                tmem_wait_st();
+            }
+            if (grow) {
+                l *= ex2(m - mx);
+                m = mx;
+            }
+            const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m, -m);
+            float2 ps[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) ps[u] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                if (act & (1u << g)) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int i = 32 * g + e;
+                        float2 x = fma2(make_float2(s[i], s[i + 1]), sc2, nm2);
+                        x.x = ex2(x.x);
+                        x.y = ex2(x.y);
+                        s[i] = x.x;
+                        s[i + 1] = x.y;
+                        ps[(e >> 1) & 3] = add2(ps[(e >> 1) & 3], x);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[32 * g + e] = 0.f;
+                }
+            }
+            l += ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
+#pragma unroll
+            for (int c = 0; c < 16; ++c) store8(c, &s[8 * c]);
+            publish();
+        }
+        // ------------------------------------------------ epilogue
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&B.o_done, 0));
+        if (ok) {
+            tc_fence_after();
+            const float inv_l = l > 0.f ? 1.0f / l : 0.f;
+            const float sg = 1.0f / (1.0f + expf(-gate[h]));
+            const float decay = powf(lam[h], (float)(r + 1));
+            __nv_bfloat16 *yr = y + ((size_t)bh * T + t) * DV;
+#pragma unroll 1
+            for (int cc = 0; cc < DV; cc += 16) {
+                float o[16], qa[16], o2[16];
+                tmem_ld16(tm + lrow + C::COL_O + cc, o);
+                tmem_ld16(tm + lrow + cc, qa);
+                if (has_l2) tmem_ld16(tm + lrow + C::COL_O2 + cc, o2);
+                tmem_wait_ld();
+                if (t < T) {
+                    uint32_t pk[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float v2[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int e = 2 * i + u;
+                            v2[u] = fmaf(o[e], inv_l, sg * fmaf(decay, qa[e], has_l2 ? o2[e] : 0.f));
+                        }
+                        pk[i] = pack_bf16(v2[0], v2[1]);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(yr + cc);
+                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                }
+            }
+        }
+        if (!ok && lane == 0) atomicOr(&g_status, kStFwdSoftmax);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) tmem_dealloc(tm, C::TCOLS);
+}
+
 struct Ws {
     __nv_bfloat16 *Aloc, *Cbf;
     float *Lfin;
@@ -796,7 +1177,20 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
     tc_l2_carry_kernel<<<dim3(ceil_div(DK * DV / 4, 128), BH), 128, 0, st>>>(w.Lfin, g.nseg, g.L, T, DK * DV, H,
                                                                             lam, w.Cbf, A_final);
     if ((rc = launched("tc_l2_carry"))) return rc;
-    {
+    if constexpr (DK == 64 && DV == 64) {
+        using Cfg = FwdRow<DK, DV>;
+        auto kern = tc_fwd_row_kernel<DK, DV>;
+        static_assert(Cfg::OFF_BARS + sizeof(FwdRowBars) <= 228 * 1024 / 2 - 1024, "two CTAs per SM");
+        const int smem = (int)(Cfg::OFF_BARS + sizeof(FwdRowBars));
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return cuda_fail(e, "tc_fwd_row smem attribute");
+        prof_begin(st);
+        kern<<<dim3(g.nch, BH), 192, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, lam, eta,
+                                                  gate, scale, (__nv_bfloat16 *)y);
+        rc = launched("tc_fwd_row");
+        prof_end(st);
+        return rc;
+    } else {
         using Cfg = Fwd<DK, DV>;
         auto kern = tc_fwd_kernel<DK, DV>;
         static_assert(sizeof(FwdBars) <= 3072, "barriers block");
@@ -805,7 +1199,7 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         if (e != cudaSuccess) return cuda_fail(e, "tc_fwd smem attribute");
         prof_begin(st);
         kern<<<dim3(g.nch, BH), 320, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, lam, eta,
-                                                       gate, scale, (__nv_bfloat16 *)y);
+                                                  gate, scale, (__nv_bfloat16 *)y);
         rc = launched("tc_fwd");
         prof_end(st);
         return rc;
