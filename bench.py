@@ -407,7 +407,7 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
         step()
     ms, dom = timed_steps(step, K, flush, torch, prof=True, binding=binding)
     fl, by = delta_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], 2)
-    summarize(name, d["B"] * d["T"], ms, fl, by, "sustained", "delta_state", dom)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "sustained", "delta_chain", dom)
     del q, k, v, beta, y, ws
 
     name = "bdh_fp32_B2_H4_T2048_N16384_dv256"

@@ -4,6 +4,8 @@ Each case allocates a few hundred MB at most, runs the call four times on
 cuda:0 and checks the device status, so an ``ncu`` capture of one launch
 (``-s 2 -c 1``) sees warm caches and ends quickly:
 
+    python -m outer_product_associative_chunked_b300.profile_cases prefill
+    python -m outer_product_associative_chunked_b300.profile_cases prefill_long
     python -m outer_product_associative_chunked_b300.profile_cases decode
     python -m outer_product_associative_chunked_b300.profile_cases delta
     python -m outer_product_associative_chunked_b300.profile_cases sparse
@@ -18,6 +20,22 @@ import sys
 import torch
 
 from . import binding, synth
+
+
+def prefill(B=4, H=8, T=4096, d=64, W=512, reps=4):
+    """Tensor Cache prefill, bf16 (the B=4 H=8 T=4096 d=64 W=512 workload)."""
+    inp = synth.tc_inputs(B, H, T, d, d, W, dtype="bf16", seed=1)
+    q, k, v, lam, eta, gate = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate)]
+    y = torch.empty_like(v)
+    ws = torch.empty(binding.tc_layer_forward_workspace_size(B, H, T, d, d, W, torch.bfloat16),
+                     dtype=torch.uint8, device="cuda")
+    for _ in range(reps):
+        binding.tc_layer_forward(q, k, v, lam, eta, gate, W, out=y, workspace=ws)
+
+
+def prefill_long(B=1, H=4, T=8192, d=128, W=2048, reps=4):
+    """Tensor Cache prefill, bf16, the long-context shape with fewer heads and tokens."""
+    prefill(B, H, T, d, W, reps)
 
 
 def decode(S=16, H=16, W=2048, d=128, reps=4):
@@ -58,7 +76,8 @@ def sparse(B=1, H=2, T=2048, N=16384, dv=256, reps=4):
         binding.sparse_linattn_forward(q, k, v, out=y, workspace=ws)
 
 
-CASES = {"decode": decode, "delta": delta, "sparse": sparse}
+CASES = {"prefill": prefill, "prefill_long": prefill_long, "decode": decode, "delta": delta,
+         "sparse": sparse}
 
 
 def main(argv=None):
