@@ -3,8 +3,9 @@
 
 Default run (N=1): the Tensor Cache bf16 prefill workload (B=4, H=8, T=4096,
 d=64, W=512) as the headline step -- one tc_layer_forward over the batch --
-timed with CUDA events after warm-up, an L2 flush (256 MiB write) between
-timed steps, plus:
+captured once into a CUDA graph and replayed, each replay timed with CUDA
+events after warm-up and an L2 flush (256 MiB write) between timed steps (the
+same step as eager Python calls is reported under "eager"), plus:
   * roofline of the dominant kernel, timed live through the library's
     profiling events, against MEASURED_PEAKS.json;
   * e2e: the same step through the public binding from pinned host buffers,
@@ -254,6 +255,39 @@ def load_traffic(kernel):
     return d["dram_bytes_per_launch"] if h == d["source_sha256_16"] else None
 
 
+def timed_graph_steps(step, K, flush, torch, binding):
+    """The step captured once into a CUDA graph, its dominant kernel bracketed
+    by the library's event nodes, then K replays, each after an L2 flush
+    (untimed) and each timed with CUDA events on the replay stream.
+    Returns (per-step ms, dominant-kernel ms, kernels per step)."""
+    ka, kb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for ev in (ka, kb, e0, e1):   # torch creates the CUDA event on first record
+        ev.record()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    binding.profile_events(ka, kb)
+    l0 = binding.kernel_launches()
+    try:
+        with torch.cuda.graph(graph):
+            step()
+    finally:
+        binding.profile_events(None, None)
+    per_step = binding.kernel_launches() - l0
+    graph.replay()
+    torch.cuda.synchronize()
+    step_ms, dom_ms = [], []
+    for _ in range(K):
+        flush.zero_()
+        e0.record()
+        graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+        dom_ms.append(ka.elapsed_time(kb))
+    return step_ms, dom_ms, per_step
+
+
 # ----------------------------------------------------------------- our arm
 def tc_prefill_setup(name, rank, torch, binding, synth):
     w = synth.WORKLOADS[name]
@@ -282,11 +316,15 @@ def bench_headline(args, rank, world, torch, binding, synth, peaks, peak_src, fl
         time.sleep(0.3)
     barrier(world)
     torch.cuda.synchronize()
-    l0 = binding.kernel_launches()
+    # Eager calls first (host enqueue included), then the same step replayed
+    # from a CUDA graph; the graph replay is the reported step.
+    eager_ms, eager_dom = timed_steps(step, args.steps, flush, torch, prof=True, binding=binding)
+    barrier(world)
+    torch.cuda.synchronize()
     t0 = time.time()
-    step_ms, dom_ms = timed_steps(step, args.steps, flush, torch, prof=True, binding=binding)
+    step_ms, dom_ms, per_step = timed_graph_steps(step, args.steps, flush, torch, binding)
     t1 = time.time()
-    launches = binding.kernel_launches() - l0
+    launches = per_step * args.steps
     barrier(world)
     if sampler:
         time.sleep(0.3)
@@ -302,6 +340,9 @@ def bench_headline(args, rank, world, torch, binding, synth, peaks, peak_src, fl
     roof["kernel"] = "tc_fwd (fused window softmax + L2 read + gate)"
     roof["kernel_ms"] = dom_s * 1e3
     roof["peak_source"] = f"of {peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "of fallback"
+    eager = {"ms_per_step": statistics.mean(eager_ms), "kernel_ms": statistics.mean(eager_dom),
+             "value": tokens / (statistics.mean(eager_ms) / 1e3),
+             "note": "same step as eager calls from Python; host enqueue time is included"}
     clocks = sampler.summary(t0, t1) if sampler else None
 
     # e2e through the public binding from pinned host memory
@@ -330,7 +371,8 @@ def bench_headline(args, rank, world, torch, binding, synth, peaks, peak_src, fl
                "ms_per_step": statistics.mean(e_ms)}
     del ws
     return {"value": value, "ms_per_step": ms_per_step, "roofline": roof, "clocks": clocks,
-            "e2e": e2e, "gpu_launches": launches, "tokens_per_step": tokens, "dims": d, "inp": inp}
+            "e2e": e2e, "gpu_launches": launches, "tokens_per_step": tokens, "dims": d, "inp": inp,
+            "eager": eager}
 
 
 def bench_extras(args, torch, binding, synth, peaks, flush):
@@ -532,9 +574,10 @@ def main(argv=None):
                 "config": {"workload": args.workload, **{k: v for k, v in d.items() if k != "dtype"},
                            "input_dtype": d["dtype"], "tokens_per_step": res["tokens_per_step"],
                            "l2": "256 MiB buffer written between timed steps (untimed)",
+                           "launch": "step captured once into a CUDA graph and replayed",
                            "parallelism": f"replicas x{world} (independent batch per GPU)"},
                 "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
-                "gpu_launches": res["gpu_launches"], "clocks": res["clocks"]}
+                "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "eager": res["eager"]}
         if extras is not None:
             line["workloads"] = extras
         print(json.dumps(line), flush=True)

@@ -221,10 +221,13 @@ int opam_device_status(int clear);
  * tc_decode_step, the sequential state pass of delta_rule_forward and the
  * chunked read of sparse_linattn_forward (summed over its launches: `start`
  * goes before the first, `stop` after the last).  Pass NULL, NULL to stop.
- * Events stay owned by the caller.  Returns OPAM_OK.
+ * The records are external, so a call captured into a CUDA graph keeps them
+ * as event nodes that fire on every replay.  Events stay owned by the caller.
+ * Returns OPAM_OK.
  *
  * opam_kernel_launches: number of kernels this library has launched in the
- * process so far (all threads). */
+ * process so far (all threads); launches recorded into a CUDA graph count
+ * once, at capture. */
 int opam_profile_events(void *start, void *stop);
 uint64_t opam_kernel_launches(void);
 

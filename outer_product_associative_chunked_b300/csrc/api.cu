@@ -5,6 +5,9 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <map>
+#include <mutex>
+#include <utility>
 
 #include "opam_internal.cuh"
 
@@ -25,16 +28,54 @@ int cuda_fail(cudaError_t e, const char *where) {
     return OPAM_ERR_CUDA;
 }
 
+int set_smem_limit(const void *func, int bytes, const char *where) {
+    // cudaFuncSetAttribute is a driver round trip; it is needed once per
+    // kernel and device (and again only if a call needs more shared memory).
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, int> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, where);
+    std::lock_guard<std::mutex> lock(mu);
+    int &have = done[{func, dev}];
+    if (have >= bytes) return OPAM_OK;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, where);
+    have = bytes;
+    return OPAM_OK;
+}
+
+int device_sm_count() {
+    static std::atomic<int> cache[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+    if (dev < 0 || dev >= 64) dev = 0;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 static std::atomic<uint64_t> g_launches{0};
 static thread_local cudaEvent_t g_prof_start = nullptr;
 static thread_local cudaEvent_t g_prof_stop = nullptr;
 
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+// Under stream capture the records are external, so that the captured graph
+// keeps its two event nodes; otherwise they are ordinary records.
+static void prof_record(cudaEvent_t ev, cudaStream_t s) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+        cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal);
+    else
+        cudaEventRecord(ev, s);
+}
 void prof_begin(cudaStream_t s) {
-    if (g_prof_start) cudaEventRecord(g_prof_start, s);
+    if (g_prof_start) prof_record(g_prof_start, s);
 }
 void prof_end(cudaStream_t s) {
-    if (g_prof_stop) cudaEventRecord(g_prof_stop, s);
+    if (g_prof_stop) prof_record(g_prof_stop, s);
 }
 
 namespace {

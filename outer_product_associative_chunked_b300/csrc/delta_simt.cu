@@ -183,15 +183,13 @@ int launch(const void *q, const void *k, const void *v, const float *beta, int B
     // the prep kernel's tail rows stay inside their own unit.
     const size_t smem1 = sizeof(float) * (2 * C * (DK + 1) + C * (DK + DV) + C * (C + 1) + C);
     auto k1 = delta_prep_kernel<T, DK, DV>;
-    cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem1);
-    if (e != cudaSuccess) return cuda_fail(e, "delta_prep smem attribute");
+    if (int rc_ = set_smem_limit((const void *)k1, (int)smem1, "delta_prep smem attribute")) return rc_;
     k1<<<dim3(nch, BH), kThreads, smem1, s>>>((const T *)q, (const T *)k, (const T *)v, beta, T_, C,
                                              l.Wt, l.Ut, l.P);
     if (int rc = launched("delta_prep")) return rc;
     const size_t smem2 = sizeof(float) * (DK * kSlice + 3 * C * (DK + 1) + C * kSlice + C * (C + 1));
     auto k2 = delta_state_kernel<T, DK, DV>;
-    e = cudaFuncSetAttribute(k2, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem2);
-    if (e != cudaSuccess) return cuda_fail(e, "delta_state smem attribute");
+    if (int rc_ = set_smem_limit((const void *)k2, (int)smem2, "delta_state smem attribute")) return rc_;
     prof_begin(s);
     k2<<<dim3(BH, DV / kSlice), kThreads, smem2, s>>>((const T *)q, (const T *)k, l.Wt, l.Ut, l.P, T_,
                                                      C, nch, S0, S_out, (T *)y);

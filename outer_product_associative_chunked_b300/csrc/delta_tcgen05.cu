@@ -522,8 +522,7 @@ int run(const void *q, const void *k, const void *v, const float *beta, int BH, 
     {
         auto kern = delta_prep_kernel<DK>;
         const int smem = (int)PrepCfg<DK>::SMEM;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return cuda_fail(e, "delta_prep smem attribute");
+        if (int rc_ = set_smem_limit((const void *)kern, smem, "delta_prep smem attribute")) return rc_;
         kern<<<dim3(nch, BH), 128, smem, st>>>(mq, mk, beta, T, nch, w.P, w.G, w.W);
         if ((rc = launched("delta_prep"))) return rc;
     }
@@ -531,8 +530,7 @@ int run(const void *q, const void *k, const void *v, const float *beta, int BH, 
         using Cfg = ChainCfg<DK>;
         auto kern = delta_chain_kernel<DK>;
         const int smem = (int)(Cfg::OFF_BARS + sizeof(ChainBars) + 16);
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return cuda_fail(e, "delta_chain smem attribute");
+        if (int rc_ = set_smem_limit((const void *)kern, smem, "delta_chain smem attribute")) return rc_;
         prof_begin(st);
         kern<<<BH, 192, smem, st>>>(mq, mk, mv, mp, mg, mw, T, nch, S0, S_out, (__nv_bfloat16 *)y);
         rc = launched("delta_chain");

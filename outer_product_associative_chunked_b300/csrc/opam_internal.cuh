@@ -12,6 +12,11 @@ namespace opam {
 // ---------------------------------------------------------------- errors
 void set_error(const char *fmt, ...);
 int cuda_fail(cudaError_t e, const char *where);
+// Raise a kernel's dynamic shared-memory limit to `bytes` (once per kernel
+// and device; later calls that need no more are free).
+int set_smem_limit(const void *func, int bytes, const char *where);
+// Number of SMs of the current device (cached).
+int device_sm_count();
 
 // ---------------------------------------------------------------- instrumentation
 // count_launch(): one kernel enqueued.  prof_begin / prof_end bracket the

@@ -185,8 +185,7 @@ int launch(const float *q, const float *k, const float *v, int BH, int T, int N,
     compact_rows_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(q, rows, N, l.qidx, l.qval, l.qcnt);
     if (int rc = launched("compact q")) return rc;
     const size_t smem = sizeof(float) * (size_t)N;
-    e = cudaFuncSetAttribute(sparse_read_kernel<DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "sparse_read smem attribute");
+    if (int rc_ = set_smem_limit((const void *)sparse_read_kernel<DV>, (int)smem, "sparse_read smem attribute")) return rc_;
     prof_begin(s);
     for (int c0 = 0; c0 < T; c0 += kC) {
         const int n = min(kC, T - c0);

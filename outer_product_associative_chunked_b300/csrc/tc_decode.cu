@@ -308,8 +308,7 @@ int launch(const opam_tc_state *st, const void *q, const void *k, const void *v,
     const Parts pr = carve(ws, SH, g.nsplit, DV);
     const size_t smem = sizeof(float) * (DK + DK + DV + (kThreads / 32) * DV + 2 * (kThreads / 32) + g.keys_per_split);
     auto k1 = tc_decode_partial_kernel<T, DK, DV>;
-    cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "tc_decode smem attribute");
+    if (int rc_ = set_smem_limit((const void *)k1, (int)smem, "tc_decode smem attribute")) return rc_;
     prof_begin(s);
     k1<<<dim3(SH, g.nsplit), kThreads, smem, s>>>(
         (const T *)st->ring_k, (const T *)st->ring_v, st->A, st->pos, (const T *)q, (const T *)k,

@@ -278,8 +278,7 @@ int launch_fwd(const void *q, const void *k, const void *v, int BH, int T_, int 
                const float *Abuf, int nch, void *y, cudaStream_t s) {
     auto kern = tc_fwd_simt_kernel<T, DK, DV>;
     const size_t smem = FwdSmem<DK, DV>::kBytes;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "tc_fwd_simt smem attribute");
+    if (int rc_ = set_smem_limit((const void *)kern, (int)smem, "tc_fwd_simt smem attribute")) return rc_;
     prof_begin(s);
     kern<<<dim3(nch, BH), 256, smem, s>>>((const T *)q, (const T *)k, (const T *)v, T_, W, H, lam,
                                           eta, gate, scale, Abuf, nch, (T *)y);
@@ -309,9 +308,7 @@ int run(const void *q, const void *k, const void *v, int B, int H, int T_, int d
     float *buf = (float *)ws;
     {
         const size_t smem = sizeof(float) * kC * (dk + dv);
-        cudaError_t e = cudaFuncSetAttribute(tc_chunk_delta_kernel<T>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return cuda_fail(e, "tc_chunk_delta smem attribute");
+        if (int rc_ = set_smem_limit((const void *)tc_chunk_delta_kernel<T>, (int)smem, "tc_chunk_delta smem attribute")) return rc_;
         tc_chunk_delta_kernel<T><<<dim3(nch, BH), 256, smem, s>>>((const T *)k, (const T *)v, T_, dk,
                                                                   dv, W, H, lam, eta, buf, nch);
         if (int rc = launched("tc_chunk_delta")) return rc;

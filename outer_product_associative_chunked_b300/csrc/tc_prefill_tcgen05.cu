@@ -743,46 +743,67 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     if (warp == 9) tmem_dealloc(tm, 512);
 }
 
-// --------------------------------------------------------------------- fused forward, one row per thread
+// --------------------------------------------------------------------- fused forward, half a row per thread
 // Variant for d_k = d_v = 64 sized so that two CTAs share an SM (256 TMEM
-// columns, ~113 KB of shared memory): while one CTA waits on its loads, MMAs
-// or prologue/epilogue, the other runs its softmax.  192 threads: warps 0-3
-// own one query row each (softmax over all 128 keys of a tile, epilogue),
-// warp 4 issues TMA loads and scales the segment carry, warp 5 issues the
-// MMAs.  TMEM: S [0,128) (q A_j lands there after the last tile), O [128,
-// 128+DV), O2 [128+DV, 128+2DV).  One P slot, two K/V stages.
+// columns, ~99 KB of shared memory): while one CTA waits on its loads, MMAs
+// or prologue/epilogue, the other runs its softmax.  288 threads: warp w < 8
+// owns rows 32 (w % 4) .. +31 (its TMEM lane quarter) and keys 64 (w / 4) ..
+// +63 of every tile -- half a row per thread; the two halves of a row agree
+// on the row maximum (and, in the shifted chunk, on the row sum) through
+// shared memory.  One thread of warp 8 issues the TMA loads and the MMAs.
+// TMEM: S [0,128) (after the last tile q A_j^loc lands in columns [0,DV) and
+// q A_{gL} in [DV,2DV)), O [128, 128+DV), P [128+DV, 128+DV+64) -- P
+// is written by the softmax threads with tcgen05.st as packed bf16 and is
+// the A operand of O += P V, so it never touches shared memory.
+//
+// The L2 part of the block (keys of the shifted chunk with l <= i) is folded
+// into O: the shifted chunk is processed last, when the row's softmax sum L
+// is final, and its decayed scores enter P as L sigmoid(g) eta lambda^(i-l)
+// <q_i, k'_l>, next to its softmax probabilities (keys l > i).  Then
+// O / L = y_local + sigmoid(g) sum_l eta lambda^(i-l) <q_i,k'_l> v'_l and the
+// epilogue adds sigmoid(g) lambda^(i+1) q A_j with A_j = A_j^loc + c A_{gL}.
+//
+// Stages: 3 K slots (the last also takes A_j^loc and A_{gL}) and 2 V slots.
+// The issuing thread learns that a slot is free from the softmax side: S(n)
+// has been read once its S columns are released, and P V(n-1) has completed
+// once P(n) has been published (P(n) is written only after it).
 template <int DK, int DV>
 struct FwdRow {
     static constexpr uint32_t QBYTES = kBlk * DK * 2;
     static constexpr uint32_t KBYTES = kBlk * DK * 2;  // also holds A_j^loc
     static constexpr uint32_t VBYTES = kBlk * DV * 2;  // also holds the segment carry
-    static constexpr uint32_t PBYTES = kBlk * kBlk * 2;
-    static constexpr int NST = 2;
+    static constexpr int NSK = 3, NSV = 2;
     static constexpr uint32_t OFF_K = QBYTES;
-    static constexpr uint32_t OFF_P = QBYTES + NST * (KBYTES + VBYTES);
-    static constexpr uint32_t OFF_BARS = OFF_P + PBYTES;
-    static constexpr uint32_t COL_O = 128, COL_O2 = 128 + DV;
-    static constexpr uint32_t TCOLS = 128 + 2 * DV <= 256 ? 256 : 512;
+    static constexpr uint32_t OFF_V = OFF_K + NSK * KBYTES;
+    static constexpr uint32_t OFF_BARS = OFF_V + NSV * VBYTES;
+    static_assert(2 * DK * DV * 2 <= KBYTES, "A_j^loc and the carry share a K slot");
+    static constexpr uint32_t COL_O = 128, COL_P = 128 + DV;
+    static constexpr uint32_t TCOLS = 256;
+    static_assert(COL_P + kBlk / 2 <= TCOLS, "TMEM budget");
+    static_assert(DV == 64, "one 32-column half of O per softmax thread");
     static constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);
     static constexpr uint32_t ID_PV = idesc_bf16_f32(128, DV, false, true);
 };
 
 struct FwdRowBars {
-    uint64_t q_full, k_full[2], v_full[2], kv_empty[2];
-    uint64_t s_full, s_empty, p_full, p_empty, c_ready, o_done, drain;
+    uint64_t q_full, k_full[3], v_full[2];
+    uint64_t s_full, s_empty, p_full, p_empty, pv2_done, o_done, drain;
+    uint64_t xchg[4];      // per lane quarter: the two halves of its rows meet here
     uint32_t tbase;
-    float pw[kBlk];  // eta lambda^d
+    float lam_h;
+    float pwz[32 + kBlk];  // [32 + d] = eta lambda^d for d >= 0; 0 for d < 0
+    float xbuf[2][2][kBlk];  // [exchange parity][half][row]
 };
 
 template <int DK, int DV>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(288, 2)
 tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ma,
                   const __grid_constant__ CUtensorMap mc, int T, int W, int H, int nch, int nseg, int L,
                   const float *__restrict__ lam, const float *__restrict__ eta,
                   const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y) {
     using C = FwdRow<DK, DV>;
-    constexpr int NST = C::NST;
+    constexpr int NSK = C::NSK, NSV = C::NSV;
     extern __shared__ __align__(1024) unsigned char sm[];
     FwdRowBars &B = *reinterpret_cast<FwdRowBars *>(sm + C::OFF_BARS);
     if ((smem_u32(sm) & 1023u) != 0) {
@@ -798,319 +819,368 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     const int j_first = (-kt0 - (kBlk - 1) > 0) ? (-kt0) / kBlk : 0;
     const int ntiles = nt_total - j_first;
     const bool has_l2 = (j_first == 0);
+    // Key tile j covers keys kt0 + 128 j ..; with an L2 part the tiles run
+    // 1, 2, .., nt-1 and the shifted chunk (j = 0) comes last.
+    auto tile_j = [&](int n) { return has_l2 ? (n + 1 < ntiles ? n + 1 : 0) : j_first + n; };
 
-    if (warp == 5) tmem_alloc(&B.tbase, C::TCOLS);
-    if (tid == 0) {
-        mbar_init(&B.q_full, 1);
-        for (int s = 0; s < NST; ++s) {
-            mbar_init(&B.k_full[s], 1);
-            mbar_init(&B.v_full[s], 1);
-            mbar_init(&B.kv_empty[s], 1);
+    const uint32_t sQ = smem_u32(sm);
+    const uint32_t sK0 = sQ + C::OFF_K;
+    const uint32_t sV0 = sQ + C::OFF_V;
+    const int nkload = ntiles + (has_l2 ? 1 : 0);  // K slot loads; the last is A_j^loc + carry
+    auto load_k = [&](int i) {
+        unsigned char *kd = sm + C::OFF_K + (i % NSK) * C::KBYTES;
+        uint64_t *bar = &B.k_full[i % NSK];
+        if (i < ntiles) {
+            const int kt = kt0 + kBlk * tile_j(i);
+            mbar_expect_tx(bar, C::KBYTES);
+#pragma unroll
+            for (int b = 0; b < DK / 64; ++b) tma_load_3d(kd + b * 16384, &mk, bar, 64 * b, kt, bh);
+        } else {
+            mbar_expect_tx(bar, 2 * DK * DV * 2);
+#pragma unroll
+            for (int b = 0; b < DV / 64; ++b) {
+                tma_load_3d(kd + b * (DK * 128), &ma, bar, 64 * b, 0, bh * nch + jq);
+                tma_load_3d(kd + DK * DV * 2 + b * (DK * 128), &mc, bar, 64 * b, 0, bh * nseg + seg);
+            }
         }
+    };
+    auto load_v = [&](int i) {
+        unsigned char *vd = sm + C::OFF_V + (i % NSV) * C::VBYTES;
+        uint64_t *bar = &B.v_full[i % NSV];
+        mbar_expect_tx(bar, C::VBYTES);
+#pragma unroll
+        for (int b = 0; b < DV / 64; ++b) tma_load_3d(vd + b * 16384, &mv, bar, 64 * b, kt0 + kBlk * tile_j(i), bh);
+    };
+    if (warp == 8 && lane == 0) {  // barriers, then the first loads, before the CTA-wide sync
+        mbar_init(&B.q_full, 1);
+        for (int s = 0; s < NSK; ++s) mbar_init(&B.k_full[s], 1);
+        for (int s = 0; s < NSV; ++s) mbar_init(&B.v_full[s], 1);
         mbar_init(&B.s_full, 1);
-        mbar_init(&B.s_empty, 4);
-        mbar_init(&B.p_full, 4);
+        mbar_init(&B.s_empty, 8);
+        mbar_init(&B.p_full, 8);
         mbar_init(&B.p_empty, 1);
-        mbar_init(&B.c_ready, 1);
+        mbar_init(&B.pv2_done, 1);
         mbar_init(&B.o_done, 1);
         mbar_init(&B.drain, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&B.xchg[i], 2);
         mbar_fence_init();
+        tma_prefetch_desc(&mq);
+        tma_prefetch_desc(&mk);
+        tma_prefetch_desc(&mv);
+        mbar_expect_tx(&B.q_full, C::QBYTES);
+#pragma unroll
+        for (int b = 0; b < DK / 64; ++b) tma_load_3d(sm + b * 16384, &mq, &B.q_full, 64 * b, t0, bh);
+        for (int i = 0; i < NSK && i < nkload; ++i) load_k(i);
+        for (int i = 0; i < NSV && i < ntiles; ++i) load_v(i);
     }
-    if (tid < kBlk) B.pw[tid] = eta[h] * powf(lam[h], (float)tid);
+    __syncwarp();
+    if (warp == 8) tmem_alloc(&B.tbase, C::TCOLS);
+    if (tid == 0) B.lam_h = lam[h];
+    if (tid < 32) B.pwz[tid] = 0.f;
+    if (tid < kBlk) B.pwz[32 + tid] = eta[h] * powf(lam[h], (float)tid);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = B.tbase;
-    const uint32_t sQ = smem_u32(sm);
-    const uint32_t sK0 = sQ + C::OFF_K;
-    const uint32_t sP = sQ + C::OFF_P;
 
-    if (warp == 4) {
-        // ------------------------------------------------ TMA producer
-        bool ok = true;
-        const int sA = ntiles % NST;
+    if (warp == 8) {
+        // ------------------------------------------------ TMA loads and MMAs (one thread)
         if (lane == 0) {
-            tma_prefetch_desc(&mq);
-            tma_prefetch_desc(&mk);
-            tma_prefetch_desc(&mv);
-            mbar_expect_tx(&B.q_full, C::QBYTES);
-#pragma unroll
-            for (int b = 0; b < DK / 64; ++b) tma_load_3d(sm + b * 16384, &mq, &B.q_full, 64 * b, t0, bh);
-            for (int n = 0; n <= ntiles && ok; ++n) {
-                const int s = n % NST;
-                if (n >= NST) ok = mbar_wait(&B.kv_empty[s], ((n / NST) - 1) & 1);
-                if (!ok) break;
-                unsigned char *kd = sm + C::OFF_K + s * (C::KBYTES + C::VBYTES);
-                if (n < ntiles) {
-                    const int kt = kt0 + kBlk * (j_first + n);
-                    mbar_expect_tx(&B.k_full[s], C::KBYTES);
-#pragma unroll
-                    for (int b = 0; b < DK / 64; ++b) tma_load_3d(kd + b * 16384, &mk, &B.k_full[s], 64 * b, kt, bh);
-                    mbar_expect_tx(&B.v_full[s], C::VBYTES);
-#pragma unroll
-                    for (int b = 0; b < DV / 64; ++b)
-                        tma_load_3d(kd + C::KBYTES + b * 16384, &mv, &B.v_full[s], 64 * b, kt, bh);
-                } else {
-                    mbar_expect_tx(&B.k_full[s], 2 * DK * DV * 2);
-#pragma unroll
-                    for (int b = 0; b < DV / 64; ++b) {
-                        tma_load_3d(kd + b * (DK * 128), &ma, &B.k_full[s], 64 * b, 0, bh * nch + jq);
-                        tma_load_3d(kd + C::KBYTES + b * (DK * 128), &mc, &B.k_full[s], 64 * b, 0, bh * nseg + seg);
-                    }
-                }
-            }
-            if (ok) ok = mbar_wait(&B.k_full[sA], (ntiles / NST) & 1);
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) {
-            const float c = powf(lam[h], (float)(kBlk * (jq - seg * L)));
-            const __nv_bfloat162 c2 = __floats2bfloat162_rn(c, c);
-            const uint32_t base = sK0 + sA * (C::KBYTES + C::VBYTES) + C::KBYTES;
-            for (int e = lane; e < DK * DV / 8; e += 32) {
-                uint32_t x[4];
-                ld_shared_v4(base + e * 16, x[0], x[1], x[2], x[3]);
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    __nv_bfloat162 hv = __hmul2(*reinterpret_cast<__nv_bfloat162 *>(&x[u]), c2);
-                    x[u] = *reinterpret_cast<uint32_t *>(&hv);
-                }
-                st_shared_v4(base + e * 16, x[0], x[1], x[2], x[3]);
-            }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.c_ready);
-        } else if (lane == 0) {
-            atomicOr(&g_status, kStFwdProducer);
-        }
-        __syncwarp();
-    } else if (warp == 5) {
-        // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
+            // descriptor halves: K-major Q / K tiles (k-step +32 B), MN-major V and A tiles (k-step +2048 B)
+            constexpr uint32_t HI = sdesc_hi(1024);
+            const uint32_t q_lo = sdesc_lo(sQ, 16);
+            const uint32_t k_lo = sdesc_lo(sK0, 16);
+            const uint32_t v_lo = sdesc_lo(sV0, 16384);
+            const uint32_t p_tm = tm + C::COL_P, o_tm = tm + C::COL_O;
             bool ok = mbar_wait(&B.q_full, 0);
-            uint32_t use = 0;
-            auto stage = [&](int s) { return sK0 + s * (C::KBYTES + C::VBYTES); };
-            auto qdesc = [&](int k) { return sdesc_sw128(sQ + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); };
-            auto pv = [&](int n) -> bool {
-                const int s = n % NST;
-                if (!mbar_wait(&B.v_full[s], (n / NST) & 1)) return false;
-                const int uses = (n == 0 && has_l2) ? 2 : 1;
-                for (int u = 0; u < uses; ++u) {
-                    if (!mbar_wait(&B.p_full, use & 1)) return false;
-                    tc_fence_after();
-                    const bool l2 = (uses == 2 && u == 0);
-                    const uint32_t dcol = l2 ? C::COL_O2 : C::COL_O;
+            auto pv = [&](int n) -> bool {  // O += P V of tile n, P from TMEM
+                if (!mbar_wait(&B.v_full[n % NSV], (n / NSV) & 1)) return false;
+                if (!mbar_wait(&B.p_full, n & 1)) return false;
+                // P(n) was written after P V(n-1) completed: V slot of tile n+1 is free
+                if (n >= 1 && n + 1 < ntiles) load_v(n + 1);
+                tc_fence_after();
+                const uint32_t vb = v_lo + (uint32_t)(n % NSV) * (C::VBYTES >> 4);
 #pragma unroll
-                    for (int k = 0; k < kBlk / 16; ++k)
-                        mma_ss(tm + dcol, sdesc_sw128(sP + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                               sdesc_sw128(stage(s) + C::KBYTES + k * 2048, 16384, 1024), C::ID_PV,
-                               (l2 ? k > 0 : (n > 0 || k > 0)) ? 1u : 0u);
-                    mma_commit(&B.p_empty);
-                    ++use;
-                }
-                mma_commit(&B.kv_empty[s]);
+                for (int k = 0; k < kBlk / 16; ++k)
+                    mma_ts_h(o_tm, p_tm + 8 * k, vb + k * (2048 >> 4), HI, C::ID_PV, (n > 0 || k > 0) ? 1u : 0u);
+                mma_commit(&B.p_empty);
                 return true;
             };
             for (int n = 0; n < ntiles && ok; ++n) {
-                const int s = n % NST;
-                ok = mbar_wait(&B.k_full[s], (n / NST) & 1);
-                if (ok && n >= 1) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
+                ok = mbar_wait(&B.k_full[n % NSK], (n / NSK) & 1);
+                if (ok && n >= 1) {
+                    ok = mbar_wait(&B.s_empty, (n - 1) & 1);
+                    // S(n-1) has been read, so its K slot is free
+                    if (ok && n - 1 + NSK < nkload) load_k(n - 1 + NSK);
+                }
                 if (!ok) break;
                 tc_fence_after();
+                const uint32_t kb = k_lo + (uint32_t)(n % NSK) * (C::KBYTES >> 4);
 #pragma unroll
-                for (int k = 0; k < DK / 16; ++k)
-                    mma_ss(tm, qdesc(k),
-                           sdesc_sw128(stage(s) + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024), C::ID_S,
-                           k > 0 ? 1u : 0u);
+                for (int k = 0; k < DK / 16; ++k) {
+                    const uint32_t off = (uint32_t)((k >> 2) * (16384 >> 4) + (k & 3) * 2);
+                    mma_ss_h(tm, q_lo + off, HI, kb + off, HI, C::ID_S, k > 0 ? 1u : 0u);
+                }
                 mma_commit(&B.s_full);
                 if (n >= 1) ok = pv(n - 1);
             }
             if (ok) ok = pv(ntiles - 1);
-            if (ok) {  // q (A_j^loc + c A_{gL}) into the S columns
-                const int n = ntiles, s = n % NST;
-                ok = mbar_wait(&B.k_full[s], (n / NST) & 1);
-                if (ok) ok = mbar_wait(&B.c_ready, 0);
-                if (ok) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
+            if (ok && has_l2) {
+                // O2 = P2 V' of the shifted chunk (the last tile): P2 over S columns [0,64),
+                // O2 into S columns [64,128); P2 was published with the tile's P.
+                const uint32_t vb = v_lo + (uint32_t)((ntiles - 1) % NSV) * (C::VBYTES >> 4);
+#pragma unroll
+                for (int k = 0; k < kBlk / 16; ++k)
+                    mma_ts_h(tm + 64, tm + 8 * k, vb + k * (2048 >> 4), HI, C::ID_PV, k > 0 ? 1u : 0u);
+                mma_commit(&B.pv2_done);
+                // then q A_j^loc into S columns [0,DV) and q A_{gL} into the P columns
+                const int i = ntiles;
+                ok = mbar_wait(&B.k_full[i % NSK], (i / NSK) & 1);
+                if (ok) ok = mbar_wait(&B.pv2_done, 0);
                 if (ok) {
                     tc_fence_after();
-                    const uint32_t aslot = stage(s);
+                    const uint32_t a_lo = sdesc_lo(sK0 + (i % NSK) * C::KBYTES, DK * 128);
 #pragma unroll
-                    for (int k = 0; k < DK / 16; ++k)
-                        mma_ss(tm, qdesc(k), sdesc_sw128(aslot + k * 2048, DK * 128, 1024), C::ID_PV,
-                               k > 0 ? 1u : 0u);
+                    for (int k = 0; k < DK / 16; ++k) {
+                        const uint32_t qo = (uint32_t)((k >> 2) * (16384 >> 4) + (k & 3) * 2);
+                        mma_ss_h(tm, q_lo + qo, HI, a_lo + k * (2048 >> 4), HI, C::ID_PV, k > 0 ? 1u : 0u);
+                    }
 #pragma unroll
-                    for (int k = 0; k < DK / 16; ++k)
-                        mma_ss(tm, qdesc(k), sdesc_sw128(aslot + C::KBYTES + k * 2048, DK * 128, 1024),
-                               C::ID_PV, 1u);
-                    mma_commit(&B.o_done);
+                    for (int k = 0; k < DK / 16; ++k) {
+                        const uint32_t qo = (uint32_t)((k >> 2) * (16384 >> 4) + (k & 3) * 2);
+                        mma_ss_h(p_tm, q_lo + qo, HI, a_lo + ((DK * DV * 2) >> 4) + k * (2048 >> 4), HI, C::ID_PV,
+                                 k > 0 ? 1u : 0u);
+                    }
                 }
             }
+            if (ok) mma_commit(&B.o_done);
             if (!ok) atomicOr(&g_status, kStFwdMma);
             mma_commit(&B.drain);
             mbar_wait(&B.drain, 0);
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------ softmax / epilogue (row r)
-        const int r = tid;
+        // ------------------------------------------------ softmax / epilogue (row r, key half hf)
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int r = 32 * q4 + lane;
         const int t = t0 + r;
-        const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+        const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
         const float sc = scale * kLog2e;
-        float m = kNegBig, l = 0.f;
-        uint32_t use = 0;
+        const float sig = 1.0f / (1.0f + expf(-gate[h]));
+        float m = kNegBig, l = 0.f;  // l: this half's share of the row sum
+        uint32_t xn = 0;             // exchanges so far (both halves count alike)
+        float Lrow = 0.f;  // the row's softmax sum over both halves, once known
         bool ok = true;
-        auto slot_free = [&]() -> bool {  // the P slot is free once the previous use's MMAs are done
-            return use == 0 || mbar_wait(&B.p_empty, (use - 1) & 1);
-        };
-        auto store8 = [&](int c, const float *p) {
-            st_shared_v4(sP + (c >> 3) * 16384 + sw128_off(r, c & 7), pack_bf16(p[0], p[1]), pack_bf16(p[2], p[3]),
-                         pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
-        };
-        auto publish = [&]() {
-            fence_async_smem();
-            tc_fence_before();
+        // Hand x to the other half of the row and return its value (NaN if
+        // the other half never arrives; ok is then cleared).
+        auto exchange = [&](float x) -> float {
+            const int p = xn & 1;
+            B.xbuf[p][hf][r] = x;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&B.p_full);
-            ++use;
+            if (lane == 0) mbar_arrive(&B.xchg[q4]);
+            const bool w = __all_sync(0xffffffffu, mbar_wait(&B.xchg[q4], p));
+            ++xn;
+            if (!w) {
+                ok = false;
+                return __int_as_float(0x7fffffff);
+            }
+            return B.xbuf[p][hf ^ 1][r];
         };
-        const int wrow_hi = warp * 32 + 31;
         for (int n = 0; n < ntiles && ok; ++n) {
-            const int j = j_first + n;
+            const int j = tile_j(n);
             const int kt = kt0 + kBlk * j;
+            const bool l2 = has_l2 && j == 0;
+            // softmax keys of this row in the tile: lo..hi (window t-W < pos <= t, pos >= 0)
+            const int lo = max(max(0, -kt), r + 1 - kBlk * j);
+            const int hi = min(kBlk - 1, r + W - kBlk * j);
+            const int lo_min = __reduce_min_sync(0xffffffffu, lo), lo_max = __reduce_max_sync(0xffffffffu, lo);
+            const int hi_min = __reduce_min_sync(0xffffffffu, hi), hi_max = __reduce_max_sync(0xffffffffu, hi);
+            // warp-uniform class of the 32 keys of chunk g: 0 none, 1 all, 2 per-row span
+            auto cls = [&](int g) -> int {
+                const int a = 32 * g, b = a + 31;
+                if (b < lo_min || a > hi_max || lo_min > hi_max) return 0;
+                if (a >= lo_max && b <= hi_min) return 1;
+                return 2;
+            };
             ok = __all_sync(0xffffffffu, mbar_wait(&B.s_full, n & 1));
             if (!ok) break;
             tc_fence_after();
-            float s[kBlk];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(tm + lrow + 32 * c, *reinterpret_cast<float(*)[32]>(&s[32 * c]));
+            float va[32], vb[32];  // keys 64 hf + 0..31 and 64 hf + 32..63
+            tmem_ld32(tm + lrow + 64 * hf, va);
+            tmem_ld32(tm + lrow + 64 * hf + 32, vb);
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.s_empty);
+            auto release_s = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&B.s_empty);
+            };
+            if (!l2) release_s();  // the shifted chunk re-reads S after its row-sum exchange
 
-            if (j == 0) {  // L2 part of the shifted chunk: keys l <= r at positions >= 0
-                const int lo = max(0, -kt);
-                ok = __all_sync(0xffffffffu, slot_free());
-                if (!ok) break;
+            // row maximum over the softmax keys, shared by the two halves
+            float mx = -INFINITY;
+            auto chunk_max = [&](const float(&v)[32], int g) {
+                const int c = cls(g);
+                if (c == 1) {
+                    float a0 = fmax3f(v[0], v[1], v[2]), a1 = fmax3f(v[8], v[9], v[10]);
+                    float a2 = fmax3f(v[16], v[17], v[18]), a3 = fmax3f(v[24], v[25], v[26]);
 #pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    const bool act = (32 * g <= wrow_hi) && (32 * g + 31 >= lo);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float p2[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int i = 32 * g + 8 * q + e;
-                            p2[e] = (act && i >= lo && i <= r) ? B.pw[(r - i) & (kBlk - 1)] * s[i] : 0.f;
-                        }
-                        store8(4 * g + q, p2);
+                    for (int e = 3; e < 8; e += 2) {
+                        const int e1 = e + 1 < 8 ? e + 1 : e;
+                        a0 = fmax3f(a0, v[e], v[e1]);
+                        a1 = fmax3f(a1, v[8 + e], v[8 + e1]);
+                        a2 = fmax3f(a2, v[16 + e], v[16 + e1]);
+                        a3 = fmax3f(a3, v[24 + e], v[24 + e1]);
                     }
-                }
-                publish();
-            }
-            const bool interior = (j >= 1) && (kt >= 0) && (kt <= t0 - (kBlk - 1));
-            unsigned act = 0xFu;
-            float pm[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) pm[u] = -INFINITY;
-            if (interior) {
-#pragma unroll
-                for (int i = 0; i < kBlk; ++i) pm[i & 7] = fmaxf(pm[i & 7], s[i]);
-            } else {
-                const int lo = max(0, t - W + 1) - kt, hi = t - kt;
-                const int wlo = __reduce_min_sync(0xffffffffu, lo), whi = __reduce_max_sync(0xffffffffu, hi);
-                act = 0;
-#pragma unroll
-                for (int g = 0; g < 4; ++g) {
-                    if (32 * g <= whi && 32 * g + 31 >= wlo) {
-                        act |= 1u << g;
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) {
-                            const int i = 32 * g + e;
-                            s[i] = (i >= lo && i <= hi) ? s[i] : -INFINITY;
-                            pm[e & 7] = fmaxf(pm[e & 7], s[i]);
-                        }
-                    }
-                }
-            }
-            const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
-                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * sc;
-            const bool grow = mx > m + kRescale;
-            // The P slot must be free before it is written; that also means every
-            // earlier P V product is in O, so O may be rescaled now.
-            ok = __all_sync(0xffffffffu, slot_free());
-            if (!ok) break;
-            if (__any_sync(0xffffffffu, grow) && use > (has_l2 && n == 0 ? 1u : 0u)) {
-                tc_fence_after();
-                const float f = grow ? ex2(m - mx) : 1.f;
-#pragma unroll 1
-                for (int cc = 0; cc < DV; cc += 32) {
-                    float v[32];
-                    tmem_ld32(tm + lrow + C::COL_O + cc, v);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= f;
-                    tmem_st32(tm + lrow + C::COL_O + cc, v);
-                }
-                tmem_wait_st();
-            }
-            if (grow) {
-                l *= ex2(m - mx);
-                m = mx;
-            }
-            const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m, -m);
-            float2 ps[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) ps[u] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                if (act & (1u << g)) {
+                    mx = fmax3f(mx, fmaxf(a0, a1), fmaxf(a2, a3));
+                } else if (c == 2) {
+                    const uint32_t bits = span_bits(lo - 32 * g, hi - 32 * g);
+                    float a0 = -INFINITY, a1 = -INFINITY;
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
-                        const int i = 32 * g + e;
-                        float2 x = fma2(make_float2(s[i], s[i + 1]), sc2, nm2);
+                        a0 = fmaxf(a0, ((bits >> e) & 1u) ? v[e] : -INFINITY);
+                        a1 = fmaxf(a1, ((bits >> (e + 1)) & 1u) ? v[e + 1] : -INFINITY);
+                    }
+                    mx = fmax3f(mx, a0, a1);
+                }
+            };
+            chunk_max(va, 2 * hf);
+            chunk_max(vb, 2 * hf + 1);
+            mx = fmaxf(mx, exchange(mx));
+            if (!ok) break;
+            const float mxs = mx * sc;
+            const bool grow = mxs > m + kRescale;
+            // P may be written (and O rescaled) once the previous P V has completed.
+            ok = __all_sync(0xffffffffu, n == 0 || mbar_wait(&B.p_empty, (n - 1) & 1));
+            if (!ok) break;
+            const float fO = grow ? ex2(m - mxs) : 1.f;  // O and l rescale when the maximum grows
+            const bool rescale = __any_sync(0xffffffffu, grow) && n > 0;
+            if (grow) {
+                l *= fO;
+                m = mxs;
+            }
+
+            const float2 sc2 = make_float2(sc, sc), nm2 = make_float2(-m, -m);
+            float2 acc[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) acc[u] = make_float2(0.f, 0.f);
+            auto tsum = [&]() {
+                return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
+            };
+            // softmax probabilities of chunk g, packed into P
+            auto chunk_soft = [&](const float(&v)[32], int g) {
+                uint32_t pk[16];
+                const int c = cls(g);
+                if (c == 1) {
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float2 x = fma2(make_float2(v[e], v[e + 1]), sc2, nm2);
                         x.x = ex2(x.x);
                         x.y = ex2(x.y);
-                        s[i] = x.x;
-                        s[i + 1] = x.y;
-                        ps[(e >> 1) & 3] = add2(ps[(e >> 1) & 3], x);
+                        acc[(e >> 1) & 1] = add2(acc[(e >> 1) & 1], x);
+                        pk[e >> 1] = pack_bf16(x.x, x.y);
+                    }
+                } else if (c == 2) {
+                    const uint32_t bits = span_bits(lo - 32 * g, hi - 32 * g);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        float2 x = fma2(make_float2(v[e], v[e + 1]), sc2, nm2);
+                        x.x = ((bits >> e) & 1u) ? ex2(x.x) : 0.f;
+                        x.y = ((bits >> (e + 1)) & 1u) ? ex2(x.y) : 0.f;
+                        acc[(e >> 1) & 1] = add2(acc[(e >> 1) & 1], x);
+                        pk[e >> 1] = pack_bf16(x.x, x.y);
                     }
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) s[32 * g + e] = 0.f;
+                    for (int e = 0; e < 16; ++e) pk[e] = 0u;
+                }
+                tmem_st16(tm + lrow + C::COL_P + 16 * g, pk);
+            };
+            if (!l2) {
+                chunk_soft(vb, 2 * hf + 1);
+                chunk_soft(va, 2 * hf);
+            } else {
+                // Shifted chunk: softmax keys (l > r) go to P as usual; the decayed L2
+                // scores eta lambda^(r-l) <q_r,k'_l> of keys l <= r go to P2, written over
+                // this tile's S columns [0,64) (both halves have read S: the max exchange
+                // came after the loads).
+                auto l2_chunk = [&](const float(&v)[32], int g) {
+                    if (g > q4) {  // no key l <= r in this chunk
+                        chunk_soft(v, g);
+                        const uint32_t z[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                        tmem_st8(tm + lrow + 16 * g, z);
+                        tmem_st8(tm + lrow + 16 * g + 8, z);
+                        return;
+                    }
+                    const uint32_t bits = g == q4 ? span_bits(lo - 32 * g, hi - 32 * g) : 0u;
+                    const float *pw = &B.pwz[32 + r - 32 * g];  // pw[-e] = eta lambda^(r-32g-e), 0 past r
+#pragma unroll
+                    for (int e0 = 0; e0 < 32; e0 += 16) {
+                        uint32_t ps[8], p2[8];
+#pragma unroll
+                        for (int e = e0; e < e0 + 16; e += 2) {
+                            float2 x = fma2(make_float2(v[e], v[e + 1]), sc2, nm2);
+                            x.x = ((bits >> e) & 1u) ? ex2(x.x) : 0.f;
+                            x.y = ((bits >> (e + 1)) & 1u) ? ex2(x.y) : 0.f;
+                            acc[(e >> 1) & 1] = add2(acc[(e >> 1) & 1], x);
+                            ps[(e - e0) >> 1] = pack_bf16(x.x, x.y);
+                            p2[(e - e0) >> 1] = pack_bf16(v[e] * pw[-e], v[e + 1] * pw[-e - 1]);
+                        }
+                        tmem_st8(tm + lrow + C::COL_P + 16 * g + e0 / 2, ps);
+                        tmem_st8(tm + lrow + 16 * g + e0 / 2, p2);
+                    }
+                };
+                l2_chunk(vb, 2 * hf + 1);
+                l2_chunk(va, 2 * hf);
+            }
+            if (rescale) {  // this half rescales O columns 32 hf .. +31 (P V(n-1) is complete)
+                tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < 32; cc += 16) {
+                    float o[16];
+                    tmem_ld16(tm + lrow + C::COL_O + 32 * hf + cc, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) o[i] *= fO;
+                    tmem_st16(tm + lrow + C::COL_O + 32 * hf + cc, reinterpret_cast<const uint32_t(&)[16]>(o));
                 }
             }
-            l += ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
-#pragma unroll
-            for (int c = 0; c < 16; ++c) store8(c, &s[8 * c]);
-            publish();
+            tmem_wait_st();
+            l += tsum();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.p_full);
         }
-        // ------------------------------------------------ epilogue
+        // ------------------------------------------------ epilogue: y = O / L + sigmoid(g) lambda^(i+1) q A_j
+        if (ok) Lrow = l + exchange(l);
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&B.o_done, 0));
         if (ok) {
             tc_fence_after();
-            const float inv_l = l > 0.f ? 1.0f / l : 0.f;
-            const float sg = 1.0f / (1.0f + expf(-gate[h]));
-            const float decay = powf(lam[h], (float)(r + 1));
-            __nv_bfloat16 *yr = y + ((size_t)bh * T + t) * DV;
+            const float inv_l = Lrow > 0.f ? 1.0f / Lrow : 0.f;
+            // sigmoid(g) lambda^(i+1), and c with A_j = A_j^loc + c A_{gL}
+            const float cq = has_l2 ? sig * powf(B.lam_h, (float)(r + 1)) : 0.f;
+            const float cA = has_l2 ? powf(B.lam_h, (float)(kBlk * (jq - seg * L))) : 0.f;
+            __nv_bfloat16 *yr = y + ((size_t)bh * T + t) * DV + 32 * hf;
 #pragma unroll 1
-            for (int cc = 0; cc < DV; cc += 16) {
-                float o[16], qa[16], o2[16];
-                tmem_ld16(tm + lrow + C::COL_O + cc, o);
-                tmem_ld16(tm + lrow + cc, qa);
-                if (has_l2) tmem_ld16(tm + lrow + C::COL_O2 + cc, o2);
-                tmem_wait_ld();
+            for (int cc = 0; cc < 32; cc += 16) {
+                float o[16], qa[16], qc[16], o2[16];
+                tmem_ld16(tm + lrow + C::COL_O + 32 * hf + cc, o);
+                if (has_l2) {  // m = O2 + lambda^(i+1) q (A_j^loc + c A_{gL}), times sigmoid(g)
+                    tmem_ld16(tm + lrow + 32 * hf + cc, qa);
+                    tmem_ld16(tm + lrow + C::COL_P + 32 * hf + cc, qc);
+                    tmem_ld16(tm + lrow + 64 + 32 * hf + cc, o2);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) qa[e] = fmaf(sig, o2[e], cq * fmaf(cA, qc[e], qa[e]));
+                } else {
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) qa[e] = 0.f;
+                }
                 if (t < T) {
                     uint32_t pk[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float v2[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int e = 2 * i + u;
-                            v2[u] = fmaf(o[e], inv_l, sg * fmaf(decay, qa[e], has_l2 ? o2[e] : 0.f));
-                        }
-                        pk[i] = pack_bf16(v2[0], v2[1]);
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        pk[i] = pack_bf16(fmaf(o[2 * i], inv_l, qa[2 * i]), fmaf(o[2 * i + 1], inv_l, qa[2 * i + 1]));
                     uint4 *dst = reinterpret_cast<uint4 *>(yr + cc);
                     dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
@@ -1121,7 +1191,7 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) tmem_dealloc(tm, C::TCOLS);
+    if (warp == 8) tmem_dealloc(tm, C::TCOLS);
 }
 
 struct Ws {
@@ -1145,11 +1215,7 @@ size_t ws_bytes(int BH, const Segments &g, int dk, int dv) {
            align_up(4 * (size_t)BH * g.nseg * dk * dv, 1024);
 }
 
-int num_sms() {
-    int dev = 0, n = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    return n > 0 ? n : 148;
-}
+int num_sms() { return device_sm_count(); }
 
 template <int DK, int DV>
 int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W, const float *lam,
@@ -1168,8 +1234,7 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
     {
         using SC = StateCfg<DK>;
         auto kern = tc_l2_state_kernel<DK, DV>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SC::SMEM);
-        if (e != cudaSuccess) return cuda_fail(e, "tc_l2_state smem attribute");
+        if (int rc_ = set_smem_limit((const void *)kern, (int)SC::SMEM, "tc_l2_state smem attribute")) return rc_;
         kern<<<dim3(DV / 64, g.nseg, BH), 192, SC::SMEM, st>>>(mk, mv, T, W, H, lam, eta, g.nch, g.L, w.Aloc,
                                                               w.Lfin);
         if ((rc = launched("tc_l2_state"))) return rc;
@@ -1182,10 +1247,9 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         auto kern = tc_fwd_row_kernel<DK, DV>;
         static_assert(Cfg::OFF_BARS + sizeof(FwdRowBars) <= 228 * 1024 / 2 - 1024, "two CTAs per SM");
         const int smem = (int)(Cfg::OFF_BARS + sizeof(FwdRowBars));
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return cuda_fail(e, "tc_fwd_row smem attribute");
+        if (int rc_ = set_smem_limit((const void *)kern, smem, "tc_fwd_row smem attribute")) return rc_;
         prof_begin(st);
-        kern<<<dim3(g.nch, BH), 192, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, lam, eta,
+        kern<<<dim3(g.nch, BH), 288, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, lam, eta,
                                                   gate, scale, (__nv_bfloat16 *)y);
         rc = launched("tc_fwd_row");
         prof_end(st);
@@ -1195,8 +1259,7 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         auto kern = tc_fwd_kernel<DK, DV>;
         static_assert(sizeof(FwdBars) <= 3072, "barriers block");
         const int smem = (int)(Cfg::OFF_BARS + sizeof(FwdBars));
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return cuda_fail(e, "tc_fwd smem attribute");
+        if (int rc_ = set_smem_limit((const void *)kern, smem, "tc_fwd smem attribute")) return rc_;
         prof_begin(st);
         kern<<<dim3(g.nch, BH), 320, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, lam, eta,
                                                   gate, scale, (__nv_bfloat16 *)y);

@@ -51,6 +51,14 @@ SMALL = [
     ("bf16", 1, 2, 640, 64, 64, 128),
     ("bf16", 1, 1, 700, 128, 128, 256),
     ("bf16", 1, 1, 150, 32, 128, 50),
+    # d = 64/64 (one-row-per-thread kernel): windows that are not a multiple
+    # of the 128-key tile, shorter than a tile, and sequences ending mid-tile
+    ("bf16", 1, 1, 300, 64, 64, 1),
+    ("bf16", 1, 2, 1100, 64, 64, 512),
+    ("bf16", 2, 1, 777, 64, 64, 300),
+    ("bf16", 1, 1, 1024, 64, 64, 129),
+    ("bf16", 1, 1, 900, 64, 64, 640),
+    ("bf16", 1, 1, 515, 64, 64, 100),
 ]
 
 
@@ -93,6 +101,39 @@ def test_fp32_workload_T256_d32_W32(cuda_lib, oracle_mod):
     ref = oracle_mod.tc_prefill(inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate, inp.W)["y"]
     err = check_parity(to_np(y), ref, "f32", "fp32 workload")
     assert err < 1e-5
+
+
+@pytest.mark.parametrize("lam,scale", [(0.0, 0.0), (1.0, 0.0), (-0.8, 0.0), (0.95, 25.0)])
+def test_decay_and_scale_extremes(cuda_lib, oracle_mod, lam, scale):
+    """lambda = 0 (only the latest eviction counts), 1 (no decay), negative
+    (alternating signs), and a softmax scale large enough that the running
+    maximum moves by many binades within a row."""
+    B, H, T, d, W = 1, 2, 700, 64, 200
+    inp = synth.tc_inputs(B, H, T, d, d, W, dtype="bf16", seed=31, lam=lam)
+    q, k, v, lam_t, eta, gate = _gpu(inp)
+    y = cuda_lib.tc_layer_forward(q, k, v, lam_t, eta, gate, W, softmax_scale=scale)
+    torch.cuda.synchronize()
+    ref = oracle_mod.tc_prefill(inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate, W,
+                                scale=None if scale == 0.0 else scale)["y"]
+    check_parity(to_np(y), ref, "bf16", f"lambda={lam} scale={scale}")
+
+
+def test_cuda_graph_replay_matches_eager(cuda_lib):
+    """A call captured into a CUDA graph and replayed gives the eager result bit for bit."""
+    inp = synth.tc_inputs(2, 2, 1000, 64, 64, 256, dtype="bf16", seed=5)
+    q, k, v, lam, eta, gate = _gpu(inp)
+    ws = torch.empty(cuda_lib.tc_layer_forward_workspace_size(2, 2, 1000, 64, 64, 256, q.dtype),
+                     dtype=torch.uint8, device="cuda")
+    y_eager = cuda_lib.tc_layer_forward(q, k, v, lam, eta, gate, 256, workspace=ws)
+    y = torch.empty_like(y_eager)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cuda_lib.tc_layer_forward(q, k, v, lam, eta, gate, 256, out=y, workspace=ws)
+    y.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(y, y_eager)
 
 
 def _sampled_positions(T, W):
