@@ -787,11 +787,12 @@ struct FwdRow {
 
 struct FwdRowBars {
     uint64_t q_full, k_full[3], v_full[2];
-    uint64_t s_full, s_empty, p_full, p_empty, pv2_done, o_done, drain;
+    uint64_t s_full, s_empty, p_full, p_empty, pv2_done, o_done, y_ready, drain;
     uint64_t xchg[4];      // per lane quarter: the two halves of its rows meet here
     uint32_t tbase;
-    float lam_h;
+    float cA;              // A_j = A_j^loc + cA A_{gL}: lambda^(C (j - gL))
     float pwz[32 + kBlk];  // [32 + d] = eta lambda^d for d >= 0; 0 for d < 0
+    float lpow[kBlk + 1];  // lambda^d
     float xbuf[2][2][kBlk];  // [exchange parity][half][row]
 };
 
@@ -799,7 +800,8 @@ template <int DK, int DV>
 __global__ void __launch_bounds__(288, 2)
 tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ma,
-                  const __grid_constant__ CUtensorMap mc, int T, int W, int H, int nch, int nseg, int L,
+                  const __grid_constant__ CUtensorMap mc, const __grid_constant__ CUtensorMap my, int T, int W,
+                  int H, int nch, int nseg, int L,
                   const float *__restrict__ lam, const float *__restrict__ eta,
                   const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y) {
     using C = FwdRow<DK, DV>;
@@ -861,12 +863,14 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         mbar_init(&B.p_empty, 1);
         mbar_init(&B.pv2_done, 1);
         mbar_init(&B.o_done, 1);
+        mbar_init(&B.y_ready, 8);
         mbar_init(&B.drain, 1);
         for (int i = 0; i < 4; ++i) mbar_init(&B.xchg[i], 2);
         mbar_fence_init();
         tma_prefetch_desc(&mq);
         tma_prefetch_desc(&mk);
         tma_prefetch_desc(&mv);
+        tma_prefetch_desc(&my);
         mbar_expect_tx(&B.q_full, C::QBYTES);
 #pragma unroll
         for (int b = 0; b < DK / 64; ++b) tma_load_3d(sm + b * 16384, &mq, &B.q_full, 64 * b, t0, bh);
@@ -875,9 +879,14 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     }
     __syncwarp();
     if (warp == 8) tmem_alloc(&B.tbase, C::TCOLS);
-    if (tid == 0) B.lam_h = lam[h];
     if (tid < 32) B.pwz[tid] = 0.f;
-    if (tid < kBlk) B.pwz[32 + tid] = eta[h] * powf(lam[h], (float)tid);
+    if (tid <= kBlk) {
+        const float lh = lam[h];
+        const float pw = powf(lh, (float)tid);
+        B.lpow[tid] = pw;
+        if (tid < kBlk) B.pwz[32 + tid] = eta[h] * pw;
+        if (tid == kBlk) B.cA = powf(lh, (float)(kBlk * (jq - seg * L)));
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -963,7 +972,6 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         // ------------------------------------------------ softmax / epilogue (row r, key half hf)
         const int q4 = warp & 3, hf = warp >> 2;
         const int r = 32 * q4 + lane;
-        const int t = t0 + r;
         const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
         const float sc = scale * kLog2e;
         const float sig = 1.0f / (1.0f + expf(-gate[h]));
@@ -1157,9 +1165,10 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
             tc_fence_after();
             const float inv_l = Lrow > 0.f ? 1.0f / Lrow : 0.f;
             // sigmoid(g) lambda^(i+1), and c with A_j = A_j^loc + c A_{gL}
-            const float cq = has_l2 ? sig * powf(B.lam_h, (float)(r + 1)) : 0.f;
-            const float cA = has_l2 ? powf(B.lam_h, (float)(kBlk * (jq - seg * L))) : 0.f;
-            __nv_bfloat16 *yr = y + ((size_t)bh * T + t) * DV + 32 * hf;
+            const float cq = has_l2 ? sig * B.lpow[r + 1] : 0.f;
+            const float cA = B.cA;
+            // y row r, columns 32 hf .. +31, staged in the (spent) Q tile with the
+            // tensor map's 128-byte swizzle, then one TMA store per CTA
 #pragma unroll 1
             for (int cc = 0; cc < 32; cc += 16) {
                 float o[16], qa[16], qc[16], o2[16];
@@ -1176,14 +1185,24 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
 #pragma unroll
                     for (int e = 0; e < 16; ++e) qa[e] = 0.f;
                 }
-                if (t < T) {
-                    uint32_t pk[8];
+                uint32_t pk[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        pk[i] = pack_bf16(fmaf(o[2 * i], inv_l, qa[2 * i]), fmaf(o[2 * i + 1], inv_l, qa[2 * i + 1]));
-                    uint4 *dst = reinterpret_cast<uint4 *>(yr + cc);
-                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                for (int i = 0; i < 8; ++i)
+                    pk[i] = pack_bf16(fmaf(o[2 * i], inv_l, qa[2 * i]), fmaf(o[2 * i + 1], inv_l, qa[2 * i + 1]));
+                const uint32_t c16 = (uint32_t)((32 * hf + cc) / 8);  // 16-byte chunk of the 128-byte row
+                st_shared_v4(sQ + sw128_off(r, c16), pk[0], pk[1], pk[2], pk[3]);
+                st_shared_v4(sQ + sw128_off(r, c16 + 1), pk[4], pk[5], pk[6], pk[7]);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.y_ready);
+            if (tid == 0) {
+                if (mbar_wait(&B.y_ready, 0)) {
+                    tma_store_3d(&my, sm, 0, t0, bh);
+                    tma_store_commit();
+                    tma_store_wait_read();
+                } else {
+                    ok = false;
                 }
             }
         }
@@ -1249,7 +1268,9 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         const int smem = (int)(Cfg::OFF_BARS + sizeof(FwdRowBars));
         if (int rc_ = set_smem_limit((const void *)kern, smem, "tc_fwd_row smem attribute")) return rc_;
         prof_begin(st);
-        kern<<<dim3(g.nch, BH), 288, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, lam, eta,
+        CUtensorMap my;
+        if ((rc = make_tmap_bf16_3d(&my, y, DV, T, BH, kBlk))) return rc;
+        kern<<<dim3(g.nch, BH), 288, smem, st>>>(mq, mk, mv, ma, mc, my, T, W, H, g.nch, g.nseg, g.L, lam, eta,
                                                   gate, scale, (__nv_bfloat16 *)y);
         rc = launched("tc_fwd_row");
         prof_end(st);
