@@ -296,6 +296,16 @@ __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ------------------------------------------------------------------ programmatic dependent launch
+// Let the next kernel in the stream (launched as a programmatic dependent)
+// start before this grid finishes.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grid this kernel depends on has completed and its writes are
+// visible (returns at once when the kernel was launched without a dependency).
+__device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ misc
 __device__ __forceinline__ float ex2(float x) {
     float y;

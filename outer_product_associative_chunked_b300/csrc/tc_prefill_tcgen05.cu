@@ -108,6 +108,7 @@ tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                    int nch, int L, __nv_bfloat16 *__restrict__ Aloc, float *__restrict__ Lfin) {
     using C = StateCfg<DK>;
     constexpr int NS = C::NS;
+    pdl_launch_dependents();  // the carry kernel may be scheduled; it waits for this grid
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     __shared__ StateBars B;
@@ -273,23 +274,40 @@ __global__ void __launch_bounds__(128)
 tc_l2_carry_kernel(const float *__restrict__ Lfin, int nseg, int L, int T, int dkdv, int H,
                    const float *__restrict__ lam, __nv_bfloat16 *__restrict__ Cbf,
                    float *__restrict__ A_final) {
+    pdl_launch_dependents();  // the forward kernel may start its window tiles now
+    pdl_wait_primary();       // segment finals of the state kernel
     const int bh = blockIdx.y;
     const int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (e >= dkdv) return;
     const float lm = lam[bh % H];
+    const float f = powf(lm, (float)(L * kBlk));  // decay across a full segment
+    const float *src = Lfin + (size_t)bh * nseg * dkdv + e;
+    __nv_bfloat16 *dst = Cbf + (size_t)bh * nseg * dkdv + e;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int g = 0; g < nseg; ++g) {
-        uint2 o;
-        o.x = pack_bf16(A.x, A.y);
-        o.y = pack_bf16(A.z, A.w);
-        *reinterpret_cast<uint2 *>(Cbf + ((size_t)bh * nseg + g) * dkdv + e) = o;
-        const float4 d = *reinterpret_cast<const float4 *>(Lfin + ((size_t)bh * nseg + g) * dkdv + e);
-        const int ntok = min(T, (g + 1) * L * kBlk) - g * L * kBlk;
-        const float f = powf(lm, (float)ntok);
-        A.x = fmaf(f, A.x, d.x);
-        A.y = fmaf(f, A.y, d.y);
-        A.z = fmaf(f, A.z, d.z);
-        A.w = fmaf(f, A.w, d.w);
+    // Segment finals are read eight at a time so their loads overlap; the
+    // recurrence itself is a chain of FMAs.
+    constexpr int kBatch = 8;
+    for (int g0 = 0; g0 < nseg; g0 += kBatch) {
+        float4 d[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+            d[u] = g0 + u < nseg ? *reinterpret_cast<const float4 *>(src + (size_t)(g0 + u) * dkdv)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+            const int g = g0 + u;
+            if (g >= nseg) break;
+            uint2 o;
+            o.x = pack_bf16(A.x, A.y);
+            o.y = pack_bf16(A.z, A.w);
+            *reinterpret_cast<uint2 *>(dst + (size_t)g * dkdv) = o;
+            // the last segment may be shorter: its decay only matters for A_final
+            const float fg = (g + 1) * L * kBlk <= T ? f : powf(lm, (float)(T - g * L * kBlk));
+            A.x = fmaf(fg, A.x, d[u].x);
+            A.y = fmaf(fg, A.y, d[u].y);
+            A.z = fmaf(fg, A.z, d[u].z);
+            A.w = fmaf(fg, A.w, d[u].w);
+        }
     }
     if (A_final) *reinterpret_cast<float4 *>(A_final + (size_t)bh * dkdv + e) = A;
 }
@@ -838,6 +856,9 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
 #pragma unroll
             for (int b = 0; b < DK / 64; ++b) tma_load_3d(kd + b * 16384, &mk, bar, 64 * b, kt, bh);
         } else {
+            // A_j^loc and the carry come from the state and carry kernels, which
+            // may still be running: wait for them (only this thread, only here)
+            pdl_wait_primary();
             mbar_expect_tx(bar, 2 * DK * DV * 2);
 #pragma unroll
             for (int b = 0; b < DV / 64; ++b) {
@@ -1258,9 +1279,24 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
                                                               w.Lfin);
         if ((rc = launched("tc_l2_state"))) return rc;
     }
-    tc_l2_carry_kernel<<<dim3(ceil_div(DK * DV / 4, 128), BH), 128, 0, st>>>(w.Lfin, g.nseg, g.L, T, DK * DV, H,
-                                                                            lam, w.Cbf, A_final);
-    if ((rc = launched("tc_l2_carry"))) return rc;
+    // The carry kernel and the d = 64 forward kernel are programmatic dependents:
+    // each may start before its predecessor finishes and waits (griddepcontrol)
+    // only where it reads that predecessor's output.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(ceil_div(DK * DV / 4, 128), BH);
+        cfg.blockDim = dim3(128);
+        cfg.stream = st;
+        cfg.attrs = pdl;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, tc_l2_carry_kernel, (const float *)w.Lfin, g.nseg, g.L, T,
+                                           DK * DV, H, lam, w.Cbf, A_final);
+        if (e != cudaSuccess) return cuda_fail(e, "tc_l2_carry launch");
+        if ((rc = launched("tc_l2_carry"))) return rc;
+    }
     if constexpr (DK == 64 && DV == 64) {
         using Cfg = FwdRow<DK, DV>;
         auto kern = tc_fwd_row_kernel<DK, DV>;
@@ -1270,9 +1306,16 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         prof_begin(st);
         CUtensorMap my;
         if ((rc = make_tmap_bf16_3d(&my, y, DV, T, BH, kBlk))) return rc;
-        kern<<<dim3(g.nch, BH), 288, smem, st>>>(mq, mk, mv, ma, mc, my, T, W, H, g.nch, g.nseg, g.L, lam, eta,
-                                                  gate, scale, (__nv_bfloat16 *)y);
-        rc = launched("tc_fwd_row");
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(g.nch, BH);
+        cfg.blockDim = dim3(288);
+        cfg.dynamicSmemBytes = (size_t)smem;
+        cfg.stream = st;
+        cfg.attrs = pdl;
+        cfg.numAttrs = 1;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, ma, mc, my, T, W, H, g.nch, g.nseg, g.L, lam, eta,
+                                           gate, scale, (__nv_bfloat16 *)y);
+        rc = e != cudaSuccess ? cuda_fail(e, "tc_fwd_row launch") : launched("tc_fwd_row");
         prof_end(st);
         return rc;
     } else {
