@@ -48,10 +48,10 @@ enum : unsigned int {
 //     TMEM lanes 0..63 hold Q K^T, lanes 64..127 hold K K^T.
 //  2. Lanes 0..63 write P = (Q K^T masked to j <= i) as bf16; lanes 64..127
 //     write diag(beta) strict_lower(K K^T) to shared memory.
-//  3. T = (I + diag(beta) L)^{-1} in fp32 in shared memory, in 16 x 16
-//     blocks (invert_unit_lower); column j of G = T diag(beta), i.e. row j of
-//     G^T, goes to shared memory (bf16, 128-byte swizzle) and to global
-//     memory.
+//  3. Threads 0..63 each solve one column of T = (I + diag(beta) L)^{-1} by
+//     forward substitution in fp32 registers; column j of G = T diag(beta),
+//     i.e. row j of G^T, goes to shared memory (bf16, 128-byte swizzle) and
+//     to global memory.
 //  4. W^T = -(K^T G^T) on tcgen05 (A = K^T read MN-major from the K rows;
 //     for d_k = 64 both 64-wide M blocks alias the same rows; B = G^T read
 //     MN-major); row a of W^T (a < d_k) goes to global memory as bf16.
@@ -60,79 +60,31 @@ struct PrepCfg {
     static constexpr uint32_t QK_BYTES = (DK / 64) * 16384;  // [Q;K], 128 rows per 64-column block
     static constexpr uint32_t OFF_G = 0;                    // G^T (64 rows x 128 B) over the Q rows of
                                                             // block 0, free after the first MMA
-    static constexpr uint32_t OFF_L = QK_BYTES;             // Lb fp32 [64][64], inverted in place to T
-    static constexpr uint32_t OFF_X = OFF_L + 64 * 64 * 4;  // X blocks fp32 [3][16][16]
-    static constexpr uint32_t SMEM = OFF_X + 3 * 16 * 16 * 4 + 1024;
+    static constexpr uint32_t OFF_L = QK_BYTES;             // Lb fp32 [64][64]
+    static constexpr uint32_t SMEM = OFF_L + 64 * 64 * 4 + 1024;
 };
 
-// T = (I + Lb)^{-1} (Lb strictly lower, 64 x 64, fp32, row-major in shared
-// memory) in place, in 16 x 16 blocks: the four diagonal blocks by forward
-// substitution (thread (b, c) of the first 64 solves column c of block b),
-// then block rows i = 1..3 with X_ij = sum_{k=j}^{i-1} Lb_ik T_kj and
-// T_ij = -T_ii X_ij, shared by all 128 threads.  Every thread of the CTA
-// must call it (it synchronises the block).
-__device__ __forceinline__ void invert_unit_lower(float *__restrict__ L, float *__restrict__ X, int tid) {
-    {
-        float t[16];
-        const int b = (tid >> 4) & 3, cc = tid & 15;
-        const float *Lbb = L + (16 * b) * kC + 16 * b;
-        if (tid < kC) {
+// Column j of T = (I + Lb)^{-1} (Lb strictly lower) by forward substitution:
+// T[i][j] = -sum_{k<i} Lb[i][k] T[k][j], T[j][j] = 1.  Every column handled
+// by the calling warp is >= K0, so T[k][j] = 0 for k < K0 and those terms
+// are skipped.
+template <int K0>
+__device__ __forceinline__ void forward_column(const float *__restrict__ Lb, int j, float (&t)[kC]) {
 #pragma unroll
-            for (int r = 0; r < 16; ++r) t[r] = (r == cc) ? 1.f : 0.f;
+    for (int i = 0; i < kC; ++i) t[i] = (i == j) ? 1.f : 0.f;
 #pragma unroll
-            for (int r = 1; r < 16; ++r) {
-                float a0 = 0.f, a1 = 0.f;
+    for (int i = K0 + 1; i < kC; ++i) {
+        const float4 *row = reinterpret_cast<const float4 *>(Lb + i * kC);
+        float2 a = make_float2(0.f, 0.f), b = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int k = 0; k < r; k += 2) {
-                    a0 = fmaf(Lbb[r * kC + k], t[k], a0);
-                    if (k + 1 < r) a1 = fmaf(Lbb[r * kC + k + 1], t[k + 1], a1);
-                }
-                t[r] = (r == cc) ? 1.f : (r > cc ? -(a0 + a1) : 0.f);
-            }
+        for (int k4 = K0; k4 < i; k4 += 4) {
+            const float4 l = row[k4 >> 2];
+            // Lb[i][k] = 0 for k >= i, so whole float4 groups may be used.
+            a = fma2(make_float2(l.x, l.y), make_float2(t[k4], t[k4 + 1]), a);
+            if (k4 + 2 < i) b = fma2(make_float2(l.z, l.w), make_float2(t[k4 + 2], t[k4 + 3]), b);
         }
-        __syncthreads();
-        if (tid < kC) {
-            float *Tbb = L + (16 * b) * kC + 16 * b;
-#pragma unroll
-            for (int r = 0; r < 16; ++r) Tbb[r * kC + cc] = t[r];
-        }
-        __syncthreads();
-    }
-    for (int bi = 1; bi < 4; ++bi) {
-        for (int e = tid; e < bi * 256; e += 128) {  // X_ij, j = e / 256
-            const int bj = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const float *lr = L + (16 * bi + r) * kC;
-            float a[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int kb = bj; kb < bi; ++kb) {
-                const float *tc = L + (16 * kb) * kC + 16 * bj + cc;
-#pragma unroll
-                for (int u = 0; u < 16; u += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4 *>(lr + 16 * kb + u);
-                    a[0] = fmaf(l4.x, tc[u * kC], a[0]);
-                    a[1] = fmaf(l4.y, tc[(u + 1) * kC], a[1]);
-                    a[2] = fmaf(l4.z, tc[(u + 2) * kC], a[2]);
-                    a[3] = fmaf(l4.w, tc[(u + 3) * kC], a[3]);
-                }
-            }
-            X[e] = (a[0] + a[1]) + (a[2] + a[3]);
-        }
-        __syncthreads();
-        for (int e = tid; e < bi * 256; e += 128) {  // T_ij = -T_ii X_ij
-            const int bj = e >> 8, r = (e >> 4) & 15, cc = e & 15;
-            const float *tr = L + (16 * bi + r) * kC + 16 * bi;
-            const float *xb = X + bj * 256 + cc;
-            float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int u = 0; u < 16; u += 4) {
-                const float4 t4 = *reinterpret_cast<const float4 *>(tr + u);
-                a[0] = fmaf(t4.x, xb[u * 16], a[0]);
-                a[1] = fmaf(t4.y, xb[(u + 1) * 16], a[1]);
-                a[2] = fmaf(t4.z, xb[(u + 2) * 16], a[2]);
-                a[3] = fmaf(t4.w, xb[(u + 3) * 16], a[3]);
-            }
-            L[(16 * bi + r) * kC + 16 * bj + cc] = -((a[0] + a[1]) + (a[2] + a[3]));
-        }
-        __syncthreads();
+        const float acc = (a.x + a.y) + (b.x + b.y);
+        t[i] = (i == j) ? 1.f : -acc;
     }
 }
 
@@ -223,19 +175,23 @@ delta_prep_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         }
     }
     ok = __syncthreads_and(ok);
-    invert_unit_lower(Lb, reinterpret_cast<float *>(sm + C::OFF_X), tid);  // Lb becomes T
-    // Row j of G^T (= column j of T, times beta_j) into the swizzled tile and to global memory.
+    // Column j of T (threads 0..63), then G[:, j] = T[:, j] beta_j.
     if (ok && tid < kC) {
         const int j = tid;
+        float t[kC];
+        if (warp == 0)
+            forward_column<0>(Lb, j, t);
+        else
+            forward_column<32>(Lb, j, t);
         const float bj = bs[j];
+        // Row j of G^T (= column j of G) into the swizzled tile and to global memory.
         uint4 *gdst = reinterpret_cast<uint4 *>(Gg + (((size_t)bh * nch + c) * kC + j) * kC);
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
-            float g[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) g[e] = Lb[(8 * ch + e) * kC + j] * bj;
-            const uint32_t w0 = pack_bf16(g[0], g[1]), w1 = pack_bf16(g[2], g[3]);
-            const uint32_t w2 = pack_bf16(g[4], g[5]), w3 = pack_bf16(g[6], g[7]);
+            const uint32_t w0 = pack_bf16(t[8 * ch] * bj, t[8 * ch + 1] * bj);
+            const uint32_t w1 = pack_bf16(t[8 * ch + 2] * bj, t[8 * ch + 3] * bj);
+            const uint32_t w2 = pack_bf16(t[8 * ch + 4] * bj, t[8 * ch + 5] * bj);
+            const uint32_t w3 = pack_bf16(t[8 * ch + 6] * bj, t[8 * ch + 7] * bj);
             st_shared_v4(s0 + C::OFF_G + sw128_off(j, ch), w0, w1, w2, w3);
             gdst[ch] = make_uint4(w0, w1, w2, w3);
         }
