@@ -15,6 +15,16 @@
 // chunk,
 //     o_t = sum_{j in supp q_t} q_t[j] S[j,:] + sum_{s in chunk, s<=t} <k_s,q_t> v_s
 // and afterwards every token of the chunk adds k_s[j] v_s into row j.
+//
+// Without a start state and without a final state to return, the same output
+// is computed in its pairwise form, which never materialises S:
+//     o_t = sum_{s <= t} <q_t, k_s> v_s = sum_{s <= t} Z[t][s] v_s.
+// Tokens are grouped in blocks of kTB; within a block the supports are
+// transposed to coordinate-major lists (csc_build_kernel).  For a pair of
+// blocks (tb >= sb), Z[tb][sb] = sum_j q_j-list x k_j-list is accumulated in
+// shared memory from the lists of each coordinate j, and Z[tb][sb] V[sb] is
+// added into o (pair_tile_kernel).  The state's traffic (every token gathering
+// and scattering ~5% of the N rows) is replaced by one pass over the lists.
 #include "opam_internal.cuh"
 
 namespace opam {
@@ -22,10 +32,25 @@ namespace {
 
 constexpr int kC = 64;
 constexpr int kThreads = 256;
+constexpr int kTB = 128;  // tokens per block of the pairwise form (token index fits a byte)
+constexpr size_t kStateL2Budget = (size_t)64 << 20;  // recurrent form: state bytes kept hot in L2
 
-__global__ void compact_rows_kernel(const float *__restrict__ x, int rows, int N,
-                                    int *__restrict__ idx, float *__restrict__ val,
-                                    int *__restrict__ cnt) {
+// One warp per row of a dense [rows][N] matrix: the ascending list of its
+// non-zero entries (index, value) and their count.  When N is a multiple of
+// 4 the row is read as float4 with four loads in flight per lane (the dense
+// rows are the largest input); a lane's four elements are consecutive, so
+// ballots over the four components give every non-zero its position in order.
+__device__ __forceinline__ float4 ldg_stream4(const float4 *p) {
+    float4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__global__ void __launch_bounds__(256)
+compact_rows_kernel(const float *__restrict__ x, int rows, int N, int *__restrict__ idx,
+                    float *__restrict__ val, int *__restrict__ cnt) {
     const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -33,16 +58,54 @@ __global__ void compact_rows_kernel(const float *__restrict__ x, int rows, int N
     int *oi = idx + (size_t)row * N;
     float *ov = val + (size_t)row * N;
     int c = 0;
-    for (int base = 0; base < N; base += 32) {
-        const int j = base + lane;
-        const float a = j < N ? src[j] : 0.f;
-        const unsigned bal = __ballot_sync(0xffffffffu, a != 0.f);
-        if (a != 0.f) {
-            const int p = c + __popc(bal & ((1u << lane) - 1u));
-            oi[p] = j;
-            ov[p] = a;
+    if ((N & 3) == 0) {
+        constexpr int U = 4;
+        const float4 *s4 = reinterpret_cast<const float4 *>(src);
+        const int n4 = N >> 2;
+        const unsigned below = (1u << lane) - 1u;
+        for (int base = 0; base < n4; base += 32 * U) {
+            float4 xv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i4 = base + 32 * u + lane;
+                xv[u] = i4 < n4 ? ldg_stream4(s4 + i4) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const float e[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+                unsigned m[4];
+                int before = 0, total = 0;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    m[k] = __ballot_sync(0xffffffffu, e[k] != 0.f);
+                    before += __popc(m[k] & below);
+                    total += __popc(m[k]);
+                }
+                int p = c + before;
+                const int j = 4 * (base + 32 * u + lane);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    if (e[k] != 0.f) {
+                        oi[p] = j + k;
+                        ov[p] = e[k];
+                        ++p;
+                    }
+                }
+                c += total;
+            }
         }
-        c += __popc(bal);
+    } else {
+        for (int base = 0; base < N; base += 32) {
+            const int j = base + lane;
+            const float a = j < N ? src[j] : 0.f;
+            const unsigned bal = __ballot_sync(0xffffffffu, a != 0.f);
+            if (a != 0.f) {
+                const int p = c + __popc(bal & ((1u << lane) - 1u));
+                oi[p] = j;
+                ov[p] = a;
+            }
+            c += __popc(bal);
+        }
     }
     if (lane == 0) cnt[row] = c;
 }
@@ -53,7 +116,7 @@ __global__ void compact_rows_kernel(const float *__restrict__ x, int rows, int N
 // of q_t in shared memory).
 template <int DV>
 __global__ void __launch_bounds__(kThreads, 3)
-sparse_read_kernel(int c0, int T_, int N, const int *__restrict__ kidx,
+sparse_read_kernel(int bh0, int c0, int T_, int N, const int *__restrict__ kidx,
                    const float *__restrict__ kval, const int *__restrict__ kcnt,
                    const int *__restrict__ qidx, const float *__restrict__ qval,
                    const int *__restrict__ qcnt, const float *__restrict__ v,
@@ -64,7 +127,7 @@ sparse_read_kernel(int c0, int T_, int N, const int *__restrict__ kidx,
     extern __shared__ float qd[];        // [N] dense copy of q_t
     __shared__ float zs[kC];
     __shared__ float4 red[kThreads];
-    const int ti = blockIdx.x, bh = blockIdx.y, tid = threadIdx.x;
+    const int ti = blockIdx.x, bh = bh0 + blockIdx.y, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5;
     const size_t row = (size_t)bh * T_ + c0 + ti;
     for (int j = tid; j < N; j += kThreads) qd[j] = 0.f;
@@ -129,11 +192,11 @@ sparse_read_kernel(int c0, int T_, int N, const int *__restrict__ kidx,
 // in the support of k_s, as float4 vector reductions.
 template <int DV>
 __global__ void __launch_bounds__(kThreads)
-sparse_write_kernel(int c0, int T_, int N, const int *__restrict__ kidx,
+sparse_write_kernel(int bh0, int c0, int T_, int N, const int *__restrict__ kidx,
                     const float *__restrict__ kval, const int *__restrict__ kcnt,
                     const float *__restrict__ v, float *__restrict__ ST) {
     constexpr int CG = DV / 4, RGN = kThreads / CG;
-    const int bh = blockIdx.y, tid = threadIdx.x;
+    const int bh = bh0 + blockIdx.y, tid = threadIdx.x;
     const size_t row = (size_t)bh * T_ + c0 + blockIdx.x;
     const int cg = tid % CG, rg = tid / CG;
     const float4 vv = reinterpret_cast<const float4 *>(v + row * DV)[cg];
@@ -148,12 +211,235 @@ sparse_write_kernel(int c0, int T_, int N, const int *__restrict__ kidx,
     }
 }
 
+// ------------------------------------------------------------------ pairwise form
+// One CTA per (token block, head, q or k): the block's supports as
+// coordinate-major lists.  off[j] .. off[j+1] index the entries of coordinate
+// j; each entry is (token within the block, value).  Counting and placement
+// use shared-memory counters, so the order inside a coordinate is arbitrary.
+__global__ void __launch_bounds__(512)
+csc_build_kernel(int T, int N, int nb, const int *__restrict__ kidx, const float *__restrict__ kval,
+                 const int *__restrict__ kcnt, const int *__restrict__ qidx, const float *__restrict__ qval,
+                 const int *__restrict__ qcnt, int *__restrict__ coff, uint8_t *__restrict__ ct,
+                 float *__restrict__ cv) {
+    extern __shared__ int cnt[];  // [N]: counts, then placement cursors
+    __shared__ int wsum[16];
+    const int b = blockIdx.x, bh = blockIdx.y, which = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int *idx = which ? qidx : kidx;
+    const float *val = which ? qval : kval;
+    const int *rc = which ? qcnt : kcnt;
+    const int t0 = b * kTB, nrows = min(kTB, T - t0);
+    const size_t blk = ((size_t)which * gridDim.y + bh) * nb + b;
+    int *off = coff + blk * (size_t)(N + 1);
+    uint8_t *et = ct + blk * (size_t)kTB * N;
+    float *ev = cv + blk * (size_t)kTB * N;
+    for (int j = tid; j < N; j += 512) cnt[j] = 0;
+    __syncthreads();
+    for (int r = warp; r < nrows; r += 16) {
+        const size_t row = (size_t)bh * T + t0 + r;
+        const int n = rc[row];
+        for (int e = lane; e < n; e += 32) atomicAdd(&cnt[idx[row * N + e]], 1);
+    }
+    __syncthreads();
+    // exclusive scan of the N counts: a contiguous segment per thread
+    const int seg = (N + 511) / 512, j0 = min(N, tid * seg), j1 = min(N, j0 + seg);
+    int local = 0;
+    for (int j = j0; j < j1; ++j) local += cnt[j];
+    int incl = local;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += x;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < 16 ? wsum[lane] : 0;
+#pragma unroll
+        for (int d = 1; d < 16; d <<= 1) {
+            const int x = __shfl_up_sync(0xffffffffu, w, d);
+            if (lane >= d) w += x;
+        }
+        if (lane < 16) wsum[lane] = w;  // inclusive warp totals
+    }
+    __syncthreads();
+    int run = incl - local + (warp > 0 ? wsum[warp - 1] : 0);
+    for (int j = j0; j < j1; ++j) {
+        const int c = cnt[j];
+        cnt[j] = run;
+        off[j] = run;
+        run += c;
+    }
+    if (tid == 0) off[N] = wsum[15];
+    __syncthreads();
+    for (int r = warp; r < nrows; r += 16) {
+        const size_t row = (size_t)bh * T + t0 + r;
+        const int n = rc[row];
+        for (int e = lane; e < n; e += 32) {
+            const int p = atomicAdd(&cnt[idx[row * N + e]], 1);
+            et[p] = (uint8_t)r;
+            ev[p] = val[row * N + e];
+        }
+    }
+}
+
+// One CTA per (pair of token blocks tb >= sb, head):
+//   Z[t][s] = sum_j q_t[j] k_s[j]  (s <= t on the diagonal block), accumulated
+//   in shared memory.  Coordinates are taken in windows of kJW: the window's
+//   list entries (contiguous in the coordinate-major arrays) are first copied
+//   to shared memory with coalesced loads, then each warp takes one
+//   coordinate at a time, its lanes an 8 x 4 grid over (query entry, key
+//   entry) pairs of that coordinate's lists.  A window whose
+//   lists do not fit the buffers (dense inputs) is read from global memory.
+//   Then o[tb] += Z V[sb]  (fp32, 128 output columns per pass, float atomics).
+constexpr int kJW = 256;    // coordinates per window
+constexpr int kCap = 3072;  // list entries per window buffered in shared memory
+
+struct PairSmem {
+    float Z[kTB * (kTB + 1)];
+    float qv[kCap], kv[kCap];
+    int qo[kJW + 1], ko[kJW + 1];
+    uint8_t qt[kCap], kt[kCap];
+};
+
+template <int DV>
+__global__ void __launch_bounds__(256)
+pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8_t *__restrict__ ct,
+                 const float *__restrict__ cv, const float *__restrict__ v, float *__restrict__ y) {
+    constexpr int ZS = kTB + 1;  // padded row stride of the Z tile
+    extern __shared__ unsigned char smraw[];
+    PairSmem &P = *reinterpret_cast<PairSmem *>(smraw);
+    float *Zs = P.Z;
+    const int tile = blockIdx.x, bh = blockIdx.y, BH = gridDim.y;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int tb = (int)((sqrtf(8.f * (float)tile + 1.f) - 1.f) * 0.5f);
+    while ((tb + 1) * (tb + 2) / 2 <= tile) ++tb;
+    while (tb * (tb + 1) / 2 > tile) --tb;
+    const int sb = tile - tb * (tb + 1) / 2;
+    const bool diag = sb == tb;
+    for (int i = tid; i < kTB * ZS; i += 256) Zs[i] = 0.f;
+    const size_t bk = (size_t)bh * nb + sb, bq = ((size_t)BH + bh) * nb + tb;  // k lists: which 0, q: 1
+    const int *ko = coff + bk * (size_t)(N + 1), *qo = coff + bq * (size_t)(N + 1);
+    const uint8_t *kt = ct + bk * (size_t)kTB * N, *qt = ct + bq * (size_t)kTB * N;
+    const float *kv = cv + bk * (size_t)kTB * N, *qv = cv + bq * (size_t)kTB * N;
+    for (int w0 = 0; w0 < N; w0 += kJW) {
+        const int nw = min(kJW, N - w0);
+        __syncthreads();  // the previous window's buffers are no longer read (and Z is zeroed)
+        for (int i = tid; i <= nw; i += 256) {
+            P.qo[i] = qo[w0 + i];
+            P.ko[i] = ko[w0 + i];
+        }
+        __syncthreads();
+        const int qb = P.qo[0], kb = P.ko[0];
+        const int nq = P.qo[nw] - qb, nk = P.ko[nw] - kb;
+        const bool fits = nq <= kCap && nk <= kCap;
+        if (fits) {
+            for (int i = tid; i < nq; i += 256) {
+                P.qt[i] = qt[qb + i];
+                P.qv[i] = qv[qb + i];
+            }
+            for (int i = tid; i < nk; i += 256) {
+                P.kt[i] = kt[kb + i];
+                P.kv[i] = kv[kb + i];
+            }
+        }
+        __syncthreads();
+        // one coordinate per warp at a time; lane (a, b) = (lane / 4, lane % 4)
+        // takes query entry a0 + a and key entry b0 + b of its lists
+        auto pairs = [&](const uint8_t *Qt, const float *Qv, const uint8_t *Kt, const float *Kv, int q0, int nqj,
+                         int k0, int nkj) {
+            for (int a0 = 0; a0 < nqj; a0 += 8) {
+                const int a = a0 + (lane >> 2);
+                const bool qa = a < nqj;
+                const int t = qa ? Qt[q0 + a] : 0;
+                const float x = qa ? Qv[q0 + a] : 0.f;
+                const int smax = diag ? t : kTB - 1;  // causal inside the diagonal block
+                for (int b0 = 0; b0 < nkj; b0 += 4) {
+                    const int b = b0 + (lane & 3);
+                    if (qa && b < nkj) {
+                        const int s = Kt[k0 + b];
+                        if (s <= smax) atomicAdd(Zs + t * ZS + s, x * Kv[k0 + b]);
+                    }
+                }
+            }
+        };
+        if (fits) {
+            for (int jl = warp; jl < nw; jl += 8) {
+                const int q0 = P.qo[jl] - qb, k0 = P.ko[jl] - kb;
+                const int nqj = P.qo[jl + 1] - qb - q0, nkj = P.ko[jl + 1] - kb - k0;
+                if (nqj > 0 && nkj > 0) pairs(P.qt, P.qv, P.kt, P.kv, q0, nqj, k0, nkj);
+            }
+        } else {
+            for (int jl = warp; jl < nw; jl += 8) {
+                const int q0 = P.qo[jl], k0 = P.ko[jl];
+                const int nqj = P.qo[jl + 1] - q0, nkj = P.ko[jl + 1] - k0;
+                if (nqj > 0 && nkj > 0) pairs(qt, qv, kt, kv, q0, nqj, k0, nkj);
+            }
+        }
+    }
+    __syncthreads();
+    const int rows = min(kTB, T - tb * kTB), cols = min(kTB, T - sb * kTB);
+    constexpr int DVP = DV < 128 ? DV : 128;  // output columns per pass
+    constexpr int CG = DVP / 16;               // column groups of 16
+    constexpr int RPT = kTB / (256 / CG);      // rows per thread
+    const int cg = tid % CG, rg = tid / CG;
+    const float *vb = v + ((size_t)bh * T + sb * kTB) * DV;
+    float *yb = y + ((size_t)bh * T + tb * kTB) * DV;
+#pragma unroll 1
+    for (int c0 = 0; c0 < DV; c0 += DVP) {
+        float acc[RPT][16];
+#pragma unroll
+        for (int i = 0; i < RPT; ++i)
+#pragma unroll
+            for (int e = 0; e < 16; ++e) acc[i][e] = 0.f;
+        const int col = c0 + 16 * cg;
+#pragma unroll 2
+        for (int s = 0; s < cols; ++s) {
+            const float4 *vr = reinterpret_cast<const float4 *>(vb + (size_t)s * DV + col);
+            const float4 v0 = vr[0], v1 = vr[1], v2 = vr[2], v3 = vr[3];
+            const float vv[16] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w,
+                                  v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+            for (int i = 0; i < RPT; ++i) {
+                const float z = Zs[(rg * RPT + i) * ZS + s];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) acc[i][e] = fmaf(z, vv[e], acc[i][e]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < RPT; ++i) {
+            const int r = rg * RPT + i;
+            if (r < rows) {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) atomicAdd(yb + (size_t)r * DV + col + e, acc[i][e]);
+            }
+        }
+    }
+}
+
 struct WsLayout {
     int *kidx, *qidx, *kcnt, *qcnt;
     float *kval, *qval, *ST;
+    int *coff;     // [2][BH][nb][N+1]   coordinate lists of the pairwise form
+    uint8_t *ct;   // [2][BH][nb][kTB*N] token within the block
+    float *cv;     // [2][BH][nb][kTB*N] value
 };
 
-WsLayout carve(void *ws, int BH, int T, int N, int dv, bool need_state) {
+size_t csr_bytes(int BH, int T, int N) {
+    const size_t ent = (size_t)BH * T * N;
+    return 2 * align_up(sizeof(int) * ent, 256) + 2 * align_up(sizeof(float) * ent, 256) +
+           2 * align_up(sizeof(int) * (size_t)BH * T, 256);
+}
+size_t pair_bytes(int BH, int T, int N) {
+    const size_t nbk = 2 * (size_t)BH * ceil_div(T, kTB);
+    return align_up(sizeof(int) * nbk * (N + 1), 256) + align_up(nbk * kTB * N, 256) +
+           align_up(sizeof(float) * nbk * kTB * N, 256);
+}
+size_t state_bytes(int BH, int N, int dv) { return align_up(sizeof(float) * (size_t)BH * N * dv, 256); }
+
+// Per-row supports first; the state (recurrent form) or the coordinate lists
+// (pairwise form) share the space after them.
+WsLayout carve(void *ws, int BH, int T, int N) {
     const size_t ent = (size_t)BH * T * N;
     char *p = (char *)ws;
     WsLayout l;
@@ -163,37 +449,69 @@ WsLayout carve(void *ws, int BH, int T, int N, int dv, bool need_state) {
     l.qval = (float *)p; p += align_up(sizeof(float) * ent, 256);
     l.kcnt = (int *)p; p += align_up(sizeof(int) * (size_t)BH * T, 256);
     l.qcnt = (int *)p; p += align_up(sizeof(int) * (size_t)BH * T, 256);
-    l.ST = need_state ? (float *)p : nullptr;
-    (void)dv;
+    l.ST = (float *)p;
+    const size_t nbk = 2 * (size_t)BH * ceil_div(T, kTB);
+    l.coff = (int *)p; p += align_up(sizeof(int) * nbk * (N + 1), 256);
+    l.ct = (uint8_t *)p; p += align_up(nbk * kTB * N, 256);
+    l.cv = (float *)p;
     return l;
 }
 
 template <int DV>
 int launch(const float *q, const float *k, const float *v, int BH, int T, int N, const float *S0,
            float *S_out, float *y, void *ws, cudaStream_t s) {
-    const WsLayout l = carve(ws, BH, T, N, DV, S_out == nullptr);
-    float *ST = S_out ? S_out : l.ST;
-    const size_t state_bytes = sizeof(float) * (size_t)BH * N * DV;
-    cudaError_t e;
-    if (S0 == nullptr) e = cudaMemsetAsync(ST, 0, state_bytes, s);
-    else if (S0 != ST) e = cudaMemcpyAsync(ST, S0, state_bytes, cudaMemcpyDeviceToDevice, s);
-    else e = cudaSuccess;
-    if (e != cudaSuccess) return cuda_fail(e, "sparse state init");
+    const WsLayout l = carve(ws, BH, T, N);
     const int rows = BH * T;
     compact_rows_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(k, rows, N, l.kidx, l.kval, l.kcnt);
     if (int rc = launched("compact k")) return rc;
     compact_rows_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(q, rows, N, l.qidx, l.qval, l.qcnt);
     if (int rc = launched("compact q")) return rc;
+    cudaError_t e;
+    if (S0 == nullptr && S_out == nullptr) {
+        // pairwise form: coordinate lists per token block, then block pairs
+        const int nb = ceil_div(T, kTB);
+        const size_t csmem = sizeof(int) * (size_t)N;
+        if (int rc_ = set_smem_limit((const void *)csc_build_kernel, (int)csmem, "csc_build smem attribute"))
+            return rc_;
+        csc_build_kernel<<<dim3(nb, BH, 2), 512, csmem, s>>>(T, N, nb, l.kidx, l.kval, l.kcnt, l.qidx, l.qval,
+                                                            l.qcnt, l.coff, l.ct, l.cv);
+        if (int rc = launched("csc_build")) return rc;
+        e = cudaMemsetAsync(y, 0, sizeof(float) * (size_t)BH * T * DV, s);
+        if (e != cudaSuccess) return cuda_fail(e, "sparse output init");
+        const size_t psmem = sizeof(PairSmem);
+        if (int rc_ = set_smem_limit((const void *)pair_tile_kernel<DV>, (int)psmem, "pair_tile smem attribute"))
+            return rc_;
+        prof_begin(s);
+        pair_tile_kernel<DV><<<dim3(nb * (nb + 1) / 2, BH), 256, psmem, s>>>(T, N, nb, l.coff, l.ct, l.cv, v, y);
+        const int rc = launched("pair_tile");
+        prof_end(s);
+        return rc;
+    }
+    // recurrent form: the state lives in S_out (or the workspace)
+    float *ST = S_out ? S_out : l.ST;
+    const size_t sbytes = sizeof(float) * (size_t)BH * N * DV;
+    if (S0 == nullptr) e = cudaMemsetAsync(ST, 0, sbytes, s);
+    else if (S0 != ST) e = cudaMemcpyAsync(ST, S0, sbytes, cudaMemcpyDeviceToDevice, s);
+    else e = cudaSuccess;
+    if (e != cudaSuccess) return cuda_fail(e, "sparse state init");
     const size_t smem = sizeof(float) * (size_t)N;
     if (int rc_ = set_smem_limit((const void *)sparse_read_kernel<DV>, (int)smem, "sparse_read smem attribute")) return rc_;
+    // Heads are taken in groups whose states fit the L2 cache together, so the
+    // row gathers and scatters of a group's chunks are served from L2.
+    const size_t head_state = sizeof(float) * (size_t)N * DV;
+    const int group = (int)max((size_t)1, min((size_t)BH, kStateL2Budget / head_state));
     prof_begin(s);
-    for (int c0 = 0; c0 < T; c0 += kC) {
-        const int n = min(kC, T - c0);
-        sparse_read_kernel<DV><<<dim3(n, BH), kThreads, smem, s>>>(c0, T, N, l.kidx, l.kval, l.kcnt, l.qidx,
-                                                                   l.qval, l.qcnt, v, ST, y);
-        if (int rc = launched("sparse_read")) return rc;
-        sparse_write_kernel<DV><<<dim3(n, BH), kThreads, 0, s>>>(c0, T, N, l.kidx, l.kval, l.kcnt, v, ST);
-        if (int rc = launched("sparse_write")) return rc;
+    for (int bh0 = 0; bh0 < BH; bh0 += group) {
+        const int gh = min(group, BH - bh0);
+        for (int c0 = 0; c0 < T; c0 += kC) {
+            const int n = min(kC, T - c0);
+            sparse_read_kernel<DV><<<dim3(n, gh), kThreads, smem, s>>>(bh0, c0, T, N, l.kidx, l.kval, l.kcnt,
+                                                                       l.qidx, l.qval, l.qcnt, v, ST, y);
+            if (int rc = launched("sparse_read")) return rc;
+            sparse_write_kernel<DV><<<dim3(n, gh), kThreads, 0, s>>>(bh0, c0, T, N, l.kidx, l.kval, l.kcnt, v,
+                                                                     ST);
+            if (int rc = launched("sparse_write")) return rc;
+        }
     }
     prof_end(s);
     return OPAM_OK;
@@ -202,11 +520,11 @@ int launch(const float *q, const float *k, const float *v, int BH, int T, int N,
 }  // namespace
 
 size_t sparse_workspace(int BH, int T, int N, int dv, bool need_state) {
-    const size_t ent = (size_t)BH * T * N;
-    size_t b = 2 * align_up(sizeof(int) * ent, 256) + 2 * align_up(sizeof(float) * ent, 256) +
-               2 * align_up(sizeof(int) * (size_t)BH * T, 256);
-    if (need_state) b += align_up(sizeof(float) * (size_t)BH * N * dv, 256);
-    return b;
+    // the state (recurrent form, when kept in the workspace) and the
+    // coordinate lists (pairwise form) use the same space after the supports
+    const size_t tail = pair_bytes(BH, T, N);
+    const size_t st = need_state ? state_bytes(BH, N, dv) : 0;
+    return csr_bytes(BH, T, N) + (tail > st ? tail : st);
 }
 
 int sparse_forward(const float *q, const float *k, const float *v, int B, int H, int T, int N, int dv,

@@ -33,6 +33,38 @@ def test_small_parity(cuda_lib, oracle_mod, B, H, T, N, dv, with_S0):
     check_parity(to_np(S_out), ref["S"], "f32", "bdh S")
 
 
+# Without a start state or a returned state the library takes the pairwise
+# form (coordinate lists per 128-token block): ragged blocks, one and several
+# blocks, every supported d_v.
+@pytest.mark.parametrize("B,H,T,N,dv", [
+    (1, 1, 1, 40, 32),
+    (1, 2, 129, 300, 64),
+    (2, 1, 300, 1000, 128),
+    (1, 1, 257, 512, 256),
+    (1, 3, 150, 2048, 32),
+    (1, 1, 640, 4096, 256),
+])
+def test_pairwise_form_parity(cuda_lib, oracle_mod, B, H, T, N, dv):
+    inp = synth.sparse_inputs(B, H, T, N, dv, seed=3 * T + N)
+    y = cuda_lib.sparse_linattn_forward(inp.q.cuda(), inp.k.cuda(), inp.v.cuda())
+    torch.cuda.synchronize()
+    ref = oracle_mod.sparse_linattn(inp.q, inp.k, inp.v)
+    check_parity(to_np(y), ref["y"], "f32", f"bdh pairwise T={T} N={N} dv={dv}")
+
+
+def test_pairwise_form_dense_and_empty_rows(cuda_lib, oracle_mod):
+    inp = synth.sparse_inputs(1, 2, 200, 300, 64, seed=19)
+    q, k = inp.q.clone(), inp.k.clone()
+    k[0, 0, 5] = torch.rand(300)           # a fully dense key
+    q[0, 1, 150] = torch.rand(300)         # a fully dense query in the second block
+    k[0, 1, :10] = 0.0                     # keys with empty support
+    q[0, 0, 120:140] = 0.0                 # queries with empty support across a block edge
+    y = cuda_lib.sparse_linattn_forward(q.cuda(), k.cuda(), inp.v.cuda())
+    torch.cuda.synchronize()
+    ref = oracle_mod.sparse_linattn(q, k, inp.v)
+    check_parity(to_np(y), ref["y"], "f32", "pairwise edge rows")
+
+
 def test_dense_and_empty_rows_in_place_state(cuda_lib, oracle_mod):
     inp = synth.sparse_inputs(1, 2, 70, 300, 32, seed=9)
     q, k = inp.q.clone(), inp.k.clone()
