@@ -475,18 +475,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         if (lane == 0) {
             bool ok = mbar_wait(&B.q_full, 0);
             uint32_t use[2] = {0, 0};  // P-slot uses so far, per key half
-            auto kdesc = [&](int s, int k) {
-                return sdesc_sw128(sK0 + s * (C::KBYTES + C::VBYTES) + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-            };
-            auto qdesc = [&](int k) { return sdesc_sw128(sQ + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); };
-            // V rows 64 hh + 16 k .. of stage s (MN-major B).
-            auto vdesc = [&](int s, int hh, int k) {
-                return sdesc_sw128(sK0 + s * (C::KBYTES + C::VBYTES) + C::KBYTES + hh * 8192 + k * 2048, 16384,
-                                   1024);
-            };
-            auto pdesc = [&](int hh, int slot, int k) {
-                return sdesc_sw128(sP0 + (slot * 2 + hh) * C::PHALF + k * 32, 16, 1024);
-            };
+            // Descriptors as a fixed upper half plus a lower half (address >> 4 |
+            // leading offset), so each k step is one 32-bit add in the issue loop.
+            constexpr uint32_t HI = sdesc_hi(1024);
+            constexpr uint32_t STG = (C::KBYTES + C::VBYTES) >> 4;  // one K/V stage, encoded
+            const uint32_t q_lo = sdesc_lo(sQ, 16), k_lo = sdesc_lo(sK0, 16);
+            const uint32_t v_lo = sdesc_lo(sK0 + C::KBYTES, 16384), p_lo = sdesc_lo(sP0, 16);
+            auto kofs = [](int k) { return (uint32_t)((k >> 2) * (16384 >> 4) + (k & 3) * 2); };  // K-major k step
             // P V products of processed tile n: per key half, O2 += P2 V' (tile 0)
             // then O_half += P V.
             auto pv = [&](int n) -> bool {
@@ -500,10 +495,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                         tc_fence_after();
                         const bool l2 = (uses == 2 && u == 0);
                         const uint32_t dcol = l2 ? C::COL_O2 : (hh ? C::COL_O1 : C::COL_O0);
+                        // V rows 64 hh + 16 k .. of stage s (MN-major B); P of key half hh, slot
+                        const uint32_t vb = v_lo + (uint32_t)s * STG + (uint32_t)hh * (8192 >> 4);
+                        const uint32_t pb = p_lo + (uint32_t)(slot * 2 + hh) * (C::PHALF >> 4);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const bool acc = l2 ? (hh > 0 || k > 0) : (n > 0 || k > 0);
-                            mma_ss(tm + dcol, pdesc(hh, slot, k), vdesc(s, hh, k), C::ID_PV, acc ? 1u : 0u);
+                            mma_ss_h(tm + dcol, pb + 2 * k, HI, vb + k * (2048 >> 4), HI, C::ID_PV, acc ? 1u : 0u);
                         }
                         mma_commit(&B.p_empty[hh][slot]);
                         ++use[hh];
@@ -518,9 +516,9 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 if (ok && n >= 1) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
+                const uint32_t kb = k_lo + (uint32_t)s * STG;
 #pragma unroll
-                for (int k = 0; k < DK / 16; ++k)
-                    mma_ss(tm, qdesc(k), kdesc(s, k), C::ID_S, k > 0 ? 1u : 0u);
+                for (int k = 0; k < DK / 16; ++k) mma_ss_h(tm, q_lo + kofs(k), HI, kb + kofs(k), HI, C::ID_S, k > 0 ? 1u : 0u);
                 mma_commit(&B.s_full);
                 if (n >= 1) ok = pv(n - 1);
             }
@@ -533,14 +531,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 if (ok) {
                     tc_fence_after();
                     const uint32_t aslot = sK0 + s * (C::KBYTES + C::VBYTES);
+                    const uint32_t a_lo = sdesc_lo(aslot, DK * 128), c_lo = sdesc_lo(aslot + C::KBYTES, DK * 128);
 #pragma unroll
                     for (int k = 0; k < DK / 16; ++k)
-                        mma_ss(tm, qdesc(k), sdesc_sw128(aslot + k * 2048, DK * 128, 1024), C::ID_PV,
-                               k > 0 ? 1u : 0u);
+                        mma_ss_h(tm, q_lo + kofs(k), HI, a_lo + k * (2048 >> 4), HI, C::ID_PV, k > 0 ? 1u : 0u);
 #pragma unroll
                     for (int k = 0; k < DK / 16; ++k)
-                        mma_ss(tm, qdesc(k), sdesc_sw128(aslot + C::KBYTES + k * 2048, DK * 128, 1024),
-                               C::ID_PV, 1u);
+                        mma_ss_h(tm, q_lo + kofs(k), HI, c_lo + k * (2048 >> 4), HI, C::ID_PV, 1u);
                     mma_commit(&B.o_done);
                 }
             }
