@@ -335,6 +335,11 @@ delta_chain_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             constexpr uint32_t ID_W = idesc_bf16_f32(128, 64, false, true);   // S0 W^T
             constexpr uint32_t ID_Q = idesc_bf16_f32(128, 64, false, false);  // S0 Q^T, U^T P^T
             constexpr uint32_t ID_K = idesc_bf16_f32(128, DK, false, true);   // U^T K
+            // Descriptors as a fixed upper half plus a lower half (address >> 4 |
+            // leading offset): each k step is one 32-bit add in the issue loop.
+            constexpr uint32_t HI = sdesc_hi(1024);
+            auto kmaj = [](int k) { return (uint32_t)((k >> 2) * (16384 >> 4) + (k & 3) * 2); };  // K-major, 64-col blocks of 16 KB
+            const uint32_t s0k = sdesc_lo(sS0, 16), uk = sdesc_lo(sU, 16);
             for (int c = 0; c < nch && ok; ++c) {
                 const int s = c & 1;
                 const uint32_t st = s0 + s * C::STAGE;
@@ -342,35 +347,34 @@ delta_chain_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 if (ok) ok = mbar_wait(&B.s0_ready, c & 1);
                 if (!ok) break;
                 tc_fence_after();
+                const uint32_t v_lo = sdesc_lo(st + C::OV, 8192), g_lo = sdesc_lo(st + C::OG, 8192);
+                const uint32_t w_lo = sdesc_lo(st + C::OW, 16384), q_lo = sdesc_lo(st + C::OQ, 16);
+                const uint32_t p_lo = sdesc_lo(st + C::OP, 16), k_lo = sdesc_lo(st + C::OK_, 8192);
                 // U^T = V^T G^T (K = 64 tokens) + S0 W^T (K = d_k)
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ss(tm + C::COL_U, sdesc_sw128(st + C::OV + k * 2048, 8192, 1024),
-                           sdesc_sw128(st + C::OG + k * 2048, 8192, 1024), ID_U, k > 0 ? 1u : 0u);
+                    mma_ss_h(tm + C::COL_U, v_lo + k * (2048 >> 4), HI, g_lo + k * (2048 >> 4), HI, ID_U,
+                             k > 0 ? 1u : 0u);
 #pragma unroll
                 for (int k = 0; k < DK / 16; ++k)
-                    mma_ss(tm + C::COL_U, sdesc_sw128(sS0 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                           sdesc_sw128(st + C::OW + k * 2048, 16384, 1024), ID_W, 1u);
+                    mma_ss_h(tm + C::COL_U, s0k + kmaj(k), HI, w_lo + k * (2048 >> 4), HI, ID_W, 1u);
                 mma_commit(&B.u_full);
-                // O^T = S0 Q^T
+                // O^T = S0 Q^T (the Q tile's 64-column blocks are 8 KB apart)
 #pragma unroll
                 for (int k = 0; k < DK / 16; ++k)
-                    mma_ss(tm + C::COL_O, sdesc_sw128(sS0 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024),
-                           sdesc_sw128(st + C::OQ + (k >> 2) * 8192 + (k & 3) * 32, 16, 1024), ID_Q,
-                           k > 0 ? 1u : 0u);
+                    mma_ss_h(tm + C::COL_O, s0k + kmaj(k), HI,
+                             q_lo + (uint32_t)((k >> 2) * (8192 >> 4) + (k & 3) * 2), HI, ID_Q, k > 0 ? 1u : 0u);
                 ok = mbar_wait(&B.ut_ready, c & 1);
                 if (!ok) break;
                 tc_fence_after();
                 // O^T += U^T P^T ; S += U^T K
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ss(tm + C::COL_O, sdesc_sw128(sU + k * 32, 16, 1024),
-                           sdesc_sw128(st + C::OP + k * 32, 16, 1024), ID_Q, 1u);
+                    mma_ss_h(tm + C::COL_O, uk + 2 * k, HI, p_lo + 2 * k, HI, ID_Q, 1u);
 #pragma unroll
                 for (int k = 0; k < 4; ++k)
-                    mma_ss(tm + C::COL_S, sdesc_sw128(sU + k * 32, 16, 1024),
-                           sdesc_sw128(st + C::OK_ + k * 2048, 8192, 1024), ID_K,
-                           (c > 0 || has_s0 || k > 0) ? 1u : 0u);
+                    mma_ss_h(tm + C::COL_S, uk + 2 * k, HI, k_lo + k * (2048 >> 4), HI, ID_K,
+                             (c > 0 || has_s0 || k > 0) ? 1u : 0u);
                 mma_commit(&B.o_full);
                 mma_commit(&B.empty[s]);
             }
