@@ -462,7 +462,7 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
     ms, dom = timed_steps(step, K, flush, torch, prof=True, binding=binding)
     fl, by = sparse_work(d["B"], d["H"], d["T"], d["N"], d["d_v"], dens)
     # fp32 path: bound by HBM (its flops are far below any fp32 peak as well)
-    summarize(name, d["B"] * d["T"], ms, fl, by, "sustained", "sparse_read (chunked)", dom)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "sustained", "pair_tile", dom)
     out[name]["density"] = dens
     del q, k, v, y, ws
     return out
