@@ -87,6 +87,15 @@ def delta_work(B, H, T, d_k, d_v, elem, C=64):
     return flops, bytes_
 
 
+def delta_decode_work(S, H, d_k, d_v, elem):
+    """Per decode step: the fp32 state read and written once (two dot products
+    and a rank-1 update, 6 d_k d_v flops), q/k/v and beta in, y out."""
+    SH = S * H
+    flops = SH * 6 * d_k * d_v
+    bytes_ = SH * (2 * d_k * d_v * 4 + (2 * d_k + 2 * d_v) * elem + 4)
+    return flops, bytes_
+
+
 def sparse_work(B, H, T, N, d_v, density):
     """Sparse write + read: 4 nnz d_v flops per token; dense q, k, v read, y written."""
     BH = B * H
@@ -447,6 +456,31 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
     fl, by = delta_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], 2)
     summarize(name, d["B"] * d["T"], ms, fl, by, "sustained", "delta_chain", dom)
     del q, k, v, beta, y, ws
+
+    dname = "delta_decode_bf16_S256_H16_d128_steps64"
+    dd = synth.WORKLOADS[dname].dims
+    S, steps = dd["S"], dd["steps"]
+    dec = synth.delta_decode_inputs(steps, S, dd["H"], dd["d_k"], dd["d_v"], dtype="bf16",
+                                    seed=synth.WORKLOADS[dname].seed)
+    dq, dk_, dv_, db = dec.q.cuda(), dec.k.cuda(), dec.v.cuda(), dec.beta.cuda()
+    Sd = dec.S0.cuda()
+    yd = torch.empty(S, dd["H"], dd["d_v"], dtype=torch.bfloat16, device="cuda")
+    counter = [0]
+
+    def ddstep():
+        i = counter[0] % steps
+        binding.delta_decode_step(Sd, dq[i], dk_[i], dv_[i], db[i], out=yd)
+        counter[0] += 1
+
+    for _ in range(Wm):
+        ddstep()
+    # One timed "step" of this workload = 64 decode steps; the state (256 MiB)
+    # is above L2, so no flush is needed.
+    ms, dom = timed_steps(ddstep, steps, None, torch, prof=True, binding=binding)
+    fl, by = delta_decode_work(S, dd["H"], dd["d_k"], dd["d_v"], 2)
+    summarize(dname, S, ms, fl, by, "sustained", "delta_decode", dom)
+    out[dname]["note"] = "value = decoded tokens/s (256 sequences x 1 token per step, averaged over 64 steps)"
+    del dq, dk_, dv_, db, Sd, yd, dec
 
     name = "bdh_fp32_B2_H4_T2048_N16384_dv256"
     d = synth.WORKLOADS[name].dims

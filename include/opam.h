@@ -12,7 +12,7 @@
  *     as m_t = q_t A; y_t = y_local,t + sigmoid(g) m_t  (tc_layer_forward,
  *     tc_decode_step);
  *   - DeltaNet delta rule e_t = beta_t (v_t - S_{t-1} k_t), S_t = S_{t-1} +
- *     e_t k_t^T, o_t = S_t q_t  (delta_rule_forward);
+ *     e_t k_t^T, o_t = S_t q_t  (delta_rule_forward, delta_decode_step);
  *   - BDH-style additive linear attention over wide, sparse, non-negative keys,
  *     S_t = S_{t-1} + v_t k_t^T, o_t = S_t q_t  (sparse_linattn_forward).
  *
@@ -178,6 +178,25 @@ int delta_rule_forward(const void *q, const void *k, const void *v,
                        float *S_out, void *y, void *workspace,
                        size_t workspace_bytes, void *stream);
 
+/* One DeltaNet decode step for a batch of independent sequences (molayo1419.me,
+ * "DeltaNet-family linear attention variants", section "DeltaNet: write the
+ * prediction error instead of the value"): for every sequence b and head h,
+ *   e = beta (v - S k),  S <- S + e k^T,  y = S q (read after the write),
+ * the same step delta_rule_forward applies to each token, taken one token at a
+ * time from a stored state.
+ *   S      [B][H][d_k][d_v] float32 key-major state (the layout of
+ *          delta_rule_forward's S_out), read and updated in place
+ *   q, k   [B][H][d_k] dtype (one token per sequence and head)
+ *   v      [B][H][d_v] dtype
+ *   beta   [B][H] float32 in [0, 1]
+ *   y      [B][H][d_v] dtype, output
+ * No workspace.  Supported: d_k, d_v in {32, 64, 128}, B*H <= 65535.  Errors
+ * as above; S, q, k, v, beta and y must all be non-NULL.  The state is read
+ * once and written once per call (memory bound). */
+int delta_decode_step(float *S, const void *q, const void *k, const void *v,
+                      const float *beta, int dtype, int B, int H, int d_k, int d_v,
+                      void *y, void *stream);
+
 /* BDH-style linear attention over wide, sparse, non-negative keys
  * (ainews.random.gg BDH memory-architecture post: keys/queries are neuron
  * activations in a very high-dimensional space, the state is the accumulated
@@ -218,9 +237,11 @@ int opam_device_status(int clear);
  * its dominant kernel and `stop` immediately after it, so the caller can time
  * that kernel alone with cudaEventElapsedTime.  The dominant kernel is the
  * fused window-softmax kernel of tc_layer_forward, the split-ring kernel of
- * tc_decode_step, the sequential state pass of delta_rule_forward and the
- * chunked read of sparse_linattn_forward (summed over its launches: `start`
- * goes before the first, `stop` after the last).  Pass NULL, NULL to stop.
+ * tc_decode_step, the sequential state pass of delta_rule_forward, the one
+ * kernel of delta_decode_step, and for sparse_linattn_forward the block-pair
+ * kernel (no start or final state) or else the chunked read and write
+ * (summed over their launches: `start` goes before the first, `stop` after
+ * the last).  Pass NULL, NULL to stop.
  * The records are external, so a call captured into a CUDA graph keeps them
  * as event nodes that fire on every replay.  Events stay owned by the caller.
  * Returns OPAM_OK.

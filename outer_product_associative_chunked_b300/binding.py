@@ -23,7 +23,7 @@ _STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "CUDA", -4: "WORKS
 EXPORTS = (
     "tc_layer_forward_workspace_size", "tc_layer_forward", "tc_layer_forward_noalloc",
     "tc_decode_step_workspace_size", "tc_decode_step",
-    "delta_rule_forward_workspace_size", "delta_rule_forward",
+    "delta_rule_forward_workspace_size", "delta_rule_forward", "delta_decode_step",
     "sparse_linattn_forward_workspace_size", "sparse_linattn_forward",
     "opam_last_error", "opam_profile_events", "opam_kernel_launches", "opam_device_status",
 )
@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.delta_rule_forward_workspace_size.argtypes = [i, i, i, i, i, i, i]
         L.delta_rule_forward.restype = i
         L.delta_rule_forward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
+        L.delta_decode_step.restype = i
+        L.delta_decode_step.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, vp, vp]
         L.sparse_linattn_forward_workspace_size.restype = sz
         L.sparse_linattn_forward_workspace_size.argtypes = [i, i, i, i, i]
         L.sparse_linattn_forward.restype = i
@@ -242,6 +244,24 @@ def delta_rule_forward(q, k, v, beta, chunk=0, S0=None, S_out=None, out=None, wo
     _check(lib().delta_rule_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), dtype_code(q.dtype), B, H,
                                     T, dk, dv, int(chunk), _ptr(S0), _ptr(S_out), _ptr(y), _ptr(ws),
                                     ws.numel(), _stream(stream)))
+    return y
+
+
+def delta_decode_step(S, q, k, v, beta, out=None, stream=None):
+    """One DeltaNet decode step; S [B,H,d_k,d_v] fp32 key-major (updated in
+    place), q,k [B,H,d_k], v [B,H,d_v], beta [B,H] fp32; returns y [B,H,d_v]."""
+    _dev(S, q, k, v, beta, out)
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    if (tuple(k.shape) != (B, H, dk) or tuple(v.shape) != (B, H, dv) or tuple(S.shape) != (B, H, dk, dv)
+            or tuple(beta.shape) != (B, H) or k.dtype != q.dtype or v.dtype != q.dtype
+            or S.dtype != torch.float32 or beta.dtype != torch.float32
+            or (out is not None and (tuple(out.shape) != (B, H, dv) or out.dtype != q.dtype))):
+        raise ValueError("delta_decode_step: shapes or dtypes do not match S [B,H,d_k,d_v] fp32, "
+                         "q,k [B,H,d_k], v [B,H,d_v], beta [B,H] fp32")
+    y = torch.empty(B, H, dv, dtype=q.dtype, device=q.device) if out is None else out
+    _check(lib().delta_decode_step(_ptr(S), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), dtype_code(q.dtype), B,
+                                   H, dk, dv, _ptr(y), _stream(stream)))
     return y
 
 

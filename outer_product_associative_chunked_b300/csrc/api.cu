@@ -296,6 +296,19 @@ int delta_rule_forward(const void *q, const void *k, const void *v, const float 
                       (cudaStream_t)stream);
 }
 
+int delta_decode_step(float *S, const void *q, const void *k, const void *v, const float *beta,
+                      int dtype, int B, int H, int d_k, int d_v, void *y, void *stream) {
+    const char *fn = "delta_decode_step";
+    if (int rc = check_tc_dims(fn, dtype, B, H, 1, d_k, d_v, 1)) return rc;
+    OPAM_CHECK_PTR(S);
+    OPAM_CHECK_PTR(q);
+    OPAM_CHECK_PTR(k);
+    OPAM_CHECK_PTR(v);
+    OPAM_CHECK_PTR(beta);
+    OPAM_CHECK_PTR(y);
+    return delta_decode(S, q, k, v, beta, dtype, B, H, d_k, d_v, y, (cudaStream_t)stream);
+}
+
 size_t sparse_linattn_forward_workspace_size(int B, int H, int T, int N, int d_v) {
     if (B < 1 || H < 1 || T < 1 || N < 1 || N > kSparseMaxN) return 0;
     if (d_v != 32 && d_v != 64 && d_v != 128 && d_v != 256) return 0;

@@ -102,6 +102,10 @@ int delta_tcgen05(const void *q, const void *k, const void *v, const float *beta
                   int dk, const float *S0, float *S_out, void *y, void *ws, cudaStream_t s);
 unsigned int delta_tcgen05_status(bool clear);
 
+// DeltaNet single-token decode (state updated in place, no scratch).
+int delta_decode(float *S, const void *q, const void *k, const void *v, const float *beta, int dtype,
+                 int B, int H, int dk, int dv, void *y, cudaStream_t s);
+
 size_t sparse_workspace(int BH, int T, int N, int dv, bool need_state);
 int sparse_forward(const float *q, const float *k, const float *v, int B, int H, int T, int N,
                    int dv, const float *S0, float *S_out, float *y, void *ws, cudaStream_t s);

@@ -8,6 +8,7 @@ cuda:0 and checks the device status, so an ``ncu`` capture of one launch
     python -m outer_product_associative_chunked_b300.profile_cases prefill_long
     python -m outer_product_associative_chunked_b300.profile_cases decode
     python -m outer_product_associative_chunked_b300.profile_cases delta
+    python -m outer_product_associative_chunked_b300.profile_cases delta_decode
     python -m outer_product_associative_chunked_b300.profile_cases sparse
 
 Inputs come from the seeded generators in ``synth``; the shapes are the
@@ -65,6 +66,14 @@ def delta(B=1, H=16, T=8192, d=128, reps=4):
         binding.delta_rule_forward(q, k, v, beta, chunk=64, out=y, workspace=ws)
 
 
+def delta_decode(S=128, H=16, d=128, reps=4):
+    """DeltaNet decode steps for S sequences x H heads (128 MiB state), bf16 tokens."""
+    dec = synth.delta_decode_inputs(reps, S, H, d, d, dtype="bf16", seed=5)
+    St = dec.S0.cuda()
+    for i in range(reps):
+        binding.delta_decode_step(St, dec.q[i].cuda(), dec.k[i].cuda(), dec.v[i].cuda(), dec.beta[i].cuda())
+
+
 def sparse(B=1, H=2, T=2048, N=16384, dv=256, reps=4):
     """BDH sparse linear attention, ~5% dense keys and queries, fp32."""
     inp = synth.sparse_inputs(B, H, T, N, dv, seed=4)
@@ -77,7 +86,7 @@ def sparse(B=1, H=2, T=2048, N=16384, dv=256, reps=4):
 
 
 CASES = {"prefill": prefill, "prefill_long": prefill_long, "decode": decode, "delta": delta,
-         "sparse": sparse}
+         "delta_decode": delta_decode, "sparse": sparse}
 
 
 def main(argv=None):

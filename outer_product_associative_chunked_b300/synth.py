@@ -13,7 +13,9 @@ Recipes (one per workload of the pages):
   gate g ~ N(0, 1) (or fixed values when given).
 * DeltaNet delta rule (molayo1419.me, "DeltaNet: writing the prediction
   error"): k unit-norm Gaussian, q and v Gaussian, beta_t = logistic(N(0,1))
-  per token and head, so beta lies in (0, 1) as the page requires.
+  per token and head, so beta lies in (0, 1) as the page requires.  Decode
+  steps draw tokens the same way and start from a Gaussian state with
+  entries of variance 1/d_k.
 * BDH-style linear attention (ainews.random.gg BDH post, "low-rank
   factorisation plus ReLU thresholding"): k = ReLU(x U_h - theta) and
   q = ReLU(x' U_h - theta) with x, x' ~ N(0, I_256) per token, one
@@ -117,6 +119,30 @@ def delta_inputs(B, H, T, d_k, d_v, dtype="bf16", seed=2) -> DeltaInputs:
                        beta.float().contiguous(), dtype)
 
 
+@dataclass
+class DeltaDecodeInputs:
+    q: torch.Tensor          # [steps, S, H, d_k]
+    k: torch.Tensor          # [steps, S, H, d_k]  unit rows
+    v: torch.Tensor          # [steps, S, H, d_v]
+    beta: torch.Tensor       # [steps, S, H] float32 in (0,1)
+    S0: torch.Tensor         # [S, H, d_k, d_v] float32 key-major start state
+    dtype: str
+
+
+def delta_decode_inputs(steps, S, H, d_k, d_v, dtype="bf16", seed=104) -> DeltaDecodeInputs:
+    """Single-token DeltaNet steps for S sequences: tokens drawn as in
+    ``delta_inputs``; the start state is Gaussian with entries of variance
+    1/d_k, the scale at which a unit-norm key reads out a unit-variance value."""
+    g = _gen(seed)
+    q = torch.randn(steps, S, H, d_k, generator=g)
+    k = _unit_rows(torch.randn(steps, S, H, d_k, generator=g))
+    v = torch.randn(steps, S, H, d_v, generator=g)
+    beta = torch.sigmoid(torch.randn(steps, S, H, generator=g))
+    S0 = torch.randn(S, H, d_k, d_v, generator=g) / math.sqrt(d_k)
+    return DeltaDecodeInputs(_round(q, dtype), _round(k, dtype), _round(v, dtype),
+                             beta.float().contiguous(), S0.float().contiguous(), dtype)
+
+
 # ---------------------------------------------------------------- BDH
 @dataclass
 class SparseInputs:
@@ -141,7 +167,7 @@ def sparse_inputs(B, H, T, N, d_v, seed=4, rank=256, theta=BDH_THETA_5PCT) -> Sp
 @dataclass
 class Workload:
     name: str
-    kind: str                # "tc" | "tc_decode" | "delta" | "sparse"
+    kind: str                # "tc" | "tc_decode" | "delta" | "delta_decode" | "sparse"
     dims: dict = field(default_factory=dict)
     seed: int = 0
 
@@ -168,6 +194,10 @@ WORKLOADS = {
         "tc_decode_bf16_S64_H16_d128_W2048_steps256", "tc_decode",
         dict(S=64, H=16, d_k=128, d_v=128, W=2048, steps=256, dtype="bf16",
              prefill="tc_bf16_B1_H16_T32768_d128_W2048"), seed=103),
+    # DeltaNet single-token decode from a stored state (state 256 MiB, above L2).
+    "delta_decode_bf16_S256_H16_d128_steps64": Workload(
+        "delta_decode_bf16_S256_H16_d128_steps64", "delta_decode",
+        dict(S=256, H=16, d_k=128, d_v=128, steps=64, dtype="bf16"), seed=104),
     # BDH-style linear attention, wide sparse non-negative keys, fp32.
     "bdh_fp32_B2_H4_T2048_N16384_dv256": Workload(
         "bdh_fp32_B2_H4_T2048_N16384_dv256", "sparse",

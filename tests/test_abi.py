@@ -106,3 +106,19 @@ def test_delta_and_sparse_reject_bad_arguments(L):
     assert s(dv=48) == -2
     assert s(N=0) == -1
     assert s(ws=wss - 1) == -4
+
+
+def test_delta_decode_rejects_bad_arguments(L):
+    call = lambda **kw: L.delta_decode_step(  # noqa: E731
+        kw.get("S", FAKE), kw.get("q", FAKE), FAKE, FAKE, kw.get("beta", FAKE), kw.get("dtype", 1),
+        kw.get("B", 2), 3, kw.get("dk", 64), kw.get("dv", 128), kw.get("y", FAKE), None)
+    assert call(S=None) == -1
+    assert call(q=FAKE + 4) == -1                 # misaligned
+    assert call(beta=None) == -1
+    assert call(y=None) == -1
+    assert call(B=0) == -1
+    assert call(dtype=5) == -1
+    assert call(dk=96) == -2
+    assert call(dv=16) == -2
+    assert call(B=70000) == -2                    # B*H above the grid limit
+    assert "delta_decode_step" in binding.last_error()

@@ -172,3 +172,18 @@ def test_split_sequence_through_exported_state(oracle_mod):
                          want_state=True)
     np.testing.assert_allclose(b["y"], full["y"][:, :, 13:], rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(b["S"], full["S"], rtol=1e-12, atol=1e-13)
+
+
+def test_token_by_token_decode_equals_whole_sequence(oracle_mod):
+    """Decode reading: one-token calls chained through the exported state give
+    the same outputs and final state as one call over the whole sequence."""
+    q, k, v, beta = _inputs(2, 3, 9, 8, 5, 41)
+    S0 = np.random.default_rng(3).standard_normal((2, 3, 8, 5)) * 0.3
+    full = oracle_mod.delta(q, k, v, beta, S0=S0, want_state=True)
+    S = S0
+    for t in range(9):
+        one = oracle_mod.delta(q[:, :, t:t + 1], k[:, :, t:t + 1], v[:, :, t:t + 1], beta[:, :, t:t + 1],
+                               S0=S, want_state=True)
+        np.testing.assert_allclose(one["y"][:, :, 0], full["y"][:, :, t], rtol=1e-12, atol=1e-13)
+        S = one["S"]
+    np.testing.assert_allclose(S, full["S"], rtol=1e-12, atol=1e-13)

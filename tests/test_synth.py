@@ -25,3 +25,15 @@ def test_delta_beta_in_open_unit_interval():
     d = synth.delta_inputs(1, 2, 50, 8, 8, dtype="f32", seed=2)
     assert torch.all((d.beta > 0) & (d.beta < 1))
     assert torch.allclose(d.k.norm(dim=-1), torch.ones(1, 2, 50), atol=1e-6)
+
+
+def test_delta_decode_inputs_shapes_and_ranges():
+    a = synth.delta_decode_inputs(3, 2, 4, 16, 8, dtype="f32", seed=7)
+    b = synth.delta_decode_inputs(3, 2, 4, 16, 8, dtype="f32", seed=7)
+    assert a.q.shape == (3, 2, 4, 16) and a.v.shape == (3, 2, 4, 8) and a.beta.shape == (3, 2, 4)
+    assert a.S0.shape == (2, 4, 16, 8) and a.S0.dtype == torch.float32
+    assert torch.equal(a.S0, b.S0) and torch.equal(a.k, b.k)
+    assert torch.all((a.beta > 0) & (a.beta < 1))
+    assert torch.allclose(a.k.norm(dim=-1), torch.ones(3, 2, 4), atol=1e-6)
+    big = synth.delta_decode_inputs(1, 8, 8, 64, 64, dtype="f32", seed=1)
+    assert abs(float(big.S0.var()) * 64 - 1.0) < 0.05
