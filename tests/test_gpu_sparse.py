@@ -65,6 +65,20 @@ def test_pairwise_form_dense_and_empty_rows(cuda_lib, oracle_mod):
     check_parity(to_np(y), ref["y"], "f32", "pairwise edge rows")
 
 
+def test_pairwise_form_overflowing_key_lists(cuda_lib, oracle_mod):
+    # A key block of fully dense rows: every window's key lists exceed the
+    # shared-memory buffer and are read from global memory; the second block
+    # stays sparse (buffered), and dense queries walk every coordinate.
+    inp = synth.sparse_inputs(1, 1, 250, 700, 128, seed=23)
+    q, k = inp.q.clone(), inp.k.clone()
+    k[0, 0, :128] = torch.rand(128, 700, generator=torch.Generator().manual_seed(2))
+    q[0, 0, 130:140] = torch.rand(10, 700, generator=torch.Generator().manual_seed(3))
+    y = cuda_lib.sparse_linattn_forward(q.cuda(), k.cuda(), inp.v.cuda())
+    torch.cuda.synchronize()
+    ref = oracle_mod.sparse_linattn(q, k, inp.v)
+    check_parity(to_np(y), ref["y"], "f32", "pairwise overflowing key lists")
+
+
 def test_dense_and_empty_rows_in_place_state(cuda_lib, oracle_mod):
     inp = synth.sparse_inputs(1, 2, 70, 300, 32, seed=9)
     q, k = inp.q.clone(), inp.k.clone()
