@@ -828,7 +828,9 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         return;
     }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int jq = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    // Head-major grid: the first wave holds the early query blocks of every
+    // head, and those without an L2 part never wait for the state kernels.
+    const int jq = blockIdx.y, bh = blockIdx.x, h = bh % H;
     const int seg = jq / L;
     const int t0 = jq * kBlk;
     const int kt0 = t0 - W;
@@ -1260,6 +1262,10 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         cudaStream_t st) {
     const int BH = B_ * H;
     const Segments g = segments(BH, T, DV, num_sms());
+    if (DK == 64 && DV == 64 && g.nch > 65535) {  // query blocks are the grid's y extent
+        set_error("tc_layer_forward: T=%d above %d tokens on this path", T, 65535 * kBlk);
+        return OPAM_ERR_UNSUPPORTED;
+    }
     const Ws w = carve(ws, BH, g, DK, DV);
     CUtensorMap mq, mk, mv, ma, mc;
     int rc;
@@ -1304,7 +1310,7 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         CUtensorMap my;
         if ((rc = make_tmap_bf16_3d(&my, y, DV, T, BH, kBlk))) return rc;
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(g.nch, BH);
+        cfg.gridDim = dim3(BH, g.nch);
         cfg.blockDim = dim3(288);
         cfg.dynamicSmemBytes = (size_t)smem;
         cfg.stream = st;
