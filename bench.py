@@ -394,6 +394,34 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
             entry["dominant_kernel_ms"] = statistics.mean(dom)
         out[name] = entry
 
+    # Window-only variant against the full layer on the headline inputs, both
+    # replayed from CUDA graphs back to back: the ratio is the cost of the L2
+    # memory (the pages compare the layer with pure sliding-window attention).
+    name = "tc_window_bf16_B4_H8_T4096_d64_W512"
+    w, d, inp = tc_prefill_setup("tc_bf16_B4_H8_T4096_d64_W512", 0, torch, binding, synth)
+    q, k, v, lam, eta, gate = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate)]
+    y = torch.empty(d["B"], d["H"], d["T"], d["d_v"], dtype=q.dtype, device="cuda")
+    ws = torch.empty(binding.tc_layer_forward_workspace_size(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"],
+                                                             q.dtype), dtype=torch.uint8, device="cuda")
+    win = lambda: binding.tc_window_forward(q, k, v, d["W"], out=y)  # noqa: E731
+    layer = lambda: binding.tc_layer_forward(q, k, v, lam, eta, gate, d["W"], out=y, workspace=ws)  # noqa: E731
+    for _ in range(Wm):
+        win()
+        layer()
+    win_ms, _ = timed_graph_steps(win, 4 * K, flush, torch, binding)
+    layer_ms, _ = timed_graph_steps(layer, 4 * K, flush, torch, binding)
+    fl, by = tc_prefill_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], 2)
+    fl -= d["B"] * d["H"] * max(0, d["T"] - d["W"]) * 2 * d["d_k"] * d["d_v"]  # no L2 read
+    summarize(name, d["B"] * d["T"], win_ms, fl, by, "burst", "tc_fwd (window only)", None)
+    ring = d["W"] * (d["d_k"] + d["d_v"]) * 2
+    out[name].update({
+        "launch": "step captured once into a CUDA graph and replayed",
+        "layer_ms_per_step": statistics.mean(layer_ms),
+        "l2_overhead": statistics.mean(layer_ms) / statistics.mean(win_ms) - 1.0,
+        "state_bytes_per_head": {"window_only": ring, "tensor_cache": ring + d["d_k"] * d["d_v"] * 4},
+    })
+    del q, k, v, y, ws
+
     # Long-context prefill, then the 64-sequence decode continuing from it.
     name = "tc_bf16_B1_H16_T32768_d128_W2048"
     w, d, inp = tc_prefill_setup(name, 0, torch, binding, synth)

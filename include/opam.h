@@ -10,7 +10,7 @@
  *   - Tensor Cache: exact softmax over a ring of the W most recent tokens; a
  *     token evicted from the ring is written A <- lambda A + eta k v^T and read
  *     as m_t = q_t A; y_t = y_local,t + sigmoid(g) m_t  (tc_layer_forward,
- *     tc_decode_step);
+ *     tc_decode_step; tc_window_forward is the ring alone);
  *   - DeltaNet delta rule e_t = beta_t (v_t - S_{t-1} k_t), S_t = S_{t-1} +
  *     e_t k_t^T, o_t = S_t q_t  (delta_rule_forward, delta_decode_step);
  *   - BDH-style additive linear attention over wide, sparse, non-negative keys,
@@ -134,6 +134,22 @@ int tc_layer_forward_noalloc(const void *q, const void *k, const void *v, int dt
                              const float *lambda, const float *eta, const float *gate,
                              float softmax_scale, void *y, opam_tc_state *state_out,
                              void *stream);
+
+/* The window-only variant of the Tensor Cache layer: the L1 ring alone,
+ * i.e. sliding-window softmax attention without the L2 memory ("Tensor
+ * Cache", Results: the layer's throughput is compared with pure
+ * sliding-window attention).  For every token t
+ *   y_t = softmax over keys max(0, t-W+1) .. t of (scale <q_t, k_s>) v_s,
+ * which is tc_layer_forward with eta = 0.  It runs the same forward kernels
+ * with their L2 part switched off and launches no state kernels, so the
+ * difference in time between the two calls is the cost of the L2 memory.
+ *   q, k [B][H][T][d_k] dtype;  v [B][H][T][d_v] dtype;  y [B][H][T][d_v]
+ *   softmax_scale  <= 0 selects 1/sqrt(d_k)
+ * No workspace and no per-head scalars.  Same support and errors as
+ * tc_layer_forward. */
+int tc_window_forward(const void *q, const void *k, const void *v, int dtype,
+                      int B, int H, int T, int d_k, int d_v, int W,
+                      float softmax_scale, void *y, void *stream);
 
 /* One Tensor Cache decode step for a batch of independent sequences
  * ("Tensor Cache", Methodology 1: when the ring overwrites an entry the

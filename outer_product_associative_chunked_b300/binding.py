@@ -21,7 +21,7 @@ _STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "CUDA", -4: "WORKS
 
 # Every symbol the C header declares (checked by the CPU test-suite).
 EXPORTS = (
-    "tc_layer_forward_workspace_size", "tc_layer_forward", "tc_layer_forward_noalloc",
+    "tc_layer_forward_workspace_size", "tc_layer_forward", "tc_layer_forward_noalloc", "tc_window_forward",
     "tc_decode_step_workspace_size", "tc_decode_step",
     "delta_rule_forward_workspace_size", "delta_rule_forward", "delta_decode_step",
     "sparse_linattn_forward_workspace_size", "sparse_linattn_forward",
@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
         L.tc_layer_forward.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, f, vp, sp, vp, sz, vp]
         L.tc_layer_forward_noalloc.restype = i
         L.tc_layer_forward_noalloc.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, f, vp, sp, vp]
+        L.tc_window_forward.restype = i
+        L.tc_window_forward.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, f, vp, vp]
         L.tc_decode_step_workspace_size.restype = sz
         L.tc_decode_step_workspace_size.argtypes = [sp]
         L.tc_decode_step.restype = i
@@ -208,6 +210,18 @@ def tc_layer_forward_noalloc(q, k, v, lam, eta, gate, W, out, softmax_scale=0.0,
                                           int(W), _ptr(lam), _ptr(eta), _ptr(gate), float(softmax_scale),
                                           _ptr(out), st, _stream(stream)))
     return out
+
+
+def tc_window_forward(q, k, v, W, softmax_scale=0.0, out=None, stream=None):
+    """Window-only variant (the ring alone, no L2 memory); q,k [B,H,T,d_k],
+    v [B,H,T,d_v]; returns y [B,H,T,d_v]."""
+    _dev(q, k, v, out)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    y = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device) if out is None else out
+    _check(lib().tc_window_forward(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), B, H, T, dk, dv, int(W),
+                                   float(softmax_scale), _ptr(y), _stream(stream)))
+    return y
 
 
 def tc_decode_step_workspace_size(state: TCState) -> int:

@@ -218,6 +218,23 @@ int tc_layer_forward(const void *q, const void *k, const void *v, int dtype, int
     return OPAM_OK;
 }
 
+int tc_window_forward(const void *q, const void *k, const void *v, int dtype, int B, int H, int T,
+                      int d_k, int d_v, int W, float softmax_scale, void *y, void *stream) {
+    const char *fn = "tc_window_forward";
+    if (int rc = check_tc_dims(fn, dtype, B, H, T, d_k, d_v, W)) return rc;
+    OPAM_CHECK_PTR(q);
+    OPAM_CHECK_PTR(k);
+    OPAM_CHECK_PTR(v);
+    OPAM_CHECK_PTR(y);
+    cudaStream_t s = (cudaStream_t)stream;
+    const float scale = resolve_scale(softmax_scale, d_k);
+    if (tc_prefill_tcgen05_supported(dtype, d_k, d_v))
+        return tc_prefill_tcgen05(q, k, v, B, H, T, d_k, d_v, W, nullptr, nullptr, nullptr, scale, y, nullptr,
+                                  nullptr, s, false);
+    return tc_prefill_simt(q, k, v, dtype, B, H, T, d_k, d_v, W, nullptr, nullptr, nullptr, scale, y, nullptr,
+                           nullptr, s, false);
+}
+
 size_t tc_decode_step_workspace_size(const opam_tc_state *st) {
     if (!st) return 0;
     if (check_tc_dims("tc_decode_step_workspace_size", st->dtype, st->B, st->H, 1, st->d_k, st->d_v,

@@ -67,10 +67,12 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // ---------------------------------------------------------------- launchers
 // Tensor Cache prefill, CUDA-core path (any supported head size / dtype).
 size_t tc_prefill_simt_workspace(int BH, int T, int dk, int dv, int W);
+// l2 = false: window only (the L1 ring); lam, eta, gate, A_final and ws are
+// then unused and may be NULL.
 int tc_prefill_simt(const void *q, const void *k, const void *v, int dtype, int B, int H,
                     int T, int dk, int dv, int W, const float *lam, const float *eta,
                     const float *gate, float scale, void *y, float *A_final,
-                    void *ws, cudaStream_t s);
+                    void *ws, cudaStream_t s, bool l2 = true);
 // Ring / pos export after a prefill (A is written by the prefill itself).
 int tc_export_ring(const void *k, const void *v, int dtype, int B, int H, int T, int dk,
                    int dv, int W, void *ring_k, void *ring_v, int64_t *pos, cudaStream_t s);
@@ -80,7 +82,7 @@ bool tc_prefill_tcgen05_supported(int dtype, int dk, int dv);
 size_t tc_prefill_tcgen05_workspace(int BH, int T, int dk, int dv);
 int tc_prefill_tcgen05(const void *q, const void *k, const void *v, int B, int H, int T, int dk,
                        int dv, int W, const float *lam, const float *eta, const float *gate,
-                       float scale, void *y, float *A_final, void *ws, cudaStream_t s);
+                       float scale, void *y, float *A_final, void *ws, cudaStream_t s, bool l2 = true);
 // Status bits recorded by bounded waits that ran out (0 = none); reads the
 // device word synchronously and optionally clears it.
 unsigned int tc_prefill_tcgen05_status(bool clear);

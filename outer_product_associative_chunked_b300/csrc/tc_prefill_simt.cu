@@ -102,7 +102,8 @@ __global__ void __launch_bounds__(256)
 tc_fwd_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                    int T_, int W, int H, const float *__restrict__ lam,
                    const float *__restrict__ eta, const float *__restrict__ gate, float scale,
-                   const float *__restrict__ Abuf, int nch, T *__restrict__ y) {
+                   const float *__restrict__ Abuf, int nch, int l2, T *__restrict__ y) {
+    // l2 == 0: window only (no L2 weights, no state read, no gate term).
     using SM = FwdSmem<DK, DV>;
     extern __shared__ float sm[];
     float *Qs = sm;                       // [kC][DK+1]
@@ -119,7 +120,7 @@ tc_fwd_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
     const int j = blockIdx.x, bh = blockIdx.y, h = bh % H;
     const int t0 = j * kC;
     const int nq = min(kC, T_ - t0);
-    const float lm = lam[h], et = eta[h];
+    const float lm = l2 ? lam[h] : 0.f, et = l2 ? eta[h] : 0.f;
     const size_t qbase = (size_t)bh * T_;
 
     for (int idx = tid; idx < kC * DK; idx += 256) {
@@ -139,7 +140,7 @@ tc_fwd_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 
     const int kstart = t0 - W, kend = t0 + nq;
     for (int kt = kstart; kt < kend; kt += kC) {
-        const bool first = (kt == kstart);
+        const bool first = l2 && (kt == kstart);  // the L2 part lives in the first tile
         if (kt + kC <= 0) continue;  // whole tile before position 0
         __syncthreads();
         for (int idx = tid; idx < kC * DK; idx += 256) {
@@ -231,21 +232,25 @@ tc_fwd_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
     }
     __syncthreads();
     // Carried-state read lambda^(i+1) q A_j and the gated fuse.
-    const float *Aj = Abuf + ((size_t)bh * (nch + 1) + j) * (size_t)(DK * DV);
-    for (int idx = tid; idx < DK * DV; idx += 256) As[idx] = Aj[idx];
+    if (l2) {
+        const float *Aj = Abuf + ((size_t)bh * (nch + 1) + j) * (size_t)(DK * DV);
+        for (int idx = tid; idx < DK * DV; idx += 256) As[idx] = Aj[idx];
+    }
     __syncthreads();
     if (prow < nq) {
         float m2[NC];
 #pragma unroll
         for (int c = 0; c < NC; ++c) m2[c] = 0.f;
-        for (int a = 0; a < DK; ++a) {
-            const float qa = Qs[prow * (DK + 1) + a];
+        if (l2) {
+            for (int a = 0; a < DK; ++a) {
+                const float qa = Qs[prow * (DK + 1) + a];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) m2[c] = fmaf(qa, As[a * DV + part + 4 * c], m2[c]);
+                for (int c = 0; c < NC; ++c) m2[c] = fmaf(qa, As[a * DV + part + 4 * c], m2[c]);
+            }
         }
         const float inv_l = 1.0f / ls[prow];
-        const float decay = powf(lm, (float)(prow + 1));
-        const float sg = 1.0f / (1.0f + expf(-gate[h]));
+        const float decay = l2 ? powf(lm, (float)(prow + 1)) : 0.f;
+        const float sg = l2 ? 1.0f / (1.0f + expf(-gate[h])) : 0.f;
         T *yr = y + (qbase + t0 + prow) * DV;
 #pragma unroll
         for (int c = 0; c < NC; ++c)
@@ -275,13 +280,13 @@ __global__ void set_pos_kernel(int64_t *pos, int B, int64_t value) {
 template <typename T, int DK, int DV>
 int launch_fwd(const void *q, const void *k, const void *v, int BH, int T_, int W, int H,
                const float *lam, const float *eta, const float *gate, float scale,
-               const float *Abuf, int nch, void *y, cudaStream_t s) {
+               const float *Abuf, int nch, int l2, void *y, cudaStream_t s) {
     auto kern = tc_fwd_simt_kernel<T, DK, DV>;
     const size_t smem = FwdSmem<DK, DV>::kBytes;
     if (int rc_ = set_smem_limit((const void *)kern, (int)smem, "tc_fwd_simt smem attribute")) return rc_;
     prof_begin(s);
     kern<<<dim3(nch, BH), 256, smem, s>>>((const T *)q, (const T *)k, (const T *)v, T_, W, H, lam,
-                                          eta, gate, scale, Abuf, nch, (T *)y);
+                                          eta, gate, scale, Abuf, nch, l2, (T *)y);
     const int rc = launched("tc_fwd_simt");
     prof_end(s);
     return rc;
@@ -290,11 +295,11 @@ int launch_fwd(const void *q, const void *k, const void *v, int BH, int T_, int 
 template <typename T, int DK>
 int dispatch_dv(int dv, const void *q, const void *k, const void *v, int BH, int T_, int W,
                 int H, const float *lam, const float *eta, const float *gate, float scale,
-                const float *Abuf, int nch, void *y, cudaStream_t s) {
+                const float *Abuf, int nch, int l2, void *y, cudaStream_t s) {
     switch (dv) {
-        case 32: return launch_fwd<T, DK, 32>(q, k, v, BH, T_, W, H, lam, eta, gate, scale, Abuf, nch, y, s);
-        case 64: return launch_fwd<T, DK, 64>(q, k, v, BH, T_, W, H, lam, eta, gate, scale, Abuf, nch, y, s);
-        case 128: return launch_fwd<T, DK, 128>(q, k, v, BH, T_, W, H, lam, eta, gate, scale, Abuf, nch, y, s);
+        case 32: return launch_fwd<T, DK, 32>(q, k, v, BH, T_, W, H, lam, eta, gate, scale, Abuf, nch, l2, y, s);
+        case 64: return launch_fwd<T, DK, 64>(q, k, v, BH, T_, W, H, lam, eta, gate, scale, Abuf, nch, l2, y, s);
+        case 128: return launch_fwd<T, DK, 128>(q, k, v, BH, T_, W, H, lam, eta, gate, scale, Abuf, nch, l2, y, s);
     }
     set_error("d_v=%d unsupported", dv);
     return OPAM_ERR_UNSUPPORTED;
@@ -303,23 +308,25 @@ int dispatch_dv(int dv, const void *q, const void *k, const void *v, int BH, int
 template <typename T>
 int run(const void *q, const void *k, const void *v, int B, int H, int T_, int dk, int dv, int W,
         const float *lam, const float *eta, const float *gate, float scale, void *y,
-        float *A_final, void *ws, cudaStream_t s) {
+        float *A_final, void *ws, cudaStream_t s, int l2) {
     const int BH = B * H, nch = ceil_div(T_, kC);
     float *buf = (float *)ws;
-    {
+    if (l2) {
         const size_t smem = sizeof(float) * kC * (dk + dv);
         if (int rc_ = set_smem_limit((const void *)tc_chunk_delta_kernel<T>, (int)smem, "tc_chunk_delta smem attribute")) return rc_;
         tc_chunk_delta_kernel<T><<<dim3(nch, BH), 256, smem, s>>>((const T *)k, (const T *)v, T_, dk,
                                                                   dv, W, H, lam, eta, buf, nch);
         if (int rc = launched("tc_chunk_delta")) return rc;
     }
-    tc_chunk_scan_kernel<<<dim3(ceil_div(dk * dv, 256), BH), 256, 0, s>>>(buf, nch, T_, dk * dv, H,
-                                                                          lam, A_final);
-    if (int rc = launched("tc_chunk_scan")) return rc;
+    if (l2) {
+        tc_chunk_scan_kernel<<<dim3(ceil_div(dk * dv, 256), BH), 256, 0, s>>>(buf, nch, T_, dk * dv, H,
+                                                                              lam, A_final);
+        if (int rc = launched("tc_chunk_scan")) return rc;
+    }
     switch (dk) {
-        case 32: return dispatch_dv<T, 32>(dv, q, k, v, BH, T_, W, H, lam, eta, gate, scale, buf, nch, y, s);
-        case 64: return dispatch_dv<T, 64>(dv, q, k, v, BH, T_, W, H, lam, eta, gate, scale, buf, nch, y, s);
-        case 128: return dispatch_dv<T, 128>(dv, q, k, v, BH, T_, W, H, lam, eta, gate, scale, buf, nch, y, s);
+        case 32: return dispatch_dv<T, 32>(dv, q, k, v, BH, T_, W, H, lam, eta, gate, scale, buf, nch, l2, y, s);
+        case 64: return dispatch_dv<T, 64>(dv, q, k, v, BH, T_, W, H, lam, eta, gate, scale, buf, nch, l2, y, s);
+        case 128: return dispatch_dv<T, 128>(dv, q, k, v, BH, T_, W, H, lam, eta, gate, scale, buf, nch, l2, y, s);
     }
     set_error("d_k=%d unsupported", dk);
     return OPAM_ERR_UNSUPPORTED;
@@ -335,10 +342,10 @@ size_t tc_prefill_simt_workspace(int BH, int T, int dk, int dv, int W) {
 
 int tc_prefill_simt(const void *q, const void *k, const void *v, int dtype, int B, int H, int T,
                     int dk, int dv, int W, const float *lam, const float *eta, const float *gate,
-                    float scale, void *y, float *A_final, void *ws, cudaStream_t s) {
+                    float scale, void *y, float *A_final, void *ws, cudaStream_t s, bool l2) {
     if (dtype == OPAM_BF16)
-        return run<__nv_bfloat16>(q, k, v, B, H, T, dk, dv, W, lam, eta, gate, scale, y, A_final, ws, s);
-    return run<float>(q, k, v, B, H, T, dk, dv, W, lam, eta, gate, scale, y, A_final, ws, s);
+        return run<__nv_bfloat16>(q, k, v, B, H, T, dk, dv, W, lam, eta, gate, scale, y, A_final, ws, s, l2);
+    return run<float>(q, k, v, B, H, T, dk, dv, W, lam, eta, gate, scale, y, A_final, ws, s, l2);
 }
 
 int tc_export_ring(const void *k, const void *v, int dtype, int B, int H, int T, int dk, int dv,

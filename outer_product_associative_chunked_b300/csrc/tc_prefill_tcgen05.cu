@@ -357,7 +357,7 @@ template <int DK, int DV>
 __global__ void __launch_bounds__(320, 1)
 tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ma,
-              const __grid_constant__ CUtensorMap mc, int T, int W, int H, int nch, int nseg, int L,
+              const __grid_constant__ CUtensorMap mc, int T, int W, int H, int nch, int nseg, int L, int l2,
               const float *__restrict__ lam, const float *__restrict__ eta,
               const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y) {
     using C = Fwd<DK, DV>;
@@ -378,7 +378,8 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const int nt_total = (W + kBlk - 1) / kBlk + 1;
     const int j_first = (-kt0 - (kBlk - 1) > 0) ? (-kt0) / kBlk : 0;
     const int ntiles = nt_total - j_first;
-    const bool has_l2 = (j_first == 0);
+    // l2 == 0: window only (no L2 part, no state loads, no q A term).
+    const bool has_l2 = l2 && (j_first == 0);
 
     if (warp == 9) tmem_alloc(&B.tbase, 512);
     if (tid == 0) {
@@ -401,7 +402,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         mbar_init(&B.drain, 1);
         mbar_fence_init();
     }
-    if (tid < kBlk) B.pw[tid] = eta[h] * powf(lam[h], (float)tid);
+    if (l2 && tid < kBlk) B.pw[tid] = eta[h] * powf(lam[h], (float)tid);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -421,7 +422,8 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             mbar_expect_tx(&B.q_full, C::QBYTES);
 #pragma unroll
             for (int b = 0; b < DK / 64; ++b) tma_load_3d(sm + b * 16384, &mq, &B.q_full, 64 * b, t0, bh);
-            for (int n = 0; n <= ntiles && ok; ++n) {
+            const int nload = ntiles + (l2 ? 1 : 0);  // the last load is A_j^loc + carry
+            for (int n = 0; n < nload && ok; ++n) {
                 const int s = n % NST;
                 if (n >= NST) ok = mbar_wait(&B.kv_empty[s], ((n / NST) - 1) & 1);
                 if (!ok) break;
@@ -444,10 +446,10 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                     }
                 }
             }
-            if (ok) ok = mbar_wait(&B.k_full[sA], (ntiles / NST) & 1);
+            if (ok && l2) ok = mbar_wait(&B.k_full[sA], (ntiles / NST) & 1);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok) {
+        if (ok && l2) {
             // Carry times lambda^(C (j - gL)), in place, so q A_j^loc and the
             // carry share one accumulator.
             const float c = powf(lam[h], (float)(kBlk * (jq - seg * L)));
@@ -466,7 +468,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             fence_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&B.c_ready);
-        } else if (lane == 0) {
+        } else if (!ok && lane == 0) {
             atomicOr(&g_status, kStFwdProducer);
         }
         __syncwarp();
@@ -523,7 +525,8 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 if (n >= 1) ok = pv(n - 1);
             }
             if (ok) ok = pv(ntiles - 1);
-            if (ok) {  // q (A_j^loc + c A_{gL}) into the S columns
+            if (ok && !l2) mma_commit(&B.o_done);
+            if (ok && l2) {  // q (A_j^loc + c A_{gL}) into the S columns
                 const int n = ntiles, s = n % NST;
                 ok = mbar_wait(&B.k_full[s], (n / NST) & 1);
                 if (ok) ok = mbar_wait(&B.c_ready, 0);
@@ -595,7 +598,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) mbar_arrive(&B.s_empty);
 
-            if (j == 0) {  // L2 part of the shifted chunk: keys l <= r at positions >= 0
+            if (has_l2 && j == 0) {  // L2 part of the shifted chunk: keys l <= r at positions >= 0
                 const int lo = max(0, -kt);
                 ok = __all_sync(0xffffffffu, wait_slot(use));
                 if (!ok) break;
@@ -720,8 +723,8 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             const float lsum = B.xl[0][r] * f0 + B.xl[1][r] * f1;
             const float inv_l = lsum > 0.f ? 1.0f / lsum : 0.f;
             const float w0 = f0 * inv_l, w1 = f1 * inv_l;
-            const float sg = 1.0f / (1.0f + expf(-gate[h]));
-            const float decay = powf(lam[h], (float)(r + 1));
+            const float sg = l2 ? 1.0f / (1.0f + expf(-gate[h])) : 0.f;
+            const float decay = l2 ? powf(lam[h], (float)(r + 1)) : 0.f;
             __nv_bfloat16 *yr = y + ((size_t)bh * T + t) * DV;
 #pragma unroll 1
             for (int cc = 0; cc < DV / 2; cc += 16) {
@@ -740,7 +743,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
                             const int e = 2 * i + u;
-                            const float mem = fmaf(decay, qa[e], has_l2 ? o2[e] : 0.f);
+                            const float mem = l2 ? fmaf(decay, qa[e], has_l2 ? o2[e] : 0.f) : 0.f;
                             v2[u] = fmaf(o0[e], w0, fmaf(o1[e], w1, sg * mem));
                         }
                         pk[i] = pack_bf16(v2[0], v2[1]);
@@ -816,7 +819,7 @@ __global__ void __launch_bounds__(288, 2)
 tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                   const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ma,
                   const __grid_constant__ CUtensorMap mc, const __grid_constant__ CUtensorMap my, int T, int W,
-                  int H, int nch, int nseg, int L,
+                  int H, int nch, int nseg, int L, int l2,
                   const float *__restrict__ lam, const float *__restrict__ eta,
                   const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y) {
     using C = FwdRow<DK, DV>;
@@ -837,7 +840,8 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     const int nt_total = (W + kBlk - 1) / kBlk + 1;
     const int j_first = (-kt0 - (kBlk - 1) > 0) ? (-kt0) / kBlk : 0;
     const int ntiles = nt_total - j_first;
-    const bool has_l2 = (j_first == 0);
+    // l2 == 0: window only (no L2 part, no state loads, no q A term).
+    const bool has_l2 = l2 && (j_first == 0);
     // Key tile j covers keys kt0 + 128 j ..; with an L2 part the tiles run
     // 1, 2, .., nt-1 and the shifted chunk (j = 0) comes last.
     auto tile_j = [&](int n) { return has_l2 ? (n + 1 < ntiles ? n + 1 : 0) : j_first + n; };
@@ -900,7 +904,7 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
     __syncwarp();
     if (warp == 8) tmem_alloc(&B.tbase, C::TCOLS);
     if (tid < 32) B.pwz[tid] = 0.f;
-    if (tid <= kBlk) {
+    if (l2 && tid <= kBlk) {
         const float lh = lam[h];
         const float pw = powf(lh, (float)tid);
         B.lpow[tid] = pw;
@@ -994,7 +998,7 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         const int r = 32 * q4 + lane;
         const uint32_t lrow = (uint32_t)(q4 * 32) << 16;
         const float sc = scale * kLog2e;
-        const float sig = 1.0f / (1.0f + expf(-gate[h]));
+        const float sig = l2 ? 1.0f / (1.0f + expf(-gate[h])) : 0.f;
         float m = kNegBig, l = 0.f;  // l: this half's share of the row sum
         uint32_t xn = 0;             // exchanges so far (both halves count alike)
         float Lrow = 0.f;  // the row's softmax sum over both halves, once known
@@ -1259,46 +1263,48 @@ int num_sms() { return device_sm_count(); }
 template <int DK, int DV>
 int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W, const float *lam,
         const float *eta, const float *gate, float scale, void *y, float *A_final, void *ws,
-        cudaStream_t st) {
+        cudaStream_t st, bool l2) {
     const int BH = B_ * H;
     const Segments g = segments(BH, T, DV, num_sms());
     if (DK == 64 && DV == 64 && g.nch > 65535) {  // query blocks are the grid's y extent
         set_error("tc_layer_forward: T=%d above %d tokens on this path", T, 65535 * kBlk);
         return OPAM_ERR_UNSUPPORTED;
     }
-    const Ws w = carve(ws, BH, g, DK, DV);
-    CUtensorMap mq, mk, mv, ma, mc;
+    CUtensorMap mq, mk, mv, ma{}, mc{};  // ma, mc stay unused (zero) without the L2 part
     int rc;
     if ((rc = make_tmap_bf16_3d(&mq, q, DK, T, BH, kBlk))) return rc;
     if ((rc = make_tmap_bf16_3d(&mk, k, DK, T, BH, kBlk))) return rc;
     if ((rc = make_tmap_bf16_3d(&mv, v, DV, T, BH, kBlk))) return rc;
-    if ((rc = make_tmap_bf16_3d(&ma, w.Aloc, DV, DK, (uint64_t)BH * g.nch, DK))) return rc;
-    if ((rc = make_tmap_bf16_3d(&mc, w.Cbf, DV, DK, (uint64_t)BH * g.nseg, DK))) return rc;
-    {
-        using SC = StateCfg<DK>;
-        auto kern = tc_l2_state_kernel<DK, DV>;
-        if (int rc_ = set_smem_limit((const void *)kern, (int)SC::SMEM, "tc_l2_state smem attribute")) return rc_;
-        kern<<<dim3(DV / 64, g.nseg, BH), 192, SC::SMEM, st>>>(mk, mv, T, W, H, lam, eta, g.nch, g.L, w.Aloc,
-                                                              w.Lfin);
-        if ((rc = launched("tc_l2_state"))) return rc;
-    }
     // The carry kernel and the d = 64 forward kernel are programmatic dependents:
     // each may start before its predecessor finishes and waits (griddepcontrol)
     // only where it reads that predecessor's output.
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
-    {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(ceil_div(DK * DV / 4, 128), BH);
-        cfg.blockDim = dim3(128);
-        cfg.stream = st;
-        cfg.attrs = pdl;
-        cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, tc_l2_carry_kernel, (const float *)w.Lfin, g.nseg, g.L, T,
-                                           DK * DV, H, lam, w.Cbf, A_final);
-        if (e != cudaSuccess) return cuda_fail(e, "tc_l2_carry launch");
-        if ((rc = launched("tc_l2_carry"))) return rc;
+    if (l2) {
+        const Ws w = carve(ws, BH, g, DK, DV);
+        if ((rc = make_tmap_bf16_3d(&ma, w.Aloc, DV, DK, (uint64_t)BH * g.nch, DK))) return rc;
+        if ((rc = make_tmap_bf16_3d(&mc, w.Cbf, DV, DK, (uint64_t)BH * g.nseg, DK))) return rc;
+        {
+            using SC = StateCfg<DK>;
+            auto kern = tc_l2_state_kernel<DK, DV>;
+            if (int rc_ = set_smem_limit((const void *)kern, (int)SC::SMEM, "tc_l2_state smem attribute")) return rc_;
+            kern<<<dim3(DV / 64, g.nseg, BH), 192, SC::SMEM, st>>>(mk, mv, T, W, H, lam, eta, g.nch, g.L, w.Aloc,
+                                                                  w.Lfin);
+            if ((rc = launched("tc_l2_state"))) return rc;
+        }
+        {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(ceil_div(DK * DV / 4, 128), BH);
+            cfg.blockDim = dim3(128);
+            cfg.stream = st;
+            cfg.attrs = pdl;
+            cfg.numAttrs = 1;
+            cudaError_t e = cudaLaunchKernelEx(&cfg, tc_l2_carry_kernel, (const float *)w.Lfin, g.nseg, g.L, T,
+                                               DK * DV, H, lam, w.Cbf, A_final);
+            if (e != cudaSuccess) return cuda_fail(e, "tc_l2_carry launch");
+            if ((rc = launched("tc_l2_carry"))) return rc;
+        }
     }
     if constexpr (DK == 64 && DV == 64) {
         using Cfg = FwdRow<DK, DV>;
@@ -1314,10 +1320,10 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         cfg.blockDim = dim3(288);
         cfg.dynamicSmemBytes = (size_t)smem;
         cfg.stream = st;
-        cfg.attrs = pdl;
-        cfg.numAttrs = 1;
-        cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, ma, mc, my, T, W, H, g.nch, g.nseg, g.L, lam, eta,
-                                           gate, scale, (__nv_bfloat16 *)y);
+        cfg.attrs = pdl;  // window only: no state kernels, so ordinary stream order
+        cfg.numAttrs = l2 ? 1 : 0;
+        cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, ma, mc, my, T, W, H, g.nch, g.nseg, g.L,
+                                           (int)l2, lam, eta, gate, scale, (__nv_bfloat16 *)y);
         rc = e != cudaSuccess ? cuda_fail(e, "tc_fwd_row launch") : launched("tc_fwd_row");
         prof_end(st);
         return rc;
@@ -1328,8 +1334,8 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         const int smem = (int)(Cfg::OFF_BARS + sizeof(FwdBars));
         if (int rc_ = set_smem_limit((const void *)kern, smem, "tc_fwd smem attribute")) return rc_;
         prof_begin(st);
-        kern<<<dim3(g.nch, BH), 320, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, lam, eta,
-                                                  gate, scale, (__nv_bfloat16 *)y);
+        kern<<<dim3(g.nch, BH), 320, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, (int)l2, lam,
+                                                  eta, gate, scale, (__nv_bfloat16 *)y);
         rc = launched("tc_fwd");
         prof_end(st);
         return rc;
@@ -1348,11 +1354,14 @@ size_t tc_prefill_tcgen05_workspace(int BH, int T, int dk, int dv) {
 
 int tc_prefill_tcgen05(const void *q, const void *k, const void *v, int B, int H, int T, int dk,
                        int dv, int W, const float *lam, const float *eta, const float *gate,
-                       float scale, void *y, float *A_final, void *ws, cudaStream_t s) {
-    if (dk == 64 && dv == 64) return run<64, 64>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s);
-    if (dk == 64 && dv == 128) return run<64, 128>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s);
-    if (dk == 128 && dv == 64) return run<128, 64>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s);
-    if (dk == 128 && dv == 128) return run<128, 128>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s);
+                       float scale, void *y, float *A_final, void *ws, cudaStream_t s, bool l2) {
+    if (dk == 64 && dv == 64) return run<64, 64>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s, l2);
+    if (dk == 64 && dv == 128)
+        return run<64, 128>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s, l2);
+    if (dk == 128 && dv == 64)
+        return run<128, 64>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s, l2);
+    if (dk == 128 && dv == 128)
+        return run<128, 128>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s, l2);
     set_error("tensor-core prefill: d_k=%d d_v=%d unsupported", dk, dv);
     return OPAM_ERR_UNSUPPORTED;
 }

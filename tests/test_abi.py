@@ -122,3 +122,16 @@ def test_delta_decode_rejects_bad_arguments(L):
     assert call(dv=16) == -2
     assert call(B=70000) == -2                    # B*H above the grid limit
     assert "delta_decode_step" in binding.last_error()
+
+
+def test_window_forward_rejects_bad_arguments(L):
+    call = lambda **kw: L.tc_window_forward(  # noqa: E731
+        kw.get("q", FAKE), FAKE, FAKE, kw.get("dtype", 1), 1, 2, kw.get("T", 16), kw.get("dk", 64), 64,
+        kw.get("W", 4), 0.0, kw.get("y", FAKE), None)
+    assert call(q=None) == -1
+    assert call(y=FAKE + 8) == -1                 # misaligned
+    assert call(T=0) == -1
+    assert call(W=0) == -1
+    assert call(dtype=3) == -1
+    assert call(dk=96) == -2
+    assert "tc_window_forward" in binding.last_error()

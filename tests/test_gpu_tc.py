@@ -159,3 +159,41 @@ def test_full_size_workload_sampled(cuda_lib, oracle_mod, name, units):
         ref.append(oracle_mod.tc_output_at(inp.q[b, h], inp.k[b, h], inp.v[b, h], float(inp.lam[h]),
                                            float(inp.eta[h]), float(inp.gate[h]), inp.W, ts))
     check_parity(np.stack(got), np.stack(ref), "bf16", name)
+
+
+# Window-only variant: the same kernels with the L2 part off.  Its reference
+# is the oracle layer with eta = 0 (A stays 0, so y is the window softmax).
+@pytest.mark.parametrize("dtype,B,H,T,dk,dv,W", [
+    ("bf16", 2, 3, 700, 64, 64, 512),     # row kernel: blocks with and without a shifted first tile
+    ("bf16", 1, 2, 1000, 64, 64, 129),
+    ("bf16", 1, 1, 300, 64, 64, 1),
+    ("bf16", 1, 1, 400, 64, 64, 1000),    # window longer than the sequence
+    ("bf16", 1, 2, 520, 128, 128, 300),   # split-key-half kernel
+    ("bf16", 2, 1, 333, 64, 128, 129),
+    ("f32", 1, 2, 333, 32, 32, 77),       # CUDA-core kernel
+    ("f32", 2, 1, 200, 64, 128, 64),
+    ("bf16", 1, 1, 150, 32, 128, 50),     # bf16 on the CUDA-core kernel
+])
+def test_window_only_matches_eta_zero(cuda_lib, oracle_mod, dtype, B, H, T, dk, dv, W):
+    inp = synth.tc_inputs(B, H, T, dk, dv, W, dtype=dtype, seed=T + W)
+    y, buf = guarded((B, H, T, dv), inp.q.dtype)
+    cuda_lib.tc_window_forward(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), W, out=y)
+    torch.cuda.synchronize()
+    assert canary_intact(buf, (B, H, T, dv))
+    ref = oracle_mod.tc_prefill(inp.q, inp.k, inp.v, inp.lam, torch.zeros(H), inp.gate, W)["y"]
+    check_parity(to_np(y), ref, dtype, f"window only {dtype} T={T} d={dk}/{dv} W={W}")
+
+
+def test_window_only_headline_workload_sampled(cuda_lib, oracle_mod):
+    w = synth.WORKLOADS["tc_bf16_B4_H8_T4096_d64_W512"]
+    d = w.dims
+    inp = synth.tc_inputs(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], dtype=d["dtype"], seed=w.seed)
+    y = cuda_lib.tc_window_forward(inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), inp.W)
+    torch.cuda.synchronize()
+    ts = _sampled_positions(d["T"], d["W"])
+    got, ref = [], []
+    for b, h in [(0, 0), (2, 5), (3, 7)]:
+        got.append(to_np(y[b, h, ts]))
+        ref.append(oracle_mod.tc_output_at(inp.q[b, h], inp.k[b, h], inp.v[b, h], float(inp.lam[h]), 0.0,
+                                           float(inp.gate[h]), inp.W, ts))
+    check_parity(np.stack(got), np.stack(ref), "bf16", "window only, headline workload")
