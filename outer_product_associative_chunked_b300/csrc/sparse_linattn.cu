@@ -291,9 +291,9 @@ csc_build_kernel(int T, int N, int nb, const int *__restrict__ kidx, const float
 //   coordinate at a time, its lanes an 8 x 4 grid over (query entry, key
 //   entry) pairs of that coordinate's lists.  A window whose
 //   lists do not fit the buffers (dense inputs) is read from global memory.
-//   Then o[tb] += Z V[sb]  (fp32, 128 output columns per pass, float atomics).
-constexpr int kJW = 256;    // coordinates per window
-constexpr int kCap = 3072;  // list entries per window buffered in shared memory
+//   Then o[tb] += Z V[sb]  (fp32, 64 output columns per pass, float4 atomics).
+constexpr int kJW = 64;    // coordinates per window
+constexpr int kCap = 768;  // list entries per window buffered in shared memory (3 CTAs per SM)
 
 struct PairSmem {
     float Z[kTB * (kTB + 1)];
@@ -303,7 +303,7 @@ struct PairSmem {
 };
 
 template <int DV>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 3)
 pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8_t *__restrict__ ct,
                  const float *__restrict__ cv, const float *__restrict__ v, float *__restrict__ y) {
     constexpr int ZS = kTB + 1;  // padded row stride of the Z tile
@@ -379,39 +379,39 @@ pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8
     }
     __syncthreads();
     const int rows = min(kTB, T - tb * kTB), cols = min(kTB, T - sb * kTB);
-    constexpr int DVP = DV < 128 ? DV : 128;  // output columns per pass
-    constexpr int CG = DVP / 16;               // column groups of 16
-    constexpr int RPT = kTB / (256 / CG);      // rows per thread
+    constexpr int DVP = DV < 64 ? DV : 64;  // output columns per pass
+    constexpr int CG = DVP / 8;             // column groups of 8
+    constexpr int RPT = kTB / (256 / CG);   // rows per thread
     const int cg = tid % CG, rg = tid / CG;
     const float *vb = v + ((size_t)bh * T + sb * kTB) * DV;
     float *yb = y + ((size_t)bh * T + tb * kTB) * DV;
 #pragma unroll 1
     for (int c0 = 0; c0 < DV; c0 += DVP) {
-        float acc[RPT][16];
+        float acc[RPT][8];
 #pragma unroll
         for (int i = 0; i < RPT; ++i)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) acc[i][e] = 0.f;
-        const int col = c0 + 16 * cg;
+            for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
+        const int col = c0 + 8 * cg;
 #pragma unroll 2
         for (int s = 0; s < cols; ++s) {
             const float4 *vr = reinterpret_cast<const float4 *>(vb + (size_t)s * DV + col);
-            const float4 v0 = vr[0], v1 = vr[1], v2 = vr[2], v3 = vr[3];
-            const float vv[16] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w,
-                                  v2.x, v2.y, v2.z, v2.w, v3.x, v3.y, v3.z, v3.w};
+            const float4 v0 = vr[0], v1 = vr[1];
+            const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
             for (int i = 0; i < RPT; ++i) {
                 const float z = Zs[(rg * RPT + i) * ZS + s];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) acc[i][e] = fmaf(z, vv[e], acc[i][e]);
+                for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(z, vv[e], acc[i][e]);
             }
         }
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {
             const int r = rg * RPT + i;
             if (r < rows) {
-#pragma unroll
-                for (int e = 0; e < 16; ++e) atomicAdd(yb + (size_t)r * DV + col + e, acc[i][e]);
+                float4 *dst = reinterpret_cast<float4 *>(yb + (size_t)r * DV + col);
+                atomicAdd(dst, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
+                atomicAdd(dst + 1, make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]));
             }
         }
     }

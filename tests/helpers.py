@@ -47,12 +47,15 @@ def to_np(t):
 
 
 def check_parity(y, ref, dtype, what=""):
-    """Apply the parity bar of the given input dtype; return the measured error."""
+    """Apply the parity bar of the given input dtype; return the measured error
+    (also printed, so `pytest -s` lists every measured error)."""
     if dtype in ("f32", "float32"):
         err = rel_l2(y, ref)
+        print(f"parity {what}: rel L2 {err:.3e} (bar {TOL_F32_REL_L2})")
         assert err <= TOL_F32_REL_L2, f"{what}: rel L2 {err:.3e} > {TOL_F32_REL_L2}"
     else:
         err = rms_rel(y, ref)
+        print(f"parity {what}: RMS {err:.3e} of output RMS (bar {TOL_BF16_RMS})")
         assert err <= TOL_BF16_RMS, f"{what}: RMS err {err:.3e} > {TOL_BF16_RMS} of output RMS"
     return err
 
