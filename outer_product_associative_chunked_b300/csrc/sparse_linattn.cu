@@ -37,7 +37,7 @@ constexpr size_t kStateL2Budget = (size_t)64 << 20;  // recurrent form: state by
 
 // One warp per row of a dense [rows][N] matrix: the ascending list of its
 // non-zero entries (index, value) and their count.  When N is a multiple of
-// 4 the row is read as float4 with four loads in flight per lane (the dense
+// 4 the row is read as float4 with eight loads in flight per lane (the dense
 // rows are the largest input); a lane's four elements are consecutive, so
 // ballots over the four components give every non-zero its position in order.
 __device__ __forceinline__ float4 ldg_stream4(const float4 *p) {
@@ -59,7 +59,7 @@ compact_rows_kernel(const float *__restrict__ x, int rows, int N, int *__restric
     float *ov = val + (size_t)row * N;
     int c = 0;
     if ((N & 3) == 0) {
-        constexpr int U = 4;
+        constexpr int U = 8;
         const float4 *s4 = reinterpret_cast<const float4 *>(src);
         const int n4 = N >> 2;
         const unsigned below = (1u << lane) - 1u;
