@@ -9,7 +9,8 @@ same step as eager Python calls is reported under "eager"), plus:
   * roofline of the dominant kernel, timed live through the library's
     profiling events, against MEASURED_PEAKS.json;
   * e2e: the same step through the public binding from pinned host buffers,
-    host<->device copies inside the timed region;
+    host<->device copies inside the timed region (per-sequence chunks on two
+    streams, so uploads, compute and downloads overlap);
   * cpu_baseline: the float64 oracle on the host cores;
   * the other workloads (long-context prefill, 64-sequence decode, DeltaNet,
     BDH sparse) under "workloads", each with its own roofline;
@@ -359,11 +360,30 @@ def bench_headline(args, rank, world, torch, binding, synth, peaks, peak_src, fl
         dq, dk_, dv_ = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         dl, de, dg = torch.empty_like(lam), torch.empty_like(eta), torch.empty_like(gate)
 
+        # The batch goes through in per-sequence chunks on two streams, so each
+        # chunk's upload overlaps the previous chunk's compute and download
+        # (the copy engines run both directions at once).  Each stream has its
+        # own workspace, since calls that share one must not overlap.
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        ws1 = binding.tc_layer_forward_workspace_size(1, d["H"], d["T"], d["d_k"], d["d_v"], d["W"], q.dtype)
+        wss = [torch.empty(ws1, dtype=torch.uint8, device="cuda") for _ in streams]
+
         def e2e_step():
-            for dst, src in ((dq, hq), (dk_, hk), (dv_, hv), (dl, hl), (de, he), (dg, hg)):
+            main = torch.cuda.current_stream()
+            for dst, src in ((dl, hl), (de, he), (dg, hg)):
                 dst.copy_(src, non_blocking=True)
-            binding.tc_layer_forward(dq, dk_, dv_, dl, de, dg, d["W"], out=y, workspace=ws)
-            hy.copy_(y, non_blocking=True)
+            ready = main.record_event()
+            for b in range(d["B"]):
+                s = streams[b % 2]
+                s.wait_event(ready)
+                with torch.cuda.stream(s):
+                    for dst, src in ((dq, hq), (dk_, hk), (dv_, hv)):
+                        dst[b].copy_(src[b], non_blocking=True)
+                    binding.tc_layer_forward(dq[b:b + 1], dk_[b:b + 1], dv_[b:b + 1], dl, de, dg, d["W"],
+                                             out=y[b:b + 1], workspace=wss[b % 2], stream=s)
+                    hy[b].copy_(y[b], non_blocking=True)
+            for s in streams:
+                main.wait_stream(s)
 
         for _ in range(max(1, args.warmup)):
             e2e_step()
