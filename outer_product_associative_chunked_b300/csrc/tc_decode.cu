@@ -16,6 +16,7 @@
 // stores the new token into its ring slot (after every reader of the evicted
 // entry has finished); kernel 3 advances pos.
 #include "opam_internal.cuh"
+#include "sm100.cuh"
 
 namespace opam {
 namespace {
@@ -257,6 +258,9 @@ __global__ void tc_decode_combine_kernel(T *__restrict__ ring_k, T *__restrict__
                                          const float *__restrict__ part_m,
                                          const float *__restrict__ part_o,
                                          const float *__restrict__ part_ml, T *__restrict__ y) {
+    // Launched as a programmatic dependent of the partial kernel: wait for its
+    // partials (and for its reads of the evicted ring slot) before anything else.
+    sm100::pdl_wait_primary();
     const int sh = blockIdx.x, b = sh / H, h = sh - b * H;
     const int tid = threadIdx.x;
     const float *ml = part_ml + (size_t)sh * nsplit * 2;
@@ -281,6 +285,7 @@ __global__ void tc_decode_combine_kernel(T *__restrict__ ring_k, T *__restrict__
 }
 
 __global__ void advance_pos_kernel(int64_t *pos, int B) {
+    sm100::pdl_wait_primary();  // every reader of pos in this step has finished
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < B) pos[b] += 1;
 }
@@ -315,11 +320,26 @@ int launch(const opam_tc_state *st, const void *q, const void *k, const void *v,
         (const T *)v, st->H, st->W, g.keys_per_split, lam, eta, scale, pr.m, pr.o, pr.ml);
     if (int rc = launched("tc_decode_partial")) return rc;
     prof_end(s);
-    tc_decode_combine_kernel<T, DK, DV><<<SH, 128, 0, s>>>(
-        (T *)st->ring_k, (T *)st->ring_v, st->pos, (const T *)k, (const T *)v, st->H, st->W,
-        g.nsplit, gate, pr.m, pr.o, pr.ml, (T *)y);
+    // The combine and pos kernels are programmatic dependents: each is set up
+    // while its predecessor finishes and waits (griddepcontrol) before reading.
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(SH);
+    cfg.blockDim = dim3(128);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, tc_decode_combine_kernel<T, DK, DV>, (T *)st->ring_k,
+                                       (T *)st->ring_v, (const int64_t *)st->pos, (const T *)k, (const T *)v,
+                                       st->H, st->W, g.nsplit, gate, (const float *)pr.m, (const float *)pr.o,
+                                       (const float *)pr.ml, (T *)y);
+    if (e != cudaSuccess) return cuda_fail(e, "tc_decode_combine launch");
     if (int rc = launched("tc_decode_combine")) return rc;
-    advance_pos_kernel<<<ceil_div(st->B, 128), 128, 0, s>>>(st->pos, st->B);
+    cfg.gridDim = dim3(ceil_div(st->B, 128));
+    e = cudaLaunchKernelEx(&cfg, advance_pos_kernel, st->pos, st->B);
+    if (e != cudaSuccess) return cuda_fail(e, "advance_pos launch");
     return launched("advance_pos");
 }
 
