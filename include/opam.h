@@ -268,6 +268,16 @@ int opam_device_status(int clear);
 int opam_profile_events(void *start, void *stop);
 uint64_t opam_kernel_launches(void);
 
+/* Self-test of the bounded waits (no counterpart on the pages; used by the
+ * tests).  Launches one warp whose lane 0 waits, through the same bounded
+ * mbarrier wait the tensor-core kernels use, on a barrier that completes only
+ * when `arrive` is non-zero.  With arrive = 0 the wait gives up after
+ * limit_cycles clock cycles (clamped to [1e3, 1e8], well under a second) and
+ * sets a status bit, so the next opam_device_status() returns
+ * OPAM_ERR_TIMEOUT; the context stays usable.  Returns OPAM_OK or
+ * OPAM_ERR_CUDA if the launch fails. */
+int opam_selftest_bounded_wait(int arrive, long long limit_cycles, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

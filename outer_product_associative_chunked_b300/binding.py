@@ -26,6 +26,7 @@ EXPORTS = (
     "delta_rule_forward_workspace_size", "delta_rule_forward", "delta_decode_step",
     "sparse_linattn_forward_workspace_size", "sparse_linattn_forward",
     "opam_last_error", "opam_profile_events", "opam_kernel_launches", "opam_device_status",
+    "opam_selftest_bounded_wait",
 )
 
 
@@ -86,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.opam_kernel_launches.argtypes = []
         L.opam_device_status.restype = i
         L.opam_device_status.argtypes = [i]
+        L.opam_selftest_bounded_wait.restype = i
+        L.opam_selftest_bounded_wait.argtypes = [i, ctypes.c_longlong, vp]
         _lib = L
     return _lib
 
@@ -110,6 +113,12 @@ def device_status(clear: bool = True) -> None:
     """Raise OpamError(TIMEOUT) if a bounded wait inside a tensor-core kernel
     ran out since the last check (synchronises the device)."""
     _check(lib().opam_device_status(1 if clear else 0))
+
+
+def selftest_bounded_wait(arrive: bool, limit_cycles: int = 1_000_000, stream=None) -> None:
+    """Run the bounded-wait self-test kernel: with arrive=False its wait runs
+    out after limit_cycles and the next device_status() raises TIMEOUT."""
+    _check(lib().opam_selftest_bounded_wait(1 if arrive else 0, int(limit_cycles), _stream(stream)))
 
 
 def _check(rc: int) -> None:

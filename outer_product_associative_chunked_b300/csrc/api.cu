@@ -1,6 +1,7 @@
 // libopam C ABI: argument validation, workspace sizing and launch sequencing.
 // Every check runs on the host before anything is enqueued, so a rejected
 // call leaves the device untouched.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -153,6 +154,11 @@ int opam_profile_events(void *start, void *stop) {
 }
 
 uint64_t opam_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int opam_selftest_bounded_wait(int arrive, long long limit_cycles, void *stream) {
+    const long long limit = std::min(std::max(limit_cycles, 1000LL), 100000000LL);
+    return bounded_wait_selftest(arrive != 0, limit, (cudaStream_t)stream);
+}
 
 int opam_device_status(int clear) {
     const unsigned int tc = tc_prefill_tcgen05_status(clear != 0);

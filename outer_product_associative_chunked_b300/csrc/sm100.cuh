@@ -68,14 +68,18 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 // Wait until the phase with the given parity has completed.  Returns false
-// after kWaitCycles without completion (the caller then abandons its work).
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+// after `limit` clock cycles without completion (the caller then abandons its
+// work); mbar_wait uses kWaitCycles.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity, long long limit) {
     if (mbar_test(bar, parity)) return true;
     const long long t0 = clock64();
     while (!mbar_test(bar, parity)) {
-        if (clock64() - t0 > kWaitCycles) return false;
+        if (clock64() - t0 > limit) return false;
     }
     return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_for(bar, parity, kWaitCycles);
 }
 
 // ------------------------------------------------------------------ TMA
