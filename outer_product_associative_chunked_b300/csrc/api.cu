@@ -163,9 +163,10 @@ int opam_selftest_bounded_wait(int arrive, long long limit_cycles, void *stream)
 int opam_device_status(int clear) {
     const unsigned int tc = tc_prefill_tcgen05_status(clear != 0);
     const unsigned int dn = delta_tcgen05_status(clear != 0);
-    if (tc == 0 && dn == 0) return OPAM_OK;
-    set_error("opam_device_status: a bounded wait ran out in a tensor-core kernel (Tensor Cache "
-              "prefill bits 0x%x, delta rule bits 0x%x); the affected outputs are not valid", tc, dn);
+    const unsigned int st = bounded_wait_selftest_status(clear != 0);
+    if (tc == 0 && dn == 0 && st == 0) return OPAM_OK;
+    set_error("opam_device_status: a bounded wait ran out (Tensor Cache prefill bits 0x%x, delta rule bits "
+              "0x%x, self-test bits 0x%x); the affected outputs are not valid", tc, dn, st);
     return OPAM_ERR_TIMEOUT;
 }
 

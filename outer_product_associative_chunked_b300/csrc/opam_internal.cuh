@@ -86,8 +86,10 @@ int tc_prefill_tcgen05(const void *q, const void *k, const void *v, int B, int H
 // Status bits recorded by bounded waits that ran out (0 = none); reads the
 // device word synchronously and optionally clears it.
 unsigned int tc_prefill_tcgen05_status(bool clear);
-// Self-test of the bounded mbarrier wait (sets a status bit when it runs out).
+// Self-test of the bounded mbarrier wait (sets a status bit when it runs out)
+// and its status word (read synchronously, optionally cleared).
 int bounded_wait_selftest(int arrive, long long limit, cudaStream_t s);
+unsigned int bounded_wait_selftest_status(bool clear);
 
 size_t tc_decode_workspace(int S, int H, int dk, int dv, int W);
 int tc_decode(const opam_tc_state *st, const void *q, const void *k, const void *v,

@@ -59,7 +59,6 @@ enum : unsigned int {
     kStFwdMma = 16u,
     kStFwdSoftmax = 32u,
     kStFwdAlign = 64u,
-    kStSelfTest = 128u,  // the bounded-wait self-test ran out (expected when nothing arrives)
 };
 
 // Chunks per segment of the state recurrence: enough segments that the state
@@ -1365,27 +1364,6 @@ int tc_prefill_tcgen05(const void *q, const void *k, const void *v, int B, int H
         return run<128, 128>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s, l2);
     set_error("tensor-core prefill: d_k=%d d_v=%d unsupported", dk, dv);
     return OPAM_ERR_UNSUPPORTED;
-}
-
-namespace {
-// One warp; lane 0 waits on an mbarrier through the same bounded wait the
-// tensor-core kernels use.  The barrier completes only if `arrive` is set;
-// otherwise the wait runs out after `limit` cycles and the status bit is set.
-__global__ void bounded_wait_selftest_kernel(int arrive, long long limit) {
-    __shared__ uint64_t bar;
-    if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
-        mbar_fence_init();
-        if (arrive) mbar_arrive(&bar);
-        if (!mbar_wait_for(&bar, 0, limit)) atomicOr(&g_status, kStSelfTest);
-    }
-    __syncwarp();
-}
-}  // namespace
-
-int bounded_wait_selftest(int arrive, long long limit, cudaStream_t s) {
-    bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(arrive, limit);
-    return launched("bounded_wait_selftest");
 }
 
 unsigned int tc_prefill_tcgen05_status(bool clear) {
