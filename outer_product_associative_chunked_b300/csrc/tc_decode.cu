@@ -14,7 +14,8 @@
 // partials (softmax max / sum / weighted values, and the partial q A of its
 // rows); kernel 2 merges them flash-decoding style, applies the gate and
 // stores the new token into its ring slot (after every reader of the evicted
-// entry has finished); kernel 3 advances pos.
+// entry has finished); kernel 3 advances pos.  Kernels 2 and 3 are launched
+// as programmatic dependents and wait for their predecessor before reading.
 #include "opam_internal.cuh"
 #include "sm100.cuh"
 

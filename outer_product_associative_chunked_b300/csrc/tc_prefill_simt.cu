@@ -21,7 +21,8 @@
 //
 // Kernels: (1) per-chunk increments dA_j, (2) a sequential scan over chunks
 // that turns them into A_j in place, (3) the fused window softmax + L2 read +
-// gate.  This path serves the fp32 inputs and every head size; the bf16
+// gate.  The window-only variant (l2 = false) runs kernel 3 alone with its L2
+// part off.  This path serves the fp32 inputs and every head size; the bf16
 // tensor-core path lives in tc_prefill_tcgen05.cu.
 #include "opam_internal.cuh"
 
