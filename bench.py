@@ -648,9 +648,11 @@ def main(argv=None):
         line = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "f32", "data": "synthetic (seeded generator, page workload shapes)",
+                "dtype": "bf16" if d["dtype"] == "bf16" else "f32",
+                "data": "synthetic (seeded generator, page workload shapes)",
                 "config": {"workload": args.workload, **{k: v for k, v in d.items() if k != "dtype"},
-                           "input_dtype": d["dtype"], "tokens_per_step": res["tokens_per_step"],
+                           "input_dtype": d["dtype"], "accumulate": "f32",
+                           "tokens_per_step": res["tokens_per_step"],
                            "l2": "256 MiB buffer written between timed steps (untimed)",
                            "launch": "step captured once into a CUDA graph and replayed",
                            "parallelism": f"replicas x{world} (independent batch per GPU)"},
