@@ -58,14 +58,15 @@ def tc_pairs(T, W):
     return W * (W + 1) // 2 + (T - W) * W
 
 
-def tc_prefill_work(B, H, T, d_k, d_v, W, elem):
-    """Algorithmic flops / bytes of the fused prefill kernel: QK^T and PV over
-    the window, the L2 read q A (2 d_k d_v per token with evictions) and the
-    intra-chunk L2 term it replaces; q, k, v read once, y written once."""
+def tc_prefill_work(B, H, T, d_k, d_v, W, elem, l2=True):
+    """Algorithmic flops / bytes of the prefill: QK^T and PV over the window;
+    with the L2 memory, per token with an eviction the write of k v^T into A
+    (2 d_k d_v) and the read q A (2 d_k d_v); q, k, v read once, y written
+    once."""
     BH = B * H
     soft = 2 * (d_k + d_v) * tc_pairs(T, W) * BH
-    l2_read = 2 * d_k * d_v * max(0, T - W) * BH
-    flops = soft + l2_read
+    l2_rw = 4 * d_k * d_v * max(0, T - W) * BH if l2 else 0
+    flops = soft + l2_rw
     bytes_ = BH * T * (2 * d_k + 2 * d_v) * elem
     return flops, bytes_
 
@@ -107,7 +108,9 @@ def sparse_work(B, H, T, N, d_v, density):
 
 
 def roofline(flops, bytes_, seconds, peaks, peak_kind, traffic=None, scope="kernel"):
-    tf_key = "bf16_tflops" if peak_kind == "burst" else "bf16_tflops_sustained"
+    """peak_kind: "burst" / "sustained" bf16 tensor peak for the bf16 paths,
+    "fp32" for the float32 paths (the measured FP32 FMA rate, bound "alu")."""
+    tf_key = {"burst": "bf16_tflops", "sustained": "bf16_tflops_sustained", "fp32": "fp32_tflops"}[peak_kind]
     t_mem = bytes_ / (peaks["hbm_gbs"] * 1e9)
     t_tc = flops / (peaks[tf_key] * 1e12)
     if t_mem >= t_tc:
@@ -115,13 +118,34 @@ def roofline(flops, bytes_, seconds, peaks, peak_kind, traffic=None, scope="kern
         out = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     else:
         ach = flops / seconds / 1e12
-        out = {"bound": "tensor", "achieved": ach, "peak": peaks[tf_key], "unit": "TFLOP/s"}
+        out = {"bound": "alu" if peak_kind == "fp32" else "tensor", "achieved": ach, "peak": peaks[tf_key],
+               "unit": "TFLOP/s"}
     out["frac"] = out["achieved"] / out["peak"]
     out["traffic"] = traffic
     out["algorithmic_bytes"] = bytes_
     out["algorithmic_flops"] = flops
     out["scope"] = scope
+    out["peak_kind"] = tf_key
     return out
+
+
+def fp32_peak(torch, binding):
+    """FP32 FMA rate of this GPU, from the library's probe kernel: 8 waves of
+    CTAs (256 threads, 8 FMA chains each), timed with CUDA events, best of 5."""
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    blocks, iters = sms * 8 * 8, 4096
+    out = torch.empty(blocks * 256, dtype=torch.float32, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    binding.fp32_fma_probe(out, blocks, iters)
+    best = None
+    for _ in range(5):
+        e0.record()
+        fl = binding.fp32_fma_probe(out, blocks, iters)
+        e1.record()
+        torch.cuda.synchronize()
+        rate = fl / (e0.elapsed_time(e1) / 1e3) / 1e12
+        best = rate if best is None else max(best, rate)
+    return best
 
 
 # ----------------------------------------------------------------- clocks
@@ -345,6 +369,11 @@ def bench_headline(args, rank, world, torch, binding, synth, peaks, peak_src, fl
     roof = roofline(fl, by, dom_s, peaks, "burst", traffic=load_traffic("tc_fwd"), scope="kernel")
     roof["kernel"] = "tc_fwd (fused window softmax + L2 read + gate)"
     roof["kernel_ms"] = dom_s * 1e3
+    # The same kernel against the tensor-core peaks as well (its arithmetic
+    # intensity sits near the ridge): achieved TFLOP/s over burst and sustained.
+    roof["tensor_tflops"] = fl / dom_s / 1e12
+    roof["tensor_frac_burst"] = roof["tensor_tflops"] / peaks["bf16_tflops"]
+    roof["tensor_frac_sustained"] = roof["tensor_tflops"] / peaks["bf16_tflops_sustained"]
     roof["peak_source"] = f"of {peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "of fallback"
     eager = {"ms_per_step": statistics.mean(eager_ms),
              "value": tokens / (statistics.mean(eager_ms) / 1e3),
@@ -412,7 +441,28 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
                  "ms_per_step": statistics.mean(ms), "roofline": r, "dominant_kernel": kernel}
         if dom:
             entry["dominant_kernel_ms"] = statistics.mean(dom)
+            entry["dominant_roofline"] = roofline(fl, by, statistics.mean(dom) / 1e3, peaks, peak_kind,
+                                                  scope="kernel")
         out[name] = entry
+
+    # The float32 Tensor Cache workload (B=H=1, T=256, d=32, W=32), replayed
+    # from a CUDA graph like the headline: it is launch-latency bound.
+    name = "tc_fp32_T256_d32_W32"
+    w, d, inp = tc_prefill_setup(name, 0, torch, binding, synth)
+    q, k, v, lam, eta, gate = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate)]
+    y = torch.empty(d["B"], d["H"], d["T"], d["d_v"], dtype=q.dtype, device="cuda")
+    ws = torch.empty(binding.tc_layer_forward_workspace_size(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"],
+                                                             q.dtype), dtype=torch.uint8, device="cuda")
+    step = lambda: binding.tc_layer_forward(q, k, v, lam, eta, gate, d["W"], out=y, workspace=ws)  # noqa: E731
+    for _ in range(Wm):
+        step()
+    ms, per_step = timed_graph_steps(step, 4 * K, flush, torch, binding)
+    fl, by = tc_prefill_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], 4)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "fp32", "tc_fwd_simt (CUDA cores)", None)
+    out[name].update({"launch": "step captured once into a CUDA graph and replayed",
+                      "kernels_per_step": per_step,
+                      "note": "2 MFLOP and 131 KB per step: bound by launch latency, not by either roof"})
+    del q, k, v, y, ws
 
     # Window-only variant against the full layer on the headline inputs, both
     # replayed from CUDA graphs back to back: the ratio is the cost of the L2
@@ -423,15 +473,15 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
     y = torch.empty(d["B"], d["H"], d["T"], d["d_v"], dtype=q.dtype, device="cuda")
     ws = torch.empty(binding.tc_layer_forward_workspace_size(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"],
                                                              q.dtype), dtype=torch.uint8, device="cuda")
-    win = lambda: binding.tc_window_forward(q, k, v, d["W"], out=y)  # noqa: E731
+    wsw = torch.empty(binding.STATUS_BYTES, dtype=torch.uint8, device="cuda")
+    win = lambda: binding.tc_window_forward(q, k, v, d["W"], out=y, workspace=wsw)  # noqa: E731
     layer = lambda: binding.tc_layer_forward(q, k, v, lam, eta, gate, d["W"], out=y, workspace=ws)  # noqa: E731
     for _ in range(Wm):
         win()
         layer()
     win_ms, _ = timed_graph_steps(win, 4 * K, flush, torch, binding)
     layer_ms, _ = timed_graph_steps(layer, 4 * K, flush, torch, binding)
-    fl, by = tc_prefill_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], 2)
-    fl -= d["B"] * d["H"] * max(0, d["T"] - d["W"]) * 2 * d["d_k"] * d["d_v"]  # no L2 read
+    fl, by = tc_prefill_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], 2, l2=False)
     summarize(name, d["B"] * d["T"], win_ms, fl, by, "burst", "tc_fwd (window only)", None)
     ring = d["W"] * (d["d_k"] + d["d_v"]) * 2
     out[name].update({
@@ -443,6 +493,8 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
     del q, k, v, y, ws
 
     # Long-context prefill, then the 64-sequence decode continuing from it.
+    # The prefill kernel runs about a millisecond on its own, so it is rated
+    # against the burst tensor peak.
     name = "tc_bf16_B1_H16_T32768_d128_W2048"
     w, d, inp = tc_prefill_setup(name, 0, torch, binding, synth)
     q, k, v, lam, eta, gate = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate)]
@@ -455,7 +507,7 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
         step()
     ms, dom = timed_steps(step, K, flush, torch, prof=True, binding=binding)
     fl, by = tc_prefill_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], 2)
-    summarize(name, d["B"] * d["T"], ms, fl, by, "sustained", "tc_fwd", dom)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "burst", "tc_fwd", dom)
     binding.tc_layer_forward(q, k, v, lam, eta, gate, d["W"], out=y, workspace=ws, state=st1)
     del ws, y, q, k, v
 
@@ -502,7 +554,7 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
         step()
     ms, dom = timed_steps(step, K, flush, torch, prof=True, binding=binding)
     fl, by = delta_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], 2)
-    summarize(name, d["B"] * d["T"], ms, fl, by, "sustained", "delta_chain", dom)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "burst", "delta_prep + delta_chain", dom)
     del q, k, v, beta, y, ws
 
     dname = "delta_decode_bf16_S256_H16_d128_steps64"
@@ -543,36 +595,172 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
         step()
     ms, dom = timed_steps(step, K, flush, torch, prof=True, binding=binding)
     fl, by = sparse_work(d["B"], d["H"], d["T"], d["N"], d["d_v"], dens)
-    # fp32 path: bound by HBM (its flops are far below any fp32 peak as well)
-    summarize(name, d["B"] * d["T"], ms, fl, by, "sustained", "pair_tile", dom)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "fp32", "pair_tile", dom)
     out[name]["density"] = dens
     del q, k, v, y, ws
     return out
 
 
-def cpu_baseline_headline(inp, d, budget_s=20.0):
-    """The float64 oracle on the host cores, on the headline workload's units
-    (all of them when they fit the time budget, else a prefix of units)."""
+# ----------------------------------------------------------------- oracle on the host cores
+def _oracle_rate(oracle, fn, tokens, threads):
+    """Run fn() with `threads` OpenMP threads, once untimed (first-touch page
+    faults of the oracle's fresh buffers) and once timed; returns (tokens/s,
+    seconds)."""
+    oracle.set_threads(threads)
+    fn()
+    t0 = time.perf_counter()
+    fn()
+    dt = time.perf_counter() - t0
+    return tokens / dt, dt
+
+
+def cpu_baseline_headline(inp, d):
+    """The float64 oracle on the host cores on the headline batch: every
+    (batch, head) unit, all threads (the same sample the reference arm
+    times per step), plus one unit on one thread."""
     from oracle import oracle
     oracle.build()
     threads = oracle.get_threads()
-    B, H, T = d["B"], d["H"], d["T"]
-    units = B * H
-    # time one unit first to size the sample
-    t0 = time.perf_counter()
-    oracle.tc_prefill(inp.q[:1, :1], inp.k[:1, :1], inp.v[:1, :1], inp.lam[:1], inp.eta[:1], inp.gate[:1], d["W"])
-    one = time.perf_counter() - t0
-    n_units = max(1, min(units, int(budget_s * threads / max(one, 1e-6))))
-    nb = max(1, n_units // H)   # whole batch rows of H heads
-    t0 = time.perf_counter()
-    oracle.tc_prefill(inp.q[:nb], inp.k[:nb], inp.v[:nb], inp.lam, inp.eta, inp.gate, d["W"])
-    dt = time.perf_counter() - t0
-    return {"value": nb * T / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"{nb} of {B} sequences x {H} heads x {T} tokens (float64, OpenMP over heads), {dt:.1f} s"}
+    B, H, T, W = d["B"], d["H"], d["T"], d["W"]
+    allv, dt = _oracle_rate(oracle, lambda: oracle.tc_prefill(inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate, W),
+                            B * T, threads)
+    one, dt1 = _oracle_rate(oracle, lambda: oracle.tc_prefill(inp.q[:1, :1], inp.k[:1, :1], inp.v[:1, :1],
+                                                              inp.lam[:1], inp.eta[:1], inp.gate[:1], W),
+                            T / H, 1)
+    oracle.set_threads(threads)
+    return {"value": allv, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"the whole batch: {B} sequences x {H} heads x {T} tokens (float64, OpenMP over the "
+                      f"{B * H} units), {dt:.2f} s",
+            "single_thread": {"value": one, "cores": 1,
+                              "sample": f"1 unit (1 head x {T} tokens) on one thread, {dt1:.2f} s; value in "
+                                        f"tokens of all {H} heads per second"}}
+
+
+def _f64(inputs):
+    """The same inputs as float64 numpy arrays (exact), so that the timed
+    oracle calls do not include the conversion."""
+    import dataclasses
+    from oracle import oracle
+    return dataclasses.replace(inputs, **{f.name: oracle.f64(getattr(inputs, f.name))
+                                          for f in dataclasses.fields(inputs)
+                                          if hasattr(getattr(inputs, f.name), "shape")})
+
+
+def cpu_baselines(synth):
+    """The float64 oracle as it stands, timed on the host cores on a bounded
+    sample of each extra workload: all threads over the sample's units, and
+    one unit on one thread.  Values are in the workload's own unit (tokens of
+    all heads per second; decoded tokens per second for decode)."""
+    import numpy as np
+    from oracle import oracle
+    oracle.build()
+    threads = oracle.get_threads()
+    res = {}
+
+    def record(name, allv, dt, sample, one, dt1, sample1):
+        res[name] = {"value": allv, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                     "sample": f"{sample}, {dt:.2f} s",
+                     "single_thread": {"value": one, "cores": 1, "sample": f"{sample1}, {dt1:.2f} s"}}
+
+    # fp32 T=256: the whole workload (one unit), repeated for a measurable time
+    d = synth.WORKLOADS["tc_fp32_T256_d32_W32"].dims
+    inp = _f64(synth.tc_inputs(1, 1, 256, 32, 32, 32, dtype="f32", seed=0, lam=d["lam"], eta=d["eta"],
+                               gate=d["gate"]))
+    reps = 200
+    f = lambda: [oracle.tc_prefill(inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate, 32) for _ in range(reps)]  # noqa: E731
+    v1, dt1 = _oracle_rate(oracle, f, reps * 256, 1)
+    record("tc_fp32_T256_d32_W32", v1, dt1, f"the whole workload x {reps} (one unit: one thread is all it uses)",
+           v1, dt1, f"the whole workload x {reps}")
+
+    # window only: the layer with eta = 0, one sequence (8 heads) / one unit
+    w = synth.WORKLOADS["tc_bf16_B4_H8_T4096_d64_W512"]
+    d = w.dims
+    inp = _f64(synth.tc_inputs(1, d["H"], d["T"], 64, 64, d["W"], dtype="bf16", seed=w.seed))
+    z = np.zeros(d["H"])
+    allv, dt = _oracle_rate(oracle, lambda: oracle.tc_prefill(inp.q, inp.k, inp.v, inp.lam, z, inp.gate, d["W"]),
+                            d["T"], threads)
+    one, dt1 = _oracle_rate(oracle, lambda: oracle.tc_prefill(inp.q[:, :1], inp.k[:, :1], inp.v[:, :1],
+                                                              inp.lam[:1], z[:1], inp.gate[:1], d["W"]),
+                            d["T"] / d["H"], 1)
+    record("tc_window_bf16_B4_H8_T4096_d64_W512", allv, dt,
+           f"1 of 4 sequences ({d['H']} heads x {d['T']} tokens) with eta = 0", one, dt1, "1 head of it")
+
+    # long prefill: a prefix of 3W tokens of every head (the per-token cost is
+    # flat once the window is full)
+    w = synth.WORKLOADS["tc_bf16_B1_H16_T32768_d128_W2048"]
+    d = w.dims
+    Tp = 3 * d["W"]
+    inp = _f64(synth.tc_inputs(1, d["H"], Tp, 128, 128, d["W"], dtype="bf16", seed=w.seed))
+    allv, dt = _oracle_rate(oracle, lambda: oracle.tc_prefill(inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate,
+                                                              d["W"]), Tp, threads)
+    one, dt1 = _oracle_rate(oracle, lambda: oracle.tc_prefill(inp.q[:, :1], inp.k[:, :1], inp.v[:, :1],
+                                                              inp.lam[:1], inp.eta[:1], inp.gate[:1], d["W"]),
+                            Tp / d["H"], 1)
+    record("tc_bf16_B1_H16_T32768_d128_W2048", allv, dt,
+           f"the first {Tp} of {d['T']} tokens, all {d['H']} heads", one, dt1, f"1 head, first {Tp} tokens")
+
+    # decode: a full ring and state (seeded), a few steps of all 64 sequences
+    w = synth.WORKLOADS["tc_decode_bf16_S64_H16_d128_W2048_steps256"]
+    d = w.dims
+    Ss = 16
+    st = {k_: oracle.f64(v_) if k_ != "pos" else v_.numpy()
+          for k_, v_ in synth.tc_decode_state(Ss, d["H"], d["W"], 128, 128, pos=32768, dtype="bf16",
+                                              seed=w.seed + 1).items()}
+    dec = _f64(synth.tc_decode_inputs(8, Ss, d["H"], 128, 128, dtype="bf16", seed=w.seed))
+    lam = np.full(d["H"], 0.95)
+    allv, dt = _oracle_rate(oracle, lambda: oracle.tc_decode(st, dec.q, dec.k, dec.v, lam, lam, lam),
+                            8 * Ss, threads)
+    st1 = {k_: v_[:1] for k_, v_ in st.items()}
+    one, dt1 = _oracle_rate(oracle, lambda: oracle.tc_decode(st1, dec.q[:, :1], dec.k[:, :1], dec.v[:, :1], lam,
+                                                             lam, lam), 8, 1)
+    record("tc_decode_bf16_S64_H16_d128_W2048_steps256", allv, dt,
+           f"8 steps of {Ss} of the {d['S']} sequences x {d['H']} heads from a seeded full state (W = "
+           f"{d['W']}, d = 128)", one, dt1, "8 steps of 1 sequence")
+
+    # DeltaNet: the first 1024 tokens of every head
+    w = synth.WORKLOADS["delta_bf16_B8_H16_T8192_d128_C64"]
+    d = w.dims
+    Tp = 1024
+    inp = _f64(synth.delta_inputs(d["B"], d["H"], Tp, 128, 128, dtype="bf16", seed=w.seed))
+    allv, dt = _oracle_rate(oracle, lambda: oracle.delta(inp.q, inp.k, inp.v, inp.beta), d["B"] * Tp, threads)
+    one, dt1 = _oracle_rate(oracle, lambda: oracle.delta(inp.q[:1, :1], inp.k[:1, :1], inp.v[:1, :1],
+                                                         inp.beta[:1, :1]), Tp / d["H"], 1)
+    record("delta_bf16_B8_H16_T8192_d128_C64", allv, dt,
+           f"the first {Tp} of {d['T']} tokens of all {d['B']}x{d['H']} units", one, dt1, f"1 unit, {Tp} tokens")
+
+    # DeltaNet decode: 4 steps of all 256 sequences
+    w = synth.WORKLOADS["delta_decode_bf16_S256_H16_d128_steps64"]
+    d = w.dims
+    dd = _f64(synth.delta_decode_inputs(4, d["S"], d["H"], 128, 128, dtype="bf16", seed=w.seed))
+    mv = lambda t: np.ascontiguousarray(np.moveaxis(t, 0, 2))  # noqa: E731  [steps,S,H,..] -> [S,H,steps,..]
+    allv, dt = _oracle_rate(oracle, lambda: oracle.delta(mv(dd.q), mv(dd.k), mv(dd.v), mv(dd.beta), S0=dd.S0),
+                            4 * d["S"], threads)
+    one, dt1 = _oracle_rate(oracle, lambda: oracle.delta(mv(dd.q)[:1], mv(dd.k)[:1], mv(dd.v)[:1],
+                                                         mv(dd.beta)[:1], S0=dd.S0[:1]), 4, 1)
+    record("delta_decode_bf16_S256_H16_d128_steps64", allv, dt,
+           f"4 steps of all {d['S']} sequences x {d['H']} heads", one, dt1, "4 steps of 1 sequence")
+
+    # BDH: the first 128 tokens of every unit (the dense oracle streams the
+    # whole N x d_v state per token)
+    w = synth.WORKLOADS["bdh_fp32_B2_H4_T2048_N16384_dv256"]
+    d = w.dims
+    Tp = 128
+    sp = _f64(synth.sparse_inputs(d["B"], d["H"], Tp, d["N"], d["d_v"], seed=w.seed))
+    allv, dt = _oracle_rate(oracle, lambda: oracle.sparse_linattn(sp.q, sp.k, sp.v), d["B"] * Tp, threads)
+    one, dt1 = _oracle_rate(oracle, lambda: oracle.sparse_linattn(sp.q[:1, :1, :32], sp.k[:1, :1, :32],
+                                                                  sp.v[:1, :1, :32]), 32 / d["H"], 1)
+    record("bdh_fp32_B2_H4_T2048_N16384_dv256", allv, dt,
+           f"the first {Tp} of {d['T']} tokens of all {d['B']}x{d['H']} units (at most 8 threads busy)",
+           one, dt1, "1 unit, 32 tokens")
+    oracle.set_threads(threads)
+    return res
 
 
 # ----------------------------------------------------------------- reference arm
 def bench_reference(args, rank, world):
+    """The oracle as the reference arm: each step is the whole headline batch
+    (every (batch, head) unit) on all host cores -- the same sample as our
+    arm's cpu_baseline."""
     if rank != 0:
         return None
     import torch  # noqa: F401
@@ -584,15 +772,14 @@ def bench_reference(args, rank, world):
     inp = synth.tc_inputs(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], dtype=d["dtype"], seed=w.seed,
                           lam=d.get("lam"), eta=d.get("eta"), gate=d.get("gate"))
     threads = oracle.get_threads()
-    # one step = one sequence of the batch (H heads x T tokens)
-    sample = lambda: oracle.tc_prefill(inp.q[:1], inp.k[:1], inp.v[:1], inp.lam, inp.eta, inp.gate, d["W"])  # noqa: E731
+    sample = lambda: oracle.tc_prefill(inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate, d["W"])  # noqa: E731
     for _ in range(args.warmup):
         sample()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         sample()
     dt = time.perf_counter() - t0
-    value = d["T"] * args.steps / dt
+    value = d["B"] * d["T"] * args.steps / dt
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
@@ -600,7 +787,8 @@ def bench_reference(args, rank, world):
             "config": {"workload": args.workload, **{k: v for k, v in d.items() if k != "dtype"},
                        "input_dtype": d["dtype"]},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": f"each step: 1 of {d['B']} sequences ({d['H']} heads x {d['T']} tokens)"},
+                             "sample": f"each step: the whole batch, {d['B']} sequences x {d['H']} heads x "
+                                       f"{d['T']} tokens, OpenMP over the {d['B'] * d['H']} units"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     return line
 
@@ -636,6 +824,7 @@ def main(argv=None):
     build.build()
     peaks, peak_src = load_peaks()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    peaks["fp32_tflops"] = fp32_peak(torch, binding)
     res = bench_headline(args, rank, world, torch, binding, synth, peaks, peak_src, flush)
     extras = None
     if rank == 0 and world == 1 and not args.no_extras:
@@ -643,6 +832,10 @@ def main(argv=None):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline_headline(res["inp"], res["dims"])
+        if extras is not None:
+            for name, cb in cpu_baselines(synth).items():
+                if name in extras:
+                    extras[name]["cpu_baseline"] = cb
     if rank == 0:
         d = res["dims"]
         line = {"metric": METRIC, "value": res["value"], "unit": "tokens/s", "n_gpus": world,
@@ -657,6 +850,9 @@ def main(argv=None):
                            "launch": "step captured once into a CUDA graph and replayed",
                            "parallelism": f"replicas x{world} (independent batch per GPU)"},
                 "roofline": res["roofline"], "cpu_baseline": cpu, "e2e": res["e2e"],
+                "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "fp32_tflops")},
+                "peak_sources": {"hbm_gbs": peak_src, "bf16_tflops": peak_src, "bf16_tflops_sustained": peak_src,
+                                 "fp32_tflops": "measured in this run (library FP32 FMA probe, best of 5)"},
                 "gpu_launches": res["gpu_launches"], "clocks": res["clocks"], "eager": res["eager"]}
         if extras is not None:
             line["workloads"] = extras

@@ -20,18 +20,28 @@
  *   - All pointers are DEVICE pointers unless stated otherwise, owned by the
  *     caller, 16-byte aligned, and every tensor is dense row-major
  *     ("contiguous") in the shape given.  The library allocates nothing and
- *     keeps no state between calls except a per-thread error string.
+ *     keeps no device state between calls: a call's device status lives in
+ *     its own workspace (below).  Host-side it keeps a per-thread error
+ *     string, the per-thread profiling hooks and process-wide launch counter
+ *     of the instrumentation section, and per-device caches of attributes
+ *     (SM count, shared-memory limits already raised); tc_layer_forward_noalloc
+ *     alone adds its built-in device array.
  *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and runs asynchronously.  The return value reports argument
- *     errors and launch failures synchronously; device-side faults surface at
- *     the caller's next synchronisation like any CUDA error.
+ *     errors and launch failures synchronously; nothing is enqueued when a
+ *     call returns an error.  Device-side outcomes (a bounded wait that ran
+ *     out, or any CUDA error) are read after the work with
+ *     opam_check_device_error(workspace, stream).
  *   - Every state is stored key-major: element (a, b) of a d_k x d_v matrix at
  *     [a * d_v + b].  For Tensor Cache that is A = sum eta lambda^.. k v^T.
  *     DeltaNet and BDH write their state as S in R^{d_v x d_k} with read S q;
  *     the stored matrix is S^T, so S_{i,j} sits at [j * d_v + i].
  *   - Scratch memory ("workspace") is caller-provided device memory of at
  *     least the size the matching *_workspace_size() returns for the same
- *     arguments; its contents on entry do not matter.  Calls that share a
+ *     arguments; its contents on entry do not matter.  Its first
+ *     OPAM_STATUS_BYTES hold the call's device status, which the call zeroes
+ *     in stream order before any of its kernels can set it, and which a
+ *     kernel sets if one of its bounded waits runs out.  Calls that share a
  *     workspace must not overlap on the GPU.
  *   - Return value: OPAM_OK, or a negative opam_status; opam_last_error()
  *     then holds a one-line message (per calling thread).
@@ -50,13 +60,18 @@ extern "C" {
  * state matrix are always float32. */
 typedef enum { OPAM_F32 = 0, OPAM_BF16 = 1 } opam_dtype;
 
+/* Bytes at the head of every workspace that hold the call's device status
+ * (the first four 32-bit words; the rest is reserved).  Every
+ * *_workspace_size() includes them. */
+#define OPAM_STATUS_BYTES 256u
+
 typedef enum {
     OPAM_OK = 0,
     OPAM_ERR_INVALID_ARG = -1,  /* null/misaligned pointer, bad extent        */
     OPAM_ERR_UNSUPPORTED = -2,  /* valid but not implemented (e.g. d = 96)    */
     OPAM_ERR_CUDA = -3,         /* a CUDA launch or API call failed           */
-    OPAM_ERR_WORKSPACE = -4,    /* workspace missing or smaller than required */
-    OPAM_ERR_TIMEOUT = -5       /* a kernel's bounded wait ran out (see below) */
+    OPAM_ERR_TIMEOUT = -4,      /* a kernel's bounded wait ran out (see below) */
+    OPAM_ERR_WORKSPACE = -5     /* workspace missing or smaller than required */
 } opam_status;
 
 /* ------------------------------------------------------------------------
@@ -124,11 +139,15 @@ int tc_layer_forward(const void *q, const void *k, const void *v, int dtype,
  * library (present on every GPU that loads the library until the process
  * exits).  Nothing is allocated.  A problem whose
  * tc_layer_forward_workspace_size() exceeds OPAM_STATIC_SCRATCH_BYTES returns
- * OPAM_ERR_WORKSPACE with both sizes in opam_last_error().  The first call on
- * each device looks up the array's device address with that device current;
- * make that first call before any stream capture.  All calls on a device share
- * the array: calls that overlap on the GPU (other streams, other threads) race
- * and must be serialised by the caller. */
+ * OPAM_ERR_WORKSPACE with both sizes in opam_last_error().  Every call made
+ * outside stream capture looks up the array's device address on the current
+ * device (so a device reset, which may move the array, is picked up by the
+ * next such call); a call under stream capture reuses the address found by
+ * the last call on that device, so make one call on each device before any
+ * capture, and again after a device reset.  All calls on a device share the
+ * array: calls that overlap on the GPU (other streams, other threads) race
+ * and must be serialised by the caller.  The call's device status sits at
+ * the head of the array: opam_check_device_error(NULL, stream) reads it. */
 int tc_layer_forward_noalloc(const void *q, const void *k, const void *v, int dtype,
                              int B, int H, int T, int d_k, int d_v, int W,
                              const float *lambda, const float *eta, const float *gate,
@@ -145,11 +164,15 @@ int tc_layer_forward_noalloc(const void *q, const void *k, const void *v, int dt
  * difference in time between the two calls is the cost of the L2 memory.
  *   q, k [B][H][T][d_k] dtype;  v [B][H][T][d_v] dtype;  y [B][H][T][d_v]
  *   softmax_scale  <= 0 selects 1/sqrt(d_k)
- * No workspace and no per-head scalars.  Same support and errors as
+ * No per-head scalars; the workspace holds only the status block
+ * (tc_window_forward_workspace_size() bytes).  Same support and errors as
  * tc_layer_forward. */
+size_t tc_window_forward_workspace_size(int B, int H, int T, int d_k, int d_v, int W,
+                                        int dtype);
 int tc_window_forward(const void *q, const void *k, const void *v, int dtype,
                       int B, int H, int T, int d_k, int d_v, int W,
-                      float softmax_scale, void *y, void *stream);
+                      float softmax_scale, void *y, void *workspace,
+                      size_t workspace_bytes, void *stream);
 
 /* One Tensor Cache decode step for a batch of independent sequences
  * ("Tensor Cache", Methodology 1: when the ring overwrites an entry the
@@ -206,7 +229,9 @@ int delta_rule_forward(const void *q, const void *k, const void *v,
  *   v      [B][H][d_v] dtype
  *   beta   [B][H] float32 in [0, 1]
  *   y      [B][H][d_v] dtype, output
- * No workspace.  Supported: d_k, d_v in {32, 64, 128}, B*H <= 65535.  Errors
+ * No workspace: the step has no bounded waits, so its only device-side
+ * failures are CUDA errors, which opam_check_device_error(NULL, stream)
+ * reports.  Supported: d_k, d_v in {32, 64, 128}, B*H <= 65535.  Errors
  * as above; S, q, k, v, beta and y must all be non-NULL.  The state is read
  * once and written once per call (memory bound). */
 int delta_decode_step(float *S, const void *q, const void *k, const void *v,
@@ -237,13 +262,23 @@ int sparse_linattn_forward(const float *q, const float *k, const float *v,
 /* Message for the last non-OK status returned on the calling thread. */
 const char *opam_last_error(void);
 
-/* Device-side status of the tensor-core kernels.  Their pipeline waits are
- * bounded (about one second each); a wait that runs out abandons the CTA's
- * work, leaves the outputs undefined and records a status bit instead of
- * hanging the GPU.  This call synchronises the device, returns OPAM_OK when
- * no bit is set and OPAM_ERR_TIMEOUT otherwise (with a message), and clears
- * the bits when `clear` is non-zero. */
-int opam_device_status(int clear);
+/* Device-side outcome of the most recent call that used `workspace`.
+ * The tensor-core kernels' pipeline waits are bounded (about one second
+ * each); a wait that runs out abandons the CTA's work, leaves that call's
+ * outputs undefined and sets a bit in the call's status word instead of
+ * hanging the GPU.  This function synchronises `stream` only (not the
+ * device), then:
+ *   - returns OPAM_ERR_CUDA if the stream holds a CUDA error (for example a
+ *     fault of any earlier work on it);
+ *   - returns OPAM_ERR_TIMEOUT, with the kernels named in opam_last_error(),
+ *     if the status at the head of `workspace` is non-zero;
+ *   - returns OPAM_OK otherwise.
+ * `workspace` is the workspace of the call in question and `stream` the
+ * stream that call ran on.  With workspace NULL it checks the built-in
+ * scratch of tc_layer_forward_noalloc on the current device (if a call has
+ * set it up there) and otherwise only the stream.  The word is not cleared
+ * here: the next call that uses the workspace zeroes it. */
+int opam_check_device_error(const void *workspace, void *stream);
 
 /* ------------------------------------------------------------------------
  * Instrumentation (no counterpart on the pages; used by benchmarks).
@@ -253,7 +288,9 @@ int opam_device_status(int clear);
  * its dominant kernel and `stop` immediately after it, so the caller can time
  * that kernel alone with cudaEventElapsedTime.  The dominant kernel is the
  * fused window-softmax kernel of tc_layer_forward, the split-ring kernel of
- * tc_decode_step, the sequential state pass of delta_rule_forward, the one
+ * tc_decode_step, the chunk preparation and the sequential state pass of
+ * delta_rule_forward together (tensor-core path; the state pass alone on the
+ * CUDA-core path), the one
  * kernel of delta_decode_step, and for sparse_linattn_forward the block-pair
  * kernel (no start or final state) or else the chunked read and write
  * (summed over their launches: `start` goes before the first, `stop` after
@@ -268,15 +305,28 @@ int opam_device_status(int clear);
 int opam_profile_events(void *start, void *stop);
 uint64_t opam_kernel_launches(void);
 
+/* FP32 FMA rate probe (no counterpart on the pages; used by benchmarks to
+ * measure the CUDA cores' float32 peak, the roof of the float32 paths).
+ * Enqueues one kernel of `blocks` CTAs x 256 threads in which every thread
+ * runs 8 independent fmaf chains for `iters` rounds and stores the chains'
+ * sum to out[block * 256 + thread] (`out` holds blocks * 256 floats).
+ * *flops (if not NULL) receives the launch's flop count, 2 per FMA:
+ * 2 * blocks * 256 * iters * 8.  Time it with events on `stream`.
+ * Returns OPAM_OK, OPAM_ERR_INVALID_ARG, or OPAM_ERR_CUDA. */
+int opam_fp32_fma_probe(float *out, int blocks, int iters, double *flops, void *stream);
+
 /* Self-test of the bounded waits (no counterpart on the pages; used by the
- * tests).  Launches one warp whose lane 0 waits, through the same bounded
- * mbarrier wait the tensor-core kernels use, on a barrier that completes only
- * when `arrive` is non-zero.  With arrive = 0 the wait gives up after
- * limit_cycles clock cycles (clamped to [1e3, 1e8], well under a second) and
- * sets a status bit, so the next opam_device_status() returns
- * OPAM_ERR_TIMEOUT; the context stays usable.  Returns OPAM_OK or
+ * tests).  Zeroes the status word of `workspace` (at least OPAM_STATUS_BYTES
+ * of device memory) and launches one warp whose lane 0 waits, through the
+ * same bounded mbarrier wait the tensor-core kernels use, on a barrier that
+ * completes only when `arrive` is non-zero.  With arrive = 0 the wait gives
+ * up after limit_cycles clock cycles (clamped to [1e3, 1e8], well under a
+ * second) and sets a status bit, so opam_check_device_error(workspace,
+ * stream) returns OPAM_ERR_TIMEOUT; the context stays usable.  Returns
+ * OPAM_OK, OPAM_ERR_INVALID_ARG for a NULL or misaligned workspace, or
  * OPAM_ERR_CUDA if the launch fails. */
-int opam_selftest_bounded_wait(int arrive, long long limit_cycles, void *stream);
+int opam_selftest_bounded_wait(int arrive, long long limit_cycles, void *workspace,
+                               void *stream);
 
 #ifdef __cplusplus
 }

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -56,6 +57,11 @@ int device_sm_count() {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
     cache[dev].store(n, std::memory_order_relaxed);
     return n;
+}
+
+int clear_status(void *ws, cudaStream_t s) {
+    return cuda_fail(cudaMemsetAsync(status_word(ws), 0, kStatusWords * sizeof(unsigned int), s),
+                     "status word clear");
 }
 
 static std::atomic<uint64_t> g_launches{0};
@@ -132,10 +138,26 @@ float resolve_scale(float s, int dk) { return s > 0.f ? s : 1.0f / std::sqrt((fl
 
 int delta_chunk(int chunk) { return chunk == 0 ? 64 : chunk; }
 
-// Scratch of the Tensor Cache prefill on the path the call takes.
+// Scratch of the Tensor Cache prefill on the path the call takes, after the
+// status block.
 size_t tc_prefill_workspace(int B, int H, int T, int dk, int dv, int W, int dtype) {
-    if (tc_prefill_tcgen05_supported(dtype, dk, dv)) return tc_prefill_tcgen05_workspace(B * H, T, dk, dv);
-    return tc_prefill_simt_workspace(B * H, T, dk, dv, W);
+    if (tc_prefill_tcgen05_supported(dtype, dk, dv))
+        return OPAM_STATUS_BYTES + tc_prefill_tcgen05_workspace(B * H, T, dk, dv);
+    return OPAM_STATUS_BYTES + tc_prefill_simt_workspace(B * H, T, dk, dv, W);
+}
+
+const char *status_names(unsigned int bits) {
+    static thread_local char buf[256];
+    buf[0] = 0;
+    const struct {
+        unsigned int mask;
+        const char *name;
+    } parts[] = {{0x7Fu * kStatusTcPrefill, "Tensor Cache prefill "},
+                 {0x1Fu * kStatusDelta, "DeltaNet tensor-core "},
+                 {kStatusSelfTest, "bounded-wait self-test "}};
+    for (const auto &p : parts)
+        if (bits & p.mask) strncat(buf, p.name, sizeof buf - strlen(buf) - 1);
+    return buf;
 }
 
 }  // namespace
@@ -155,18 +177,35 @@ int opam_profile_events(void *start, void *stop) {
 
 uint64_t opam_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
-int opam_selftest_bounded_wait(int arrive, long long limit_cycles, void *stream) {
+int opam_selftest_bounded_wait(int arrive, long long limit_cycles, void *workspace, void *stream) {
+    const char *fn = "opam_selftest_bounded_wait";
+    OPAM_CHECK_PTR(workspace);
     const long long limit = std::min(std::max(limit_cycles, 1000LL), 100000000LL);
-    return bounded_wait_selftest(arrive != 0, limit, (cudaStream_t)stream);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (int rc = clear_status(workspace, s)) return rc;
+    return bounded_wait_selftest(arrive != 0, limit, status_word(workspace), s);
 }
 
-int opam_device_status(int clear) {
-    const unsigned int tc = tc_prefill_tcgen05_status(clear != 0);
-    const unsigned int dn = delta_tcgen05_status(clear != 0);
-    const unsigned int st = bounded_wait_selftest_status(clear != 0);
-    if (tc == 0 && dn == 0 && st == 0) return OPAM_OK;
-    set_error("opam_device_status: a bounded wait ran out (Tensor Cache prefill bits 0x%x, delta rule bits "
-              "0x%x, self-test bits 0x%x); the affected outputs are not valid", tc, dn, st);
+int opam_check_device_error(const void *workspace, void *stream) {
+    const char *fn = "opam_check_device_error";
+    if (workspace && !aligned16(workspace)) {
+        set_error("%s: workspace is not 16-byte aligned", fn);
+        return OPAM_ERR_INVALID_ARG;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "opam_check_device_error: work on the stream failed");
+    const void *ws = workspace ? workspace : noalloc_scratch_if_ready();
+    if (!ws) return OPAM_OK;
+    unsigned int words[kStatusWords] = {};
+    e = cudaMemcpyAsync(words, ws, sizeof words, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "opam_check_device_error: reading the status words");
+    unsigned int bits = 0;
+    for (unsigned int w : words) bits |= w;
+    if (bits == 0) return OPAM_OK;
+    set_error("%s: a bounded wait ran out in the %skernels (status 0x%x); that call's outputs are not "
+              "valid", fn, status_names(bits), bits);
     return OPAM_ERR_TIMEOUT;
 }
 
@@ -213,11 +252,14 @@ int tc_layer_forward(const void *q, const void *k, const void *v, int dtype, int
     cudaStream_t s = (cudaStream_t)stream;
     const float scale = resolve_scale(softmax_scale, d_k);
     float *A_final = state_out ? state_out->A : nullptr;
+    // The tensor-core path zeroes the status words inside its first kernel.
+    if (!tc_prefill_tcgen05_supported(dtype, d_k, d_v))
+        if (int rc = clear_status(workspace, s)) return rc;
     const int rc = tc_prefill_tcgen05_supported(dtype, d_k, d_v)
                        ? tc_prefill_tcgen05(q, k, v, B, H, T, d_k, d_v, W, lambda, eta, gate, scale, y,
-                                            A_final, workspace, s)
+                                            A_final, status_body(workspace), status_word(workspace), s)
                        : tc_prefill_simt(q, k, v, dtype, B, H, T, d_k, d_v, W, lambda, eta, gate, scale,
-                                         y, A_final, workspace, s);
+                                         y, A_final, status_body(workspace), s);
     if (rc) return rc;
     if (state_out)
         return tc_export_ring(k, v, dtype, B, H, T, d_k, d_v, W, state_out->ring_k, state_out->ring_v,
@@ -225,19 +267,31 @@ int tc_layer_forward(const void *q, const void *k, const void *v, int dtype, int
     return OPAM_OK;
 }
 
+size_t tc_window_forward_workspace_size(int B, int H, int T, int d_k, int d_v, int W, int dtype) {
+    if (check_tc_dims("tc_window_forward_workspace_size", dtype, B, H, T, d_k, d_v, W) != OPAM_OK) return 0;
+    return OPAM_STATUS_BYTES;
+}
+
 int tc_window_forward(const void *q, const void *k, const void *v, int dtype, int B, int H, int T,
-                      int d_k, int d_v, int W, float softmax_scale, void *y, void *stream) {
+                      int d_k, int d_v, int W, float softmax_scale, void *y, void *workspace,
+                      size_t workspace_bytes, void *stream) {
     const char *fn = "tc_window_forward";
     if (int rc = check_tc_dims(fn, dtype, B, H, T, d_k, d_v, W)) return rc;
     OPAM_CHECK_PTR(q);
     OPAM_CHECK_PTR(k);
     OPAM_CHECK_PTR(v);
     OPAM_CHECK_PTR(y);
+    if (!workspace || workspace_bytes < OPAM_STATUS_BYTES) {
+        set_error("%s: workspace %zu bytes, %u required", fn, workspace_bytes, OPAM_STATUS_BYTES);
+        return OPAM_ERR_WORKSPACE;
+    }
+    OPAM_CHECK_PTR(workspace);
     cudaStream_t s = (cudaStream_t)stream;
     const float scale = resolve_scale(softmax_scale, d_k);
+    if (int rc = clear_status(workspace, s)) return rc;
     if (tc_prefill_tcgen05_supported(dtype, d_k, d_v))
         return tc_prefill_tcgen05(q, k, v, B, H, T, d_k, d_v, W, nullptr, nullptr, nullptr, scale, y, nullptr,
-                                  nullptr, s, false);
+                                  nullptr, status_word(workspace), s, false);
     return tc_prefill_simt(q, k, v, dtype, B, H, T, d_k, d_v, W, nullptr, nullptr, nullptr, scale, y, nullptr,
                            nullptr, s, false);
 }
@@ -247,7 +301,7 @@ size_t tc_decode_step_workspace_size(const opam_tc_state *st) {
     if (check_tc_dims("tc_decode_step_workspace_size", st->dtype, st->B, st->H, 1, st->d_k, st->d_v,
                       st->W) != OPAM_OK)
         return 0;
-    return tc_decode_workspace(st->B, st->H, st->d_k, st->d_v, st->W);
+    return OPAM_STATUS_BYTES + tc_decode_workspace(st->B, st->H, st->d_k, st->d_v, st->W);
 }
 
 int tc_decode_step(opam_tc_state *st, const void *q, const void *k, const void *v,
@@ -270,14 +324,16 @@ int tc_decode_step(opam_tc_state *st, const void *q, const void *k, const void *
     OPAM_CHECK_PTR(eta);
     OPAM_CHECK_PTR(gate);
     OPAM_CHECK_PTR(y);
-    const size_t need = tc_decode_workspace(st->B, st->H, st->d_k, st->d_v, st->W);
+    const size_t need = OPAM_STATUS_BYTES + tc_decode_workspace(st->B, st->H, st->d_k, st->d_v, st->W);
     if (!workspace || workspace_bytes < need) {
         set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
         return OPAM_ERR_WORKSPACE;
     }
     OPAM_CHECK_PTR(workspace);
+    // The decode kernels have no bounded waits; the last of them zeroes the
+    // status word, so no separate clear is enqueued on this hot path.
     return tc_decode(st, q, k, v, lambda, eta, gate, resolve_scale(softmax_scale, st->d_k), y,
-                     workspace, (cudaStream_t)stream);
+                     status_body(workspace), status_word(workspace), (cudaStream_t)stream);
 }
 
 size_t delta_rule_forward_workspace_size(int B, int H, int T, int d_k, int d_v, int chunk, int dtype) {
@@ -285,8 +341,8 @@ size_t delta_rule_forward_workspace_size(int B, int H, int T, int d_k, int d_v, 
     if (check_tc_dims(fn, dtype, B, H, T, d_k, d_v, 1) != OPAM_OK) return 0;
     const int C = delta_chunk(chunk);
     if (C != 16 && C != 32 && C != 64) return 0;
-    if (delta_tcgen05_supported(dtype, d_k, d_v, C)) return delta_tcgen05_workspace(B * H, T, d_k);
-    return delta_simt_workspace(B * H, T, d_k, d_v, C);
+    if (delta_tcgen05_supported(dtype, d_k, d_v, C)) return OPAM_STATUS_BYTES + delta_tcgen05_workspace(B * H, T, d_k);
+    return OPAM_STATUS_BYTES + delta_simt_workspace(B * H, T, d_k, d_v, C);
 }
 
 int delta_rule_forward(const void *q, const void *k, const void *v, const float *beta, int dtype,
@@ -308,16 +364,19 @@ int delta_rule_forward(const void *q, const void *k, const void *v, const float 
     OPAM_CHECK_OPT_PTR(S0);
     OPAM_CHECK_OPT_PTR(S_out);
     const bool tc = delta_tcgen05_supported(dtype, d_k, d_v, C);
-    const size_t need = tc ? delta_tcgen05_workspace(B * H, T, d_k) : delta_simt_workspace(B * H, T, d_k, d_v, C);
+    const size_t need = OPAM_STATUS_BYTES +
+                        (tc ? delta_tcgen05_workspace(B * H, T, d_k) : delta_simt_workspace(B * H, T, d_k, d_v, C));
     if (!workspace || workspace_bytes < need) {
         set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
         return OPAM_ERR_WORKSPACE;
     }
     OPAM_CHECK_PTR(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (int rc = clear_status(workspace, s)) return rc;
     if (tc)
-        return delta_tcgen05(q, k, v, beta, B, H, T, d_k, S0, S_out, y, workspace, (cudaStream_t)stream);
-    return delta_simt(q, k, v, beta, dtype, B, H, T, d_k, d_v, C, S0, S_out, y, workspace,
-                      (cudaStream_t)stream);
+        return delta_tcgen05(q, k, v, beta, B, H, T, d_k, S0, S_out, y, status_body(workspace),
+                             status_word(workspace), s);
+    return delta_simt(q, k, v, beta, dtype, B, H, T, d_k, d_v, C, S0, S_out, y, status_body(workspace), s);
 }
 
 int delta_decode_step(float *S, const void *q, const void *k, const void *v, const float *beta,
@@ -338,7 +397,7 @@ size_t sparse_linattn_forward_workspace_size(int B, int H, int T, int N, int d_v
     if (d_v != 32 && d_v != 64 && d_v != 128 && d_v != 256) return 0;
     // The state lives in S_out when the caller supplies it; size for the
     // worst case (no S_out) so one query serves both.
-    return sparse_workspace(B * H, T, N, d_v, true);
+    return OPAM_STATUS_BYTES + sparse_workspace(B * H, T, N, d_v, true);
 }
 
 int sparse_linattn_forward(const float *q, const float *k, const float *v, int B, int H, int T, int N,
@@ -363,13 +422,15 @@ int sparse_linattn_forward(const float *q, const float *k, const float *v, int B
     OPAM_CHECK_PTR(y);
     OPAM_CHECK_OPT_PTR(S0);
     OPAM_CHECK_OPT_PTR(S_out);
-    const size_t need = sparse_workspace(B * H, T, N, d_v, S_out == nullptr);
+    const size_t need = OPAM_STATUS_BYTES + sparse_workspace(B * H, T, N, d_v, S_out == nullptr);
     if (!workspace || workspace_bytes < need) {
         set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
         return OPAM_ERR_WORKSPACE;
     }
     OPAM_CHECK_PTR(workspace);
-    return sparse_forward(q, k, v, B, H, T, N, d_v, S0, S_out, y, workspace, (cudaStream_t)stream);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (int rc = clear_status(workspace, s)) return rc;
+    return sparse_forward(q, k, v, B, H, T, N, d_v, S0, S_out, y, status_body(workspace), s);
 }
 
 }  // extern "C"

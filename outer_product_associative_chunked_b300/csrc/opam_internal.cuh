@@ -58,6 +58,25 @@ __device__ __forceinline__ float warp_max(float x) {
     return x;
 }
 
+// ---------------------------------------------------------------- device status
+// Every workspace begins with an OPAM_STATUS_BYTES block whose first
+// kStatusWords words hold the call's device status: zero, or (OR-ed over the
+// words) the bits below, set by a bounded wait that ran out.  Each call zeroes
+// the words in stream order before they can be set -- with clear_status, or
+// inside its own first kernel where that is race-free -- and
+// opam_check_device_error reads them.
+constexpr unsigned int kStatusTcPrefill = 1u << 0;   // 7 bits: Tensor Cache prefill kernels
+constexpr unsigned int kStatusDelta = 1u << 8;       // 5 bits: DeltaNet tensor-core kernels
+constexpr unsigned int kStatusSelfTest = 1u << 16;   // the bounded-wait self-test
+constexpr int kStatusWords = 4;
+inline unsigned int *status_word(void *ws) { return (unsigned int *)ws; }
+inline void *status_body(void *ws) { return ws ? (char *)ws + OPAM_STATUS_BYTES : nullptr; }
+// Zero the status words on the call's stream (enqueued before its kernels).
+int clear_status(void *ws, cudaStream_t s);
+// Device address of the built-in scratch of tc_layer_forward_noalloc on the
+// current device, or NULL if no call has set it up there.
+void *noalloc_scratch_if_ready();
+
 // Finite stand-in for -infinity in running maxima (keeps exp() finite).
 constexpr float kNegBig = -1.0e30f;
 
@@ -82,19 +101,16 @@ bool tc_prefill_tcgen05_supported(int dtype, int dk, int dv);
 size_t tc_prefill_tcgen05_workspace(int BH, int T, int dk, int dv);
 int tc_prefill_tcgen05(const void *q, const void *k, const void *v, int B, int H, int T, int dk,
                        int dv, int W, const float *lam, const float *eta, const float *gate,
-                       float scale, void *y, float *A_final, void *ws, cudaStream_t s, bool l2 = true);
-// Status bits recorded by bounded waits that ran out (0 = none); reads the
-// device word synchronously and optionally clears it.
-unsigned int tc_prefill_tcgen05_status(bool clear);
-// Self-test of the bounded mbarrier wait (sets a status bit when it runs out)
-// and its status word (read synchronously, optionally cleared).
-int bounded_wait_selftest(int arrive, long long limit, cudaStream_t s);
-unsigned int bounded_wait_selftest_status(bool clear);
+                       float scale, void *y, float *A_final, void *ws, unsigned int *status,
+                       cudaStream_t s, bool l2 = true);
+// Self-test of the bounded mbarrier wait (sets kStatusSelfTest in *status
+// when it runs out).
+int bounded_wait_selftest(int arrive, long long limit, unsigned int *status, cudaStream_t s);
 
 size_t tc_decode_workspace(int S, int H, int dk, int dv, int W);
 int tc_decode(const opam_tc_state *st, const void *q, const void *k, const void *v,
               const float *lam, const float *eta, const float *gate, float scale, void *y,
-              void *ws, cudaStream_t s);
+              void *ws, unsigned int *status, cudaStream_t s);
 
 size_t delta_simt_workspace(int BH, int T, int dk, int dv, int C);
 int delta_simt(const void *q, const void *k, const void *v, const float *beta, int dtype,
@@ -105,12 +121,16 @@ int delta_simt(const void *q, const void *k, const void *v, const float *beta, i
 bool delta_tcgen05_supported(int dtype, int dk, int dv, int chunk);
 size_t delta_tcgen05_workspace(int BH, int T, int dk);
 int delta_tcgen05(const void *q, const void *k, const void *v, const float *beta, int B, int H, int T,
-                  int dk, const float *S0, float *S_out, void *y, void *ws, cudaStream_t s);
-unsigned int delta_tcgen05_status(bool clear);
+                  int dk, const float *S0, float *S_out, void *y, void *ws, unsigned int *status,
+                  cudaStream_t s);
 
 // DeltaNet single-token decode (state updated in place, no scratch).
 int delta_decode(float *S, const void *q, const void *k, const void *v, const float *beta, int dtype,
                  int B, int H, int dk, int dv, void *y, cudaStream_t s);
+
+// FP32 FMA rate probe (instrumentation): FMAs one launch performs, and the launch.
+double kChainsTotal(int blocks, int iters);
+int fp32_fma_probe(float *out, int blocks, int iters, cudaStream_t s);
 
 size_t sparse_workspace(int BH, int T, int N, int dv, bool need_state);
 int sparse_forward(const float *q, const float *k, const float *v, int B, int H, int T, int N,

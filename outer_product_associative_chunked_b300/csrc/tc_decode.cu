@@ -285,10 +285,14 @@ __global__ void tc_decode_combine_kernel(T *__restrict__ ring_k, T *__restrict__
         ring_v[((size_t)sh * W + slot) * DV + c] = v[(size_t)sh * DV + c];
 }
 
-__global__ void advance_pos_kernel(int64_t *pos, int B) {
+// Also zeroes the call's status words: no kernel of the decode step has a
+// bounded wait, so nothing else writes it and the word reads clean after the
+// step.
+__global__ void advance_pos_kernel(int64_t *pos, int B, unsigned int *status) {
     sm100::pdl_wait_primary();  // every reader of pos in this step has finished
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < B) pos[b] += 1;
+    if (b < kStatusWords) status[b] = 0u;
 }
 
 struct Parts {
@@ -308,7 +312,8 @@ Parts carve(void *ws, int SH, int nsplit, int dv) {
 
 template <typename T, int DK, int DV>
 int launch(const opam_tc_state *st, const void *q, const void *k, const void *v, const float *lam,
-           const float *eta, const float *gate, float scale, void *y, void *ws, cudaStream_t s) {
+           const float *eta, const float *gate, float scale, void *y, void *ws, unsigned int *status,
+           cudaStream_t s) {
     const int SH = st->B * st->H;
     const DecodeGeom g = geom(st->W);
     const Parts pr = carve(ws, SH, g.nsplit, DV);
@@ -339,18 +344,19 @@ int launch(const opam_tc_state *st, const void *q, const void *k, const void *v,
     if (e != cudaSuccess) return cuda_fail(e, "tc_decode_combine launch");
     if (int rc = launched("tc_decode_combine")) return rc;
     cfg.gridDim = dim3(ceil_div(st->B, 128));
-    e = cudaLaunchKernelEx(&cfg, advance_pos_kernel, st->pos, st->B);
+    e = cudaLaunchKernelEx(&cfg, advance_pos_kernel, st->pos, st->B, status);
     if (e != cudaSuccess) return cuda_fail(e, "advance_pos launch");
     return launched("advance_pos");
 }
 
 template <typename T, int DK>
 int by_dv(const opam_tc_state *st, const void *q, const void *k, const void *v, const float *lam,
-          const float *eta, const float *gate, float scale, void *y, void *ws, cudaStream_t s) {
+          const float *eta, const float *gate, float scale, void *y, void *ws, unsigned int *status,
+          cudaStream_t s) {
     switch (st->d_v) {
-        case 32: return launch<T, DK, 32>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
-        case 64: return launch<T, DK, 64>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
-        case 128: return launch<T, DK, 128>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
+        case 32: return launch<T, DK, 32>(st, q, k, v, lam, eta, gate, scale, y, ws, status, s);
+        case 64: return launch<T, DK, 64>(st, q, k, v, lam, eta, gate, scale, y, ws, status, s);
+        case 128: return launch<T, DK, 128>(st, q, k, v, lam, eta, gate, scale, y, ws, status, s);
     }
     set_error("d_v=%d unsupported", st->d_v);
     return OPAM_ERR_UNSUPPORTED;
@@ -358,11 +364,12 @@ int by_dv(const opam_tc_state *st, const void *q, const void *k, const void *v, 
 
 template <typename T>
 int by_dk(const opam_tc_state *st, const void *q, const void *k, const void *v, const float *lam,
-          const float *eta, const float *gate, float scale, void *y, void *ws, cudaStream_t s) {
+          const float *eta, const float *gate, float scale, void *y, void *ws, unsigned int *status,
+          cudaStream_t s) {
     switch (st->d_k) {
-        case 32: return by_dv<T, 32>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
-        case 64: return by_dv<T, 64>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
-        case 128: return by_dv<T, 128>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
+        case 32: return by_dv<T, 32>(st, q, k, v, lam, eta, gate, scale, y, ws, status, s);
+        case 64: return by_dv<T, 64>(st, q, k, v, lam, eta, gate, scale, y, ws, status, s);
+        case 128: return by_dv<T, 128>(st, q, k, v, lam, eta, gate, scale, y, ws, status, s);
     }
     set_error("d_k=%d unsupported", st->d_k);
     return OPAM_ERR_UNSUPPORTED;
@@ -380,10 +387,10 @@ size_t tc_decode_workspace(int S, int H, int dk, int dv, int W) {
 
 int tc_decode(const opam_tc_state *st, const void *q, const void *k, const void *v,
               const float *lam, const float *eta, const float *gate, float scale, void *y,
-              void *ws, cudaStream_t s) {
+              void *ws, unsigned int *status, cudaStream_t s) {
     if (st->dtype == OPAM_BF16)
-        return by_dk<__nv_bfloat16>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
-    return by_dk<float>(st, q, k, v, lam, eta, gate, scale, y, ws, s);
+        return by_dk<__nv_bfloat16>(st, q, k, v, lam, eta, gate, scale, y, ws, status, s);
+    return by_dk<float>(st, q, k, v, lam, eta, gate, scale, y, ws, status, s);
 }
 
 }  // namespace opam

@@ -15,14 +15,18 @@
 //    GPU that loads this library, for as long as the process runs.
 //  - Problems whose scratch need (tc_layer_forward_workspace_size) exceeds it
 //    are rejected with OPAM_ERR_WORKSPACE and a message naming both sizes.
-//  - The first call on each device looks up the array's device address
-//    (cudaGetSymbolAddress, with that device current) and caches it; make
-//    that first call before any stream capture.
+//  - A call made outside stream capture looks up the array's device address
+//    (cudaGetSymbolAddress, with the call's device current) and remembers it
+//    per device; a call under stream capture uses the remembered address.
+//    So the first call on each device, and the first after a device reset
+//    (which reloads the module and may move the array), must come before any
+//    capture.
 //  - All calls on a device share the one array, and it keeps the previous
-//    call's contents.  Every kernel writes each scratch element before it
-//    reads it, so stale contents never reach a result; but calls that
-//    overlap on the GPU (different streams, or different host threads)
-//    race on the array and must be serialised by the caller.
+//    call's contents.  The head of the array is the call's status block,
+//    which the call zeroes first; every kernel writes each other scratch
+//    element before it reads it, so stale contents never reach a result.
+//    Calls that overlap on the GPU (different streams, or different host
+//    threads) race on the array and must be serialised by the caller.
 #include <mutex>
 
 #include "opam_internal.cuh"
@@ -37,27 +41,58 @@ constexpr int kMaxDevices = 64;
 void *g_scratch_ptr[kMaxDevices] = {};
 std::mutex g_scratch_mu;
 
-// Device address of the static scratch on the current device (set up once).
-int static_scratch(void **out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return opam::cuda_fail(e, "tc_layer_forward_noalloc: cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices) {
-        opam::set_error("tc_layer_forward_noalloc: device %d above the supported %d", dev, kMaxDevices);
+int current_device(int *dev, const char *fn) {
+    cudaError_t e = cudaGetDevice(dev);
+    if (e != cudaSuccess) return opam::cuda_fail(e, fn);
+    if (*dev < 0 || *dev >= kMaxDevices) {
+        opam::set_error("%s: device %d above the supported %d", fn, *dev, kMaxDevices);
         return OPAM_ERR_UNSUPPORTED;
     }
+    return OPAM_OK;
+}
+
+// Device address of the static scratch on the current device: looked up
+// afresh unless `stream` is capturing, in which case the last address found
+// on this device is used.
+int static_scratch(cudaStream_t stream, void **out) {
+    const char *fn = "tc_layer_forward_noalloc";
+    int dev = -1;
+    if (int rc = current_device(&dev, fn)) return rc;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) return opam::cuda_fail(e, "tc_layer_forward_noalloc: cudaStreamIsCapturing");
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (cs == cudaStreamCaptureStatusNone) {
         void *p = nullptr;
         e = cudaGetSymbolAddress(&p, g_static_scratch);
         if (e != cudaSuccess) return opam::cuda_fail(e, "tc_layer_forward_noalloc: cudaGetSymbolAddress");
         g_scratch_ptr[dev] = p;
+    } else if (!g_scratch_ptr[dev]) {
+        opam::set_error("%s: first call on device %d is under stream capture; make one call on this "
+                        "device outside capture first", fn, dev);
+        return OPAM_ERR_INVALID_ARG;
     }
     *out = g_scratch_ptr[dev];
     return OPAM_OK;
 }
 
 }  // namespace
+
+namespace opam {
+
+void *noalloc_scratch_if_ready() {
+    int dev = -1;
+    if (current_device(&dev, "opam_check_device_error") != OPAM_OK) return nullptr;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) return nullptr;
+    // Look it up again, in case the device was reset since the last call.
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return nullptr;
+    g_scratch_ptr[dev] = p;
+    return p;
+}
+
+}  // namespace opam
 
 extern "C" int tc_layer_forward_noalloc(const void *q, const void *k, const void *v, int dtype, int B,
                                         int H, int T, int d_k, int d_v, int W, const float *lambda,
@@ -73,7 +108,7 @@ extern "C" int tc_layer_forward_noalloc(const void *q, const void *k, const void
     }
     void *scratch = nullptr;
     if (need > 0)  // need == 0: invalid arguments, reported by tc_layer_forward below
-        if (int rc = static_scratch(&scratch)) return rc;
+        if (int rc = static_scratch((cudaStream_t)stream, &scratch)) return rc;
     return tc_layer_forward(q, k, v, dtype, B, H, T, d_k, d_v, W, lambda, eta, gate, softmax_scale, y,
                             state_out, scratch, (size_t)OPAM_STATIC_SCRATCH_BYTES, stream);
 }

@@ -33,8 +33,8 @@
 //                       lambda^(C (j - gL)) A_{gL}), and the gate.
 //
 // Every wait inside these kernels is bounded; a wait that runs out records a
-// status bit (tc_prefill_tcgen05_status) and the CTA winds down without
-// hanging.
+// bit in the call's status word (the head of its workspace, read by
+// opam_check_device_error) and the CTA winds down without hanging.
 #include <math.h>
 
 #include "opam_internal.cuh"
@@ -50,15 +50,16 @@ constexpr int kBlk = 128;          // query rows per CTA = keys per tile = chunk
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescale = 8.0f;   // lazy-rescale threshold (log2 units)
 
-__device__ unsigned int g_status = 0;
+// Bits recorded in the call's status word (the head of its workspace) when a
+// bounded wait runs out.
 enum : unsigned int {
-    kStStateProducer = 1u,
-    kStStateMma = 2u,
-    kStStateScan = 4u,
-    kStFwdProducer = 8u,
-    kStFwdMma = 16u,
-    kStFwdSoftmax = 32u,
-    kStFwdAlign = 64u,
+    kStStateProducer = kStatusTcPrefill << 0,
+    kStStateMma = kStatusTcPrefill << 1,
+    kStStateScan = kStatusTcPrefill << 2,
+    kStFwdProducer = kStatusTcPrefill << 3,
+    kStFwdMma = kStatusTcPrefill << 4,
+    kStFwdSoftmax = kStatusTcPrefill << 5,
+    kStFwdAlign = kStatusTcPrefill << 6,
 };
 
 // Chunks per segment of the state recurrence: enough segments that the state
@@ -98,16 +99,30 @@ struct StateCfg {
 struct StateBars {
     uint64_t kv_full[4], scaled[4], kv_empty[4], mma_done[2], tm_free[2], drain;
     uint32_t tbase;
-    float pw[kBlk];  // eta lambda^d
+    unsigned int st;  // this CTA's status bits
+    float pw[kBlk];   // eta lambda^d
 };
 
 template <int DK, int DV>
 __global__ void __launch_bounds__(192, 2)
 tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mv,
                    int T, int W, int H, const float *__restrict__ lam, const float *__restrict__ eta,
-                   int nch, int L, __nv_bfloat16 *__restrict__ Aloc, float *__restrict__ Lfin) {
+                   int nch, int L, __nv_bfloat16 *__restrict__ Aloc, float *__restrict__ Lfin,
+                   unsigned int *__restrict__ cta_status, unsigned int *__restrict__ status) {
     using C = StateCfg<DK>;
     constexpr int NS = C::NS;
+    // Status words of the call (see the launcher): this kernel is the call's
+    // first, launched after all earlier work on the stream, so its first CTA
+    // zeroes the words of the later kernels before any of them can start (the
+    // fence completes the stores before this CTA's launch trigger).  Its own
+    // bits go to a per-CTA slot written at exit, which the carry kernel folds
+    // into word 0, so no word is both cleared and set by one grid.
+    if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && threadIdx.x == 0) {
+        status[1] = 0u;
+        status[2] = 0u;
+        status[3] = 0u;
+        __threadfence();
+    }
     pdl_launch_dependents();  // the carry kernel may be scheduled; it waits for this grid
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
@@ -130,6 +145,7 @@ tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         }
         mbar_init(&B.drain, 1);
         mbar_fence_init();
+        B.st = 0u;
     }
     if (tid < kBlk) B.pw[tid] = eta[h] * powf(lam[h], (float)tid);
     tc_fence_before();
@@ -154,7 +170,7 @@ tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 tma_load_3d(kd + C::KBYTES, &mv, &B.kv_full[s], 64 * slice, kt, bh);
                 ++issued;
             }
-            if (!ok) atomicOr(&g_status, kStStateProducer);
+            if (!ok) atomicOr(&B.st, kStStateProducer);
             bool dok = true;
             for (int i = max(0, issued - NS); i < issued && dok; ++i)
                 dok = mbar_wait(&B.kv_full[i % NS], (i / NS) & 1);
@@ -178,7 +194,7 @@ tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 mma_commit(&B.mma_done[b]);
                 mma_commit(&B.kv_empty[s]);
             }
-            if (!ok) atomicOr(&g_status, kStStateMma);
+            if (!ok) atomicOr(&B.st, kStStateMma);
             mma_commit(&B.drain);
             mbar_wait(&B.drain, 0);
         }
@@ -260,11 +276,12 @@ tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
                 for (int u = 0; u < 16; ++u) dst[u] = make_float4(A[4 * u], A[4 * u + 1], A[4 * u + 2], A[4 * u + 3]);
             }
         }
-        if (!ok && lane == 0) atomicOr(&g_status, kStStateScan);
+        if (!ok && lane == 0) atomicOr(&B.st, kStStateScan);
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 5) tmem_dealloc(tm, 128);
+    if (tid == 0) cta_status[((size_t)bh * gridDim.y + seg) * gridDim.x + slice] = B.st;
 }
 
 // --------------------------------------------------------------------- segment carries
@@ -273,9 +290,20 @@ tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
 __global__ void __launch_bounds__(128)
 tc_l2_carry_kernel(const float *__restrict__ Lfin, int nseg, int L, int T, int dkdv, int H,
                    const float *__restrict__ lam, __nv_bfloat16 *__restrict__ Cbf,
-                   float *__restrict__ A_final) {
+                   float *__restrict__ A_final, const unsigned int *__restrict__ cta_status, int n_cta,
+                   unsigned int *__restrict__ status) {
     pdl_launch_dependents();  // the forward kernel may start its window tiles now
-    pdl_wait_primary();       // segment finals of the state kernel
+    pdl_wait_primary();       // segment finals and CTA status slots of the state kernel
+    if (blockIdx.x == 0 && blockIdx.y == 0) {  // word 0 of the call: the state CTAs' bits
+        __shared__ unsigned int st;
+        if (threadIdx.x == 0) st = 0u;
+        __syncthreads();
+        unsigned int bits = 0u;
+        for (int i = threadIdx.x; i < n_cta; i += blockDim.x) bits |= cta_status[i];
+        if (bits) atomicOr(&st, bits);
+        __syncthreads();
+        if (threadIdx.x == 0) status[0] = st;
+    }
     const int bh = blockIdx.y;
     const int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (e >= dkdv) return;
@@ -359,7 +387,8 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ma,
               const __grid_constant__ CUtensorMap mc, int T, int W, int H, int nch, int nseg, int L, int l2,
               const float *__restrict__ lam, const float *__restrict__ eta,
-              const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y) {
+              const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y,
+              unsigned int *__restrict__ status) {
     using C = Fwd<DK, DV>;
     constexpr int NST = C::NST;
     // All shared memory is dynamic: with no static shared memory its base is
@@ -367,7 +396,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     extern __shared__ __align__(1024) unsigned char sm[];
     FwdBars &B = *reinterpret_cast<FwdBars *>(sm + C::OFF_BARS);
     if ((smem_u32(sm) & 1023u) != 0) {
-        if (threadIdx.x == 0) atomicOr(&g_status, kStFwdAlign);
+        if (threadIdx.x == 0) atomicOr(status, kStFwdAlign);
         return;
     }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -469,7 +498,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             __syncwarp();
             if (lane == 0) mbar_arrive(&B.c_ready);
         } else if (!ok && lane == 0) {
-            atomicOr(&g_status, kStFwdProducer);
+            atomicOr(status, kStFwdProducer);
         }
         __syncwarp();
     } else if (warp == 9) {
@@ -544,7 +573,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                     mma_commit(&B.o_done);
                 }
             }
-            if (!ok) atomicOr(&g_status, kStFwdMma);
+            if (!ok) atomicOr(status, kStFwdMma);
             // Every MMA issued by this thread has completed before TMEM is freed.
             mma_commit(&B.drain);
             mbar_wait(&B.drain, 0);
@@ -754,7 +783,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 }
             }
         }
-        if (!ok && lane == 0) atomicOr(&g_status, kStFwdSoftmax);
+        if (!ok && lane == 0) atomicOr(status, kStFwdSoftmax);
     }
     tc_fence_before();
     __syncthreads();
@@ -821,13 +850,14 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                   const __grid_constant__ CUtensorMap mc, const __grid_constant__ CUtensorMap my, int T, int W,
                   int H, int nch, int nseg, int L, int l2,
                   const float *__restrict__ lam, const float *__restrict__ eta,
-                  const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y) {
+                  const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y,
+              unsigned int *__restrict__ status) {
     using C = FwdRow<DK, DV>;
     constexpr int NSK = C::NSK, NSV = C::NSV;
     extern __shared__ __align__(1024) unsigned char sm[];
     FwdRowBars &B = *reinterpret_cast<FwdRowBars *>(sm + C::OFF_BARS);
     if ((smem_u32(sm) & 1023u) != 0) {
-        if (threadIdx.x == 0) atomicOr(&g_status, kStFwdAlign);
+        if (threadIdx.x == 0) atomicOr(status, kStFwdAlign);
         return;
     }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -987,7 +1017,7 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 }
             }
             if (ok) mma_commit(&B.o_done);
-            if (!ok) atomicOr(&g_status, kStFwdMma);
+            if (!ok) atomicOr(status, kStFwdMma);
             mma_commit(&B.drain);
             mbar_wait(&B.drain, 0);
         }
@@ -1230,7 +1260,7 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
                 }
             }
         }
-        if (!ok && lane == 0) atomicOr(&g_status, kStFwdSoftmax);
+        if (!ok && lane == 0) atomicOr(status, kStFwdSoftmax);
     }
     tc_fence_before();
     __syncthreads();
@@ -1240,7 +1270,10 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
 struct Ws {
     __nv_bfloat16 *Aloc, *Cbf;
     float *Lfin;
+    unsigned int *cta_status;  // one word per state CTA
 };
+
+size_t n_state_ctas(int BH, const Segments &g, int dv) { return (size_t)(dv / 64) * g.nseg * BH; }
 
 Ws carve(void *ws, int BH, const Segments &g, int dk, int dv) {
     char *p = (char *)ws;
@@ -1250,20 +1283,27 @@ Ws carve(void *ws, int BH, const Segments &g, int dk, int dv) {
     w.Cbf = (__nv_bfloat16 *)p;
     p += align_up(2 * (size_t)BH * g.nseg * dk * dv, 1024);
     w.Lfin = (float *)p;
+    p += align_up(4 * (size_t)BH * g.nseg * dk * dv, 1024);
+    w.cta_status = (unsigned int *)p;
     return w;
 }
 
 size_t ws_bytes(int BH, const Segments &g, int dk, int dv) {
     return align_up(2 * (size_t)BH * g.nch * dk * dv, 1024) + align_up(2 * (size_t)BH * g.nseg * dk * dv, 1024) +
-           align_up(4 * (size_t)BH * g.nseg * dk * dv, 1024);
+           align_up(4 * (size_t)BH * g.nseg * dk * dv, 1024) + align_up(4 * n_state_ctas(BH, g, dv), 1024);
 }
 
 int num_sms() { return device_sm_count(); }
 
+// Status words of the call (status[0..3], the head of its workspace): with the
+// L2 part, word 0 receives the state CTAs' bits from the carry kernel and
+// word 1 the forward kernel's, and the state kernel zeroes words 1..3 first,
+// so the call needs no separate clear.  Window only (no state kernels), the
+// caller zeroes the words before the launch.
 template <int DK, int DV>
 int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W, const float *lam,
         const float *eta, const float *gate, float scale, void *y, float *A_final, void *ws,
-        cudaStream_t st, bool l2) {
+        unsigned int *status, cudaStream_t st, bool l2) {
     const int BH = B_ * H;
     const Segments g = segments(BH, T, DV, num_sms());
     if (DK == 64 && DV == 64 && g.nch > 65535) {  // query blocks are the grid's y extent
@@ -1290,7 +1330,7 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
             auto kern = tc_l2_state_kernel<DK, DV>;
             if (int rc_ = set_smem_limit((const void *)kern, (int)SC::SMEM, "tc_l2_state smem attribute")) return rc_;
             kern<<<dim3(DV / 64, g.nseg, BH), 192, SC::SMEM, st>>>(mk, mv, T, W, H, lam, eta, g.nch, g.L, w.Aloc,
-                                                                  w.Lfin);
+                                                                  w.Lfin, w.cta_status, status);
             if ((rc = launched("tc_l2_state"))) return rc;
         }
         {
@@ -1301,7 +1341,8 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
             cfg.attrs = pdl;
             cfg.numAttrs = 1;
             cudaError_t e = cudaLaunchKernelEx(&cfg, tc_l2_carry_kernel, (const float *)w.Lfin, g.nseg, g.L, T,
-                                               DK * DV, H, lam, w.Cbf, A_final);
+                                               DK * DV, H, lam, w.Cbf, A_final, (const unsigned int *)w.cta_status,
+                                               (int)n_state_ctas(BH, g, DV), status);
             if (e != cudaSuccess) return cuda_fail(e, "tc_l2_carry launch");
             if ((rc = launched("tc_l2_carry"))) return rc;
         }
@@ -1323,7 +1364,7 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         cfg.attrs = pdl;  // window only: no state kernels, so ordinary stream order
         cfg.numAttrs = l2 ? 1 : 0;
         cudaError_t e = cudaLaunchKernelEx(&cfg, kern, mq, mk, mv, ma, mc, my, T, W, H, g.nch, g.nseg, g.L,
-                                           (int)l2, lam, eta, gate, scale, (__nv_bfloat16 *)y);
+                                           (int)l2, lam, eta, gate, scale, (__nv_bfloat16 *)y, status + 1);
         rc = e != cudaSuccess ? cuda_fail(e, "tc_fwd_row launch") : launched("tc_fwd_row");
         prof_end(st);
         return rc;
@@ -1335,7 +1376,7 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         if (int rc_ = set_smem_limit((const void *)kern, smem, "tc_fwd smem attribute")) return rc_;
         prof_begin(st);
         kern<<<dim3(g.nch, BH), 320, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, (int)l2, lam,
-                                                  eta, gate, scale, (__nv_bfloat16 *)y);
+                                                  eta, gate, scale, (__nv_bfloat16 *)y, status + 1);
         rc = launched("tc_fwd");
         prof_end(st);
         return rc;
@@ -1354,26 +1395,17 @@ size_t tc_prefill_tcgen05_workspace(int BH, int T, int dk, int dv) {
 
 int tc_prefill_tcgen05(const void *q, const void *k, const void *v, int B, int H, int T, int dk,
                        int dv, int W, const float *lam, const float *eta, const float *gate,
-                       float scale, void *y, float *A_final, void *ws, cudaStream_t s, bool l2) {
-    if (dk == 64 && dv == 64) return run<64, 64>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s, l2);
+                       float scale, void *y, float *A_final, void *ws, unsigned int *status,
+                       cudaStream_t s, bool l2) {
+    if (dk == 64 && dv == 64) return run<64, 64>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, status, s, l2);
     if (dk == 64 && dv == 128)
-        return run<64, 128>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s, l2);
+        return run<64, 128>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, status, s, l2);
     if (dk == 128 && dv == 64)
-        return run<128, 64>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s, l2);
+        return run<128, 64>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, status, s, l2);
     if (dk == 128 && dv == 128)
-        return run<128, 128>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, s, l2);
+        return run<128, 128>(q, k, v, B, H, T, W, lam, eta, gate, scale, y, A_final, ws, status, s, l2);
     set_error("tensor-core prefill: d_k=%d d_v=%d unsupported", dk, dv);
     return OPAM_ERR_UNSUPPORTED;
-}
-
-unsigned int tc_prefill_tcgen05_status(bool clear) {
-    unsigned int v = 0;
-    cudaMemcpyFromSymbol(&v, g_status, sizeof v);
-    if (clear && v) {
-        const unsigned int z = 0;
-        cudaMemcpyToSymbol(g_status, &z, sizeof z);
-    }
-    return v;
 }
 
 }  // namespace opam

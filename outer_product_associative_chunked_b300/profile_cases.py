@@ -96,7 +96,7 @@ def main(argv=None):
     torch.cuda.set_device(0)
     CASES[argv[0]]()
     torch.cuda.synchronize()
-    binding.device_status()
+    binding.check_device_errors()
     print(f"{argv[0]} ok")
 
 

@@ -99,6 +99,19 @@ def tc_decode_inputs(steps, S, H, d_k, d_v, dtype="bf16", seed=103) -> TCDecodeI
     return TCDecodeInputs(_round(q, dtype), _round(k, dtype), _round(v, dtype), dtype)
 
 
+def tc_decode_state(S, H, W, d_k, d_v, pos, dtype="bf16", seed=104) -> dict:
+    """A full Tensor Cache streaming state to start decode steps from, for
+    timing: ring keys unit rows and ring values Gaussian (as tokens are drawn),
+    A Gaussian with entries of variance 1/d_k, every sequence at position
+    ``pos`` (>= W, so the ring is full and every step evicts)."""
+    g = _gen(seed)
+    ring_k = _unit_rows(torch.randn(S, H, W, d_k, generator=g))
+    ring_v = torch.randn(S, H, W, d_v, generator=g)
+    A = torch.randn(S, H, d_k, d_v, generator=g) / math.sqrt(d_k)
+    return dict(ring_k=_round(ring_k, dtype), ring_v=_round(ring_v, dtype), A=A.float().contiguous(),
+                pos=torch.full((S,), int(pos), dtype=torch.int64))
+
+
 # ---------------------------------------------------------------- DeltaNet
 @dataclass
 class DeltaInputs:

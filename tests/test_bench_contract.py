@@ -25,13 +25,20 @@ def test_roofline_picks_the_binding_roof():
     assert r["bound"] == "tensor" and r["peak"] == 1000.0
     assert r["achieved"] == pytest.approx(500.0) and r["frac"] == pytest.approx(0.5)
     assert r["traffic"] == 123 and r["scope"] == "step"
+    # float32 paths: the FP32 FMA rate is the compute roof, reported as "alu"
+    r = bench.roofline(1e12, 1e9, 2e-2, dict(PEAKS, fp32_tflops=100.0), "fp32")
+    assert r["bound"] == "alu" and r["peak"] == 100.0 and r["frac"] == pytest.approx(0.5)
 
 
 def test_work_models_against_hand_counts():
     # window pairs: T=4, W=2 -> 1 + 2 + 2 + 2 = 7 (query, key) pairs
     assert bench.tc_pairs(4, 2) == 7
+    # with the L2 memory: per evicted token the write k v^T and the read q A,
+    # 2 d_k d_v each
     fl, by = bench.tc_prefill_work(1, 1, 4, 2, 2, 2, 2)
-    assert fl == 2 * (2 + 2) * 7 + 2 * 2 * 2 * (4 - 2)
+    assert fl == 2 * (2 + 2) * 7 + 4 * 2 * 2 * (4 - 2)
+    fl_w, by_w = bench.tc_prefill_work(1, 1, 4, 2, 2, 2, 2, l2=False)
+    assert fl_w == 2 * (2 + 2) * 7 and by_w == by
     assert by == 4 * (2 * 2 + 2 * 2) * 2
     fl, by = bench.delta_decode_work(3, 2, 4, 8, 2)
     assert fl == 6 * 6 * 4 * 8

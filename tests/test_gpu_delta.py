@@ -63,7 +63,7 @@ def test_tensor_core_shapes(cuda_lib, oracle_mod, B, H, T, dk, with_S0):
     S_out = S if S is not None else torch.empty(B, H, dk, 128, device="cuda")  # in place when given
     y = cuda_lib.delta_rule_forward(q, k, v, beta, chunk=64, S0=S, S_out=S_out)
     torch.cuda.synchronize()
-    cuda_lib.device_status(clear=True)
+    cuda_lib.check_device_errors()
     ref = oracle_mod.delta(inp.q, inp.k, inp.v, inp.beta, S0=S0, want_state=True)
     check_parity(to_np(y), ref["y"], "bf16", "delta y (tensor cores)")
     check_parity(to_np(S_out), ref["S"], "bf16", "delta S (tensor cores)")

@@ -57,7 +57,7 @@ def test_decode_continues_a_gpu_prefill(cuda_lib, oracle_mod):
                                      v[:, :, t].contiguous(), beta[:, :, t].contiguous())
           for t in range(T0, T0 + n)]
     torch.cuda.synchronize()
-    cuda_lib.device_status(clear=True)
+    cuda_lib.check_device_errors()
     ref = oracle_mod.delta(inp.q, inp.k, inp.v, inp.beta, want_state=True)
     check_parity(to_np(y0), ref["y"][:, :, :T0], "bf16", "prefill part")
     check_parity(to_np(torch.stack(ys, dim=2)), ref["y"][:, :, T0:], "bf16", "decode part")

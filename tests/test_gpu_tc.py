@@ -18,10 +18,11 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(autouse=True)
 def _no_device_timeouts(cuda_lib):
-    """Every case must leave the tensor-core kernels' wait status clean."""
-    cuda_lib.device_status(clear=True)
+    """Every case must leave its calls' device status clean (no bounded wait
+    ran out, no CUDA error)."""
+    cuda_lib.check_device_errors()
     yield
-    cuda_lib.device_status(clear=True)
+    cuda_lib.check_device_errors()
 
 
 def _gpu(inp):
