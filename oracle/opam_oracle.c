@@ -400,3 +400,262 @@ void oracle_sparse_linattn_output_at(int T, int N, int dv,
         }
     }
 }
+
+/* ======================================================================
+ * Backward passes (gradients of a scalar loss through the layers above).
+ *
+ * The Tensor Cache page presents the parallel weighted-sum scan as what makes
+ * the layer trainable without chunk averaging (Methodology 2; Main
+ * contributions); training needs the gradient of the layer.  The pages print
+ * no backward formulas, so the definition used here is the plain one: the
+ * derivative of L = sum_t <dy_t, y_t> with respect to every input, for a
+ * given upstream gradient dy.  Each function below is reverse-mode
+ * differentiation of the per-token recurrence above, written step by step:
+ * the forward recurrence is run first and its states kept, then the steps
+ * are undone in reverse order, each forward operation contributing its
+ * partial derivatives.  Nothing is blocked or fused.
+ * ====================================================================== */
+
+/* Tensor Cache layer backward from an empty state.  Forward step t (see
+ * tc_step): (c) if t >= W the token e = t-W is written,
+ * A_t = lambda A_{t-1} + eta k_e v_e^T; the new token enters the ring;
+ * (b) y_loc = sum_s p_s v_s over s in [max(0,t-W+1), t], p = softmax_s of
+ * scale <q_t, k_s>; (a) m_t = q_t A_t, y_t = y_loc + sigmoid(g) m_t.
+ * Reverse step t, with dA the gradient with respect to A_t:
+ *   (a) dg += sigmoid'(g) <dy_t, m_t>; dm = sigmoid(g) dy_t;
+ *       dq_t += A_t dm; dA += q_t dm^T
+ *   (b) dv_s += p_s dy_t; dp_s = <dy_t, v_s>; D = sum_s p_s dp_s;
+ *       ds_s = p_s (dp_s - D); dq_t += scale sum_s ds_s k_s;
+ *       dk_s += scale ds_s q_t
+ *   (c) if t >= W: dlambda += <dA, A_{t-1}>; deta += k_e^T dA v_e;
+ *       dk_e += eta dA v_e; dv_e += eta dA^T k_e; then dA <- lambda dA
+ *       (the gradient with respect to A_{t-1}).
+ * q,k: [B][H][T][dk]; v, dy: [B][H][T][dv]; lam, eta, gate: [H].
+ * Outputs dq, dk: [B][H][T][dk]; dv: [B][H][T][dv]; dlam, deta, dgate: [H]
+ * (summed over the batch).  Returns 0, or -1 on allocation failure. */
+int oracle_tc_backward(int B, int H, int T, int dk, int dv, int W,
+                       const double *q, const double *k, const double *v,
+                       const double *lam, const double *eta, const double *gate,
+                       double scale, const double *dy,
+                       double *dq, double *dk_out, double *dv_out,
+                       double *dlam, double *deta, double *dgate)
+{
+    int err = 0;
+    const int units = B * H;
+    double *gl = (double *)calloc((size_t)units * 3, sizeof(double)); /* per-unit scalar grads */
+    if (!gl) return -1;
+    memset(dq, 0, sizeof(double) * (size_t)units * T * dk);
+    memset(dk_out, 0, sizeof(double) * (size_t)units * T * dk);
+    memset(dv_out, 0, sizeof(double) * (size_t)units * T * dv);
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int bh = 0; bh < units; ++bh) {
+        const int h = bh % H;
+        const double lm = lam[h], et = eta[h], sg = logistic(gate[h]);
+        const size_t dd = (size_t)dk * dv;
+        const double *Q = q + (size_t)bh * T * dk, *K = k + (size_t)bh * T * dk;
+        const double *V = v + (size_t)bh * T * dv, *DY = dy + (size_t)bh * T * dv;
+        double *DQ = dq + (size_t)bh * T * dk, *DK = dk_out + (size_t)bh * T * dk;
+        double *DV = dv_out + (size_t)bh * T * dv;
+        /* States A_t after step t's write, t = -1..T-1 (A_{-1} = 0). */
+        double *As = (double *)calloc((size_t)(T + 1) * dd, sizeof(double));
+        double *dA = (double *)calloc(dd, sizeof(double));
+        double *p = (double *)malloc(sizeof(double) * (size_t)(W + 1));
+        double *dp = (double *)malloc(sizeof(double) * (size_t)(W + 1));
+        double *m = (double *)malloc(sizeof(double) * (size_t)dv);
+        double *dm = (double *)malloc(sizeof(double) * (size_t)dv);
+        if (!As || !dA || !p || !dp || !m || !dm) {
+            err |= 1;
+            free(As); free(dA); free(p); free(dp); free(m); free(dm);
+            continue;
+        }
+        for (int t = 0; t < T; ++t) {            /* forward: the states only */
+            const double *prev = As + (size_t)t * dd;
+            double *cur = As + (size_t)(t + 1) * dd;
+            memcpy(cur, prev, sizeof(double) * dd);
+            if (t >= W) {
+                const double *ke = K + (size_t)(t - W) * dk, *ve = V + (size_t)(t - W) * dv;
+                for (int a = 0; a < dk; ++a)
+                    for (int b = 0; b < dv; ++b)
+                        cur[(size_t)a * dv + b] = lm * prev[(size_t)a * dv + b] + et * ke[a] * ve[b];
+            }
+        }
+        double g_lam = 0.0, g_eta = 0.0, g_gate = 0.0;
+        for (int t = T - 1; t >= 0; --t) {
+            const double *qt = Q + (size_t)t * dk, *dyt = DY + (size_t)t * dv;
+            const double *At = As + (size_t)(t + 1) * dd;
+            /* (a) read and gate */
+            for (int b = 0; b < dv; ++b) {
+                double s = 0.0;
+                for (int a = 0; a < dk; ++a) s += qt[a] * At[(size_t)a * dv + b];
+                m[b] = s;
+                dm[b] = sg * dyt[b];
+            }
+            double dym = 0.0;
+            for (int b = 0; b < dv; ++b) dym += dyt[b] * m[b];
+            g_gate += sg * (1.0 - sg) * dym;
+            for (int a = 0; a < dk; ++a) {
+                double s = 0.0;
+                for (int b = 0; b < dv; ++b) s += At[(size_t)a * dv + b] * dm[b];
+                DQ[(size_t)t * dk + a] += s;
+                for (int b = 0; b < dv; ++b) dA[(size_t)a * dv + b] += qt[a] * dm[b];
+            }
+            /* (b) window softmax */
+            const int s0 = t - W + 1 > 0 ? t - W + 1 : 0, n = t - s0 + 1;
+            double mx = -INFINITY;
+            for (int i = 0; i < n; ++i) {
+                const double *ks = K + (size_t)(s0 + i) * dk;
+                double s = 0.0;
+                for (int a = 0; a < dk; ++a) s += qt[a] * ks[a];
+                p[i] = s * scale;
+                if (p[i] > mx) mx = p[i];
+            }
+            double z = 0.0;
+            for (int i = 0; i < n; ++i) { p[i] = exp(p[i] - mx); z += p[i]; }
+            double D = 0.0;
+            for (int i = 0; i < n; ++i) {
+                p[i] /= z;
+                const double *vs = V + (size_t)(s0 + i) * dv;
+                double s = 0.0;
+                for (int b = 0; b < dv; ++b) s += dyt[b] * vs[b];
+                dp[i] = s;
+                D += p[i] * s;
+            }
+            for (int i = 0; i < n; ++i) {
+                const double *ks = K + (size_t)(s0 + i) * dk;
+                const double ds = p[i] * (dp[i] - D);
+                for (int b = 0; b < dv; ++b) DV[(size_t)(s0 + i) * dv + b] += p[i] * dyt[b];
+                for (int a = 0; a < dk; ++a) {
+                    DQ[(size_t)t * dk + a] += scale * ds * ks[a];
+                    DK[(size_t)(s0 + i) * dk + a] += scale * ds * qt[a];
+                }
+            }
+            /* (c) the eviction write of step t */
+            if (t >= W) {
+                const int e = t - W;
+                const double *ke = K + (size_t)e * dk, *ve = V + (size_t)e * dv;
+                const double *Ap = As + (size_t)t * dd;  /* A_{t-1} */
+                for (int a = 0; a < dk; ++a) {
+                    double sv = 0.0;
+                    for (int b = 0; b < dv; ++b) {
+                        const double g = dA[(size_t)a * dv + b];
+                        g_lam += g * Ap[(size_t)a * dv + b];
+                        sv += g * ve[b];
+                    }
+                    g_eta += ke[a] * sv;
+                    DK[(size_t)e * dk + a] += et * sv;
+                }
+                for (int b = 0; b < dv; ++b) {
+                    double sk = 0.0;
+                    for (int a = 0; a < dk; ++a) sk += dA[(size_t)a * dv + b] * ke[a];
+                    DV[(size_t)e * dv + b] += et * sk;
+                }
+                for (size_t i = 0; i < dd; ++i) dA[i] *= lm;
+            }
+        }
+        gl[(size_t)bh * 3 + 0] = g_lam;
+        gl[(size_t)bh * 3 + 1] = g_eta;
+        gl[(size_t)bh * 3 + 2] = g_gate;
+        free(As); free(dA); free(p); free(dp); free(m); free(dm);
+    }
+    if (!err) {
+        for (int h = 0; h < H; ++h) dlam[h] = deta[h] = dgate[h] = 0.0;
+        for (int bh = 0; bh < units; ++bh) {  /* batch sums in a fixed order */
+            dlam[bh % H] += gl[(size_t)bh * 3 + 0];
+            deta[bh % H] += gl[(size_t)bh * 3 + 1];
+            dgate[bh % H] += gl[(size_t)bh * 3 + 2];
+        }
+    }
+    free(gl);
+    return err ? -1 : 0;
+}
+
+/* DeltaNet delta-rule backward.  Forward step t (oracle_delta):
+ * u_t = v_t - S_{t-1} k_t, S_t = S_{t-1} + beta_t u_t k_t^T, o_t = S_t q_t
+ * (S is d_v x d_k).  Reverse step t, with dS the gradient with respect to S_t:
+ *   dq_t = S_t^T do_t;  dS += do_t q_t^T;
+ *   g = dS k_t;  dv_t = beta_t g;  dbeta_t = <u_t, g>;
+ *   dk_t = beta_t dS^T u_t - S_{t-1}^T (beta_t g);
+ *   dS <- dS - beta_t g k_t^T  (the gradient with respect to S_{t-1}).
+ * q,k: [B][H][T][dk]; v, dy: [B][H][T][dv]; beta: [B][H][T];
+ * S0: NULL or [B][H][dk][dv] key-major start state; dS_T: NULL or the
+ * gradient with respect to the final state, same layout.  Outputs dq, dk,
+ * dv, dbeta as their inputs; dS0: NULL or the gradient with respect to S0.
+ * Returns 0, or -1 on allocation failure. */
+int oracle_delta_backward(int B, int H, int T, int dk, int dv,
+                          const double *q, const double *k, const double *v,
+                          const double *beta, const double *S0, const double *dy,
+                          const double *dS_T, double *dq, double *dk_out,
+                          double *dv_out, double *dbeta, double *dS0)
+{
+    int err = 0;
+    const int units = B * H;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : err)
+    for (int bh = 0; bh < units; ++bh) {
+        const size_t dd = (size_t)dk * dv;
+        const double *Q = q + (size_t)bh * T * dk, *K = k + (size_t)bh * T * dk;
+        const double *V = v + (size_t)bh * T * dv, *DY = dy + (size_t)bh * T * dv;
+        const double *Bt = beta + (size_t)bh * T;
+        /* Ss[t] = S_{t-1} (t = 0..T), stored key-major like the API: element
+         * S_{i,j} (row i of d_v, column j of d_k) at [j * dv + i]. */
+        double *Ss = (double *)calloc((size_t)(T + 1) * dd, sizeof(double));
+        double *U = (double *)malloc(sizeof(double) * (size_t)T * dv);
+        double *dS = (double *)calloc(dd, sizeof(double));
+        double *g = (double *)malloc(sizeof(double) * (size_t)dv);
+        if (!Ss || !U || !dS || !g) {
+            err |= 1;
+            free(Ss); free(U); free(dS); free(g);
+            continue;
+        }
+        if (S0) memcpy(Ss, S0 + (size_t)bh * dd, sizeof(double) * dd);
+        for (int t = 0; t < T; ++t) {
+            const double *Sp = Ss + (size_t)t * dd;
+            double *Sc = Ss + (size_t)(t + 1) * dd;
+            const double *kt = K + (size_t)t * dk, *vt = V + (size_t)t * dv;
+            double *ut = U + (size_t)t * dv;
+            for (int i = 0; i < dv; ++i) {
+                double s = 0.0;
+                for (int j = 0; j < dk; ++j) s += Sp[(size_t)j * dv + i] * kt[j];
+                ut[i] = vt[i] - s;
+            }
+            for (int j = 0; j < dk; ++j)
+                for (int i = 0; i < dv; ++i)
+                    Sc[(size_t)j * dv + i] = Sp[(size_t)j * dv + i] + Bt[t] * ut[i] * kt[j];
+        }
+        if (dS_T) memcpy(dS, dS_T + (size_t)bh * dd, sizeof(double) * dd);
+        for (int t = T - 1; t >= 0; --t) {
+            const double *St = Ss + (size_t)(t + 1) * dd, *Sp = Ss + (size_t)t * dd;
+            const double *qt = Q + (size_t)t * dk, *kt = K + (size_t)t * dk;
+            const double *dot = DY + (size_t)t * dv, *ut = U + (size_t)t * dv;
+            const double bt = Bt[t];
+            double *dqt = dq + ((size_t)bh * T + t) * dk, *dkt = dk_out + ((size_t)bh * T + t) * dk;
+            double *dvt = dv_out + ((size_t)bh * T + t) * dv;
+            for (int j = 0; j < dk; ++j) {                 /* dq = S_t^T do */
+                double s = 0.0;
+                for (int i = 0; i < dv; ++i) s += St[(size_t)j * dv + i] * dot[i];
+                dqt[j] = s;
+            }
+            for (int j = 0; j < dk; ++j)                   /* dS += do q^T */
+                for (int i = 0; i < dv; ++i) dS[(size_t)j * dv + i] += dot[i] * qt[j];
+            double db = 0.0;
+            for (int i = 0; i < dv; ++i) {                 /* g = dS k */
+                double s = 0.0;
+                for (int j = 0; j < dk; ++j) s += dS[(size_t)j * dv + i] * kt[j];
+                g[i] = s;
+                dvt[i] = bt * s;
+                db += ut[i] * s;
+            }
+            dbeta[(size_t)bh * T + t] = db;
+            for (int j = 0; j < dk; ++j) {                 /* dk = beta dS^T u - S_{t-1}^T (beta g) */
+                double s = 0.0;
+                for (int i = 0; i < dv; ++i)
+                    s += bt * dS[(size_t)j * dv + i] * ut[i] - Sp[(size_t)j * dv + i] * bt * g[i];
+                dkt[j] = s;
+            }
+            for (int j = 0; j < dk; ++j)                   /* dS -= beta g k^T */
+                for (int i = 0; i < dv; ++i) dS[(size_t)j * dv + i] -= bt * g[i] * kt[j];
+        }
+        if (dS0) memcpy(dS0 + (size_t)bh * dd, dS, sizeof(double) * dd);
+        free(Ss); free(U); free(dS); free(g);
+    }
+    return err ? -1 : 0;
+}

@@ -54,6 +54,10 @@ def _load():
             lib.oracle_sparse_linattn.argtypes = [i, i, i, i, i, _D, _D, _D, _D, _D, _D]
             lib.oracle_sparse_linattn_output_at.argtypes = [i, i, i, _D, _D, _D, _D, i, _I64, _D]
             lib.oracle_sparse_linattn_output_at.restype = None
+            lib.oracle_tc_backward.argtypes = [i, i, i, i, i, i, _D, _D, _D, _D, _D, _D, d, _D,
+                                               _D, _D, _D, _D, _D, _D]
+            lib.oracle_delta_backward.argtypes = [i, i, i, i, i, _D, _D, _D, _D, _D, _D, _D, _D, _D,
+                                                  _D, _D, _D]
             lib.oracle_set_threads.argtypes = [i]
             lib.oracle_set_threads.restype = None
             lib.oracle_get_threads.restype = i
@@ -212,3 +216,40 @@ def sparse_linattn_output_at(q, k, v, ts, S0=None):
     _load().oracle_sparse_linattn_output_at(T, N, dv, _p(q), _p(k), _p(v), _p(S0), len(ts),
                                             ts.ctypes.data_as(_I64), _p(y))
     return y
+
+
+def tc_backward(q, k, v, lam, eta, gate, W, dy, scale=None):
+    """Gradient of L = sum <dy, y> through the Tensor Cache layer (prefill from
+    an empty state).  Returns dict dq, dk [B,H,T,d_k], dv [B,H,T,d_v] and
+    dlam, deta, dgate [H] (summed over the batch)."""
+    q, k, v, dy = f64(q), f64(k), f64(v), f64(dy)
+    lam, eta, gate = f64(lam), f64(eta), f64(gate)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    scale = default_scale(dk) if scale is None else float(scale)
+    out = {"dq": np.zeros((B, H, T, dk)), "dk": np.zeros((B, H, T, dk)), "dv": np.zeros((B, H, T, dv)),
+           "dlam": np.zeros(H), "deta": np.zeros(H), "dgate": np.zeros(H)}
+    rc = _load().oracle_tc_backward(B, H, T, dk, dv, int(W), _p(q), _p(k), _p(v), _p(lam), _p(eta),
+                                    _p(gate), scale, _p(dy), _p(out["dq"]), _p(out["dk"]), _p(out["dv"]),
+                                    _p(out["dlam"]), _p(out["deta"]), _p(out["dgate"]))
+    if rc != 0:
+        raise MemoryError("oracle_tc_backward failed to allocate")
+    return out
+
+
+def delta_backward(q, k, v, beta, dy, S0=None, dS_T=None):
+    """Gradient of L = sum <dy, o> (+ <dS_T, S_T>) through the delta rule.
+    Returns dict dq, dk, dv, dbeta and dS0 (key-major [B,H,d_k,d_v])."""
+    q, k, v, beta, dy = f64(q), f64(k), f64(v), f64(beta), f64(dy)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    S0 = None if S0 is None else f64(S0)
+    dS_T = None if dS_T is None else f64(dS_T)
+    out = {"dq": np.zeros((B, H, T, dk)), "dk": np.zeros((B, H, T, dk)), "dv": np.zeros((B, H, T, dv)),
+           "dbeta": np.zeros((B, H, T)), "dS0": np.zeros((B, H, dk, dv))}
+    rc = _load().oracle_delta_backward(B, H, T, dk, dv, _p(q), _p(k), _p(v), _p(beta), _p(S0), _p(dy),
+                                       _p(dS_T), _p(out["dq"]), _p(out["dk"]), _p(out["dv"]),
+                                       _p(out["dbeta"]), _p(out["dS0"]))
+    if rc != 0:
+        raise MemoryError("oracle_delta_backward failed to allocate")
+    return out
