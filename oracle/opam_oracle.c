@@ -659,3 +659,31 @@ int oracle_delta_backward(int B, int H, int T, int dk, int dv,
     }
     return err ? -1 : 0;
 }
+
+/* ======================================================================
+ * BDH key generation (ainews.random.gg, BDH memory-architecture post: the
+ * wide, sparse, non-negative activations come from a low-rank factorisation
+ * followed by ReLU thresholding).  For one head h, a token's R-dimensional
+ * input x is lifted to the N-wide activation
+ *     a[n] = max(0, sum_r x[r] U_h[r][n] - theta),
+ * the same U_h serving queries and keys.  Plain float64 loops, no blocking.
+ * x: [B][H][T][R]; U: [H][R][N]; out: [B][H][T][N].
+ * ====================================================================== */
+void oracle_bdh_keys(int B, int H, int T, int R, int N, const double *x, const double *U,
+                     double theta, double *out)
+{
+    const long rows = (long)B * H * T;
+#pragma omp parallel for schedule(static)
+    for (long row = 0; row < rows; ++row) {
+        const int h = (int)((row / T) % H);
+        const double *xr = x + (size_t)row * R;
+        const double *Uh = U + (size_t)h * R * N;
+        double *o = out + (size_t)row * N;
+        for (int n = 0; n < N; ++n) {
+            double s = 0.0;
+            for (int r = 0; r < R; ++r) s += xr[r] * Uh[(size_t)r * N + n];
+            s -= theta;
+            o[n] = s > 0.0 ? s : 0.0;
+        }
+    }
+}

@@ -58,6 +58,8 @@ def _load():
                                                _D, _D, _D, _D, _D, _D]
             lib.oracle_delta_backward.argtypes = [i, i, i, i, i, _D, _D, _D, _D, _D, _D, _D, _D, _D,
                                                   _D, _D, _D]
+            lib.oracle_bdh_keys.argtypes = [i, i, i, i, i, _D, _D, d, _D]
+            lib.oracle_bdh_keys.restype = None
             lib.oracle_set_threads.argtypes = [i]
             lib.oracle_set_threads.restype = None
             lib.oracle_get_threads.restype = i
@@ -252,4 +254,15 @@ def delta_backward(q, k, v, beta, dy, S0=None, dS_T=None):
                                        _p(out["dbeta"]), _p(out["dS0"]))
     if rc != 0:
         raise MemoryError("oracle_delta_backward failed to allocate")
+    return out
+
+
+def bdh_keys(x, U, theta):
+    """BDH activations max(0, x U_h - theta): x [B,H,T,R], U [H,R,N];
+    returns [B,H,T,N] float64."""
+    x, U = f64(x), f64(U)
+    B, H, T, R = x.shape
+    N = U.shape[-1]
+    out = np.zeros((B, H, T, N))
+    _load().oracle_bdh_keys(B, H, T, R, N, _p(x), _p(U), float(theta), _p(out))
     return out

@@ -176,6 +176,28 @@ def sparse_inputs(B, H, T, N, d_v, seed=4, rank=256, theta=BDH_THETA_5PCT) -> Sp
     return SparseInputs(q.contiguous(), k.contiguous(), v.contiguous(), float(theta))
 
 
+@dataclass
+class KeygenInputs:
+    xq: torch.Tensor         # [B,H,T,R] bf16 query-side token inputs
+    xk: torch.Tensor         # [B,H,T,R] bf16 key-side token inputs
+    U: torch.Tensor          # [H,R,N] bf16, one factor per head
+    v: torch.Tensor          # [B,H,T,d_v] float32
+    theta: float
+
+
+def sparse_keygen_inputs(B, H, T, N, d_v, seed=5, rank=256, theta=BDH_THETA_5PCT) -> KeygenInputs:
+    """The inputs of the BDH recipe before the ReLU threshold: x, x' ~ N(0, I_R)
+    per token, U_h ~ N(0, 1/R)^{R x N} per head, v Gaussian; x and U rounded
+    to bf16 (the tensor-core operand type) so that both sides read the same
+    values.  The activations themselves are not formed here."""
+    g = _gen(seed)
+    xq = torch.randn(B, H, T, rank, generator=g)
+    xk = torch.randn(B, H, T, rank, generator=g)
+    v = torch.randn(B, H, T, d_v, generator=g)
+    U = torch.randn(H, rank, N, generator=g) / math.sqrt(rank)
+    return KeygenInputs(_round(xq, "bf16"), _round(xk, "bf16"), _round(U, "bf16"), v.contiguous(), float(theta))
+
+
 # ---------------------------------------------------------------- workloads
 @dataclass
 class Workload:
@@ -215,4 +237,9 @@ WORKLOADS = {
     "bdh_fp32_B2_H4_T2048_N16384_dv256": Workload(
         "bdh_fp32_B2_H4_T2048_N16384_dv256", "sparse",
         dict(B=2, H=4, T=2048, N=16384, d_v=256), seed=4),
+    # The same attention with the keys and queries generated on the GPU from
+    # their 256-wide inputs (bf16 x and U, fp32 accumulation and state).
+    "bdh_keygen_B2_H4_T2048_R256_N16384_dv256": Workload(
+        "bdh_keygen_B2_H4_T2048_R256_N16384_dv256", "sparse_keygen",
+        dict(B=2, H=4, T=2048, R=256, N=16384, d_v=256), seed=5),
 }

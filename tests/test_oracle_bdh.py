@@ -97,3 +97,34 @@ def test_synthetic_keys_are_sparse_and_nonnegative():
         assert torch.all(x >= 0)
         dens = float((x > 0).double().mean())
         assert 0.04 < dens < 0.06, dens
+
+
+# ------------------------------------------------------------------ key generation
+def test_bdh_keys_match_library_matmul(oracle_mod):
+    """oracle.bdh_keys against torch's float64 matmul and ReLU."""
+    import torch
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(2, 3, 5, 16, generator=g, dtype=torch.float64)
+    U = torch.randn(3, 16, 40, generator=g, dtype=torch.float64) / 4
+    for theta in (-0.5, 0.0, 0.7):
+        ref = torch.relu(torch.einsum("bhtr,hrn->bhtn", x, U) - theta).numpy()
+        np.testing.assert_allclose(oracle_mod.bdh_keys(x, U, theta), ref, rtol=1e-13, atol=1e-14)
+
+
+def test_bdh_keys_reproduce_the_recipe(oracle_mod):
+    """From the same inputs, the oracle's keys are the recipe's float32 keys
+    up to float32 rounding, and the 95th-percentile threshold keeps about 5%
+    of the entries; a very low threshold keeps every positive pre-activation
+    (shifted), a very high one none."""
+    from outer_product_associative_chunked_b300 import synth
+    import torch
+    kg = synth.sparse_keygen_inputs(1, 2, 64, 4096, 8, seed=7)
+    keys = oracle_mod.bdh_keys(kg.xk, kg.U, kg.theta)
+    f32 = torch.relu(torch.einsum("bhtr,hrn->bhtn", kg.xk.float(), kg.U.float()) - kg.theta).double().numpy()
+    assert np.abs(keys - f32).max() < 1e-5
+    dens = float((keys > 0).mean())
+    assert 0.04 < dens < 0.06, dens
+    assert np.all(oracle_mod.bdh_keys(kg.xk, kg.U, 1e3) == 0.0)
+    low = oracle_mod.bdh_keys(kg.xk, kg.U, -1e3)
+    pre = np.einsum("bhtr,hrn->bhtn", oracle_mod.f64(kg.xk), oracle_mod.f64(kg.U))
+    np.testing.assert_allclose(low, pre + 1e3, rtol=1e-14)
