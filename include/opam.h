@@ -121,6 +121,29 @@ int tc_layer_forward(const void *q, const void *k, const void *v, int dtype,
                      float softmax_scale, void *y, opam_tc_state *state_out,
                      void *workspace, size_t workspace_bytes, void *stream);
 
+/* Tensor Cache layer backward: the gradient of L = sum_t <dy_t, y_t> through
+ * tc_layer_forward ("Tensor Cache", Methodology 2: the parallel weighted-sum
+ * scan is what makes the layer trainable without chunk averaging; the pages
+ * print no backward formulas, so the gradient is the exact derivative of
+ * the forward definition above).  Same inputs as tc_layer_forward, plus
+ *   dy        [B][H][T][d_v]  dtype, upstream gradient of y
+ * and outputs (all written, none accumulated into):
+ *   dq, dk    [B][H][T][d_k]  dtype
+ *   dv        [B][H][T][d_v]  dtype
+ *   dlambda, deta, dgate  [H] float32, summed over the batch.
+ * Nothing from the forward call is needed: the softmax statistics and the
+ * chunk states are recomputed.  Arithmetic is float32 throughout (bf16
+ * inputs are widened on load).  Supported sizes and errors as
+ * tc_layer_forward; workspace: tc_layer_backward_workspace_size() bytes. */
+size_t tc_layer_backward_workspace_size(int B, int H, int T, int d_k, int d_v, int W,
+                                        int dtype);
+int tc_layer_backward(const void *q, const void *k, const void *v, int dtype,
+                      int B, int H, int T, int d_k, int d_v, int W,
+                      const float *lambda, const float *eta, const float *gate,
+                      float softmax_scale, const void *dy, void *dq, void *dk, void *dv,
+                      float *dlambda, float *deta, float *dgate, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
 /* Bytes of scratch built into the library for tc_layer_forward_noalloc. */
 #define OPAM_STATIC_SCRATCH_BYTES (64u << 20)
 
@@ -217,6 +240,28 @@ int delta_rule_forward(const void *q, const void *k, const void *v,
                        float *S_out, void *y, void *workspace,
                        size_t workspace_bytes, void *stream);
 
+/* DeltaNet delta-rule backward: the gradient of
+ * L = sum_t <dy_t, o_t> + <dS_T, S_T> through delta_rule_forward (same page
+ * and section; the pages print no backward formulas, so the gradient is the
+ * exact derivative of the recurrence above, taken step by step in reverse).
+ *   q, k, v, beta, dtype, B, H, T, d_k, d_v, S0  as delta_rule_forward
+ *   dy     [B][H][T][d_v] dtype, upstream gradient of o
+ *   dS_T   NULL (zero) or [B][H][d_k][d_v] float32 key-major gradient of the
+ *          final state
+ *   dq, dk [B][H][T][d_k] dtype;  dv [B][H][T][d_v] dtype;  dbeta [B][H][T]
+ *          float32 (all written)
+ *   dS0    NULL or [B][H][d_k][d_v] float32, receives the gradient of S0
+ * Arithmetic is float32; the state is carried per token (no chunking), so
+ * the time is a sequential walk of 2T steps per (batch, head).  Supported:
+ * d_k, d_v in {32, 64, 128}; workspace: delta_rule_backward_workspace_size()
+ * bytes.  Errors as above. */
+size_t delta_rule_backward_workspace_size(int B, int H, int T, int d_k, int d_v, int dtype);
+int delta_rule_backward(const void *q, const void *k, const void *v, const float *beta,
+                        int dtype, int B, int H, int T, int d_k, int d_v, const float *S0,
+                        const void *dy, const float *dS_T, void *dq, void *dk, void *dv,
+                        float *dbeta, float *dS0, void *workspace, size_t workspace_bytes,
+                        void *stream);
+
 /* One DeltaNet decode step for a batch of independent sequences (molayo1419.me,
  * "DeltaNet-family linear attention variants", section "DeltaNet: write the
  * prediction error instead of the value"): for every sequence b and head h,
@@ -258,6 +303,31 @@ int sparse_linattn_forward(const float *q, const float *k, const float *v,
                            int B, int H, int T, int N, int d_v,
                            const float *S0, float *S_out, float *y,
                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* The same BDH-style attention with the wide keys and queries generated on
+ * the GPU (the BDH post: the sparse non-negative activations come from a
+ * low-rank factorisation followed by ReLU thresholding):
+ *   k_t = max(0, xk_t U_h - theta),   q_t = max(0, xq_t U_h - theta),
+ * one U_h per head shared by queries and keys.  Each tile of x U_h is a
+ * tensor-core product (bf16 operands, float32 accumulation) whose epilogue
+ * keeps only the entries above theta as the row's support list, so the dense
+ * N-wide q and k never exist in memory; the attention itself is then the
+ * same float32 computation as sparse_linattn_forward.
+ *   xq, xk [B][H][T][R] bf16 (the R-dimensional token inputs)
+ *   U      [H][R][N] bf16
+ *   theta  threshold (finite; about 1.645 gives 5% density for unit-variance
+ *          x U_h entries)
+ *   v, S0, S_out, y  as sparse_linattn_forward (float32)
+ * Supported: R in {64, 128, 256}, N a multiple of 128 up to 49152, d_v in
+ * {32, 64, 128, 256}.  Workspace:
+ * sparse_linattn_keygen_forward_workspace_size() bytes.  Errors as above;
+ * a bounded wait of the key-generation kernel that runs out is reported by
+ * opam_check_device_error. */
+size_t sparse_linattn_keygen_forward_workspace_size(int B, int H, int T, int R, int N, int d_v);
+int sparse_linattn_keygen_forward(const void *xq, const void *xk, const void *U, float theta,
+                                  const float *v, int B, int H, int T, int R, int N, int d_v,
+                                  const float *S0, float *S_out, float *y, void *workspace,
+                                  size_t workspace_bytes, void *stream);
 
 /* Message for the last non-OK status returned on the calling thread. */
 const char *opam_last_error(void);

@@ -28,10 +28,13 @@ STATUS_BYTES = 256  # OPAM_STATUS_BYTES in include/opam.h
 # Every symbol the C header declares (checked by the CPU test-suite).
 EXPORTS = (
     "tc_layer_forward_workspace_size", "tc_layer_forward", "tc_layer_forward_noalloc",
+    "tc_layer_backward_workspace_size", "tc_layer_backward",
+    "delta_rule_backward_workspace_size", "delta_rule_backward",
     "tc_window_forward_workspace_size", "tc_window_forward",
     "tc_decode_step_workspace_size", "tc_decode_step",
     "delta_rule_forward_workspace_size", "delta_rule_forward", "delta_decode_step",
     "sparse_linattn_forward_workspace_size", "sparse_linattn_forward",
+    "sparse_linattn_keygen_forward_workspace_size", "sparse_linattn_keygen_forward",
     "opam_last_error", "opam_profile_events", "opam_kernel_launches", "opam_check_device_error", "opam_fp32_fma_probe",
     "opam_selftest_bounded_wait",
 )
@@ -72,6 +75,16 @@ def lib() -> ctypes.CDLL:
         L.tc_layer_forward.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, f, vp, sp, vp, sz, vp]
         L.tc_layer_forward_noalloc.restype = i
         L.tc_layer_forward_noalloc.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, f, vp, sp, vp]
+        L.tc_layer_backward_workspace_size.restype = sz
+        L.tc_layer_backward_workspace_size.argtypes = [i, i, i, i, i, i, i]
+        L.tc_layer_backward.restype = i
+        L.tc_layer_backward.argtypes = [vp, vp, vp, i, i, i, i, i, i, i, vp, vp, vp, f, vp, vp, vp, vp, vp, vp,
+                                        vp, vp, sz, vp]
+        L.delta_rule_backward_workspace_size.restype = sz
+        L.delta_rule_backward_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.delta_rule_backward.restype = i
+        L.delta_rule_backward.argtypes = [vp, vp, vp, vp, i, i, i, i, i, i, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          sz, vp]
         L.tc_window_forward_workspace_size.restype = sz
         L.tc_window_forward_workspace_size.argtypes = [i, i, i, i, i, i, i]
         L.tc_window_forward.restype = i
@@ -90,6 +103,10 @@ def lib() -> ctypes.CDLL:
         L.sparse_linattn_forward_workspace_size.argtypes = [i, i, i, i, i]
         L.sparse_linattn_forward.restype = i
         L.sparse_linattn_forward.argtypes = [vp, vp, vp, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
+        L.sparse_linattn_keygen_forward_workspace_size.restype = sz
+        L.sparse_linattn_keygen_forward_workspace_size.argtypes = [i, i, i, i, i, i]
+        L.sparse_linattn_keygen_forward.restype = i
+        L.sparse_linattn_keygen_forward.argtypes = [vp, vp, vp, f, vp, i, i, i, i, i, i, vp, vp, vp, vp, sz, vp]
         L.opam_profile_events.restype = i
         L.opam_profile_events.argtypes = [vp, vp]
         L.opam_kernel_launches.restype = ctypes.c_uint64
@@ -318,6 +335,39 @@ def tc_layer_forward_noalloc(q, k, v, lam, eta, gate, W, out, softmax_scale=0.0,
     return out
 
 
+def tc_layer_backward_workspace_size(B, H, T, d_k, d_v, W, dtype) -> int:
+    return int(lib().tc_layer_backward_workspace_size(B, H, T, d_k, d_v, W, dtype_code(dtype)))
+
+
+def tc_layer_backward(q, k, v, lam, eta, gate, W, dy, softmax_scale=0.0, out=None, workspace=None,
+                      stream=None):
+    """Gradient of sum <dy, y> through tc_layer_forward.  Returns
+    (dq, dk, dv, dlam, deta, dgate); ``out`` may give those six tensors."""
+    fn = "tc_layer_backward"
+    _dev(q, k, v, lam, eta, gate, dy, workspace)
+    B, H, T, dk, dv = _check_tc_prefill(fn, q, k, v, lam, eta, gate, None, None, W)
+    _expect(fn, "dy", dy, (B, H, T, dv), q.dtype, q.device)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+               torch.empty(H, dtype=torch.float32, device=q.device), torch.empty(H, dtype=torch.float32, device=q.device),
+               torch.empty(H, dtype=torch.float32, device=q.device))
+    gq, gk, gv, glam, geta, ggate = out
+    _dev(*out)
+    _expect(fn, "dq", gq, (B, H, T, dk), q.dtype, q.device)
+    _expect(fn, "dk", gk, (B, H, T, dk), q.dtype, q.device)
+    _expect(fn, "dv", gv, (B, H, T, dv), q.dtype, q.device)
+    for name, t in (("dlambda", glam), ("deta", geta), ("dgate", ggate)):
+        _expect(fn, name, t, (H,), torch.float32, q.device)
+    ws = _workspace(tc_layer_backward_workspace_size(B, H, T, dk, dv, W, q.dtype), workspace, q.device)
+    s = _stream(stream)
+    _check(lib().tc_layer_backward(_ptr(q), _ptr(k), _ptr(v), dtype_code(q.dtype), B, H, T, dk, dv, int(W),
+                                   _ptr(lam), _ptr(eta), _ptr(gate), float(softmax_scale), _ptr(dy), _ptr(gq),
+                                   _ptr(gk), _ptr(gv), _ptr(glam), _ptr(geta), _ptr(ggate), _ptr(ws), ws.numel(),
+                                   s))
+    _remember(fn, ws, s)
+    return out
+
+
 def tc_window_forward_workspace_size(B, H, T, d_k, d_v, W, dtype) -> int:
     return int(lib().tc_window_forward_workspace_size(B, H, T, d_k, d_v, W, dtype_code(dtype)))
 
@@ -395,6 +445,46 @@ def delta_rule_forward(q, k, v, beta, chunk=0, S0=None, S_out=None, out=None, wo
     return y
 
 
+def delta_rule_backward_workspace_size(B, H, T, d_k, d_v, dtype) -> int:
+    return int(lib().delta_rule_backward_workspace_size(B, H, T, d_k, d_v, dtype_code(dtype)))
+
+
+def delta_rule_backward(q, k, v, beta, dy, S0=None, dS_T=None, want_dS0=False, out=None, workspace=None,
+                        stream=None):
+    """Gradient of sum <dy, o> (+ <dS_T, S_T>) through delta_rule_forward.
+    Returns (dq, dk, dv, dbeta, dS0 or None)."""
+    fn = "delta_rule_backward"
+    _dev(q, k, v, beta, dy, S0, dS_T, workspace)
+    _ndim(fn, "q", q, 4)
+    _ndim(fn, "v", v, 4)
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    dev, dt = q.device, q.dtype
+    _expect(fn, "k", k, (B, H, T, dk), dt, dev)
+    _expect(fn, "v", v, (B, H, T, dv), dt, dev)
+    _expect(fn, "beta", beta, (B, H, T), torch.float32, dev)
+    _expect(fn, "dy", dy, (B, H, T, dv), dt, dev)
+    _expect(fn, "S0", S0, (B, H, dk, dv), torch.float32, dev)
+    _expect(fn, "dS_T", dS_T, (B, H, dk, dv), torch.float32, dev)
+    if out is None:
+        out = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(beta),
+               torch.empty(B, H, dk, dv, dtype=torch.float32, device=dev) if want_dS0 else None)
+    gq, gk, gv, gb, gS0 = out
+    _dev(*out)
+    _expect(fn, "dq", gq, (B, H, T, dk), dt, dev)
+    _expect(fn, "dk", gk, (B, H, T, dk), dt, dev)
+    _expect(fn, "dv", gv, (B, H, T, dv), dt, dev)
+    _expect(fn, "dbeta", gb, (B, H, T), torch.float32, dev)
+    _expect(fn, "dS0", gS0, (B, H, dk, dv), torch.float32, dev)
+    ws = _workspace(delta_rule_backward_workspace_size(B, H, T, dk, dv, dt), workspace, dev)
+    s = _stream(stream)
+    _check(lib().delta_rule_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), dtype_code(dt), B, H, T, dk, dv,
+                                     _ptr(S0), _ptr(dy), _ptr(dS_T), _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gb),
+                                     _ptr(gS0), _ptr(ws), ws.numel(), s))
+    _remember(fn, ws, s)
+    return out
+
+
 def delta_decode_step(S, q, k, v, beta, out=None, stream=None):
     """One DeltaNet decode step; S [B,H,d_k,d_v] fp32 key-major (updated in
     place), q,k [B,H,d_k], v [B,H,d_v], beta [B,H] fp32; returns y [B,H,d_v]."""
@@ -442,4 +532,38 @@ def sparse_linattn_forward(q, k, v, S0=None, S_out=None, out=None, workspace=Non
     _check(lib().sparse_linattn_forward(_ptr(q), _ptr(k), _ptr(v), B, H, T, N, dv, _ptr(S0),
                                         _ptr(S_out), _ptr(y), _ptr(ws), ws.numel(), s))
     _remember("sparse_linattn_forward", ws, s)
+    return y
+
+
+def sparse_linattn_keygen_forward_workspace_size(B, H, T, R, N, d_v) -> int:
+    return int(lib().sparse_linattn_keygen_forward_workspace_size(B, H, T, R, N, d_v))
+
+
+def sparse_linattn_keygen_forward(xq, xk, U, theta, v, S0=None, S_out=None, out=None, workspace=None,
+                                  stream=None):
+    """BDH-style attention with q = ReLU(xq U_h - theta), k = ReLU(xk U_h - theta)
+    generated on the GPU: xq, xk [B,H,T,R] bf16, U [H,R,N] bf16, v [B,H,T,d_v]
+    fp32; returns y [B,H,T,d_v] fp32."""
+    fn = "sparse_linattn_keygen_forward"
+    _dev(xq, xk, U, v, S0, S_out, out, workspace)
+    _ndim(fn, "xq", xq, 4)
+    _ndim(fn, "U", U, 3)
+    _ndim(fn, "v", v, 4)
+    B, H, T, R = xq.shape
+    N = U.shape[-1]
+    dv = v.shape[-1]
+    dev, f32, bf = xq.device, torch.float32, torch.bfloat16
+    _expect(fn, "xq", xq, (B, H, T, R), bf, dev)
+    _expect(fn, "xk", xk, (B, H, T, R), bf, dev)
+    _expect(fn, "U", U, (H, R, N), bf, dev)
+    _expect(fn, "v", v, (B, H, T, dv), f32, dev)
+    _expect(fn, "S0", S0, (B, H, N, dv), f32, dev)
+    _expect(fn, "S_out", S_out, (B, H, N, dv), f32, dev)
+    _expect(fn, "out", out, (B, H, T, dv), f32, dev)
+    y = torch.empty(B, H, T, dv, dtype=f32, device=dev) if out is None else out
+    ws = _workspace(sparse_linattn_keygen_forward_workspace_size(B, H, T, R, N, dv), workspace, dev)
+    s = _stream(stream)
+    _check(lib().sparse_linattn_keygen_forward(_ptr(xq), _ptr(xk), _ptr(U), float(theta), _ptr(v), B, H, T, R, N,
+                                               dv, _ptr(S0), _ptr(S_out), _ptr(y), _ptr(ws), ws.numel(), s))
+    _remember(fn, ws, s)
     return y

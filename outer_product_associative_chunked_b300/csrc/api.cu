@@ -154,6 +154,7 @@ const char *status_names(unsigned int bits) {
         const char *name;
     } parts[] = {{0x7Fu * kStatusTcPrefill, "Tensor Cache prefill "},
                  {0x1Fu * kStatusDelta, "DeltaNet tensor-core "},
+                 {0x7u * kStatusKeygen, "BDH key generation "},
                  {kStatusSelfTest, "bounded-wait self-test "}};
     for (const auto &p : parts)
         if (bits & p.mask) strncat(buf, p.name, sizeof buf - strlen(buf) - 1);
@@ -296,6 +297,43 @@ int tc_window_forward(const void *q, const void *k, const void *v, int dtype, in
                            nullptr, s, false);
 }
 
+size_t tc_layer_backward_workspace_size(int B, int H, int T, int d_k, int d_v, int W, int dtype) {
+    if (check_tc_dims("tc_layer_backward_workspace_size", dtype, B, H, T, d_k, d_v, W) != OPAM_OK) return 0;
+    return OPAM_STATUS_BYTES + tc_backward_workspace(B * H, T, d_k, d_v);
+}
+
+int tc_layer_backward(const void *q, const void *k, const void *v, int dtype, int B, int H, int T, int d_k,
+                      int d_v, int W, const float *lambda, const float *eta, const float *gate,
+                      float softmax_scale, const void *dy, void *dq, void *dk, void *dv, float *dlambda,
+                      float *deta, float *dgate, void *workspace, size_t workspace_bytes, void *stream) {
+    const char *fn = "tc_layer_backward";
+    if (int rc = check_tc_dims(fn, dtype, B, H, T, d_k, d_v, W)) return rc;
+    OPAM_CHECK_PTR(q);
+    OPAM_CHECK_PTR(k);
+    OPAM_CHECK_PTR(v);
+    OPAM_CHECK_PTR(lambda);
+    OPAM_CHECK_PTR(eta);
+    OPAM_CHECK_PTR(gate);
+    OPAM_CHECK_PTR(dy);
+    OPAM_CHECK_PTR(dq);
+    OPAM_CHECK_PTR(dk);
+    OPAM_CHECK_PTR(dv);
+    OPAM_CHECK_PTR(dlambda);
+    OPAM_CHECK_PTR(deta);
+    OPAM_CHECK_PTR(dgate);
+    const size_t need = OPAM_STATUS_BYTES + tc_backward_workspace(B * H, T, d_k, d_v);
+    if (!workspace || workspace_bytes < need) {
+        set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
+        return OPAM_ERR_WORKSPACE;
+    }
+    OPAM_CHECK_PTR(workspace);
+    // No kernel of the backward waits on a barrier; its last kernel zeroes
+    // the status words.
+    return tc_backward(q, k, v, dtype, B, H, T, d_k, d_v, W, lambda, eta, gate,
+                       resolve_scale(softmax_scale, d_k), dy, dq, dk, dv, dlambda, deta, dgate,
+                       status_body(workspace), status_word(workspace), (cudaStream_t)stream);
+}
+
 size_t tc_decode_step_workspace_size(const opam_tc_state *st) {
     if (!st) return 0;
     if (check_tc_dims("tc_decode_step_workspace_size", st->dtype, st->B, st->H, 1, st->d_k, st->d_v,
@@ -379,6 +417,39 @@ int delta_rule_forward(const void *q, const void *k, const void *v, const float 
     return delta_simt(q, k, v, beta, dtype, B, H, T, d_k, d_v, C, S0, S_out, y, status_body(workspace), s);
 }
 
+size_t delta_rule_backward_workspace_size(int B, int H, int T, int d_k, int d_v, int dtype) {
+    if (check_tc_dims("delta_rule_backward_workspace_size", dtype, B, H, T, d_k, d_v, 1) != OPAM_OK) return 0;
+    return OPAM_STATUS_BYTES + delta_backward_workspace(B * H, T, d_v);
+}
+
+int delta_rule_backward(const void *q, const void *k, const void *v, const float *beta, int dtype, int B, int H,
+                        int T, int d_k, int d_v, const float *S0, const void *dy, const float *dS_T, void *dq,
+                        void *dk, void *dv, float *dbeta, float *dS0, void *workspace, size_t workspace_bytes,
+                        void *stream) {
+    const char *fn = "delta_rule_backward";
+    if (int rc = check_tc_dims(fn, dtype, B, H, T, d_k, d_v, 1)) return rc;
+    OPAM_CHECK_PTR(q);
+    OPAM_CHECK_PTR(k);
+    OPAM_CHECK_PTR(v);
+    OPAM_CHECK_PTR(beta);
+    OPAM_CHECK_PTR(dy);
+    OPAM_CHECK_PTR(dq);
+    OPAM_CHECK_PTR(dk);
+    OPAM_CHECK_PTR(dv);
+    OPAM_CHECK_PTR(dbeta);
+    OPAM_CHECK_OPT_PTR(S0);
+    OPAM_CHECK_OPT_PTR(dS_T);
+    OPAM_CHECK_OPT_PTR(dS0);
+    const size_t need = OPAM_STATUS_BYTES + delta_backward_workspace(B * H, T, d_v);
+    if (!workspace || workspace_bytes < need) {
+        set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
+        return OPAM_ERR_WORKSPACE;
+    }
+    OPAM_CHECK_PTR(workspace);
+    return delta_backward(q, k, v, beta, dtype, B, H, T, d_k, d_v, S0, dy, dS_T, dq, dk, dv, dbeta, dS0,
+                          status_body(workspace), status_word(workspace), (cudaStream_t)stream);
+}
+
 int delta_decode_step(float *S, const void *q, const void *k, const void *v, const float *beta,
                       int dtype, int B, int H, int d_k, int d_v, void *y, void *stream) {
     const char *fn = "delta_decode_step";
@@ -431,6 +502,52 @@ int sparse_linattn_forward(const float *q, const float *k, const float *v, int B
     cudaStream_t s = (cudaStream_t)stream;
     if (int rc = clear_status(workspace, s)) return rc;
     return sparse_forward(q, k, v, B, H, T, N, d_v, S0, S_out, y, status_body(workspace), s);
+}
+
+size_t sparse_linattn_keygen_forward_workspace_size(int B, int H, int T, int R, int N, int d_v) {
+    if (!bdh_keygen_supported(R, N)) return 0;
+    return sparse_linattn_forward_workspace_size(B, H, T, N, d_v);
+}
+
+int sparse_linattn_keygen_forward(const void *xq, const void *xk, const void *U, float theta, const float *v,
+                                  int B, int H, int T, int R, int N, int d_v, const float *S0, float *S_out,
+                                  float *y, void *workspace, size_t workspace_bytes, void *stream) {
+    const char *fn = "sparse_linattn_keygen_forward";
+    if (B < 1 || H < 1 || T < 1 || R < 1 || N < 1) {
+        set_error("%s: extents must be positive (B=%d H=%d T=%d R=%d N=%d)", fn, B, H, T, R, N);
+        return OPAM_ERR_INVALID_ARG;
+    }
+    if (!bdh_keygen_supported(R, N) || N > kSparseMaxN ||
+        (d_v != 32 && d_v != 64 && d_v != 128 && d_v != 256)) {
+        set_error("%s: R=%d (64/128/256), N=%d (a multiple of 128, at most %d) or d_v=%d (32/64/128/256) "
+                  "unsupported", fn, R, N, kSparseMaxN, d_v);
+        return OPAM_ERR_UNSUPPORTED;
+    }
+    if ((long long)B * H > kMaxGridY) {
+        set_error("%s: B*H above %d", fn, kMaxGridY);
+        return OPAM_ERR_UNSUPPORTED;
+    }
+    if (!std::isfinite(theta)) {
+        set_error("%s: theta is not finite", fn);
+        return OPAM_ERR_INVALID_ARG;
+    }
+    OPAM_CHECK_PTR(xq);
+    OPAM_CHECK_PTR(xk);
+    OPAM_CHECK_PTR(U);
+    OPAM_CHECK_PTR(v);
+    OPAM_CHECK_PTR(y);
+    OPAM_CHECK_OPT_PTR(S0);
+    OPAM_CHECK_OPT_PTR(S_out);
+    const size_t need = OPAM_STATUS_BYTES + sparse_workspace(B * H, T, N, d_v, S_out == nullptr);
+    if (!workspace || workspace_bytes < need) {
+        set_error("%s: workspace %zu bytes, %zu required", fn, workspace_bytes, need);
+        return OPAM_ERR_WORKSPACE;
+    }
+    OPAM_CHECK_PTR(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (int rc = clear_status(workspace, s)) return rc;
+    return sparse_keygen_forward(xq, xk, U, theta, v, B, H, T, R, N, d_v, S0, S_out, y, status_body(workspace),
+                                 status_word(workspace), s);
 }
 
 }  // extern "C"

@@ -1,0 +1,214 @@
+// BDH key generation fused with support compaction (tcgen05 + TMA).
+//
+// ainews.random.gg, BDH memory-architecture post: the wide, sparse,
+// non-negative activations of queries and keys come from a low-rank
+// factorisation followed by ReLU thresholding.  For one head h and a token's
+// R-dimensional input x,
+//     a[n] = max(0, sum_r x[r] U_h[r][n] - theta),   n < N,
+// with one U_h shared by queries and keys.  This kernel computes a tile of
+// x U_h on the tensor cores and, in the epilogue, keeps only the entries
+// above theta as the row's ascending (index, value) support list -- the
+// input format of the sparse attention kernels -- so the dense N-wide rows
+// are never written to or read from memory.
+//
+// One CTA per (128 tokens, batch x head, queries or keys), 192 threads:
+//   warp 4 (lane 0)  TMA: the 128 x R x tile once, then U_h in column tiles of
+//                    kNT = 128 (R x 128, MN-major, double-buffered);
+//   warp 5 (lane 0)  tcgen05.mma M = 128, N = 128, K = R into one of two TMEM
+//                    accumulators (256 columns), so the epilogue of tile i
+//                    overlaps the MMAs of tile i + 1;
+//   warps 0-3        epilogue, one token row per thread (its TMEM lane):
+//                    a = acc - theta; if a > 0 append (n, a) to the row list.
+// Operands are bf16 with fp32 accumulation; x rows past T read as zero and
+// are not written.  Every wait is bounded; a wait that runs out sets a bit in
+// the call's status word and the CTA winds down.
+#include "opam_internal.cuh"
+#include "sm100.cuh"
+
+namespace opam {
+
+using namespace sm100;
+
+namespace {
+
+constexpr int kM = 128;   // token rows per CTA
+constexpr int kNT = 128;  // columns of U_h per tile
+
+enum : unsigned int {
+    kStKgProducer = kStatusKeygen << 0,
+    kStKgMma = kStatusKeygen << 1,
+    kStKgEpi = kStatusKeygen << 2,
+};
+
+template <int R>
+struct KgCfg {
+    static constexpr uint32_t ABYTES = kM * R * 2;      // x tile, R/64 K-major blocks of 16 KB
+    static constexpr uint32_t BBYTES = R * kNT * 2;     // U tile, two MN-major blocks of R x 64
+    static constexpr uint32_t OFF_B = ABYTES;
+    static constexpr uint32_t SMEM = ABYTES + 2 * BBYTES + 1024;  // + alignment slack
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+struct KgBars {
+    uint64_t a_full, b_full[2], b_empty[2], acc_full[2], acc_empty[2], drain;
+    uint32_t tbase;
+};
+
+template <int R>
+__global__ void __launch_bounds__(192, 1)
+bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant__ CUtensorMap mxq,
+                  const __grid_constant__ CUtensorMap mu, int T, int H, int N, float theta,
+                  int *__restrict__ kidx, float *__restrict__ kval, int *__restrict__ kcnt,
+                  int *__restrict__ qidx, float *__restrict__ qval, int *__restrict__ qcnt,
+                  unsigned int *__restrict__ status) {
+    using C = KgCfg<R>;
+    extern __shared__ unsigned char smraw[];
+    unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
+    __shared__ KgBars B;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int blk = blockIdx.x, bh = blockIdx.y, h = bh % H;
+    const bool is_q = blockIdx.z == 1;
+    const CUtensorMap *mx = is_q ? &mxq : &mxk;
+    const int ntile = N / kNT;
+    if (warp == 5) tmem_alloc(&B.tbase, 256);
+    if (tid == 0) {
+        mbar_init(&B.a_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&B.b_full[s], 1);
+            mbar_init(&B.b_empty[s], 1);
+            mbar_init(&B.acc_full[s], 1);
+            mbar_init(&B.acc_empty[s], 4);
+        }
+        mbar_init(&B.drain, 1);
+        mbar_fence_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = B.tbase;
+    const uint32_t sA = smem_u32(sm), sB = sA + C::OFF_B;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            bool ok = true;
+            mbar_expect_tx(&B.a_full, C::ABYTES);
+#pragma unroll
+            for (int b = 0; b < R / 64; ++b) tma_load_3d(sm + b * 16384, mx, &B.a_full, 64 * b, blk * kM, bh);
+            int issued = 0;
+            for (int i = 0; i < ntile && ok; ++i) {
+                const int s = i & 1;
+                if (i >= 2) ok = mbar_wait(&B.b_empty[s], ((i >> 1) - 1) & 1);
+                if (!ok) break;
+                unsigned char *dst = sm + C::OFF_B + s * C::BBYTES;
+                mbar_expect_tx(&B.b_full[s], C::BBYTES);
+                tma_load_3d(dst, &mu, &B.b_full[s], i * kNT, 0, h);
+                tma_load_3d(dst + C::BBYTES / 2, &mu, &B.b_full[s], i * kNT + 64, 0, h);
+                ++issued;
+            }
+            if (!ok) atomicOr(status, kStKgProducer);
+            // wait for this thread's copies still in flight before the CTA exits
+            bool dok = mbar_wait(&B.a_full, 0);
+            for (int i = max(0, issued - 2); i < issued && dok; ++i) dok = mbar_wait(&B.b_full[i & 1], (i >> 1) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16_f32(kM, kNT, false, true);
+            constexpr uint32_t HI = sdesc_hi(1024);
+            const uint32_t a_lo = sdesc_lo(sA, 16);
+            // K-major x: 16 k per step, four steps per 64-column block of 16 KB
+            auto aofs = [](int k) { return (uint32_t)((k >> 2) * (16384 >> 4) + (k & 3) * 2); };
+            bool ok = mbar_wait(&B.a_full, 0);
+            for (int i = 0; i < ntile && ok; ++i) {
+                const int s = i & 1;
+                ok = mbar_wait(&B.b_full[s], (i >> 1) & 1);
+                if (ok && i >= 2) ok = mbar_wait(&B.acc_empty[s], ((i >> 1) - 1) & 1);
+                if (!ok) break;
+                tc_fence_after();
+                // MN-major U: 16 contraction rows (2048 B) per step; the two
+                // 64-column blocks are R rows x 128 B apart
+                const uint32_t b_lo = sdesc_lo(sB + s * C::BBYTES, R * 128);
+#pragma unroll
+                for (int k = 0; k < R / 16; ++k)
+                    mma_ss_h(tm + s * kNT, a_lo + aofs(k), HI, b_lo + k * (2048 >> 4), HI, idesc, k > 0 ? 1u : 0u);
+                mma_commit(&B.acc_full[s]);
+                mma_commit(&B.b_empty[s]);
+            }
+            if (!ok) atomicOr(status, kStKgMma);
+            mma_commit(&B.drain);
+            mbar_wait(&B.drain, 0);
+        }
+        __syncwarp();
+    } else {
+        // epilogue: thread = token row (TMEM lane)
+        const int r = tid, t = blk * kM + r;
+        const bool live = t < T;
+        const size_t row = (size_t)bh * T + t;
+        int *oi = (is_q ? qidx : kidx) + row * (size_t)N;
+        float *ov = (is_q ? qval : kval) + row * (size_t)N;
+        const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+        int cnt = 0;
+        bool ok = true;
+        for (int i = 0; i < ntile && ok; ++i) {
+            const int s = i & 1;
+            ok = __all_sync(0xffffffffu, mbar_wait(&B.acc_full[s], (i >> 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            float a[kNT];
+#pragma unroll
+            for (int c = 0; c < kNT / 32; ++c)
+                tmem_ld32(tm + lrow + s * kNT + 32 * c, *reinterpret_cast<float(*)[32]>(a + 32 * c));
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.acc_empty[s]);
+            if (live) {
+                const int n0 = i * kNT;
+#pragma unroll
+                for (int c = 0; c < kNT; ++c) {
+                    const float x = a[c] - theta;
+                    if (x > 0.f) {
+                        oi[cnt] = n0 + c;
+                        ov[cnt] = x;
+                        ++cnt;
+                    }
+                }
+            }
+        }
+        if (!ok && lane == 0) atomicOr(status, kStKgEpi);
+        if (live) (is_q ? qcnt : kcnt)[row] = cnt;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) tmem_dealloc(tm, 256);
+}
+
+}  // namespace
+
+bool bdh_keygen_supported(int R, int N) { return (R == 64 || R == 128 || R == 256) && N % kNT == 0; }
+
+int bdh_keygen(const void *xq, const void *xk, const void *U, float theta, int B, int H, int T, int R, int N,
+               int *kidx, float *kval, int *kcnt, int *qidx, float *qval, int *qcnt, unsigned int *status,
+               cudaStream_t s) {
+    const int BH = B * H;
+    CUtensorMap mxk, mxq, mu;
+    int rc;
+    if ((rc = make_tmap_bf16_3d(&mxk, xk, R, T, BH, kM))) return rc;
+    if ((rc = make_tmap_bf16_3d(&mxq, xq, R, T, BH, kM))) return rc;
+    if ((rc = make_tmap_bf16_3d(&mu, U, N, R, H, R))) return rc;
+    const dim3 grid(ceil_div(T, kM), BH, 2);
+    auto go = [&](auto kern, uint32_t smem) -> int {
+        if (int rc_ = set_smem_limit((const void *)kern, (int)smem, "bdh_keygen smem attribute")) return rc_;
+        kern<<<grid, 192, smem, s>>>(mxk, mxq, mu, T, H, N, theta, kidx, kval, kcnt, qidx, qval, qcnt, status);
+        return launched("bdh_keygen");
+    };
+    switch (R) {
+        case 64: return go(bdh_keygen_kernel<64>, KgCfg<64>::SMEM);
+        case 128: return go(bdh_keygen_kernel<128>, KgCfg<128>::SMEM);
+        case 256: return go(bdh_keygen_kernel<256>, KgCfg<256>::SMEM);
+    }
+    set_error("BDH key generation: R=%d not in {64, 128, 256}", R);
+    return OPAM_ERR_UNSUPPORTED;
+}
+
+}  // namespace opam

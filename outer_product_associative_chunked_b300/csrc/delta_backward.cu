@@ -1,0 +1,226 @@
+// DeltaNet delta-rule backward (CUDA cores, fp32 state; bf16 or fp32 tokens).
+//
+// molayo1419.me, "DeltaNet-family linear attention variants", section
+// "DeltaNet: write the prediction error instead of the value": the forward
+// step is u_t = v_t - S_{t-1} k_t, S_t = S_{t-1} + beta_t u_t k_t^T,
+// o_t = S_t q_t (S is d_v x d_k).  Given do, the gradient of
+// sum_t <do_t, o_t> (+ <dS_T, S_T>) follows from undoing the steps in
+// reverse, with dS the gradient with respect to S_t:
+//   dq_t = S_t^T do_t;  dS += do_t q_t^T;  g = dS k_t;
+//   dv_t = beta_t g;  dbeta_t = <u_t, g>;
+//   dk_t = beta_t dS^T u_t - S_{t-1}^T (beta_t g);
+//   dS <- dS - beta_t g k_t^T.
+//
+// One CTA per (batch, head); its d_v/16 warps each own 16 rows of S and of
+// dS in registers, a lane holding d_k/32 columns of each row, so every row
+// update is lane-local and every column sum over the warp's rows is too.
+// Row sums over the columns (S k, dS k) go through a transposing warp
+// reduction: 31 shuffles leave the total of row (lane mod 16) in each lane.
+// Column sums over all d_v rows (dq, dk) and dbeta are combined across the
+// warps in shared memory, one barrier per token.
+//
+// Pass 1 runs the recurrence forward from S_0 and stores every u_t; pass 2
+// walks back from S_T, recovering S_{t-1} = S_t - beta_t u_t k_t^T exactly
+// from the stored u_t (no division; rounding adds up linearly over the
+// sequence), so no per-token state is kept.
+#include <math.h>
+
+#include "opam_internal.cuh"
+
+namespace opam {
+namespace {
+
+constexpr int kRows = 16;  // rows of S per warp
+
+// x[0..15] summed over the 32 lanes; returns the total of row (lane & 15).
+__device__ __forceinline__ float transpose_reduce16(float (&x)[kRows]) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < kRows; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], 16);
+#pragma unroll
+    for (int o = 8, n = 16; o >= 1; o >>= 1, n >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int j = 0; j < n / 2; ++j) {
+            const float send = up ? x[j] : x[j + n / 2];
+            const float keep = up ? x[j + n / 2] : x[j];
+            x[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+    return x[0];
+}
+
+template <typename T, int DK, int DV>
+__global__ void __launch_bounds__(DV / kRows * 32)
+delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                      const float *__restrict__ beta, const float *__restrict__ S0, const T *__restrict__ dy,
+                      const float *__restrict__ dST, int Tn, float *__restrict__ U, T *__restrict__ dq,
+                      T *__restrict__ dk, T *__restrict__ dv, float *__restrict__ dbeta, float *__restrict__ dS0,
+                      unsigned int *__restrict__ status) {
+    constexpr int CPL = DK / 32;          // columns per lane
+    constexpr int NW = DV / kRows;        // warps
+    __shared__ float red[2][NW][2 * DK + 1];
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, row = w * kRows + (lane & 15);
+    const int bh = blockIdx.x;
+    const size_t tk = (size_t)bh * Tn * DK, tv = (size_t)bh * Tn * DV;
+    float S[kRows][CPL], dS[kRows][CPL];
+    // S stored key-major: S_{i,j} at [j * DV + i]
+#pragma unroll
+    for (int i = 0; i < kRows; ++i)
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            const size_t at = (size_t)bh * DK * DV + (size_t)(lane + 32 * c) * DV + w * kRows + i;
+            S[i][c] = S0 ? S0[at] : 0.f;
+            dS[i][c] = dST ? dST[at] : 0.f;
+        }
+    // ---- pass 1: forward, storing u_t
+    for (int t = 0; t < Tn; ++t) {
+        float kc[CPL], x[kRows];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) kc[c] = Elem<T>::load(k + tk + (size_t)t * DK + lane + 32 * c);
+        const float bt = beta[(size_t)bh * Tn + t];
+        const float vr = Elem<T>::load(v + tv + (size_t)t * DV + row);
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            float s = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) s = fmaf(S[i][c], kc[c], s);
+            x[i] = s;
+        }
+        const float u = vr - transpose_reduce16(x);
+        if (lane < kRows) U[tv + (size_t)t * DV + row] = u;
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const float bu = bt * __shfl_sync(0xffffffffu, u, i);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) S[i][c] = fmaf(bu, kc[c], S[i][c]);
+        }
+    }
+    // ---- pass 2: reverse
+    for (int t = Tn - 1; t >= 0; --t) {
+        float qc[CPL], kc[CPL], x[kRows], dqp[CPL], dkp[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            qc[c] = Elem<T>::load(q + tk + (size_t)t * DK + lane + 32 * c);
+            kc[c] = Elem<T>::load(k + tk + (size_t)t * DK + lane + 32 * c);
+            dqp[c] = 0.f;
+            dkp[c] = 0.f;
+        }
+        const float bt = beta[(size_t)bh * Tn + t];
+        const float dor = Elem<T>::load(dy + tv + (size_t)t * DV + row);
+        const float ur = U[tv + (size_t)t * DV + row];
+        // dq = S_t^T do;  dS += do q^T;  g = dS k
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const float di = __shfl_sync(0xffffffffu, dor, i);
+            float s = 0.f;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                dqp[c] = fmaf(S[i][c], di, dqp[c]);
+                dS[i][c] = fmaf(di, qc[c], dS[i][c]);
+                s = fmaf(dS[i][c], kc[c], s);
+            }
+            x[i] = s;
+        }
+        const float g = transpose_reduce16(x);
+        const float du = bt * g;
+        if (lane < kRows) Elem<T>::store(dv + tv + (size_t)t * DV + row, du);
+        float db = lane < kRows ? ur * g : 0.f;
+        db = warp_sum(db);
+        // S <- S_{t-1};  dk = beta dS^T u - S_{t-1}^T du;  dS -= du k^T
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const float ui = __shfl_sync(0xffffffffu, ur, i);
+            const float dui = __shfl_sync(0xffffffffu, du, i);
+            const float bu = bt * ui;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) {
+                S[i][c] = fmaf(-bu, kc[c], S[i][c]);
+                dkp[c] = fmaf(bu, dS[i][c], fmaf(-dui, S[i][c], dkp[c]));
+                dS[i][c] = fmaf(-dui, kc[c], dS[i][c]);
+            }
+        }
+        float(*buf)[2 * DK + 1] = red[t & 1];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            buf[w][lane + 32 * c] = dqp[c];
+            buf[w][DK + lane + 32 * c] = dkp[c];
+        }
+        if (lane == 0) buf[w][2 * DK] = db;
+        __syncthreads();
+        for (int idx = tid; idx <= 2 * DK; idx += NW * 32) {
+            float s = 0.f;
+#pragma unroll
+            for (int ww = 0; ww < NW; ++ww) s += buf[ww][idx];
+            if (idx < DK)
+                Elem<T>::store(dq + tk + (size_t)t * DK + idx, s);
+            else if (idx < 2 * DK)
+                Elem<T>::store(dk + tk + (size_t)t * DK + idx - DK, s);
+            else
+                dbeta[(size_t)bh * Tn + t] = s;
+        }
+    }
+    if (dS0) {
+#pragma unroll
+        for (int i = 0; i < kRows; ++i)
+#pragma unroll
+            for (int c = 0; c < CPL; ++c)
+                dS0[(size_t)bh * DK * DV + (size_t)(lane + 32 * c) * DV + w * kRows + i] = dS[i][c];
+    }
+    // nothing here waits on a barrier: the call's status words only need zeroing
+    if (bh == 0 && tid < kStatusWords) status[tid] = 0u;
+}
+
+template <typename T, int DK, int DV>
+int launch(const void *q, const void *k, const void *v, const float *beta, const float *S0, const void *dy,
+           const float *dST, int BH, int Tn, void *dq, void *dk, void *dv, float *dbeta, float *dS0, void *ws,
+           unsigned int *status, cudaStream_t s) {
+    delta_backward_kernel<T, DK, DV><<<BH, DV / kRows * 32, 0, s>>>(
+        (const T *)q, (const T *)k, (const T *)v, beta, S0, (const T *)dy, dST, Tn, (float *)ws, (T *)dq,
+        (T *)dk, (T *)dv, dbeta, dS0, status);
+    return launched("delta_backward");
+}
+
+template <typename T, int DK>
+int by_dv(int dvv, const void *q, const void *k, const void *v, const float *beta, const float *S0,
+          const void *dy, const float *dST, int BH, int Tn, void *dq, void *dk, void *dv, float *dbeta,
+          float *dS0, void *ws, unsigned int *status, cudaStream_t s) {
+    switch (dvv) {
+        case 32: return launch<T, DK, 32>(q, k, v, beta, S0, dy, dST, BH, Tn, dq, dk, dv, dbeta, dS0, ws, status, s);
+        case 64: return launch<T, DK, 64>(q, k, v, beta, S0, dy, dST, BH, Tn, dq, dk, dv, dbeta, dS0, ws, status, s);
+        case 128: return launch<T, DK, 128>(q, k, v, beta, S0, dy, dST, BH, Tn, dq, dk, dv, dbeta, dS0, ws, status, s);
+    }
+    set_error("delta_rule_backward: d_v=%d unsupported", dvv);
+    return OPAM_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+size_t delta_backward_workspace(int BH, int T, int dv) { return align_up(sizeof(float) * (size_t)BH * T * dv, 256); }
+
+int delta_backward(const void *q, const void *k, const void *v, const float *beta, int dtype, int B, int H, int T,
+                   int dkk, int dvv, const float *S0, const void *dy, const float *dST, void *dq, void *dk,
+                   void *dv, float *dbeta, float *dS0, void *ws, unsigned int *status, cudaStream_t s) {
+    const int BH = B * H;
+    prof_begin(s);
+    int rc;
+    if (dtype == OPAM_BF16) {
+        switch (dkk) {
+            case 32: rc = by_dv<__nv_bfloat16, 32>(dvv, q, k, v, beta, S0, dy, dST, BH, T, dq, dk, dv, dbeta, dS0, ws, status, s); break;
+            case 64: rc = by_dv<__nv_bfloat16, 64>(dvv, q, k, v, beta, S0, dy, dST, BH, T, dq, dk, dv, dbeta, dS0, ws, status, s); break;
+            case 128: rc = by_dv<__nv_bfloat16, 128>(dvv, q, k, v, beta, S0, dy, dST, BH, T, dq, dk, dv, dbeta, dS0, ws, status, s); break;
+            default: set_error("delta_rule_backward: d_k=%d unsupported", dkk); return OPAM_ERR_UNSUPPORTED;
+        }
+    } else {
+        switch (dkk) {
+            case 32: rc = by_dv<float, 32>(dvv, q, k, v, beta, S0, dy, dST, BH, T, dq, dk, dv, dbeta, dS0, ws, status, s); break;
+            case 64: rc = by_dv<float, 64>(dvv, q, k, v, beta, S0, dy, dST, BH, T, dq, dk, dv, dbeta, dS0, ws, status, s); break;
+            case 128: rc = by_dv<float, 128>(dvv, q, k, v, beta, S0, dy, dST, BH, T, dq, dk, dv, dbeta, dS0, ws, status, s); break;
+            default: set_error("delta_rule_backward: d_k=%d unsupported", dkk); return OPAM_ERR_UNSUPPORTED;
+        }
+    }
+    prof_end(s);
+    return rc;
+}
+
+}  // namespace opam

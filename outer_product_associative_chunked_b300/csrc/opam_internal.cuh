@@ -68,6 +68,7 @@ __device__ __forceinline__ float warp_max(float x) {
 constexpr unsigned int kStatusTcPrefill = 1u << 0;   // 7 bits: Tensor Cache prefill kernels
 constexpr unsigned int kStatusDelta = 1u << 8;       // 5 bits: DeltaNet tensor-core kernels
 constexpr unsigned int kStatusSelfTest = 1u << 16;   // the bounded-wait self-test
+constexpr unsigned int kStatusKeygen = 1u << 20;     // 3 bits: BDH key generation
 constexpr int kStatusWords = 4;
 inline unsigned int *status_word(void *ws) { return (unsigned int *)ws; }
 inline void *status_body(void *ws) { return ws ? (char *)ws + OPAM_STATUS_BYTES : nullptr; }
@@ -107,6 +108,13 @@ int tc_prefill_tcgen05(const void *q, const void *k, const void *v, int B, int H
 // when it runs out).
 int bounded_wait_selftest(int arrive, long long limit, unsigned int *status, cudaStream_t s);
 
+// Tensor Cache layer backward (CUDA cores; bf16 or fp32 inputs).
+size_t tc_backward_workspace(int BH, int T, int dk, int dv);
+int tc_backward(const void *q, const void *k, const void *v, int dtype, int B, int H, int T, int dk, int dv, int W,
+                const float *lam, const float *eta, const float *gate, float scale, const void *dy, void *dq,
+                void *dkk, void *dvv, float *dlam, float *deta, float *dgate, void *ws, unsigned int *status,
+                cudaStream_t s);
+
 size_t tc_decode_workspace(int S, int H, int dk, int dv, int W);
 int tc_decode(const opam_tc_state *st, const void *q, const void *k, const void *v,
               const float *lam, const float *eta, const float *gate, float scale, void *y,
@@ -124,6 +132,12 @@ int delta_tcgen05(const void *q, const void *k, const void *v, const float *beta
                   int dk, const float *S0, float *S_out, void *y, void *ws, unsigned int *status,
                   cudaStream_t s);
 
+// DeltaNet backward (CUDA cores, per-token reverse recurrence).
+size_t delta_backward_workspace(int BH, int T, int dv);
+int delta_backward(const void *q, const void *k, const void *v, const float *beta, int dtype, int B, int H, int T,
+                   int dkk, int dvv, const float *S0, const void *dy, const float *dST, void *dq, void *dk,
+                   void *dv, float *dbeta, float *dS0, void *ws, unsigned int *status, cudaStream_t s);
+
 // DeltaNet single-token decode (state updated in place, no scratch).
 int delta_decode(float *S, const void *q, const void *k, const void *v, const float *beta, int dtype,
                  int B, int H, int dk, int dv, void *y, cudaStream_t s);
@@ -132,8 +146,19 @@ int delta_decode(float *S, const void *q, const void *k, const void *v, const fl
 double kChainsTotal(int blocks, int iters);
 int fp32_fma_probe(float *out, int blocks, int iters, cudaStream_t s);
 
+// BDH key generation fused with support compaction (bf16 x and U, fp32
+// accumulation): writes the per-row support lists of q and k.
+bool bdh_keygen_supported(int R, int N);
+int bdh_keygen(const void *xq, const void *xk, const void *U, float theta, int B, int H, int T, int R, int N,
+               int *kidx, float *kval, int *kcnt, int *qidx, float *qval, int *qcnt, unsigned int *status,
+               cudaStream_t s);
+
 size_t sparse_workspace(int BH, int T, int N, int dv, bool need_state);
 int sparse_forward(const float *q, const float *k, const float *v, int B, int H, int T, int N,
                    int dv, const float *S0, float *S_out, float *y, void *ws, cudaStream_t s);
+// The same attention with q and k generated on chip from x and U_h.
+int sparse_keygen_forward(const void *xq, const void *xk, const void *U, float theta, const float *v, int B,
+                          int H, int T, int R, int N, int dv, const float *S0, float *S_out, float *y, void *ws,
+                          unsigned int *status, cudaStream_t s);
 
 }  // namespace opam

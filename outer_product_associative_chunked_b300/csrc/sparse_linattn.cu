@@ -457,15 +457,10 @@ WsLayout carve(void *ws, int BH, int T, int N) {
     return l;
 }
 
+// Everything after the per-row supports are in the workspace.
 template <int DV>
-int launch(const float *q, const float *k, const float *v, int BH, int T, int N, const float *S0,
-           float *S_out, float *y, void *ws, cudaStream_t s) {
-    const WsLayout l = carve(ws, BH, T, N);
-    const int rows = BH * T;
-    compact_rows_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(k, rows, N, l.kidx, l.kval, l.kcnt);
-    if (int rc = launched("compact k")) return rc;
-    compact_rows_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(q, rows, N, l.qidx, l.qval, l.qcnt);
-    if (int rc = launched("compact q")) return rc;
+int attend(const WsLayout &l, const float *v, int BH, int T, int N, const float *S0, float *S_out, float *y,
+           cudaStream_t s) {
     cudaError_t e;
     if (S0 == nullptr && S_out == nullptr) {
         // pairwise form: coordinate lists per token block, then block pairs
@@ -517,7 +512,37 @@ int launch(const float *q, const float *k, const float *v, int BH, int T, int N,
     return OPAM_OK;
 }
 
+template <int DV>
+int launch(const float *q, const float *k, const float *v, int BH, int T, int N, const float *S0,
+           float *S_out, float *y, void *ws, cudaStream_t s) {
+    const WsLayout l = carve(ws, BH, T, N);
+    const int rows = BH * T;
+    compact_rows_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(k, rows, N, l.kidx, l.kval, l.kcnt);
+    if (int rc = launched("compact k")) return rc;
+    compact_rows_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(q, rows, N, l.qidx, l.qval, l.qcnt);
+    if (int rc = launched("compact q")) return rc;
+    return attend<DV>(l, v, BH, T, N, S0, S_out, y, s);
+}
+
 }  // namespace
+
+int sparse_keygen_forward(const void *xq, const void *xk, const void *U, float theta, const float *v, int B,
+                          int H, int T, int R, int N, int dv, const float *S0, float *S_out, float *y, void *ws,
+                          unsigned int *status, cudaStream_t s) {
+    const int BH = B * H;
+    const WsLayout l = carve(ws, BH, T, N);
+    if (int rc = bdh_keygen(xq, xk, U, theta, B, H, T, R, N, l.kidx, l.kval, l.kcnt, l.qidx, l.qval, l.qcnt,
+                            status, s))
+        return rc;
+    switch (dv) {
+        case 32: return attend<32>(l, v, BH, T, N, S0, S_out, y, s);
+        case 64: return attend<64>(l, v, BH, T, N, S0, S_out, y, s);
+        case 128: return attend<128>(l, v, BH, T, N, S0, S_out, y, s);
+        case 256: return attend<256>(l, v, BH, T, N, S0, S_out, y, s);
+    }
+    set_error("d_v=%d unsupported", dv);
+    return OPAM_ERR_UNSUPPORTED;
+}
 
 size_t sparse_workspace(int BH, int T, int N, int dv, bool need_state) {
     // the state (recurrent form, when kept in the workspace) and the
