@@ -98,6 +98,42 @@ def delta_decode_work(S, H, d_k, d_v, elem):
     return flops, bytes_
 
 
+def tc_backward_work(B, H, T, d_k, d_v, W, elem):
+    """Backward of the prefill: the window part recomputes S = QK^T and the
+    statistics (2 d_k per pair), y_loc (2 d_v), then dP = dy V^T (2 d_v),
+    dQ, dK (2 d_k each) and dV (2 d_v) per (query, key) pair in the window;
+    the L2 part is four d_k x d_v contractions per evicted token (dq, dk',
+    dv', and the state write it replays), plus the same for the lambda
+    derivative.  Bytes: q, k, v, dy read once; dq, dk, dv written once."""
+    BH = B * H
+    pairs = tc_pairs(T, W) * BH
+    flops = pairs * (2 * d_k + 2 * d_v + 2 * d_v + 2 * d_k + 2 * d_k + 2 * d_v)
+    flops += 10 * d_k * d_v * max(0, T - W) * BH
+    bytes_ = BH * T * (3 * d_k + 3 * d_v) * elem + BH * T * 0
+    return flops, bytes_
+
+
+def delta_backward_work(B, H, T, d_k, d_v, elem):
+    """Per token-head: the forward replay (S k and the rank-1 write, 4 d_k d_v)
+    and the reverse step (S^T do, dS update, dS k, the state reversal, dk and
+    the dS write-back: 12 d_k d_v).  Bytes: q, k, v, dy read, dq, dk, dv
+    written, beta and dbeta (fp32)."""
+    BH = B * H
+    flops = BH * T * 16 * d_k * d_v
+    bytes_ = BH * T * ((3 * d_k + 3 * d_v) * elem + 8)
+    return flops, bytes_
+
+
+def sparse_keygen_work(B, H, T, R, N, d_v, density):
+    """Key generation (2 R N flops per token-head for q and for k, on the
+    tensor cores) plus the sparse attention; bytes: x (bf16) for q and k, U
+    once per head (bf16), v read and y written (fp32)."""
+    BH = B * H
+    flops = BH * T * (4 * R * N + 4 * density * N * d_v)
+    bytes_ = BH * T * (2 * R * 2 + 2 * d_v * 4) + H * R * N * 2
+    return flops, bytes_
+
+
 def sparse_work(B, H, T, N, d_v, density):
     """Sparse write + read: 4 nnz d_v flops per token; dense q, k, v read, y written."""
     BH = B * H
@@ -581,6 +617,60 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
     summarize(dname, S, ms, fl, by, "sustained", "delta_decode", dom)
     out[dname]["note"] = "value = decoded tokens/s (256 sequences x 1 token per step, averaged over 64 steps)"
     del dq, dk_, dv_, db, Sd, yd, dec
+
+    # Backward of the headline prefill (fp32 arithmetic on the CUDA cores).
+    name = "tc_backward_bf16_B4_H8_T4096_d64_W512"
+    w, d, inp = tc_prefill_setup("tc_bf16_B4_H8_T4096_d64_W512", 0, torch, binding, synth)
+    q, k, v, lam, eta, gate = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate)]
+    dy = torch.randn(q.shape[:-1] + (d["d_v"],), generator=torch.Generator().manual_seed(9)).to(q.dtype).cuda()
+    outs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(lam),
+            torch.empty_like(eta), torch.empty_like(gate))
+    ws = torch.empty(binding.tc_layer_backward_workspace_size(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"],
+                                                              q.dtype), dtype=torch.uint8, device="cuda")
+    step = lambda: binding.tc_layer_backward(q, k, v, lam, eta, gate, d["W"], dy, out=outs, workspace=ws)  # noqa: E731
+    for _ in range(Wm):
+        step()
+    ms, dom = timed_steps(step, K, flush, torch, prof=True, binding=binding)
+    fl, by = tc_backward_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], 2)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "fp32", "tcb_window_dq .. tcb_finalize (all five)", dom)
+    out[name]["note"] = "value = tokens/s of the backward pass; fp32 arithmetic on the CUDA cores"
+    del q, k, v, dy, outs, ws
+
+    # Backward of the delta rule at the DeltaNet workload's shape.
+    name = "delta_backward_bf16_B8_H16_T8192_d128"
+    d = synth.WORKLOADS["delta_bf16_B8_H16_T8192_d128_C64"].dims
+    inp = synth.delta_inputs(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], dtype="bf16", seed=2)
+    q, k, v, beta = inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), inp.beta.cuda()
+    dy = torch.randn(v.shape, generator=torch.Generator().manual_seed(10)).to(v.dtype).cuda()
+    outs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(beta), None)
+    ws = torch.empty(binding.delta_rule_backward_workspace_size(d["B"], d["H"], d["T"], d["d_k"], d["d_v"],
+                                                                torch.bfloat16), dtype=torch.uint8, device="cuda")
+    step = lambda: binding.delta_rule_backward(q, k, v, beta, dy, out=outs, workspace=ws)  # noqa: E731
+    step()
+    ms, dom = timed_steps(step, max(1, K // 2), flush, torch, prof=True, binding=binding)
+    fl, by = delta_backward_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], 2)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "fp32", "delta_backward", dom)
+    out[name]["note"] = ("value = tokens/s of the backward pass; per-token reverse recurrence on the CUDA cores, "
+                         "one CTA per (batch, head)")
+    del q, k, v, beta, dy, outs, ws
+
+    # BDH attention with keys and queries generated on the GPU.
+    name = "bdh_keygen_B2_H4_T2048_R256_N16384_dv256"
+    d = synth.WORKLOADS[name].dims
+    kg = synth.sparse_keygen_inputs(d["B"], d["H"], d["T"], d["N"], d["d_v"], seed=synth.WORKLOADS[name].seed,
+                                    rank=d["R"])
+    xq, xk, U, v = kg.xq.cuda(), kg.xk.cuda(), kg.U.cuda(), kg.v.cuda()
+    y = torch.empty_like(v)
+    ws = torch.empty(binding.sparse_linattn_keygen_forward_workspace_size(d["B"], d["H"], d["T"], d["R"], d["N"],
+                                                                          d["d_v"]), dtype=torch.uint8, device="cuda")
+    step = lambda: binding.sparse_linattn_keygen_forward(xq, xk, U, kg.theta, v, out=y, workspace=ws)  # noqa: E731
+    for _ in range(Wm):
+        step()
+    ms, dom = timed_steps(step, K, flush, torch, prof=True, binding=binding)
+    fl, by = sparse_keygen_work(d["B"], d["H"], d["T"], d["R"], d["N"], d["d_v"], 0.05)
+    summarize(name, d["B"] * d["T"], ms, fl, by, "fp32", "pair_tile", dom)
+    out[name]["note"] = "keys and queries generated on chip (bf16 x U, fp32 accumulation); attention in fp32"
+    del xq, xk, U, v, y, ws
 
     name = "bdh_fp32_B2_H4_T2048_N16384_dv256"
     d = synth.WORKLOADS[name].dims

@@ -14,11 +14,20 @@
 // One CTA per (128 tokens, batch x head, queries or keys), 192 threads:
 //   warp 4 (lane 0)  TMA: the 128 x R x tile once, then U_h in column tiles of
 //                    kNT = 128 (R x 128, MN-major, double-buffered);
-//   warp 5 (lane 0)  tcgen05.mma M = 128, N = 128, K = R into one of two TMEM
-//                    accumulators (256 columns), so the epilogue of tile i
-//                    overlaps the MMAs of tile i + 1;
-//   warps 0-3        epilogue, one token row per thread (its TMEM lane):
-//                    a = acc - theta; if a > 0 append (n, a) to the row list.
+//   warp 5 (lane 0)  tcgen05.mma with K = R into one of two TMEM accumulators
+//                    (256 columns), so the epilogue of tile i overlaps the
+//                    MMAs of tile i + 1;
+//   warps 0-3        epilogue, one TMEM lane per thread.
+// Two output forms:
+//   row lists (ROWS): D = x U (M = tokens), thread = token row: a = acc -
+//     theta; if a > 0 append (n, a) to the row's list (the per-row format the
+//     recurrent attention reads);
+//   coordinate lists (!ROWS): D = U^T x^T (M = coordinates, the U tile as the
+//     MN-major A operand), thread = coordinate: it holds its 128 token values,
+//     so after a scan of the tile's counts over the 128 threads it writes its
+//     (token, value) entries in ascending token order -- the 128-token block's
+//     coordinate-major lists that the pairwise attention reads, with no
+//     per-row lists in between.
 // Operands are bf16 with fp32 accumulation; x rows past T read as zero and
 // are not written.  Every wait is bounded; a wait that runs out sets a bit in
 // the call's status word and the CTA winds down.
@@ -54,17 +63,36 @@ struct KgBars {
     uint32_t tbase;
 };
 
-template <int R>
+// Named barrier 1 over the four epilogue warps (128 threads); the second form
+// also returns whether `ok` holds in every one of them, so that all four
+// leave their loop together.
+__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool epi_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok)
+        : "memory");
+    return r != 0;
+}
+
+template <int R, bool ROWS>
 __global__ void __launch_bounds__(192, 1)
 bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant__ CUtensorMap mxq,
                   const __grid_constant__ CUtensorMap mu, int T, int H, int N, float theta,
                   int *__restrict__ kidx, float *__restrict__ kval, int *__restrict__ kcnt,
                   int *__restrict__ qidx, float *__restrict__ qval, int *__restrict__ qcnt,
+                  int *__restrict__ coff, uint8_t *__restrict__ ct, float *__restrict__ cv,
                   unsigned int *__restrict__ status) {
     using C = KgCfg<R>;
     extern __shared__ unsigned char smraw[];
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     __shared__ KgBars B;
+    __shared__ int wtot[2][4];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int blk = blockIdx.x, bh = blockIdx.y, h = bh % H;
     const bool is_q = blockIdx.z == 1;
@@ -113,11 +141,13 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
         __syncwarp();
     } else if (warp == 5) {
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(kM, kNT, false, true);
+            // ROWS: D = x U, A = x (K-major), B = U (MN-major);
+            // otherwise D = U^T x^T, A = U (MN-major), B = x (K-major).
+            constexpr uint32_t idesc = ROWS ? idesc_bf16_f32(kM, kNT, false, true) : idesc_bf16_f32(kNT, kM, true, false);
             constexpr uint32_t HI = sdesc_hi(1024);
-            const uint32_t a_lo = sdesc_lo(sA, 16);
+            const uint32_t x_lo = sdesc_lo(sA, 16);
             // K-major x: 16 k per step, four steps per 64-column block of 16 KB
-            auto aofs = [](int k) { return (uint32_t)((k >> 2) * (16384 >> 4) + (k & 3) * 2); };
+            auto xofs = [](int k) { return (uint32_t)((k >> 2) * (16384 >> 4) + (k & 3) * 2); };
             bool ok = mbar_wait(&B.a_full, 0);
             for (int i = 0; i < ntile && ok; ++i) {
                 const int s = i & 1;
@@ -127,10 +157,14 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
                 tc_fence_after();
                 // MN-major U: 16 contraction rows (2048 B) per step; the two
                 // 64-column blocks are R rows x 128 B apart
-                const uint32_t b_lo = sdesc_lo(sB + s * C::BBYTES, R * 128);
+                const uint32_t u_lo = sdesc_lo(sB + s * C::BBYTES, R * 128);
 #pragma unroll
-                for (int k = 0; k < R / 16; ++k)
-                    mma_ss_h(tm + s * kNT, a_lo + aofs(k), HI, b_lo + k * (2048 >> 4), HI, idesc, k > 0 ? 1u : 0u);
+                for (int k = 0; k < R / 16; ++k) {
+                    if constexpr (ROWS)
+                        mma_ss_h(tm + s * kNT, x_lo + xofs(k), HI, u_lo + k * (2048 >> 4), HI, idesc, k > 0 ? 1u : 0u);
+                    else
+                        mma_ss_h(tm + s * kNT, u_lo + k * (2048 >> 4), HI, x_lo + xofs(k), HI, idesc, k > 0 ? 1u : 0u);
+                }
                 mma_commit(&B.acc_full[s]);
                 mma_commit(&B.b_empty[s]);
             }
@@ -139,6 +173,57 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
             mbar_wait(&B.drain, 0);
         }
         __syncwarp();
+    } else if constexpr (!ROWS) {
+        // epilogue: thread = coordinate n0 + c (TMEM lane c), columns = tokens
+        const int c = tid;
+        const int nlive = min(kM, T - blk * kM);
+        const size_t cb = ((size_t)(is_q ? 1 : 0) * gridDim.y + bh) * gridDim.x + blk;  // block of the lists
+        int *off = coff + cb * (size_t)(N + 1);
+        uint8_t *et = ct + cb * (size_t)kM * N;
+        float *ev = cv + cb * (size_t)kM * N;
+        const uint32_t lrow = (uint32_t)(warp * 32) << 16;
+        int base = 0;
+        bool ok = true;
+        for (int i = 0; i < ntile && ok; ++i) {
+            const int s = i & 1;
+            ok = epi_all(mbar_wait(&B.acc_full[s], (i >> 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            float a[kM];
+#pragma unroll
+            for (int cc = 0; cc < kM / 32; ++cc)
+                tmem_ld32(tm + lrow + s * kNT + 32 * cc, *reinterpret_cast<float(*)[32]>(a + 32 * cc));
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.acc_empty[s]);
+            int n = 0;
+#pragma unroll
+            for (int t = 0; t < kM; ++t) n += (t < nlive && a[t] - theta > 0.f) ? 1 : 0;
+            int incl = n;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            if (lane == 31) wtot[s][warp] = incl;
+            epi_barrier();
+            int p = base + incl - n;
+            for (int w = 0; w < warp; ++w) p += wtot[s][w];
+            off[i * kNT + c] = p;
+#pragma unroll
+            for (int t = 0; t < kM; ++t) {
+                const float x = a[t] - theta;
+                if (t < nlive && x > 0.f) {
+                    et[p] = (uint8_t)t;
+                    ev[p] = x;
+                    ++p;
+                }
+            }
+            base += wtot[s][0] + wtot[s][1] + wtot[s][2] + wtot[s][3];
+        }
+        if (!ok && lane == 0) atomicOr(status, kStKgEpi);
+        if (ok && c == 0) off[N] = base;
     } else {
         // epilogue: thread = token row (TMEM lane)
         const int r = tid, t = blk * kM + r;
@@ -188,8 +273,9 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
 bool bdh_keygen_supported(int R, int N) { return (R == 64 || R == 128 || R == 256) && N % kNT == 0; }
 
 int bdh_keygen(const void *xq, const void *xk, const void *U, float theta, int B, int H, int T, int R, int N,
-               int *kidx, float *kval, int *kcnt, int *qidx, float *qval, int *qcnt, unsigned int *status,
-               cudaStream_t s) {
+               int *kidx, float *kval, int *kcnt, int *qidx, float *qval, int *qcnt, int *coff, uint8_t *ct,
+               float *cv, unsigned int *status, cudaStream_t s) {
+    const bool rows = coff == nullptr;
     const int BH = B * H;
     CUtensorMap mxk, mxq, mu;
     int rc;
@@ -199,13 +285,14 @@ int bdh_keygen(const void *xq, const void *xk, const void *U, float theta, int B
     const dim3 grid(ceil_div(T, kM), BH, 2);
     auto go = [&](auto kern, uint32_t smem) -> int {
         if (int rc_ = set_smem_limit((const void *)kern, (int)smem, "bdh_keygen smem attribute")) return rc_;
-        kern<<<grid, 192, smem, s>>>(mxk, mxq, mu, T, H, N, theta, kidx, kval, kcnt, qidx, qval, qcnt, status);
+        kern<<<grid, 192, smem, s>>>(mxk, mxq, mu, T, H, N, theta, kidx, kval, kcnt, qidx, qval, qcnt, coff, ct, cv,
+                                     status);
         return launched("bdh_keygen");
     };
     switch (R) {
-        case 64: return go(bdh_keygen_kernel<64>, KgCfg<64>::SMEM);
-        case 128: return go(bdh_keygen_kernel<128>, KgCfg<128>::SMEM);
-        case 256: return go(bdh_keygen_kernel<256>, KgCfg<256>::SMEM);
+        case 64: return rows ? go(bdh_keygen_kernel<64, true>, KgCfg<64>::SMEM) : go(bdh_keygen_kernel<64, false>, KgCfg<64>::SMEM);
+        case 128: return rows ? go(bdh_keygen_kernel<128, true>, KgCfg<128>::SMEM) : go(bdh_keygen_kernel<128, false>, KgCfg<128>::SMEM);
+        case 256: return rows ? go(bdh_keygen_kernel<256, true>, KgCfg<256>::SMEM) : go(bdh_keygen_kernel<256, false>, KgCfg<256>::SMEM);
     }
     set_error("BDH key generation: R=%d not in {64, 128, 256}", R);
     return OPAM_ERR_UNSUPPORTED;

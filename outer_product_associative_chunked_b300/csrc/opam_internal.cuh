@@ -149,9 +149,11 @@ int fp32_fma_probe(float *out, int blocks, int iters, cudaStream_t s);
 // BDH key generation fused with support compaction (bf16 x and U, fp32
 // accumulation): writes the per-row support lists of q and k.
 bool bdh_keygen_supported(int R, int N);
+// With coff == NULL it writes the per-row lists (recurrent form); otherwise
+// the coordinate-major lists of each 128-token block (pairwise form).
 int bdh_keygen(const void *xq, const void *xk, const void *U, float theta, int B, int H, int T, int R, int N,
-               int *kidx, float *kval, int *kcnt, int *qidx, float *qval, int *qcnt, unsigned int *status,
-               cudaStream_t s);
+               int *kidx, float *kval, int *kcnt, int *qidx, float *qval, int *qcnt, int *coff, uint8_t *ct,
+               float *cv, unsigned int *status, cudaStream_t s);
 
 size_t sparse_workspace(int BH, int T, int N, int dv, bool need_state);
 int sparse_forward(const float *q, const float *k, const float *v, int B, int H, int T, int N,

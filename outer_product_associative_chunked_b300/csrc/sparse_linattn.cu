@@ -283,27 +283,117 @@ csc_build_kernel(int T, int N, int nb, const int *__restrict__ kidx, const float
     }
 }
 
+// Pairwise form straight from the dense rows: one CTA per (token block,
+// head, q or k) reads the block's 128 rows once, in column tiles of 128, and
+// writes the coordinate-major lists of the block (the output of
+// csc_build_kernel) without per-row lists in between.  A tile goes through
+// shared memory ([128 rows][128 columns]); thread c scans column c over half
+// of the rows, a scan over the tile's 128 columns places the lists, and each
+// coordinate's entries come out in ascending token order.  The next tile's
+// loads are issued before the current tile is scanned.
+constexpr int kCT = 128;  // columns per tile
+
+__global__ void __launch_bounds__(256)
+dense_csc_kernel(const float *__restrict__ q, const float *__restrict__ k, int T, int N, int nb,
+                 int *__restrict__ coff, uint8_t *__restrict__ ct, float *__restrict__ cv) {
+    constexpr int LD = kCT + 4;  // padded row stride (float4-aligned)
+    extern __shared__ float tilef[];  // [kTB][LD]
+    __shared__ int cnt2[2][kCT];   // non-zeros of column c in the lower / upper 64 rows
+    __shared__ int start[kCT];     // first entry of column c
+    __shared__ int wtot[4];
+    const int b = blockIdx.x, bh = blockIdx.y, which = blockIdx.z;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float *x = which ? q : k;
+    const int t0 = b * kTB, nrows = min(kTB, T - t0);
+    const size_t blk = ((size_t)which * gridDim.y + bh) * nb + b;
+    int *off = coff + blk * (size_t)(N + 1);
+    uint8_t *et = ct + blk * (size_t)kTB * N;
+    float *ev = cv + blk * (size_t)kTB * N;
+    const float *src = x + ((size_t)bh * T + t0) * N;
+    // loads: warp w reads rows w, w + 8, ..; a lane reads one float4 of the row's tile segment
+    constexpr int RPW = kTB / 8;
+    float4 buf[RPW];
+    auto fetch = [&](int n0) {
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+            const int r = warp + 8 * i;
+            buf[i] = r < nrows ? ldg_stream4(reinterpret_cast<const float4 *>(src + (size_t)r * N + n0) + lane)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    const int c = tid & (kCT - 1), half = tid >> 7;
+    int base = 0;
+    fetch(0);
+    for (int n0 = 0; n0 < N; n0 += kCT) {
+        __syncthreads();  // the previous tile is no longer read
+#pragma unroll
+        for (int i = 0; i < RPW; ++i)
+            *reinterpret_cast<float4 *>(tilef + (warp + 8 * i) * LD + 4 * lane) = buf[i];
+        __syncthreads();
+        if (n0 + kCT < N) fetch(n0 + kCT);
+        // count column c over rows [64 half, 64 half + 64)
+        int n = 0;
+        for (int r = 64 * half; r < 64 * half + 64; ++r) n += tilef[r * LD + c] != 0.f;
+        cnt2[half][c] = n;
+        __syncthreads();
+        // exclusive scan of the column totals (threads 0..127 = warps 0..3)
+        int excl = 0;
+        if (half == 0) {
+            const int tot = cnt2[0][c] + cnt2[1][c];
+            int incl = tot;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += y;
+            }
+            if (lane == 31) wtot[warp] = incl;
+            excl = incl - tot;
+        }
+        __syncthreads();
+        if (half == 0) {
+            for (int w = 0; w < warp; ++w) excl += wtot[w];
+            off[n0 + c] = base + excl;
+            start[c] = base + excl;
+        }
+        __syncthreads();
+        int p = start[c] + (half ? cnt2[0][c] : 0);  // the upper rows follow the lower rows' entries
+        for (int r = 64 * half; r < 64 * half + 64; ++r) {
+            const float val = tilef[r * LD + c];
+            if (val != 0.f) {
+                et[p] = (uint8_t)r;
+                ev[p] = val;
+                ++p;
+            }
+        }
+        base += wtot[0] + wtot[1] + wtot[2] + wtot[3];
+    }
+    if (tid == 0) off[N] = base;
+}
+
 // One CTA per (pair of token blocks tb >= sb, head):
 //   Z[t][s] = sum_j q_t[j] k_s[j]  (s <= t on the diagonal block), accumulated
 //   in shared memory.  Coordinates are taken in windows of kJW: the window's
-//   list entries (contiguous in the coordinate-major arrays) are first copied
-//   to shared memory with coalesced loads, then each warp takes one
-//   coordinate at a time, its lanes an 8 x 4 grid over (query entry, key
-//   entry) pairs of that coordinate's lists.  A window whose
-//   lists do not fit the buffers (dense inputs) is read from global memory.
+//   list entries (contiguous in the coordinate-major arrays) are copied to
+//   shared memory with coalesced loads, each query entry tagged with its
+//   coordinate.  Then every thread takes query entries (t, q_t[j]) one after
+//   another and walks the key list of the same coordinate j, adding
+//   q_t[j] k_s[j] into Z[t][s]: with about six key entries per coordinate and
+//   block, a lane does a few products per entry and no lane waits for a
+//   coordinate's setup.  A window whose lists do not fit the buffers (dense
+//   inputs) is read from global memory, one coordinate per warp.
 //   Then o[tb] += Z V[sb]  (fp32, 64 output columns per pass, float4 atomics).
-constexpr int kJW = 64;    // coordinates per window
-constexpr int kCap = 768;  // list entries per window buffered in shared memory (3 CTAs per SM)
+constexpr int kJW = 256;    // coordinates per window
+constexpr int kCap = 2048;  // list entries per window buffered in shared memory
 
 struct PairSmem {
     float Z[kTB * (kTB + 1)];
     float qv[kCap], kv[kCap];
     int qo[kJW + 1], ko[kJW + 1];
-    uint8_t qt[kCap], kt[kCap];
+    uint8_t qt[kCap], kt[kCap], qj[kCap];
 };
 
 template <int DV>
-__global__ void __launch_bounds__(256, 3)
+__global__ void __launch_bounds__(256, 2)
 pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8_t *__restrict__ ct,
                  const float *__restrict__ cv, const float *__restrict__ v, float *__restrict__ y) {
     constexpr int ZS = kTB + 1;  // padded row stride of the Z tile
@@ -342,38 +432,40 @@ pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8
                 P.kt[i] = kt[kb + i];
                 P.kv[i] = kv[kb + i];
             }
-        }
-        __syncthreads();
-        // one coordinate per warp at a time; lane (a, b) = (lane / 4, lane % 4)
-        // takes query entry a0 + a and key entry b0 + b of its lists
-        auto pairs = [&](const uint8_t *Qt, const float *Qv, const uint8_t *Kt, const float *Kv, int q0, int nqj,
-                         int k0, int nkj) {
-            for (int a0 = 0; a0 < nqj; a0 += 8) {
-                const int a = a0 + (lane >> 2);
-                const bool qa = a < nqj;
-                const int t = qa ? Qt[q0 + a] : 0;
-                const float x = qa ? Qv[q0 + a] : 0.f;
+            for (int jl = tid; jl < nw; jl += 256)  // tag each query entry with its coordinate
+                for (int e = P.qo[jl] - qb; e < P.qo[jl + 1] - qb; ++e) P.qj[e] = (uint8_t)jl;
+            __syncthreads();
+            for (int e = tid; e < nq; e += 256) {
+                const int jl = P.qj[e], t = P.qt[e];
+                const float x = P.qv[e];
+                const int b0 = P.ko[jl] - kb, b1 = P.ko[jl + 1] - kb;
                 const int smax = diag ? t : kTB - 1;  // causal inside the diagonal block
-                for (int b0 = 0; b0 < nkj; b0 += 4) {
-                    const int b = b0 + (lane & 3);
-                    if (qa && b < nkj) {
-                        const int s = Kt[k0 + b];
-                        if (s <= smax) atomicAdd(Zs + t * ZS + s, x * Kv[k0 + b]);
-                    }
+                float *zrow = Zs + t * ZS;
+                for (int b = b0; b < b1; ++b) {
+                    const int s = P.kt[b];
+                    if (s <= smax) atomicAdd(zrow + s, x * P.kv[b]);
                 }
             }
-        };
-        if (fits) {
-            for (int jl = warp; jl < nw; jl += 8) {
-                const int q0 = P.qo[jl] - qb, k0 = P.ko[jl] - kb;
-                const int nqj = P.qo[jl + 1] - qb - q0, nkj = P.ko[jl + 1] - kb - k0;
-                if (nqj > 0 && nkj > 0) pairs(P.qt, P.qv, P.kt, P.kv, q0, nqj, k0, nkj);
-            }
         } else {
+            // one coordinate per warp; lane (a, b) = (lane / 4, lane % 4) takes
+            // query entry a0 + a and key entry b0 + b of the two lists
             for (int jl = warp; jl < nw; jl += 8) {
                 const int q0 = P.qo[jl], k0 = P.ko[jl];
                 const int nqj = P.qo[jl + 1] - q0, nkj = P.ko[jl + 1] - k0;
-                if (nqj > 0 && nkj > 0) pairs(qt, qv, kt, kv, q0, nqj, k0, nkj);
+                for (int a0 = 0; a0 < nqj; a0 += 8) {
+                    const int a = a0 + (lane >> 2);
+                    const bool qa = a < nqj;
+                    const int t = qa ? qt[q0 + a] : 0;
+                    const float x = qa ? qv[q0 + a] : 0.f;
+                    const int smax = diag ? t : kTB - 1;
+                    for (int b0 = 0; b0 < nkj; b0 += 4) {
+                        const int b = b0 + (lane & 3);
+                        if (qa && b < nkj) {
+                            const int s = kt[k0 + b];
+                            if (s <= smax) atomicAdd(Zs + t * ZS + s, x * kv[k0 + b]);
+                        }
+                    }
+                }
             }
         }
     }
@@ -457,6 +549,22 @@ WsLayout carve(void *ws, int BH, int T, int N) {
     return l;
 }
 
+// Block pairs over the coordinate lists of the workspace: y = sum of Z V.
+template <int DV>
+int pairs(const WsLayout &l, const float *v, int BH, int T, int N, float *y, cudaStream_t s) {
+    const int nb = ceil_div(T, kTB);
+    cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * (size_t)BH * T * DV, s);
+    if (e != cudaSuccess) return cuda_fail(e, "sparse output init");
+    const size_t psmem = sizeof(PairSmem);
+    if (int rc_ = set_smem_limit((const void *)pair_tile_kernel<DV>, (int)psmem, "pair_tile smem attribute"))
+        return rc_;
+    prof_begin(s);
+    pair_tile_kernel<DV><<<dim3(nb * (nb + 1) / 2, BH), 256, psmem, s>>>(T, N, nb, l.coff, l.ct, l.cv, v, y);
+    const int rc = launched("pair_tile");
+    prof_end(s);
+    return rc;
+}
+
 // Everything after the per-row supports are in the workspace.
 template <int DV>
 int attend(const WsLayout &l, const float *v, int BH, int T, int N, const float *S0, float *S_out, float *y,
@@ -471,16 +579,7 @@ int attend(const WsLayout &l, const float *v, int BH, int T, int N, const float 
         csc_build_kernel<<<dim3(nb, BH, 2), 512, csmem, s>>>(T, N, nb, l.kidx, l.kval, l.kcnt, l.qidx, l.qval,
                                                             l.qcnt, l.coff, l.ct, l.cv);
         if (int rc = launched("csc_build")) return rc;
-        e = cudaMemsetAsync(y, 0, sizeof(float) * (size_t)BH * T * DV, s);
-        if (e != cudaSuccess) return cuda_fail(e, "sparse output init");
-        const size_t psmem = sizeof(PairSmem);
-        if (int rc_ = set_smem_limit((const void *)pair_tile_kernel<DV>, (int)psmem, "pair_tile smem attribute"))
-            return rc_;
-        prof_begin(s);
-        pair_tile_kernel<DV><<<dim3(nb * (nb + 1) / 2, BH), 256, psmem, s>>>(T, N, nb, l.coff, l.ct, l.cv, v, y);
-        const int rc = launched("pair_tile");
-        prof_end(s);
-        return rc;
+        return pairs<DV>(l, v, BH, T, N, y, s);
     }
     // recurrent form: the state lives in S_out (or the workspace)
     float *ST = S_out ? S_out : l.ST;
@@ -517,6 +616,15 @@ int launch(const float *q, const float *k, const float *v, int BH, int T, int N,
            float *S_out, float *y, void *ws, cudaStream_t s) {
     const WsLayout l = carve(ws, BH, T, N);
     const int rows = BH * T;
+    if (S0 == nullptr && S_out == nullptr && N % kCT == 0) {
+        // pairwise form: coordinate lists straight from the dense rows
+        const int nb = ceil_div(T, kTB);
+        const int smem = (int)(sizeof(float) * kTB * (kCT + 4));
+        if (int rc_ = set_smem_limit((const void *)dense_csc_kernel, smem, "dense_csc smem attribute")) return rc_;
+        dense_csc_kernel<<<dim3(nb, BH, 2), 256, smem, s>>>(q, k, T, N, nb, l.coff, l.ct, l.cv);
+        if (int rc = launched("dense_csc")) return rc;
+        return pairs<DV>(l, v, BH, T, N, y, s);
+    }
     compact_rows_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(k, rows, N, l.kidx, l.kval, l.kcnt);
     if (int rc = launched("compact k")) return rc;
     compact_rows_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(q, rows, N, l.qidx, l.qval, l.qcnt);
@@ -531,9 +639,20 @@ int sparse_keygen_forward(const void *xq, const void *xk, const void *U, float t
                           unsigned int *status, cudaStream_t s) {
     const int BH = B * H;
     const WsLayout l = carve(ws, BH, T, N);
+    const bool pairwise = S0 == nullptr && S_out == nullptr;
+    // pairwise form: the key generation writes the blocks' coordinate lists
+    // itself; recurrent form: per-row lists
     if (int rc = bdh_keygen(xq, xk, U, theta, B, H, T, R, N, l.kidx, l.kval, l.kcnt, l.qidx, l.qval, l.qcnt,
-                            status, s))
+                            pairwise ? l.coff : nullptr, l.ct, l.cv, status, s))
         return rc;
+    if (pairwise) {
+        switch (dv) {
+            case 32: return pairs<32>(l, v, BH, T, N, y, s);
+            case 64: return pairs<64>(l, v, BH, T, N, y, s);
+            case 128: return pairs<128>(l, v, BH, T, N, y, s);
+            case 256: return pairs<256>(l, v, BH, T, N, y, s);
+        }
+    }
     switch (dv) {
         case 32: return attend<32>(l, v, BH, T, N, S0, S_out, y, s);
         case 64: return attend<64>(l, v, BH, T, N, S0, S_out, y, s);

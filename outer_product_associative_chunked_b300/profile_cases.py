@@ -10,6 +10,9 @@ cuda:0 and checks the device status, so an ``ncu`` capture of one launch
     python -m outer_product_associative_chunked_b300.profile_cases delta
     python -m outer_product_associative_chunked_b300.profile_cases delta_decode
     python -m outer_product_associative_chunked_b300.profile_cases sparse
+    python -m outer_product_associative_chunked_b300.profile_cases sparse_keygen
+    python -m outer_product_associative_chunked_b300.profile_cases tc_backward
+    python -m outer_product_associative_chunked_b300.profile_cases delta_backward
 
 Inputs come from the seeded generators in ``synth``; the shapes are the
 page workloads with fewer sequences or heads.
@@ -85,8 +88,42 @@ def sparse(B=1, H=2, T=2048, N=16384, dv=256, reps=4):
         binding.sparse_linattn_forward(q, k, v, out=y, workspace=ws)
 
 
+def sparse_keygen(B=1, H=2, T=2048, R=256, N=16384, dv=256, reps=4):
+    """BDH attention with the keys and queries generated on the GPU."""
+    kg = synth.sparse_keygen_inputs(B, H, T, N, dv, seed=5, rank=R)
+    xq, xk, U, v = kg.xq.cuda(), kg.xk.cuda(), kg.U.cuda(), kg.v.cuda()
+    y = torch.empty_like(v)
+    ws = torch.empty(binding.sparse_linattn_keygen_forward_workspace_size(B, H, T, R, N, dv), dtype=torch.uint8,
+                     device="cuda")
+    for _ in range(reps):
+        binding.sparse_linattn_keygen_forward(xq, xk, U, kg.theta, v, out=y, workspace=ws)
+
+
+def tc_backward(B=4, H=8, T=4096, d=64, W=512, reps=4):
+    """Tensor Cache backward on the headline shape, bf16."""
+    inp = synth.tc_inputs(B, H, T, d, d, W, dtype="bf16", seed=1)
+    q, k, v, lam, eta, gate = [x.cuda() for x in (inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate)]
+    dy = torch.randn(B, H, T, d, generator=torch.Generator().manual_seed(9)).to(torch.bfloat16).cuda()
+    ws = torch.empty(binding.tc_layer_backward_workspace_size(B, H, T, d, d, W, torch.bfloat16), dtype=torch.uint8,
+                     device="cuda")
+    for _ in range(reps):
+        binding.tc_layer_backward(q, k, v, lam, eta, gate, W, dy, workspace=ws)
+
+
+def delta_backward(B=1, H=16, T=2048, d=128, reps=4):
+    """DeltaNet backward, bf16, the DeltaNet head size over 2048 tokens."""
+    inp = synth.delta_inputs(B, H, T, d, d, dtype="bf16", seed=2)
+    q, k, v, beta = inp.q.cuda(), inp.k.cuda(), inp.v.cuda(), inp.beta.cuda()
+    dy = torch.randn(B, H, T, d, generator=torch.Generator().manual_seed(10)).to(torch.bfloat16).cuda()
+    ws = torch.empty(binding.delta_rule_backward_workspace_size(B, H, T, d, d, torch.bfloat16), dtype=torch.uint8,
+                     device="cuda")
+    for _ in range(reps):
+        binding.delta_rule_backward(q, k, v, beta, dy, workspace=ws)
+
+
 CASES = {"prefill": prefill, "prefill_long": prefill_long, "decode": decode, "delta": delta,
-         "delta_decode": delta_decode, "sparse": sparse}
+         "delta_decode": delta_decode, "sparse": sparse, "sparse_keygen": sparse_keygen,
+         "tc_backward": tc_backward, "delta_backward": delta_backward}
 
 
 def main(argv=None):

@@ -137,6 +137,28 @@ def test_cuda_graph_replay_matches_eager(cuda_lib):
     assert torch.equal(y, y_eager)
 
 
+def test_multi_chunk_segments_full_tensor(cuda_lib, oracle_mod):
+    """Every output element of a batch whose state recurrence is split into
+    segments of several chunks: 64 (batch, head) units leave about four
+    segments per head on a 148-SM GPU, so T = 2048 (16 chunks of 128) gives
+    segments of four chunks, and the carry lambda^(C (j - gL)) A_{gL} and the
+    local states A_j^loc are both exercised at every chunk."""
+    B, H, T, d, W = 8, 8, 2048, 64, 256
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nch = -(-T // 128)
+    want = max(1, min(nch, (2 * sms) // (B * H)))
+    chunks_per_segment = -(-nch // want)
+    assert chunks_per_segment > 1 and -(-nch // chunks_per_segment) < nch
+    inp = synth.tc_inputs(B, H, T, d, d, W, dtype="bf16", seed=55)
+    q, k, v, lam, eta, gate = _gpu(inp)
+    st = cuda_lib.TCState(B, H, W, d, d, dtype=torch.bfloat16)
+    y = cuda_lib.tc_layer_forward(q, k, v, lam, eta, gate, W, state=st)
+    torch.cuda.synchronize()
+    ref = oracle_mod.tc_prefill(inp.q, inp.k, inp.v, inp.lam, inp.eta, inp.gate, W, want_state=True)
+    check_parity(to_np(y), ref["y"], "bf16", f"multi-chunk segments ({chunks_per_segment} chunks each)")
+    check_parity(to_np(st.A), ref["A"], "bf16", "multi-chunk segments, final A")
+
+
 def _sampled_positions(T, W):
     ts = {0, 1, W - 1, W, W + 1, T // 2, T - 2, T - 1}
     ts |= set(np.random.default_rng(T).integers(0, T, 8).tolist())
