@@ -341,7 +341,8 @@ const char *opam_last_error(void);
  *   - returns OPAM_ERR_CUDA if the stream holds a CUDA error (for example a
  *     fault of any earlier work on it);
  *   - returns OPAM_ERR_TIMEOUT, with the kernels named in opam_last_error(),
- *     if the status at the head of `workspace` is non-zero;
+ *     if the status at the head of `workspace` is non-zero (in a
+ *     debug-bounds build, OPAM_ERR_INVALID_ARG if an index check failed);
  *   - returns OPAM_OK otherwise.
  * `workspace` is the workspace of the call in question and `stream` the
  * stream that call ran on.  With workspace NULL it checks the built-in
@@ -397,6 +398,20 @@ int opam_fp32_fma_probe(float *out, int blocks, int iters, double *flops, void *
  * OPAM_ERR_CUDA if the launch fails. */
 int opam_selftest_bounded_wait(int arrive, long long limit_cycles, void *workspace,
                                void *stream);
+
+/* Debug-bounds builds (no counterpart on the pages; used by the tests).  A
+ * library compiled with -DOPAM_DEBUG_BOUNDS checks the indexes of its
+ * kernels' global-memory writes (and of the BDH pair kernel's shared-memory
+ * accumulator): a failed check skips the access, never traps, and sets a bit
+ * that opam_check_device_error reports as OPAM_ERR_INVALID_ARG.
+ * opam_debug_bounds_build returns 1 for such a build and 0 otherwise.
+ * opam_selftest_bounds zeroes the status of `workspace` (at least
+ * OPAM_STATUS_BYTES) and runs one warp in which thread i checks i < n: with
+ * n < 32 a debug-bounds build reports the failed checks, a normal build
+ * nothing.  No memory is accessed.  Returns OPAM_OK, OPAM_ERR_INVALID_ARG or
+ * OPAM_ERR_CUDA. */
+int opam_debug_bounds_build(void);
+int opam_selftest_bounds(int n, void *workspace, void *stream);
 
 #ifdef __cplusplus
 }

@@ -18,7 +18,9 @@ import threading
 import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libopam.so")
+# OPAM_LIBRARY selects another build of the same library (for instance the
+# debug-bounds build, libopam_debug.so); the default is the normal build.
+LIB_PATH = os.environ.get("OPAM_LIBRARY") or os.path.join(_PKG, "libopam.so")
 
 OPAM_F32, OPAM_BF16 = 0, 1
 _STATUS = {0: "OK", -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "CUDA", -4: "TIMEOUT", -5: "WORKSPACE"}
@@ -36,7 +38,7 @@ EXPORTS = (
     "sparse_linattn_forward_workspace_size", "sparse_linattn_forward",
     "sparse_linattn_keygen_forward_workspace_size", "sparse_linattn_keygen_forward",
     "opam_last_error", "opam_profile_events", "opam_kernel_launches", "opam_check_device_error", "opam_fp32_fma_probe",
-    "opam_selftest_bounded_wait",
+    "opam_selftest_bounded_wait", "opam_selftest_bounds", "opam_debug_bounds_build",
 )
 
 
@@ -115,6 +117,10 @@ def lib() -> ctypes.CDLL:
         L.opam_fp32_fma_probe.argtypes = [vp, i, i, ctypes.POINTER(ctypes.c_double), vp]
         L.opam_check_device_error.restype = i
         L.opam_check_device_error.argtypes = [vp, vp]
+        L.opam_selftest_bounds.restype = i
+        L.opam_selftest_bounds.argtypes = [i, vp, vp]
+        L.opam_debug_bounds_build.restype = i
+        L.opam_debug_bounds_build.argtypes = []
         L.opam_selftest_bounded_wait.restype = i
         L.opam_selftest_bounded_wait.argtypes = [i, ctypes.c_longlong, vp, vp]
         _lib = L
@@ -186,6 +192,19 @@ def selftest_bounded_wait(arrive: bool, limit_cycles: int = 1_000_000, workspace
     limit_cycles and check_device_error(workspace) raises TIMEOUT."""
     ws = torch.empty(STATUS_BYTES, dtype=torch.uint8, device="cuda") if workspace is None else workspace
     _check(lib().opam_selftest_bounded_wait(1 if arrive else 0, int(limit_cycles), _ptr(ws), _stream(stream)))
+    return ws
+
+
+def debug_bounds_build() -> bool:
+    """True when the loaded library was built with its index checks on."""
+    return bool(lib().opam_debug_bounds_build())
+
+
+def selftest_bounds(n: int, workspace=None, stream=None):
+    """Run the index-check self-test (thread i of one warp checks i < n) into
+    `workspace` (a fresh status block if None, returned)."""
+    ws = torch.empty(STATUS_BYTES, dtype=torch.uint8, device="cuda") if workspace is None else workspace
+    _check(lib().opam_selftest_bounds(int(n), _ptr(ws), _stream(stream)))
     return ws
 
 

@@ -18,6 +18,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libopam.so")
+# The same sources with -DOPAM_DEBUG_BOUNDS: index checks that record a status
+# bit and skip the access (never trap), for running the tests under checks.
+DEBUG_OBJDIR = os.path.join(ROOT, "_build_debug")
+DEBUG_LIB = os.path.join(PKG, "libopam_debug.so")
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
@@ -32,15 +36,15 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+def needs_build(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def _compile(src, extra):
-    obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
+def _compile(src, extra, objdir=OBJDIR):
+    obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
     cmd = [NVCC, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -48,25 +52,29 @@ def _compile(src, extra):
     return obj, r.stderr
 
 
-def build(force: bool = False, verbose: bool = False, extra=()) -> str:
-    if not force and not needs_build():
-        return LIB
-    os.makedirs(OBJDIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra=(), debug_bounds: bool = False) -> str:
+    lib, objdir = (DEBUG_LIB, DEBUG_OBJDIR) if debug_bounds else (LIB, OBJDIR)
+    if debug_bounds:
+        extra = list(extra) + ["-DOPAM_DEBUG_BOUNDS"]
+    if not force and not needs_build(lib):
+        return lib
+    os.makedirs(objdir, exist_ok=True)
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
-        results = list(ex.map(lambda s: _compile(s, list(extra)), _sources()))
+        results = list(ex.map(lambda s: _compile(s, list(extra), objdir), _sources()))
     if verbose:
         for _, err in results:
             if err.strip():
                 print(err, file=sys.stderr)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *[o for o, _ in results], "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose=True,
-                extra=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else []))
+                extra=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else [],
+                debug_bounds="--debug-bounds" in sys.argv))

@@ -155,7 +155,8 @@ const char *status_names(unsigned int bits) {
     } parts[] = {{0x7Fu * kStatusTcPrefill, "Tensor Cache prefill "},
                  {0x1Fu * kStatusDelta, "DeltaNet tensor-core "},
                  {0x7u * kStatusKeygen, "BDH key generation "},
-                 {kStatusSelfTest, "bounded-wait self-test "}};
+                 {kStatusSelfTest, "bounded-wait self-test "},
+                 {kStatusBounds, "(index check of a debug-bounds build) "}};
     for (const auto &p : parts)
         if (bits & p.mask) strncat(buf, p.name, sizeof buf - strlen(buf) - 1);
     return buf;
@@ -187,6 +188,22 @@ int opam_selftest_bounded_wait(int arrive, long long limit_cycles, void *workspa
     return bounded_wait_selftest(arrive != 0, limit, status_word(workspace), s);
 }
 
+int opam_selftest_bounds(int n, void *workspace, void *stream) {
+    const char *fn = "opam_selftest_bounds";
+    OPAM_CHECK_PTR(workspace);
+    cudaStream_t s = (cudaStream_t)stream;
+    if (int rc = clear_status(workspace, s)) return rc;
+    return bounds_selftest(n, status_word(workspace), s);
+}
+
+int opam_debug_bounds_build(void) {
+#ifdef OPAM_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
 int opam_check_device_error(const void *workspace, void *stream) {
     const char *fn = "opam_check_device_error";
     if (workspace && !aligned16(workspace)) {
@@ -205,6 +222,11 @@ int opam_check_device_error(const void *workspace, void *stream) {
     unsigned int bits = 0;
     for (unsigned int w : words) bits |= w;
     if (bits == 0) return OPAM_OK;
+    if (bits & kStatusBounds) {
+        set_error("%s: an index check failed in a debug-bounds build (status 0x%x, %s); that call's outputs "
+                  "are not valid", fn, bits, status_names(bits));
+        return OPAM_ERR_INVALID_ARG;
+    }
     set_error("%s: a bounded wait ran out in the %skernels (status 0x%x); that call's outputs are not "
               "valid", fn, status_names(bits), bits);
     return OPAM_ERR_TIMEOUT;
@@ -501,7 +523,7 @@ int sparse_linattn_forward(const float *q, const float *k, const float *v, int B
     OPAM_CHECK_PTR(workspace);
     cudaStream_t s = (cudaStream_t)stream;
     if (int rc = clear_status(workspace, s)) return rc;
-    return sparse_forward(q, k, v, B, H, T, N, d_v, S0, S_out, y, status_body(workspace), s);
+    return sparse_forward(q, k, v, B, H, T, N, d_v, S0, S_out, y, status_body(workspace), status_word(workspace), s);
 }
 
 size_t sparse_linattn_keygen_forward_workspace_size(int B, int H, int T, int R, int N, int d_v) {

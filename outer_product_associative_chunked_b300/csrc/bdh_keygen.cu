@@ -11,13 +11,16 @@
 // input format of the sparse attention kernels -- so the dense N-wide rows
 // are never written to or read from memory.
 //
-// One CTA per (128 tokens, batch x head, queries or keys), 192 threads:
-//   warp 4 (lane 0)  TMA: the 128 x R x tile once, then U_h in column tiles of
+// One CTA per (128 tokens, batch x head, queries or keys), 320 threads:
+//   warp 8 (lane 0)  TMA: the 128 x R x tile once, then U_h in column tiles of
 //                    kNT = 128 (R x 128, MN-major, double-buffered);
-//   warp 5 (lane 0)  tcgen05.mma with K = R into one of two TMEM accumulators
+//   warp 9 (lane 0)  tcgen05.mma with K = R into one of two TMEM accumulators
 //                    (256 columns), so the epilogue of tile i overlaps the
 //                    MMAs of tile i + 1;
-//   warps 0-3        epilogue, one TMEM lane per thread.
+//   warps 0-7        epilogue: warps w and w + 4 share TMEM lane quarter w and
+//                    take 64 columns each; a thread first counts the entries
+//                    above theta in its 64 values, the two halves exchange
+//                    counts, then each writes its entries in place.
 // Two output forms:
 //   row lists (ROWS): D = x U (M = tokens), thread = token row: a = acc -
 //     theta; if a > 0 append (n, a) to the row's list (the per-row format the
@@ -63,16 +66,16 @@ struct KgBars {
     uint32_t tbase;
 };
 
-// Named barrier 1 over the four epilogue warps (128 threads); the second form
-// also returns whether `ok` holds in every one of them, so that all four
+// Named barrier 1 over the eight epilogue warps (256 threads); the second form
+// also returns whether `ok` holds in every one of them, so that all eight
 // leave their loop together.
-__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ bool epi_all(bool ok) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 q, %1, 0;\n\t"
-        "bar.red.and.pred p, 1, 128, q;\n\t"
+        "bar.red.and.pred p, 1, 256, q;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(r)
         : "r"((uint32_t)ok)
@@ -81,7 +84,7 @@ __device__ __forceinline__ bool epi_all(bool ok) {
 }
 
 template <int R, bool ROWS>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
 bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant__ CUtensorMap mxq,
                   const __grid_constant__ CUtensorMap mu, int T, int H, int N, float theta,
                   int *__restrict__ kidx, float *__restrict__ kval, int *__restrict__ kcnt,
@@ -93,19 +96,20 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
     unsigned char *sm = (unsigned char *)(((uintptr_t)smraw + 1023) & ~(uintptr_t)1023);
     __shared__ KgBars B;
     __shared__ int wtot[2][4];
+    __shared__ int hcnt[2][2][kM];  // [tile parity][column half][TMEM lane]: entries in that half
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int blk = blockIdx.x, bh = blockIdx.y, h = bh % H;
     const bool is_q = blockIdx.z == 1;
     const CUtensorMap *mx = is_q ? &mxq : &mxk;
     const int ntile = N / kNT;
-    if (warp == 5) tmem_alloc(&B.tbase, 256);
+    if (warp == 9) tmem_alloc(&B.tbase, 256);
     if (tid == 0) {
         mbar_init(&B.a_full, 1);
         for (int s = 0; s < 2; ++s) {
             mbar_init(&B.b_full[s], 1);
             mbar_init(&B.b_empty[s], 1);
             mbar_init(&B.acc_full[s], 1);
-            mbar_init(&B.acc_empty[s], 4);
+            mbar_init(&B.acc_empty[s], 8);
         }
         mbar_init(&B.drain, 1);
         mbar_fence_init();
@@ -116,7 +120,7 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
     const uint32_t tm = B.tbase;
     const uint32_t sA = smem_u32(sm), sB = sA + C::OFF_B;
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
             bool ok = true;
             mbar_expect_tx(&B.a_full, C::ABYTES);
@@ -139,7 +143,7 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
             for (int i = max(0, issued - 2); i < issued && dok; ++i) dok = mbar_wait(&B.b_full[i & 1], (i >> 1) & 1);
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             // ROWS: D = x U, A = x (K-major), B = U (MN-major);
             // otherwise D = U^T x^T, A = U (MN-major), B = x (K-major).
@@ -173,99 +177,99 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
             mbar_wait(&B.drain, 0);
         }
         __syncwarp();
-    } else if constexpr (!ROWS) {
-        // epilogue: thread = coordinate n0 + c (TMEM lane c), columns = tokens
-        const int c = tid;
+    } else {
+        // epilogue: TMEM lane r = 32 (warp % 4) + lane, columns [64 hf, 64 hf + 64)
+        // of the tile's 128.  ROWS: lane = token row, columns = coordinates;
+        // otherwise lane = coordinate, columns = tokens.
+        const int qd = warp & 3, hf = warp >> 2, r = qd * 32 + lane;
+        const uint32_t tcol = (uint32_t)(qd * 32) << 16;
         const int nlive = min(kM, T - blk * kM);
-        const size_t cb = ((size_t)(is_q ? 1 : 0) * gridDim.y + bh) * gridDim.x + blk;  // block of the lists
+        const bool row_live = r < nlive;
+        const size_t cb = ((size_t)(is_q ? 1 : 0) * gridDim.y + bh) * gridDim.x + blk;  // list block (!ROWS)
         int *off = coff + cb * (size_t)(N + 1);
         uint8_t *et = ct + cb * (size_t)kM * N;
         float *ev = cv + cb * (size_t)kM * N;
-        const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-        int base = 0;
+        const size_t row = (size_t)bh * T + blk * kM + r;                               // list row (ROWS)
+        int *oi = (is_q ? qidx : kidx) + row * (size_t)N;
+        float *ov = (is_q ? qval : kval) + row * (size_t)N;
+        int base = 0;  // ROWS: entries of row r so far; otherwise entries of the block so far
         bool ok = true;
         for (int i = 0; i < ntile && ok; ++i) {
             const int s = i & 1;
             ok = epi_all(mbar_wait(&B.acc_full[s], (i >> 1) & 1));
             if (!ok) break;
             tc_fence_after();
-            float a[kM];
-#pragma unroll
-            for (int cc = 0; cc < kM / 32; ++cc)
-                tmem_ld32(tm + lrow + s * kNT + 32 * cc, *reinterpret_cast<float(*)[32]>(a + 32 * cc));
+            float a[64];
+            tmem_ld32(tm + tcol + s * kNT + 64 * hf, *reinterpret_cast<float(*)[32]>(a));
+            tmem_ld32(tm + tcol + s * kNT + 64 * hf + 32, *reinterpret_cast<float(*)[32]>(a + 32));
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&B.acc_empty[s]);
+            // a value counts when it is above theta and its token is in the sequence
             int n = 0;
 #pragma unroll
-            for (int t = 0; t < kM; ++t) n += (t < nlive && a[t] - theta > 0.f) ? 1 : 0;
-            int incl = n;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, d);
-                if (lane >= d) incl += y;
+            for (int c = 0; c < 64; ++c) {
+                const bool live = ROWS ? row_live : (64 * hf + c < nlive);
+                n += (live && a[c] - theta > 0.f) ? 1 : 0;
             }
-            if (lane == 31) wtot[s][warp] = incl;
+            hcnt[s][hf][r] = n;
             epi_barrier();
-            int p = base + incl - n;
-            for (int w = 0; w < warp; ++w) p += wtot[s][w];
-            off[i * kNT + c] = p;
+            const int lo = hcnt[s][0][r];
+            int p;
+            if constexpr (ROWS) {
+                p = base + (hf ? lo : 0);
+                base += lo + hcnt[s][1][r];
+            } else {
+                // exclusive scan of the coordinates' totals over the 128 lanes
+                const int tot = lo + hcnt[s][1][r];
+                int incl = tot;
 #pragma unroll
-            for (int t = 0; t < kM; ++t) {
-                const float x = a[t] - theta;
-                if (t < nlive && x > 0.f) {
-                    et[p] = (uint8_t)t;
-                    ev[p] = x;
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d) incl += y;
+                }
+                if (hf == 0 && lane == 31) wtot[s][qd] = incl;
+                epi_barrier();
+                int start = base + incl - tot;
+                for (int w = 0; w < qd; ++w) start += wtot[s][w];
+                if (hf == 0 && OPAM_BOUNDS(i * kNT + r < N, status)) off[i * kNT + r] = start;
+                p = start + (hf ? lo : 0);
+                base += wtot[s][0] + wtot[s][1] + wtot[s][2] + wtot[s][3];
+            }
+            const int c0 = i * kNT + 64 * hf;  // ROWS: first coordinate of these columns
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const bool live = ROWS ? row_live : (64 * hf + c < nlive);
+                const float x = a[c] - theta;
+                if (live && x > 0.f) {
+                    if constexpr (ROWS) {
+                        if (OPAM_BOUNDS(p < N, status)) {
+                            oi[p] = c0 + c;
+                            ov[p] = x;
+                        }
+                    } else {
+                        if (OPAM_BOUNDS(p < kM * N, status)) {
+                            et[p] = (uint8_t)(64 * hf + c);
+                            ev[p] = x;
+                        }
+                    }
                     ++p;
                 }
             }
-            base += wtot[s][0] + wtot[s][1] + wtot[s][2] + wtot[s][3];
         }
         if (!ok && lane == 0) atomicOr(status, kStKgEpi);
-        if (ok && c == 0) off[N] = base;
-    } else {
-        // epilogue: thread = token row (TMEM lane)
-        const int r = tid, t = blk * kM + r;
-        const bool live = t < T;
-        const size_t row = (size_t)bh * T + t;
-        int *oi = (is_q ? qidx : kidx) + row * (size_t)N;
-        float *ov = (is_q ? qval : kval) + row * (size_t)N;
-        const uint32_t lrow = (uint32_t)(warp * 32) << 16;
-        int cnt = 0;
-        bool ok = true;
-        for (int i = 0; i < ntile && ok; ++i) {
-            const int s = i & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&B.acc_full[s], (i >> 1) & 1));
-            if (!ok) break;
-            tc_fence_after();
-            float a[kNT];
-#pragma unroll
-            for (int c = 0; c < kNT / 32; ++c)
-                tmem_ld32(tm + lrow + s * kNT + 32 * c, *reinterpret_cast<float(*)[32]>(a + 32 * c));
-            tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.acc_empty[s]);
-            if (live) {
-                const int n0 = i * kNT;
-#pragma unroll
-                for (int c = 0; c < kNT; ++c) {
-                    const float x = a[c] - theta;
-                    if (x > 0.f) {
-                        oi[cnt] = n0 + c;
-                        ov[cnt] = x;
-                        ++cnt;
-                    }
-                }
+        if (ok) {
+            if constexpr (ROWS) {
+                if (hf == 0 && row_live) (is_q ? qcnt : kcnt)[row] = base;
+            } else {
+                if (hf == 0 && r == 0) off[N] = base;
             }
         }
-        if (!ok && lane == 0) atomicOr(status, kStKgEpi);
-        if (live) (is_q ? qcnt : kcnt)[row] = cnt;
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) tmem_dealloc(tm, 256);
+    if (warp == 9) tmem_dealloc(tm, 256);
 }
 
 }  // namespace
@@ -285,7 +289,7 @@ int bdh_keygen(const void *xq, const void *xk, const void *U, float theta, int B
     const dim3 grid(ceil_div(T, kM), BH, 2);
     auto go = [&](auto kern, uint32_t smem) -> int {
         if (int rc_ = set_smem_limit((const void *)kern, (int)smem, "bdh_keygen smem attribute")) return rc_;
-        kern<<<grid, 192, smem, s>>>(mxk, mxq, mu, T, H, N, theta, kidx, kval, kcnt, qidx, qval, qcnt, coff, ct, cv,
+        kern<<<grid, 320, smem, s>>>(mxk, mxq, mu, T, H, N, theta, kidx, kval, kcnt, qidx, qval, qcnt, coff, ct, cv,
                                      status);
         return launched("bdh_keygen");
     };

@@ -11,11 +11,13 @@
 //   dk_t = beta_t dS^T u_t - S_{t-1}^T (beta_t g);
 //   dS <- dS - beta_t g k_t^T.
 //
-// One CTA per (batch, head); its d_v/16 warps each own 16 rows of S and of
-// dS in registers, a lane holding d_k/32 columns of each row, so every row
-// update is lane-local and every column sum over the warp's rows is too.
+// One CTA per (batch, head); its d_v/8 warps each own 8 rows of S and of dS
+// in registers, a lane holding d_k/32 columns of each row, so every row
+// update is lane-local and every column sum over the warp's rows is too.  The
+// walk is sequential, so the time is the length of one warp's chain of
+// instructions per token: fewer rows per warp (more warps) shorten it.
 // Row sums over the columns (S k, dS k) go through a transposing warp
-// reduction: 31 shuffles leave the total of row (lane mod 16) in each lane.
+// reduction: 23 shuffles leave the total of row (lane mod 8) in each lane.
 // Column sums over all d_v rows (dq, dk) and dbeta are combined across the
 // warps in shared memory, one barrier per token.
 //
@@ -30,15 +32,17 @@
 namespace opam {
 namespace {
 
-constexpr int kRows = 16;  // rows of S per warp
+constexpr int kRows = 8;  // rows of S per warp
 
-// x[0..15] summed over the 32 lanes; returns the total of row (lane & 15).
-__device__ __forceinline__ float transpose_reduce16(float (&x)[kRows]) {
+// x[0..7] summed over the 32 lanes; returns the total of row (lane & 7).
+__device__ __forceinline__ float transpose_reduce(float (&x)[kRows]) {
     const int lane = threadIdx.x & 31;
 #pragma unroll
-    for (int i = 0; i < kRows; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], 16);
+    for (int o = 16; o >= kRows; o >>= 1)
 #pragma unroll
-    for (int o = 8, n = 16; o >= 1; o >>= 1, n >>= 1) {
+        for (int i = 0; i < kRows; ++i) x[i] += __shfl_xor_sync(0xffffffffu, x[i], o);
+#pragma unroll
+    for (int o = kRows / 2, n = kRows; o >= 1; o >>= 1, n >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
         for (int j = 0; j < n / 2; ++j) {
@@ -60,7 +64,7 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
     constexpr int CPL = DK / 32;          // columns per lane
     constexpr int NW = DV / kRows;        // warps
     __shared__ float red[2][NW][2 * DK + 1];
-    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, row = w * kRows + (lane & 15);
+    const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, row = w * kRows + (lane & (kRows - 1));
     const int bh = blockIdx.x;
     const size_t tk = (size_t)bh * Tn * DK, tv = (size_t)bh * Tn * DV;
     float S[kRows][CPL], dS[kRows][CPL];
@@ -73,13 +77,23 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
             S[i][c] = S0 ? S0[at] : 0.f;
             dS[i][c] = dST ? dST[at] : 0.f;
         }
-    // ---- pass 1: forward, storing u_t
+    // ---- pass 1: forward, storing u_t.  The next token's inputs are loaded
+    // while the current one is processed (the walk is sequential, so a load
+    // issued at the top of its own step would expose the whole latency).
+    float kn[CPL], bn = 0.f, vn = 0.f;
+    auto fetch1 = [&](int t) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) kn[c] = Elem<T>::load(k + tk + (size_t)t * DK + lane + 32 * c);
+        bn = beta[(size_t)bh * Tn + t];
+        vn = Elem<T>::load(v + tv + (size_t)t * DV + row);
+    };
+    if (Tn > 0) fetch1(0);
     for (int t = 0; t < Tn; ++t) {
         float kc[CPL], x[kRows];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) kc[c] = Elem<T>::load(k + tk + (size_t)t * DK + lane + 32 * c);
-        const float bt = beta[(size_t)bh * Tn + t];
-        const float vr = Elem<T>::load(v + tv + (size_t)t * DV + row);
+        for (int c = 0; c < CPL; ++c) kc[c] = kn[c];
+        const float bt = bn, vr = vn;
+        if (t + 1 < Tn) fetch1(t + 1);
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             float s = 0.f;
@@ -87,8 +101,9 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
             for (int c = 0; c < CPL; ++c) s = fmaf(S[i][c], kc[c], s);
             x[i] = s;
         }
-        const float u = vr - transpose_reduce16(x);
-        if (lane < kRows) U[tv + (size_t)t * DV + row] = u;
+        const float u = vr - transpose_reduce(x);
+        if (lane < kRows && OPAM_BOUNDS(tv + (size_t)t * DV + row < (size_t)gridDim.x * Tn * DV, status))
+            U[tv + (size_t)t * DV + row] = u;
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             const float bu = bt * __shfl_sync(0xffffffffu, u, i);
@@ -96,19 +111,31 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
             for (int c = 0; c < CPL; ++c) S[i][c] = fmaf(bu, kc[c], S[i][c]);
         }
     }
-    // ---- pass 2: reverse
+    // ---- pass 2: reverse (next token's inputs prefetched as in pass 1)
+    float qn[CPL], dn = 0.f, un = 0.f;
+    auto fetch2 = [&](int t) {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+            qn[c] = Elem<T>::load(q + tk + (size_t)t * DK + lane + 32 * c);
+            kn[c] = Elem<T>::load(k + tk + (size_t)t * DK + lane + 32 * c);
+        }
+        bn = beta[(size_t)bh * Tn + t];
+        dn = Elem<T>::load(dy + tv + (size_t)t * DV + row);
+        un = U[tv + (size_t)t * DV + row];
+    };
+    __syncwarp();  // this lane's u stores of pass 1 precede its reloads
+    if (Tn > 0) fetch2(Tn - 1);
     for (int t = Tn - 1; t >= 0; --t) {
         float qc[CPL], kc[CPL], x[kRows], dqp[CPL], dkp[CPL];
 #pragma unroll
         for (int c = 0; c < CPL; ++c) {
-            qc[c] = Elem<T>::load(q + tk + (size_t)t * DK + lane + 32 * c);
-            kc[c] = Elem<T>::load(k + tk + (size_t)t * DK + lane + 32 * c);
+            qc[c] = qn[c];
+            kc[c] = kn[c];
             dqp[c] = 0.f;
             dkp[c] = 0.f;
         }
-        const float bt = beta[(size_t)bh * Tn + t];
-        const float dor = Elem<T>::load(dy + tv + (size_t)t * DV + row);
-        const float ur = U[tv + (size_t)t * DV + row];
+        const float bt = bn, dor = dn, ur = un;
+        if (t > 0) fetch2(t - 1);
         // dq = S_t^T do;  dS += do q^T;  g = dS k
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
@@ -122,9 +149,10 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
             }
             x[i] = s;
         }
-        const float g = transpose_reduce16(x);
+        const float g = transpose_reduce(x);
         const float du = bt * g;
-        if (lane < kRows) Elem<T>::store(dv + tv + (size_t)t * DV + row, du);
+        if (lane < kRows && OPAM_BOUNDS(tv + (size_t)t * DV + row < (size_t)gridDim.x * Tn * DV, status))
+            Elem<T>::store(dv + tv + (size_t)t * DV + row, du);
         float db = lane < kRows ? ur * g : 0.f;
         db = warp_sum(db);
         // S <- S_{t-1};  dk = beta dS^T u - S_{t-1}^T du;  dS -= du k^T
@@ -152,6 +180,7 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
             float s = 0.f;
 #pragma unroll
             for (int ww = 0; ww < NW; ++ww) s += buf[ww][idx];
+            if (!OPAM_BOUNDS(tk + (size_t)t * DK + DK <= (size_t)gridDim.x * Tn * DK, status)) continue;
             if (idx < DK)
                 Elem<T>::store(dq + tk + (size_t)t * DK + idx, s);
             else if (idx < 2 * DK)

@@ -69,7 +69,18 @@ constexpr unsigned int kStatusTcPrefill = 1u << 0;   // 7 bits: Tensor Cache pre
 constexpr unsigned int kStatusDelta = 1u << 8;       // 5 bits: DeltaNet tensor-core kernels
 constexpr unsigned int kStatusSelfTest = 1u << 16;   // the bounded-wait self-test
 constexpr unsigned int kStatusKeygen = 1u << 20;     // 3 bits: BDH key generation
+constexpr unsigned int kStatusBounds = 1u << 24;     // an index check failed (debug-bounds builds)
 constexpr int kStatusWords = 4;
+
+// Index checks of a debug-bounds build (compiled with -DOPAM_DEBUG_BOUNDS):
+// OPAM_BOUNDS(cond, status) is false, and sets kStatusBounds in *status, when
+// `cond` fails, so the caller skips the access; it never traps.  In a normal
+// build it is `true` and costs nothing.
+#ifdef OPAM_DEBUG_BOUNDS
+#define OPAM_BOUNDS(cond, status) ((cond) ? true : (atomicOr((status), ::opam::kStatusBounds), false))
+#else
+#define OPAM_BOUNDS(cond, status) true
+#endif
 inline unsigned int *status_word(void *ws) { return (unsigned int *)ws; }
 inline void *status_body(void *ws) { return ws ? (char *)ws + OPAM_STATUS_BYTES : nullptr; }
 // Zero the status words on the call's stream (enqueued before its kernels).
@@ -107,6 +118,9 @@ int tc_prefill_tcgen05(const void *q, const void *k, const void *v, int B, int H
 // Self-test of the bounded mbarrier wait (sets kStatusSelfTest in *status
 // when it runs out).
 int bounded_wait_selftest(int arrive, long long limit, unsigned int *status, cudaStream_t s);
+// Self-test of the debug-bounds index check (sets kStatusBounds in *status in
+// a debug-bounds build when n < 32).
+int bounds_selftest(int n, unsigned int *status, cudaStream_t s);
 
 // Tensor Cache layer backward (CUDA cores; bf16 or fp32 inputs).
 size_t tc_backward_workspace(int BH, int T, int dk, int dv);
@@ -157,7 +171,8 @@ int bdh_keygen(const void *xq, const void *xk, const void *U, float theta, int B
 
 size_t sparse_workspace(int BH, int T, int N, int dv, bool need_state);
 int sparse_forward(const float *q, const float *k, const float *v, int B, int H, int T, int N,
-                   int dv, const float *S0, float *S_out, float *y, void *ws, cudaStream_t s);
+                   int dv, const float *S0, float *S_out, float *y, void *ws, unsigned int *status,
+                   cudaStream_t s);
 // The same attention with q and k generated on chip from x and U_h.
 int sparse_keygen_forward(const void *xq, const void *xk, const void *U, float theta, const float *v, int B,
                           int H, int T, int R, int N, int dv, const float *S0, float *S_out, float *y, void *ws,

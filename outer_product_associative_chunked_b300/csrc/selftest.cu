@@ -25,7 +25,21 @@ __global__ void bounded_wait_selftest_kernel(int arrive, long long limit, unsign
     __syncwarp();
 }
 
+// Every thread checks threadIdx.x < n through the debug-bounds index check;
+// with n below the block size some checks fail, which in a debug-bounds
+// build sets kStatusBounds (and in a normal build does nothing).  No memory
+// is accessed either way.
+__global__ void bounds_selftest_kernel(int n, unsigned int *status) {
+    if (OPAM_BOUNDS(threadIdx.x < (unsigned)n, status)) {
+    }
+}
+
 }  // namespace
+
+int bounds_selftest(int n, unsigned int *status, cudaStream_t s) {
+    bounds_selftest_kernel<<<1, 32, 0, s>>>(n, status);
+    return launched("bounds_selftest");
+}
 
 int bounded_wait_selftest(int arrive, long long limit, unsigned int *status, cudaStream_t s) {
     bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(arrive, limit, status);

@@ -295,7 +295,8 @@ constexpr int kCT = 128;  // columns per tile
 
 __global__ void __launch_bounds__(256)
 dense_csc_kernel(const float *__restrict__ q, const float *__restrict__ k, int T, int N, int nb,
-                 int *__restrict__ coff, uint8_t *__restrict__ ct, float *__restrict__ cv) {
+                 int *__restrict__ coff, uint8_t *__restrict__ ct, float *__restrict__ cv,
+                 unsigned int *__restrict__ status) {
     constexpr int LD = kCT + 4;  // padded row stride (float4-aligned)
     extern __shared__ float tilef[];  // [kTB][LD]
     __shared__ int cnt2[2][kCT];   // non-zeros of column c in the lower / upper 64 rows
@@ -360,8 +361,10 @@ dense_csc_kernel(const float *__restrict__ q, const float *__restrict__ k, int T
         for (int r = 64 * half; r < 64 * half + 64; ++r) {
             const float val = tilef[r * LD + c];
             if (val != 0.f) {
-                et[p] = (uint8_t)r;
-                ev[p] = val;
+                if (OPAM_BOUNDS(p < kTB * N, status)) {
+                    et[p] = (uint8_t)r;
+                    ev[p] = val;
+                }
                 ++p;
             }
         }
@@ -382,6 +385,12 @@ dense_csc_kernel(const float *__restrict__ q, const float *__restrict__ k, int T
 //   coordinate's setup.  A window whose lists do not fit the buffers (dense
 //   inputs) is read from global memory, one coordinate per warp.
 //   Then o[tb] += Z V[sb]  (fp32, 64 output columns per pass, float4 atomics).
+// Z[t][s] += x in shared memory with no value returned (a reduction, not an
+// atomic read-modify-write that hands back the old value).
+__device__ __forceinline__ void red_add_shared(float *p, float x) {
+    asm volatile("red.shared.add.f32 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(p)), "f"(x) : "memory");
+}
+
 constexpr int kJW = 256;    // coordinates per window
 constexpr int kCap = 2048;  // list entries per window buffered in shared memory
 
@@ -395,7 +404,8 @@ struct PairSmem {
 template <int DV>
 __global__ void __launch_bounds__(256, 2)
 pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8_t *__restrict__ ct,
-                 const float *__restrict__ cv, const float *__restrict__ v, float *__restrict__ y) {
+                 const float *__restrict__ cv, const float *__restrict__ v, float *__restrict__ y,
+                 unsigned int *__restrict__ status) {
     constexpr int ZS = kTB + 1;  // padded row stride of the Z tile
     extern __shared__ unsigned char smraw[];
     PairSmem &P = *reinterpret_cast<PairSmem *>(smraw);
@@ -412,26 +422,91 @@ pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8
     const int *ko = coff + bk * (size_t)(N + 1), *qo = coff + bq * (size_t)(N + 1);
     const uint8_t *kt = ct + bk * (size_t)kTB * N, *qt = ct + bq * (size_t)kTB * N;
     const float *kv = cv + bk * (size_t)kTB * N, *qv = cv + bq * (size_t)kTB * N;
-    for (int w0 = 0; w0 < N; w0 += kJW) {
-        const int nw = min(kJW, N - w0);
-        __syncthreads();  // the previous window's buffers are no longer read (and Z is zeroed)
-        for (int i = tid; i <= nw; i += 256) {
-            P.qo[i] = qo[w0 + i];
-            P.ko[i] = ko[w0 + i];
+    // The coordinate windows are software-pipelined: while window w's
+    // products run, the next window's offsets and list entries are already
+    // on their way into registers (its bounds were read one window earlier),
+    // so the staging costs no exposed global-memory latency.
+    constexpr int EPT = kCap / 256;  // list entries per thread and list, at most
+    const int nwin = (N + kJW - 1) / kJW;
+    int pqo = 0, pko = 0;                       // next window's offsets (entry tid)
+    uint32_t pqt[EPT], pkt[EPT];
+    float pqv[EPT], pkv[EPT];
+    int nb_qb = 0, nb_qe = 0, nb_kb = 0, nb_ke = 0;  // bounds of the window after next
+    auto fetch_bounds = [&](int w, int &qb_, int &qe_, int &kb_, int &ke_) {
+        if (w < nwin) {
+            const int ws = w * kJW, we = min(N, ws + kJW);
+            qb_ = qo[ws];
+            qe_ = qo[we];
+            kb_ = ko[ws];
+            ke_ = ko[we];
         }
-        __syncthreads();
-        const int qb = P.qo[0], kb = P.ko[0];
-        const int nq = P.qo[nw] - qb, nk = P.ko[nw] - kb;
+    };
+    auto fetch_window = [&](int w, int qb_, int qe_, int kb_, int ke_) {
+        if (w >= nwin) return;
+        const int ws = w * kJW, nw_ = min(kJW, N - ws);
+        if (tid < nw_) {
+            pqo = qo[ws + tid];
+            pko = ko[ws + tid];
+        }
+        const int nq_ = qe_ - qb_, nk_ = ke_ - kb_;
+        if (nq_ <= kCap && nk_ <= kCap) {
+#pragma unroll
+            for (int u = 0; u < EPT; ++u) {
+                const int i = tid + 256 * u;
+                if (i < nq_) {
+                    pqt[u] = qt[qb_ + i];
+                    pqv[u] = qv[qb_ + i];
+                }
+                if (i < nk_) {
+                    pkt[u] = kt[kb_ + i];
+                    pkv[u] = kv[kb_ + i];
+                }
+            }
+        }
+    };
+    auto store_window = [&](int w, int qb_, int qe_, int kb_, int ke_) {
+        const int ws = w * kJW, nw_ = min(kJW, N - ws);
+        if (tid < nw_) {
+            P.qo[tid] = pqo;
+            P.ko[tid] = pko;
+        }
+        if (tid == 0) {  // the window's closing offsets are its bounds
+            P.qo[nw_] = qe_;
+            P.ko[nw_] = ke_;
+        }
+        const int nq_ = qe_ - qb_, nk_ = ke_ - kb_;
+        if (nq_ <= kCap && nk_ <= kCap) {
+#pragma unroll
+            for (int u = 0; u < EPT; ++u) {
+                const int i = tid + 256 * u;
+                if (i < nq_) {
+                    P.qt[i] = (uint8_t)pqt[u];
+                    P.qv[i] = pqv[u];
+                }
+                if (i < nk_) {
+                    P.kt[i] = (uint8_t)pkt[u];
+                    P.kv[i] = pkv[u];
+                }
+            }
+        }
+    };
+    int cq_b = 0, cq_e = 0, ck_b = 0, ck_e = 0;  // bounds of the window being staged / processed
+    fetch_bounds(0, cq_b, cq_e, ck_b, ck_e);
+    fetch_window(0, cq_b, cq_e, ck_b, ck_e);
+    fetch_bounds(1, nb_qb, nb_qe, nb_kb, nb_ke);
+    for (int w = 0; w < nwin; ++w) {
+        const int w0 = w * kJW, nw = min(kJW, N - w0);
+        __syncthreads();  // the previous window's buffers are no longer read (and Z is zeroed)
+        store_window(w, cq_b, cq_e, ck_b, ck_e);
+        const int qb = cq_b, kb = ck_b;
+        const int nq = cq_e - cq_b, nk = ck_e - ck_b;
         const bool fits = nq <= kCap && nk <= kCap;
+        __syncthreads();
+        // next window: its bounds are known, so its entries can be requested now
+        cq_b = nb_qb; cq_e = nb_qe; ck_b = nb_kb; ck_e = nb_ke;
+        fetch_window(w + 1, cq_b, cq_e, ck_b, ck_e);
+        fetch_bounds(w + 2, nb_qb, nb_qe, nb_kb, nb_ke);
         if (fits) {
-            for (int i = tid; i < nq; i += 256) {
-                P.qt[i] = qt[qb + i];
-                P.qv[i] = qv[qb + i];
-            }
-            for (int i = tid; i < nk; i += 256) {
-                P.kt[i] = kt[kb + i];
-                P.kv[i] = kv[kb + i];
-            }
             for (int jl = tid; jl < nw; jl += 256)  // tag each query entry with its coordinate
                 for (int e = P.qo[jl] - qb; e < P.qo[jl + 1] - qb; ++e) P.qj[e] = (uint8_t)jl;
             __syncthreads();
@@ -443,7 +518,7 @@ pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8
                 float *zrow = Zs + t * ZS;
                 for (int b = b0; b < b1; ++b) {
                     const int s = P.kt[b];
-                    if (s <= smax) atomicAdd(zrow + s, x * P.kv[b]);
+                    if (s <= smax && OPAM_BOUNDS(t < kTB && s < kTB, status)) red_add_shared(zrow + s, x * P.kv[b]);
                 }
             }
         } else {
@@ -462,7 +537,8 @@ pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8
                         const int b = b0 + (lane & 3);
                         if (qa && b < nkj) {
                             const int s = kt[k0 + b];
-                            if (s <= smax) atomicAdd(Zs + t * ZS + s, x * kv[k0 + b]);
+                            if (s <= smax && OPAM_BOUNDS(t < kTB && s < kTB, status))
+                                red_add_shared(Zs + t * ZS + s, x * kv[k0 + b]);
                         }
                     }
                 }
@@ -485,22 +561,40 @@ pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
         const int col = c0 + 8 * cg;
-#pragma unroll 2
-        for (int s = 0; s < cols; ++s) {
-            const float4 *vr = reinterpret_cast<const float4 *>(vb + (size_t)s * DV + col);
-            const float4 v0 = vr[0], v1 = vr[1];
-            const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        // V rows are read from L2: keep kLook rows of loads in flight
+        constexpr int kLook = 4;
+        float4 va[kLook][2];
+        auto vload = [&](int s, float4 (&dst)[2]) {
+            if (s < cols) {
+                const float4 *vr = reinterpret_cast<const float4 *>(vb + (size_t)s * DV + col);
+                dst[0] = vr[0];
+                dst[1] = vr[1];
+            }
+        };
 #pragma unroll
-            for (int i = 0; i < RPT; ++i) {
-                const float z = Zs[(rg * RPT + i) * ZS + s];
+        for (int u = 0; u < kLook; ++u) vload(u, va[u]);
+        for (int s0 = 0; s0 < cols; s0 += kLook) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(z, vv[e], acc[i][e]);
+            for (int u = 0; u < kLook; ++u) {
+                const int s = s0 + u;
+                if (s < cols) {
+                    const float vv[8] = {va[u][0].x, va[u][0].y, va[u][0].z, va[u][0].w,
+                                         va[u][1].x, va[u][1].y, va[u][1].z, va[u][1].w};
+                    vload(s + kLook, va[u]);
+#pragma unroll
+                    for (int i = 0; i < RPT; ++i) {
+                        const float z = Zs[(rg * RPT + i) * ZS + s];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(z, vv[e], acc[i][e]);
+                    }
+                }
             }
         }
 #pragma unroll
         for (int i = 0; i < RPT; ++i) {
             const int r = rg * RPT + i;
-            if (r < rows) {
+            if (r < rows && OPAM_BOUNDS(((size_t)bh * T + tb * kTB + r) * DV + col + 8 <= (size_t)BH * T * DV,
+                                        status)) {
                 float4 *dst = reinterpret_cast<float4 *>(yb + (size_t)r * DV + col);
                 atomicAdd(dst, make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]));
                 atomicAdd(dst + 1, make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]));
@@ -551,7 +645,7 @@ WsLayout carve(void *ws, int BH, int T, int N) {
 
 // Block pairs over the coordinate lists of the workspace: y = sum of Z V.
 template <int DV>
-int pairs(const WsLayout &l, const float *v, int BH, int T, int N, float *y, cudaStream_t s) {
+int pairs(const WsLayout &l, const float *v, int BH, int T, int N, float *y, unsigned int *status, cudaStream_t s) {
     const int nb = ceil_div(T, kTB);
     cudaError_t e = cudaMemsetAsync(y, 0, sizeof(float) * (size_t)BH * T * DV, s);
     if (e != cudaSuccess) return cuda_fail(e, "sparse output init");
@@ -559,7 +653,8 @@ int pairs(const WsLayout &l, const float *v, int BH, int T, int N, float *y, cud
     if (int rc_ = set_smem_limit((const void *)pair_tile_kernel<DV>, (int)psmem, "pair_tile smem attribute"))
         return rc_;
     prof_begin(s);
-    pair_tile_kernel<DV><<<dim3(nb * (nb + 1) / 2, BH), 256, psmem, s>>>(T, N, nb, l.coff, l.ct, l.cv, v, y);
+    pair_tile_kernel<DV><<<dim3(nb * (nb + 1) / 2, BH), 256, psmem, s>>>(T, N, nb, l.coff, l.ct, l.cv, v, y,
+                                                                          status);
     const int rc = launched("pair_tile");
     prof_end(s);
     return rc;
@@ -568,7 +663,7 @@ int pairs(const WsLayout &l, const float *v, int BH, int T, int N, float *y, cud
 // Everything after the per-row supports are in the workspace.
 template <int DV>
 int attend(const WsLayout &l, const float *v, int BH, int T, int N, const float *S0, float *S_out, float *y,
-           cudaStream_t s) {
+           unsigned int *status, cudaStream_t s) {
     cudaError_t e;
     if (S0 == nullptr && S_out == nullptr) {
         // pairwise form: coordinate lists per token block, then block pairs
@@ -579,7 +674,7 @@ int attend(const WsLayout &l, const float *v, int BH, int T, int N, const float 
         csc_build_kernel<<<dim3(nb, BH, 2), 512, csmem, s>>>(T, N, nb, l.kidx, l.kval, l.kcnt, l.qidx, l.qval,
                                                             l.qcnt, l.coff, l.ct, l.cv);
         if (int rc = launched("csc_build")) return rc;
-        return pairs<DV>(l, v, BH, T, N, y, s);
+        return pairs<DV>(l, v, BH, T, N, y, status, s);
     }
     // recurrent form: the state lives in S_out (or the workspace)
     float *ST = S_out ? S_out : l.ST;
@@ -613,7 +708,7 @@ int attend(const WsLayout &l, const float *v, int BH, int T, int N, const float 
 
 template <int DV>
 int launch(const float *q, const float *k, const float *v, int BH, int T, int N, const float *S0,
-           float *S_out, float *y, void *ws, cudaStream_t s) {
+           float *S_out, float *y, void *ws, unsigned int *status, cudaStream_t s) {
     const WsLayout l = carve(ws, BH, T, N);
     const int rows = BH * T;
     if (S0 == nullptr && S_out == nullptr && N % kCT == 0) {
@@ -621,15 +716,15 @@ int launch(const float *q, const float *k, const float *v, int BH, int T, int N,
         const int nb = ceil_div(T, kTB);
         const int smem = (int)(sizeof(float) * kTB * (kCT + 4));
         if (int rc_ = set_smem_limit((const void *)dense_csc_kernel, smem, "dense_csc smem attribute")) return rc_;
-        dense_csc_kernel<<<dim3(nb, BH, 2), 256, smem, s>>>(q, k, T, N, nb, l.coff, l.ct, l.cv);
+        dense_csc_kernel<<<dim3(nb, BH, 2), 256, smem, s>>>(q, k, T, N, nb, l.coff, l.ct, l.cv, status);
         if (int rc = launched("dense_csc")) return rc;
-        return pairs<DV>(l, v, BH, T, N, y, s);
+        return pairs<DV>(l, v, BH, T, N, y, status, s);
     }
     compact_rows_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(k, rows, N, l.kidx, l.kval, l.kcnt);
     if (int rc = launched("compact k")) return rc;
     compact_rows_kernel<<<ceil_div(rows, 8), 256, 0, s>>>(q, rows, N, l.qidx, l.qval, l.qcnt);
     if (int rc = launched("compact q")) return rc;
-    return attend<DV>(l, v, BH, T, N, S0, S_out, y, s);
+    return attend<DV>(l, v, BH, T, N, S0, S_out, y, status, s);
 }
 
 }  // namespace
@@ -647,17 +742,17 @@ int sparse_keygen_forward(const void *xq, const void *xk, const void *U, float t
         return rc;
     if (pairwise) {
         switch (dv) {
-            case 32: return pairs<32>(l, v, BH, T, N, y, s);
-            case 64: return pairs<64>(l, v, BH, T, N, y, s);
-            case 128: return pairs<128>(l, v, BH, T, N, y, s);
-            case 256: return pairs<256>(l, v, BH, T, N, y, s);
+            case 32: return pairs<32>(l, v, BH, T, N, y, status, s);
+            case 64: return pairs<64>(l, v, BH, T, N, y, status, s);
+            case 128: return pairs<128>(l, v, BH, T, N, y, status, s);
+            case 256: return pairs<256>(l, v, BH, T, N, y, status, s);
         }
     }
     switch (dv) {
-        case 32: return attend<32>(l, v, BH, T, N, S0, S_out, y, s);
-        case 64: return attend<64>(l, v, BH, T, N, S0, S_out, y, s);
-        case 128: return attend<128>(l, v, BH, T, N, S0, S_out, y, s);
-        case 256: return attend<256>(l, v, BH, T, N, S0, S_out, y, s);
+        case 32: return attend<32>(l, v, BH, T, N, S0, S_out, y, status, s);
+        case 64: return attend<64>(l, v, BH, T, N, S0, S_out, y, status, s);
+        case 128: return attend<128>(l, v, BH, T, N, S0, S_out, y, status, s);
+        case 256: return attend<256>(l, v, BH, T, N, S0, S_out, y, status, s);
     }
     set_error("d_v=%d unsupported", dv);
     return OPAM_ERR_UNSUPPORTED;
@@ -672,13 +767,13 @@ size_t sparse_workspace(int BH, int T, int N, int dv, bool need_state) {
 }
 
 int sparse_forward(const float *q, const float *k, const float *v, int B, int H, int T, int N, int dv,
-                   const float *S0, float *S_out, float *y, void *ws, cudaStream_t s) {
+                   const float *S0, float *S_out, float *y, void *ws, unsigned int *status, cudaStream_t s) {
     const int BH = B * H;
     switch (dv) {
-        case 32: return launch<32>(q, k, v, BH, T, N, S0, S_out, y, ws, s);
-        case 64: return launch<64>(q, k, v, BH, T, N, S0, S_out, y, ws, s);
-        case 128: return launch<128>(q, k, v, BH, T, N, S0, S_out, y, ws, s);
-        case 256: return launch<256>(q, k, v, BH, T, N, S0, S_out, y, ws, s);
+        case 32: return launch<32>(q, k, v, BH, T, N, S0, S_out, y, ws, status, s);
+        case 64: return launch<64>(q, k, v, BH, T, N, S0, S_out, y, ws, status, s);
+        case 128: return launch<128>(q, k, v, BH, T, N, S0, S_out, y, ws, status, s);
+        case 256: return launch<256>(q, k, v, BH, T, N, S0, S_out, y, ws, status, s);
     }
     set_error("d_v=%d unsupported", dv);
     return OPAM_ERR_UNSUPPORTED;

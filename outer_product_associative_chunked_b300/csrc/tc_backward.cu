@@ -88,17 +88,91 @@ __device__ __forceinline__ void zero(float (&acc)[TM][TN]) {
 }
 
 // Rows r0 .. r0+63 of a [rows][d] tensor into shared [64][lds] as fp32,
-// columns c0 .. c0+w-1, times `mul`; rows outside [lo, hi) read as zero.
-template <typename T>
-__device__ void load_rows(float *s, int lds, const T *g, int d, int r0, int lo, int hi, int c0, int w,
-                          float mul = 1.f) {
-    for (int idx = threadIdx.x; idx < kR * w; idx += kThr) {
-        const int r = idx / w, c = idx - r * w, gr = r0 + r;
-        float x = 0.f;
-        if (gr >= lo && gr < hi) x = Elem<T>::load(g + (size_t)gr * d + c0 + c) * mul;
-        s[r * lds + c] = x;
+// columns c0 .. c0+WC-1, times `mul`; rows outside [lo, hi) read as zero.
+// Global reads are 16-byte vectors (8 bf16 or 4 fp32); d, c0 and WC are
+// multiples of the vector length, and the tensors are 16-byte aligned.
+template <typename T> struct Vec16;
+template <> struct Vec16<float> {
+    static constexpr int N = 4;
+    static __device__ __forceinline__ void load(const float *p, float (&x)[4]) {
+        const float4 v = *reinterpret_cast<const float4 *>(p);
+        x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+    }
+};
+template <> struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    static __device__ __forceinline__ void load(const __nv_bfloat16 *p, float (&x)[8]) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(p);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+template <typename T, int WC>
+__device__ __forceinline__ void load_rows(float *s, int lds, const T *g, int d, int r0, int lo, int hi, int c0,
+                                          float mul = 1.f) {
+    constexpr int V = Vec16<T>::N, VPR = WC / V;
+    static_assert(WC % V == 0, "row width must be a whole number of vectors");
+    for (int idx = threadIdx.x; idx < kR * VPR; idx += kThr) {
+        const int r = idx / VPR, cv = (idx % VPR) * V, gr = r0 + r;
+        float x[V];
+        if (gr >= lo && gr < hi) {
+            Vec16<T>::load(g + (size_t)gr * d + c0 + cv, x);
+        } else {
+#pragma unroll
+            for (int e = 0; e < V; ++e) x[e] = 0.f;
+        }
+#pragma unroll
+        for (int e = 0; e < V; ++e) s[r * lds + cv + e] = x[e] * mul;
     }
 }
+
+// The same tile in two steps, so that the global loads of the next tile can
+// be in flight while the current one is used: fetch() issues the 16-byte
+// loads into registers, commit() widens them into shared memory.
+template <typename T, int WC>
+struct TileFetch {
+    static constexpr int V = Vec16<T>::N, VPR = WC / V, NV = (kR * VPR + kThr - 1) / kThr;
+    uint4 raw[NV];
+    __device__ __forceinline__ void fetch(const T *g, int d, int r0, int lo, int hi, int c0) {
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int idx = threadIdx.x + kThr * u;
+            const int r = idx / VPR, cv = (idx % VPR) * V, gr = r0 + r;
+            raw[u] = (idx < kR * VPR && gr >= lo && gr < hi)
+                         ? *reinterpret_cast<const uint4 *>(g + (size_t)gr * d + c0 + cv)
+                         : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    __device__ __forceinline__ void commit(float *s, int lds, float mul = 1.f) const {
+#pragma unroll
+        for (int u = 0; u < NV; ++u) {
+            const int idx = threadIdx.x + kThr * u;
+            if (idx >= kR * VPR) continue;
+            const int r = idx / VPR, cv = (idx % VPR) * V;
+            float x[V];
+            if constexpr (V == 8) {
+                const uint32_t w[4] = {raw[u].x, raw[u].y, raw[u].z, raw[u].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    x[2 * i] = __uint_as_float(w[i] << 16);
+                    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+                }
+            } else {
+                x[0] = __uint_as_float(raw[u].x);
+                x[1] = __uint_as_float(raw[u].y);
+                x[2] = __uint_as_float(raw[u].z);
+                x[3] = __uint_as_float(raw[u].w);
+            }
+#pragma unroll
+            for (int e = 0; e < V; ++e) s[r * lds + cv + e] = x[e] * mul;
+        }
+    }
+};
 
 __device__ __forceinline__ float block_sum(float x, float *red) {
     x = warp_sum(x);
@@ -124,7 +198,7 @@ template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThr)
 tcb_window_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                      const T *__restrict__ dy, int Tn, int W, float scale, float *__restrict__ lse_g,
-                     float *__restrict__ D_g, float *__restrict__ dQacc) {
+                     float *__restrict__ D_g, float *__restrict__ dQacc, unsigned int *__restrict__ status) {
     using C = WinCfg<DK, DV>;
     constexpr int LQ = C::LQ, LV = C::LV, TNV = DV / 16, TNK = DK / 16;
     extern __shared__ float sm[];
@@ -134,8 +208,8 @@ tcb_window_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *
     const int bh = blockIdx.y, q0 = blockIdx.x * kR;
     const T *qh = q + (size_t)bh * Tn * DK, *kh = k + (size_t)bh * Tn * DK;
     const T *vh = v + (size_t)bh * Tn * DV, *dyh = dy + (size_t)bh * Tn * DV;
-    load_rows(Qs, LQ, qh, DK, q0, 0, Tn, 0, DK);
-    load_rows(dYs, LV, dyh, DV, q0, 0, Tn, 0, DV);
+    load_rows<T, DK>(Qs, LQ, qh, DK, q0, 0, Tn, 0);
+    load_rows<T, DV>(dYs, LV, dyh, DV, q0, 0, Tn, 0);
     if (tid < kR) {
         rm[tid] = kNegBig;
         rl[tid] = 0.f;
@@ -149,8 +223,8 @@ tcb_window_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *
     for (int kt = kt0; kt <= kt1; ++kt) {
         const int k0 = kt * kR;
         __syncthreads();
-        load_rows(Ks, LQ, kh, DK, k0, 0, Tn, 0, DK);
-        load_rows(Vs, LV, vh, DV, k0, 0, Tn, 0, DV);
+        load_rows<T, DK>(Ks, LQ, kh, DK, k0, 0, Tn, 0);
+        load_rows<T, DV>(Vs, LV, vh, DV, k0, 0, Tn, 0);
         __syncthreads();
         float S[4][4];
         zero(S);
@@ -213,9 +287,10 @@ tcb_window_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *
             const float ls = l > 0.f ? rm[r] + __logf(l) : 0.f;
             rD[r] = d;
             rf[r] = ls;
-            if (q0 + r < Tn) {
-                lse_g[(size_t)bh * Tn + q0 + r] = ls;
-                D_g[(size_t)bh * Tn + q0 + r] = d;
+            const size_t at = (size_t)bh * Tn + q0 + r;
+            if (q0 + r < Tn && OPAM_BOUNDS(at < (size_t)gridDim.y * Tn, status)) {
+                lse_g[at] = ls;
+                D_g[at] = d;
             }
         }
     }
@@ -225,8 +300,8 @@ tcb_window_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *
     for (int kt = kt0; kt <= kt1; ++kt) {
         const int k0 = kt * kR;
         __syncthreads();
-        load_rows(Ks, LQ, kh, DK, k0, 0, Tn, 0, DK);
-        load_rows(Vs, LV, vh, DV, k0, 0, Tn, 0, DV);
+        load_rows<T, DK>(Ks, LQ, kh, DK, k0, 0, Tn, 0);
+        load_rows<T, DV>(Vs, LV, vh, DV, k0, 0, Tn, 0);
         __syncthreads();
         float S[4][4], dP[4][4];
         zero(S);
@@ -249,7 +324,10 @@ tcb_window_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *
         const int t = q0 + ty + 16 * i;
         if (t >= Tn) continue;
 #pragma unroll
-        for (int j = 0; j < TNK; ++j) dQacc[((size_t)bh * Tn + t) * DK + tx + 16 * j] = scale * dQ[i][j];
+        for (int j = 0; j < TNK; ++j) {
+            const size_t at = ((size_t)bh * Tn + t) * DK + tx + 16 * j;
+            if (OPAM_BOUNDS(at < (size_t)gridDim.y * Tn * DK, status)) dQacc[at] = scale * dQ[i][j];
+        }
     }
 }
 
@@ -258,7 +336,8 @@ template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThr)
 tcb_window_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                        const T *__restrict__ dy, int Tn, int W, float scale, const float *__restrict__ lse_g,
-                       const float *__restrict__ D_g, float *__restrict__ dKacc, float *__restrict__ dVacc) {
+                       const float *__restrict__ D_g, float *__restrict__ dKacc, float *__restrict__ dVacc,
+                       unsigned int *__restrict__ status) {
     using C = WinCfg<DK, DV>;
     constexpr int LQ = C::LQ, LV = C::LV, TNV = DV / 16, TNK = DK / 16;
     extern __shared__ float sm[];
@@ -268,8 +347,8 @@ tcb_window_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
     const int bh = blockIdx.y, k0 = blockIdx.x * kR;
     const T *qh = q + (size_t)bh * Tn * DK, *kh = k + (size_t)bh * Tn * DK;
     const T *vh = v + (size_t)bh * Tn * DV, *dyh = dy + (size_t)bh * Tn * DV;
-    load_rows(Ks, LQ, kh, DK, k0, 0, Tn, 0, DK);
-    load_rows(Vs, LV, vh, DV, k0, 0, Tn, 0, DV);
+    load_rows<T, DK>(Ks, LQ, kh, DK, k0, 0, Tn, 0);
+    load_rows<T, DV>(Vs, LV, vh, DV, k0, 0, Tn, 0);
     const int t_hi = min(Tn - 1, k0 + kR - 1 + W - 1);
     const int qt0 = k0 / kR, qt1 = t_hi / kR;
     float dK[4][TNK], dV[4][TNV];
@@ -278,8 +357,8 @@ tcb_window_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
     for (int qt = qt0; qt <= qt1; ++qt) {
         const int t0 = qt * kR;
         __syncthreads();
-        load_rows(Qs, LQ, qh, DK, t0, 0, Tn, 0, DK);
-        load_rows(dYs, LV, dyh, DV, t0, 0, Tn, 0, DV);
+        load_rows<T, DK>(Qs, LQ, qh, DK, t0, 0, Tn, 0);
+        load_rows<T, DV>(dYs, LV, dyh, DV, t0, 0, Tn, 0);
         if (tid < kR) {
             const bool ok = t0 + tid < Tn;
             rL[tid] = ok ? lse_g[(size_t)bh * Tn + t0 + tid] : 0.f;
@@ -317,9 +396,15 @@ tcb_window_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
         const int s = k0 + ty + 16 * i;
         if (s >= Tn) continue;
 #pragma unroll
-        for (int j = 0; j < TNK; ++j) dKacc[((size_t)bh * Tn + s) * DK + tx + 16 * j] = scale * dK[i][j];
+        for (int j = 0; j < TNK; ++j) {
+            const size_t at = ((size_t)bh * Tn + s) * DK + tx + 16 * j;
+            if (OPAM_BOUNDS(at < (size_t)gridDim.y * Tn * DK, status)) dKacc[at] = scale * dK[i][j];
+        }
 #pragma unroll
-        for (int j = 0; j < TNV; ++j) dVacc[((size_t)bh * Tn + s) * DV + tx + 16 * j] = dV[i][j];
+        for (int j = 0; j < TNV; ++j) {
+            const size_t at = ((size_t)bh * Tn + s) * DV + tx + 16 * j;
+            if (OPAM_BOUNDS(at < (size_t)gridDim.y * Tn * DV, status)) dVacc[at] = dV[i][j];
+        }
     }
 }
 
@@ -344,7 +429,8 @@ __global__ void __launch_bounds__(kThr)
 tcb_l2_intra_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                     const T *__restrict__ dy, int Tn, int W, int H, const float *__restrict__ lam,
                     const float *__restrict__ eta, const float *__restrict__ gate, float *__restrict__ dQacc,
-                    float *__restrict__ dKacc, float *__restrict__ dVacc, float *__restrict__ part) {
+                    float *__restrict__ dKacc, float *__restrict__ dVacc, float *__restrict__ part,
+                    unsigned int *__restrict__ status) {
     using C = IntraCfg<DK, DV>;
     constexpr int LQ = C::LQ, LV = C::LV, TNV = DV / 16, TNK = DK / 16;
     extern __shared__ float sm[];
@@ -356,10 +442,10 @@ tcb_l2_intra_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
     const T *qh = q + (size_t)bh * Tn * DK, *kh = k + (size_t)bh * Tn * DK;
     const T *vh = v + (size_t)bh * Tn * DV, *dyh = dy + (size_t)bh * Tn * DV;
     // positions u = u0 + r < Tn; the evicted token is u - W (valid when >= 0)
-    load_rows(Qs, LQ, qh, DK, u0, 0, Tn, 0, DK);
-    load_rows(dMs, LV, dyh, DV, u0, 0, Tn, 0, DV, sg);
-    load_rows(Kp, LQ, kh, DK, u0 - W, 0, Tn - W, 0, DK);
-    load_rows(Vp, LV, vh, DV, u0 - W, 0, Tn - W, 0, DV);
+    load_rows<T, DK>(Qs, LQ, qh, DK, u0, 0, Tn, 0);
+    load_rows<T, DV>(dMs, LV, dyh, DV, u0, 0, Tn, 0, sg);
+    load_rows<T, DK>(Kp, LQ, kh, DK, u0 - W, 0, Tn - W, 0);
+    load_rows<T, DV>(Vp, LV, vh, DV, u0 - W, 0, Tn - W, 0);
     power_tables(pw, dpw, lm);
     __syncthreads();
     float S1[4][4], S2[4][4];
@@ -396,10 +482,16 @@ tcb_l2_intra_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
             const int r = ty + 16 * i, u = u0 + r;
             if (u >= Tn) continue;
 #pragma unroll
-            for (int j = 0; j < TNK; ++j) dQacc[((size_t)bh * Tn + u) * DK + tx + 16 * j] += a[i][j];
+            for (int j = 0; j < TNK; ++j) {
+                const size_t at = ((size_t)bh * Tn + u) * DK + tx + 16 * j;
+                if (OPAM_BOUNDS(at < (size_t)gridDim.y * Tn * DK, status)) dQacc[at] += a[i][j];
+            }
             if (u - W >= 0)
 #pragma unroll
-                for (int j = 0; j < TNK; ++j) dKacc[((size_t)bh * Tn + u - W) * DK + tx + 16 * j] += b[i][j];
+                for (int j = 0; j < TNK; ++j) {
+                    const size_t at = ((size_t)bh * Tn + u - W) * DK + tx + 16 * j;
+                    if (OPAM_BOUNDS(at < (size_t)gridDim.y * Tn * DK, status)) dKacc[at] += b[i][j];
+                }
         }
     }
     __syncthreads();
@@ -422,7 +514,10 @@ tcb_l2_intra_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
             for (int j = 0; j < TNV; ++j) sdm = fmaf(dMs[r * LV + tx + 16 * j], b[i][j], sdm);
             if (u >= Tn || u - W < 0) continue;
 #pragma unroll
-            for (int j = 0; j < TNV; ++j) dVacc[((size_t)bh * Tn + u - W) * DV + tx + 16 * j] += a[i][j];
+            for (int j = 0; j < TNV; ++j) {
+                const size_t at = ((size_t)bh * Tn + u - W) * DV + tx + 16 * j;
+                if (OPAM_BOUNDS(at < (size_t)gridDim.y * Tn * DV, status)) dVacc[at] += a[i][j];
+            }
         }
     }
     const float s0 = block_sum(g_lam, red);
@@ -451,7 +546,7 @@ tcb_l2_scan_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
                    const T *__restrict__ dy, int Tn, int W, int H, const float *__restrict__ lam,
                    const float *__restrict__ eta, const float *__restrict__ gate, float *__restrict__ dQacc,
                    float *__restrict__ dKacc, float *__restrict__ dVacc, float *__restrict__ part_f,
-                   float *__restrict__ part_r) {
+                   float *__restrict__ part_r, unsigned int *__restrict__ status) {
     using C = ScanCfg<DK>;
     constexpr int LQ = C::LQ, LW = C::LW, TNK = DK / 16, TMK = DK / 16;
     constexpr int NSL = DV / kSW;
@@ -469,14 +564,26 @@ tcb_l2_scan_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
     power_tables(pw, dpw, lm);
     for (int i = tid; i < 2 * DK * LW; i += kThr) St[i] = 0.f;  // St, St2 contiguous
     float g0 = 0.f, g1 = 0.f;
+    // the next chunk's tiles are fetched into registers while this one is used
+    TileFetch<T, DK> fq, fk;
+    TileFetch<T, kSW> fm, fv;
+    auto fetch = [&](int step) {
+        const int c = reverse ? nch - 1 - step : step, u0 = c * kR;
+        fq.fetch(qh, DK, u0, 0, Tn, 0);
+        fm.fetch(dyh, DV, u0, 0, Tn, b0);
+        fk.fetch(kh, DK, u0 - W, 0, Tn - W, 0);
+        fv.fetch(vh, DV, u0 - W, 0, Tn - W, b0);
+    };
+    fetch(0);
     for (int step = 0; step < nch; ++step) {
         const int c = reverse ? nch - 1 - step : step, u0 = c * kR, n = min(kR, Tn - u0);
         __syncthreads();
-        load_rows(Qs, LQ, qh, DK, u0, 0, Tn, 0, DK);
-        load_rows(dMs, LW, dyh, DV, u0, 0, Tn, b0, kSW, sg);
-        load_rows(Kp, LQ, kh, DK, u0 - W, 0, Tn - W, 0, DK);
-        load_rows(Vp, LW, vh, DV, u0 - W, 0, Tn - W, b0, kSW);
+        fq.commit(Qs, LQ);
+        fm.commit(dMs, LW, sg);
+        fk.commit(Kp, LQ);
+        fv.commit(Vp, LW);
         __syncthreads();
+        if (step + 1 < nch) fetch(step + 1);
         if (!reverse) {
             // X = Q A_c, X' = Q A'_c on this slice; dq += lambda^(i+1) dM A_c^T
             float X[4][1], Xp[4][1], dq[4][TNK];
@@ -494,8 +601,11 @@ tcb_l2_scan_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
                 g0 = fmaf(dpw[r + 1] * X[i][0] + pw[r + 1] * Xp[i][0], dm, g0);             // dlambda
                 if (u < Tn)
 #pragma unroll
-                    for (int j = 0; j < TNK; ++j)
-                        atomicAdd(&dQacc[((size_t)bh * Tn + u) * DK + tx + 16 * j], pw[r + 1] * dq[i][j]);
+                    for (int j = 0; j < TNK; ++j) {
+                        const size_t at = ((size_t)bh * Tn + u) * DK + tx + 16 * j;
+                        if (OPAM_BOUNDS(at < (size_t)gridDim.y * Tn * DK, status))
+                            atomicAdd(&dQacc[at], pw[r + 1] * dq[i][j]);
+                    }
             }
             // weighted V' rows for the state update
             for (int idx = tid; idx < kR * kSW; idx += kThr) {
@@ -532,9 +642,12 @@ tcb_l2_scan_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
                 g0 = fmaf(f * dvv[i][0], Vp[j * LW + tx], g0);                               // deta
                 if (u >= Tn || u - W < 0) continue;
 #pragma unroll
-                for (int jj = 0; jj < TNK; ++jj)
-                    atomicAdd(&dKacc[((size_t)bh * Tn + u - W) * DK + tx + 16 * jj], et * f * dk[i][jj]);
-                dVacc[((size_t)bh * Tn + u - W) * DV + b0 + tx] += et * f * dvv[i][0];
+                for (int jj = 0; jj < TNK; ++jj) {
+                    const size_t at = ((size_t)bh * Tn + u - W) * DK + tx + 16 * jj;
+                    if (OPAM_BOUNDS(at < (size_t)gridDim.y * Tn * DK, status)) atomicAdd(&dKacc[at], et * f * dk[i][jj]);
+                }
+                const size_t av = ((size_t)bh * Tn + u - W) * DV + b0 + tx;
+                if (OPAM_BOUNDS(av < (size_t)gridDim.y * Tn * DV, status)) dVacc[av] += et * f * dvv[i][0];
             }
             // R <- lambda^n R + sum_i lambda^i q_i dm_i^T
             for (int idx = tid; idx < kR * kSW; idx += kThr) {
@@ -654,21 +767,22 @@ int run_bwd(const void *q, const void *k, const void *v, int B, int H, int Tn, i
         const int smem = (int)WinCfg<DK, DV>::SMEM;
         if ((rc = set_smem_limit((const void *)kern, smem, "tcb_window_dq smem attribute"))) return rc;
         prof_begin(s);
-        kern<<<dim3(nch, BH), kThr, smem, s>>>(Q, K, V, dY, Tn, W, scale, w.lse, w.D, w.dQ);
+        kern<<<dim3(nch, BH), kThr, smem, s>>>(Q, K, V, dY, Tn, W, scale, w.lse, w.D, w.dQ, status);
         if ((rc = launched("tcb_window_dq"))) return rc;
     }
     {
         auto kern = tcb_window_dkdv_kernel<T, DK, DV>;
         const int smem = (int)WinCfg<DK, DV>::SMEM;
         if ((rc = set_smem_limit((const void *)kern, smem, "tcb_window_dkdv smem attribute"))) return rc;
-        kern<<<dim3(nch, BH), kThr, smem, s>>>(Q, K, V, dY, Tn, W, scale, w.lse, w.D, w.dK, w.dV);
+        kern<<<dim3(nch, BH), kThr, smem, s>>>(Q, K, V, dY, Tn, W, scale, w.lse, w.D, w.dK, w.dV, status);
         if ((rc = launched("tcb_window_dkdv"))) return rc;
     }
     {
         auto kern = tcb_l2_intra_kernel<T, DK, DV>;
         const int smem = (int)IntraCfg<DK, DV>::SMEM;
         if ((rc = set_smem_limit((const void *)kern, smem, "tcb_l2_intra smem attribute"))) return rc;
-        kern<<<dim3(nch, BH), kThr, smem, s>>>(Q, K, V, dY, Tn, W, H, lam, eta, gate, w.dQ, w.dK, w.dV, w.part);
+        kern<<<dim3(nch, BH), kThr, smem, s>>>(Q, K, V, dY, Tn, W, H, lam, eta, gate, w.dQ, w.dK, w.dV, w.part,
+                                               status);
         if ((rc = launched("tcb_l2_intra"))) return rc;
     }
     {
@@ -676,7 +790,7 @@ int run_bwd(const void *q, const void *k, const void *v, int B, int H, int Tn, i
         const int smem = (int)ScanCfg<DK>::SMEM;
         if ((rc = set_smem_limit((const void *)kern, smem, "tcb_l2_scan smem attribute"))) return rc;
         kern<<<dim3(nsl, BH, 2), kThr, smem, s>>>(Q, K, V, dY, Tn, W, H, lam, eta, gate, w.dQ, w.dK, w.dV,
-                                                  w.part_f, w.part_r);
+                                                  w.part_f, w.part_r, status);
         if ((rc = launched("tcb_l2_scan"))) return rc;
     }
     {

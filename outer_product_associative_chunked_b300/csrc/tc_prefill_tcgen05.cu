@@ -232,6 +232,7 @@ tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
             return true;
         };
         auto emit = [&](int j) {  // A_j^loc as bf16, 128 contiguous bytes per row
+            if (!OPAM_BOUNDS(j < nch && r < DK, &B.st)) return;
             uint4 *dst = reinterpret_cast<uint4 *>(arow + (size_t)j * DK * DV);
 #pragma unroll
             for (int u = 0; u < 8; ++u)
@@ -270,7 +271,7 @@ tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         }
         if (ok && scan_row) {
             ok = absorb(nj - 1);
-            if (ok) {
+            if (ok && OPAM_BOUNDS(seg < nseg && slice * 64 + 64 <= DV, &B.st)) {
                 float4 *dst = reinterpret_cast<float4 *>(Lfin + (((size_t)bh * nseg + seg) * DK + r) * DV + slice * 64);
 #pragma unroll
                 for (int u = 0; u < 16; ++u) dst[u] = make_float4(A[4 * u], A[4 * u + 1], A[4 * u + 2], A[4 * u + 3]);
@@ -328,7 +329,7 @@ tc_l2_carry_kernel(const float *__restrict__ Lfin, int nseg, int L, int T, int d
             uint2 o;
             o.x = pack_bf16(A.x, A.y);
             o.y = pack_bf16(A.z, A.w);
-            *reinterpret_cast<uint2 *>(dst + (size_t)g * dkdv) = o;
+            if (OPAM_BOUNDS(e + 4 <= dkdv, status)) *reinterpret_cast<uint2 *>(dst + (size_t)g * dkdv) = o;
             // the last segment may be shorter: its decay only matters for A_final
             const float fg = (g + 1) * L * kBlk <= T ? f : powf(lm, (float)(T - g * L * kBlk));
             A.x = fmaf(fg, A.x, d[u].x);
@@ -337,7 +338,7 @@ tc_l2_carry_kernel(const float *__restrict__ Lfin, int nseg, int L, int T, int d
             A.w = fmaf(fg, A.w, d[u].w);
         }
     }
-    if (A_final) *reinterpret_cast<float4 *>(A_final + (size_t)bh * dkdv + e) = A;
+    if (A_final && OPAM_BOUNDS(e + 4 <= dkdv, status)) *reinterpret_cast<float4 *>(A_final + (size_t)bh * dkdv + e) = A;
 }
 
 // --------------------------------------------------------------------- fused forward
