@@ -106,6 +106,32 @@ __device__ __forceinline__ void warp_tile_mma(float (&d)[4], int lane, FA fa, FB
     }
 }
 
+// The same for two adjacent 16 x 8 tiles (output columns n and 8 + n of fb)
+// that share their A fragments.
+template <int K, class FA, class FB>
+__device__ __forceinline__ void warp_tile_mma2(float (&d0)[4], float (&d1)[4], int lane, FA fa, FB fb) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        const float av[4] = {fa(g, k0 + t), fa(g + 8, k0 + t), fa(g, k0 + t + 4), fa(g + 8, k0 + t + 4)};
+        const float bv[4] = {fb(k0 + t, g), fb(k0 + t + 4, g), fb(k0 + t, 8 + g), fb(k0 + t + 4, 8 + g)};
+        uint32_t ah[4], al[4], bh[4], bl[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            split_tf32(av[e], ah[e], al[e]);
+            split_tf32(bv[e], bh[e], bl[e]);
+        }
+        const uint32_t bh0[2] = {bh[0], bh[1]}, bl0[2] = {bl[0], bl[1]};
+        const uint32_t bh1[2] = {bh[2], bh[3]}, bl1[2] = {bl[2], bl[3]};
+        mma_tf32(d0, al, bh0);
+        mma_tf32(d1, al, bh1);
+        mma_tf32(d0, ah, bl0);
+        mma_tf32(d1, ah, bl1);
+        mma_tf32(d0, ah, bh0);
+        mma_tf32(d1, ah, bh1);
+    }
+}
+
 // T = (I + Lb)^{-1} for the strictly lower 64 x 64 Lb held in shared memory
 // (fp32, swizzled rows), computed in place by the 128 chunk-local threads:
 // on return the tile holds the strictly lower part of T (T is unit lower
@@ -181,36 +207,36 @@ __device__ __forceinline__ void unit_lower_inverse(float *__restrict__ S, float 
     // ---- 3. warp w: rows 32 + 16 (w / 2).., output columns 16 (w % 2) + {0, 8}
     {
         constexpr int XS = 40;  // padded row stride of the 32 x 32 scratch
-        const int m0 = (warp >> 1) * 16;
+        const int m0 = (warp >> 1) * 16, n0 = (warp & 1) * 16;
         float d[2][4];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int n0 = (warp & 1) * 16 + 8 * h;
-            d[h][0] = at(32 + m0 + g, n0 + 2 * t);
-            d[h][1] = at(32 + m0 + g, n0 + 2 * t + 1);
-            d[h][2] = at(32 + m0 + g + 8, n0 + 2 * t);
-            d[h][3] = at(32 + m0 + g + 8, n0 + 2 * t + 1);
-            warp_tile_mma<32>(d[h], lane, [&](int r, int k) { return at(32 + m0 + r, k); },
-                              [&](int k, int n) { return at(k, n0 + n); });
+        for (int h = 0; h < 2; ++h) {  // L T_(0,0): the identity's share
+            d[h][0] = at(32 + m0 + g, n0 + 8 * h + 2 * t);
+            d[h][1] = at(32 + m0 + g, n0 + 8 * h + 2 * t + 1);
+            d[h][2] = at(32 + m0 + g + 8, n0 + 8 * h + 2 * t);
+            d[h][3] = at(32 + m0 + g + 8, n0 + 8 * h + 2 * t + 1);
         }
+        warp_tile_mma2<32>(d[0], d[1], lane, [&](int r, int k) { return at(32 + m0 + r, k); },
+                           [&](int k, int n) { return at(k, n0 + n); });
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int n0 = (warp & 1) * 16 + 8 * h;
-            X[(m0 + g) * XS + n0 + 2 * t] = d[h][0];
-            X[(m0 + g) * XS + n0 + 2 * t + 1] = d[h][1];
-            X[(m0 + g + 8) * XS + n0 + 2 * t] = d[h][2];
-            X[(m0 + g + 8) * XS + n0 + 2 * t + 1] = d[h][3];
+            const int nc = n0 + 8 * h;
+            X[(m0 + g) * XS + nc + 2 * t] = d[h][0];
+            X[(m0 + g) * XS + nc + 2 * t + 1] = d[h][1];
+            X[(m0 + g + 8) * XS + nc + 2 * t] = d[h][2];
+            X[(m0 + g + 8) * XS + nc + 2 * t + 1] = d[h][3];
         }
         prep_sync(bar);
+        // T_(1,1) X: the identity's share is X itself (already in d)
+        warp_tile_mma2<32>(d[0], d[1], lane, [&](int r, int k) { return at(32 + m0 + r, 32 + k); },
+                           [&](int k, int n) { return X[k * XS + n0 + n]; });
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int n0 = (warp & 1) * 16 + 8 * h;
-            warp_tile_mma<32>(d[h], lane, [&](int r, int k) { return at(32 + m0 + r, 32 + k); },
-                              [&](int k, int n) { return X[k * XS + n0 + n]; });
-            at(32 + m0 + g, n0 + 2 * t) = -d[h][0];
-            at(32 + m0 + g, n0 + 2 * t + 1) = -d[h][1];
-            at(32 + m0 + g + 8, n0 + 2 * t) = -d[h][2];
-            at(32 + m0 + g + 8, n0 + 2 * t + 1) = -d[h][3];
+            const int nc = n0 + 8 * h;
+            at(32 + m0 + g, nc + 2 * t) = -d[h][0];
+            at(32 + m0 + g, nc + 2 * t + 1) = -d[h][1];
+            at(32 + m0 + g + 8, nc + 2 * t) = -d[h][2];
+            at(32 + m0 + g + 8, nc + 2 * t + 1) = -d[h][3];
         }
         prep_sync(bar);
     }
@@ -593,11 +619,13 @@ delta_fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             if (ok && c >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&B.pw_empty[g], ((c >> 1) - 1) & 1));
             tc_fence_after();
             if (ok) {
+                float vv[2][32];  // [Q; K] K^T row, both halves in flight at once
+                tmem_ld32(tm + lrow + C::COL_P + 64 * g, vv[0]);
+                tmem_ld32(tm + lrow + C::COL_P + 64 * g + 32, vv[1]);
+                tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {  // 32 columns of [Q; K] K^T at a time
-                    float v[32];
-                    tmem_ld32(tm + lrow + C::COL_P + 64 * g + 32 * h, v);
-                    tmem_wait_ld();
+                for (int h = 0; h < 2; ++h) {  // 32 columns at a time
+                    const float(&v)[32] = vv[h];
                     if (row < kC) {  // P row i = (Q K^T)[i][j] for j <= i
                         const int i = row;
 #pragma unroll
@@ -648,11 +676,13 @@ delta_fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             ok = __all_sync(0xffffffffu, mbar_wait(&B.w_full[g], (c >> 1) & 1));
             tc_fence_after();
             if (ok && row < DK) {  // row a of W^T = -(K^T G^T)[a]
+                float aa[2][32];
+                tmem_ld32(tm + lrow + C::COL_P + 64 * g, aa[0]);
+                tmem_ld32(tm + lrow + C::COL_P + 64 * g + 32, aa[1]);
+                tmem_wait_ld();
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    float a[32];
-                    tmem_ld32(tm + lrow + C::COL_P + 64 * g + 32 * h, a);
-                    tmem_wait_ld();
+                    const float(&a)[32] = aa[h];
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
                         st_shared_v4(wt + sw128_off(row, 4 * h + u), pack_bf16(-a[8 * u], -a[8 * u + 1]),

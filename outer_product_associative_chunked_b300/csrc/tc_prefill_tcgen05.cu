@@ -132,8 +132,17 @@ tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
     const int nseg = gridDim.y;
     const int j0 = seg * L, j1 = min(nch, j0 + L), nj = j1 - j0;
     const uint32_t s0 = smem_u32(sm);
-    if (warp == 5) tmem_alloc(&B.tbase, 128);
-    if (tid == 0) {
+    auto stage_k = [&](int s) { return s0 + s * (C::KBYTES + C::VBYTES); };
+    auto load_kv = [&](int i) {  // K' and the V' slice of local chunk i into stage i % NS
+        const int s = i % NS;
+        unsigned char *kd = sm + (stage_k(s) - s0);
+        const int kt = (j0 + i) * kBlk - W;
+        mbar_expect_tx(&B.kv_full[s], C::KBYTES + C::VBYTES);
+#pragma unroll
+        for (int b = 0; b < DK / 64; ++b) tma_load_3d(kd + b * 16384, &mk, &B.kv_full[s], 64 * b, kt, bh);
+        tma_load_3d(kd + C::KBYTES, &mv, &B.kv_full[s], 64 * slice, kt, bh);
+    };
+    if (warp == 4 && lane == 0) {  // barriers, then the first loads, before the CTA-wide sync
         for (int s = 0; s < NS; ++s) {
             mbar_init(&B.kv_full[s], 1);
             mbar_init(&B.scaled[s], 4);
@@ -145,29 +154,24 @@ tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
         }
         mbar_init(&B.drain, 1);
         mbar_fence_init();
-        B.st = 0u;
+        for (int i = 0; i < NS && i < nj; ++i) load_kv(i);
     }
+    if (warp == 5) tmem_alloc(&B.tbase, 128);
+    if (tid == 0) B.st = 0u;
     if (tid < kBlk) B.pw[tid] = eta[h] * powf(lam[h], (float)tid);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = B.tbase;
-    auto stage_k = [&](int s) { return s0 + s * (C::KBYTES + C::VBYTES); };
 
     if (warp == 4) {
         if (lane == 0) {
             bool ok = true;
-            int issued = 0;
-            for (int i = 0; i < nj && ok; ++i) {
-                const int s = i % NS;
-                if (i >= NS) ok = mbar_wait(&B.kv_empty[s], ((i / NS) - 1) & 1);
+            int issued = min(NS, nj);  // issued before the CTA-wide sync
+            for (int i = issued; i < nj && ok; ++i) {
+                ok = mbar_wait(&B.kv_empty[i % NS], ((i / NS) - 1) & 1);
                 if (!ok) break;
-                unsigned char *kd = sm + (stage_k(s) - s0);
-                const int kt = (j0 + i) * kBlk - W;
-                mbar_expect_tx(&B.kv_full[s], C::KBYTES + C::VBYTES);
-#pragma unroll
-                for (int b = 0; b < DK / 64; ++b) tma_load_3d(kd + b * 16384, &mk, &B.kv_full[s], 64 * b, kt, bh);
-                tma_load_3d(kd + C::KBYTES, &mv, &B.kv_full[s], 64 * slice, kt, bh);
+                load_kv(i);
                 ++issued;
             }
             if (!ok) atomicOr(&B.st, kStStateProducer);
