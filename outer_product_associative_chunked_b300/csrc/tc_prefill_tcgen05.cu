@@ -866,9 +866,10 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
         return;
     }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // Head-major grid: the first wave holds the early query blocks of every
-    // head, and those without an L2 part never wait for the state kernels.
-    const int jq = blockIdx.y, bh = blockIdx.x, h = bh % H;
+    // Head-major grid in descending query-block order: the late blocks of
+    // every head run first, and the early ones, which have no L2 part and
+    // fewer key tiles, fill the last wave.
+    const int jq = (int)gridDim.y - 1 - (int)blockIdx.y, bh = blockIdx.x, h = bh % H;
     const int seg = jq / L;
     const int t0 = jq * kBlk;
     const int kt0 = t0 - W;
