@@ -353,12 +353,18 @@ struct Fwd {
     static constexpr uint32_t VBYTES = kBlk * DV * 2;  // also holds the segment carry
     static constexpr uint32_t PHALF = kBlk * 64 * 2;   // P of one key half: 128 rows x 64 keys
     static constexpr uint32_t kBudget = 227 * 1024 - 3072;  // 3 KB kept for the barriers block
-    static constexpr int kStagesFit = (int)((kBudget - QBYTES - 4 * PHALF) / (KBYTES + VBYTES));
-    static constexpr int NST = kStagesFit > 4 ? 4 : kStagesFit;
-    static_assert(NST >= 2, "need two K/V stages");
+    // Three K slots and two V slots: a K slot is free once its S product has
+    // completed, so K tiles can be requested two softmax steps ahead; V is
+    // needed one step later than K.  P gets two slots per key half where they
+    // fit, else one (its writers compute the exponentials before they need it).
+    static constexpr int NSK = 3, NSV = 2;
+    static constexpr uint32_t KV_END = QBYTES + NSK * KBYTES + NSV * VBYTES;
+    static constexpr int PS = KV_END + 4 * PHALF <= kBudget ? 2 : 1;
+    static_assert(KV_END + 2 * PS * PHALF <= kBudget, "shared-memory budget");
     static constexpr uint32_t OFF_K = QBYTES;
-    static constexpr uint32_t OFF_P = QBYTES + NST * (KBYTES + VBYTES);
-    static constexpr uint32_t OFF_BARS = OFF_P + 4 * PHALF;
+    static constexpr uint32_t OFF_V = OFF_K + NSK * KBYTES;
+    static constexpr uint32_t OFF_P = KV_END;
+    static constexpr uint32_t OFF_BARS = OFF_P + 2 * PS * PHALF;
     // TMEM columns: S [0,128); O of key half 0 / 1; O2 (the L2 term).  q A_j
     // lands in the S columns after the last tile.
     static constexpr uint32_t COL_O0 = 128, COL_O1 = 128 + DV, COL_O2 = 128 + 2 * DV;
@@ -369,9 +375,9 @@ struct Fwd {
 
 struct FwdBars {
     uint64_t q_full;
-    uint64_t k_full[4], v_full[4], kv_empty[4];
+    uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];  // the K and V halves of a stage are freed apart
     uint64_t s_full, s_empty;
-    uint64_t p_full[2][2], p_empty[2][2];  // [key half][slot]
+    uint64_t p_full[2][2], p_empty[2][2];  // [key half][slot], PS slots used
     uint64_t c_ready, xe, o_done, drain;
     uint32_t tbase;
     float pw[kBlk];      // eta lambda^d, d = 0..127
@@ -395,7 +401,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
               const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y,
               unsigned int *__restrict__ status) {
     using C = Fwd<DK, DV>;
-    constexpr int NST = C::NST;
+    constexpr int NSK = C::NSK, NSV = C::NSV, PS = C::PS;
     // All shared memory is dynamic: with no static shared memory its base is
     // 1024-byte aligned, as the 128-byte-swizzle tiles require (checked).
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -418,10 +424,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     if (warp == 9) tmem_alloc(&B.tbase, 512);
     if (tid == 0) {
         mbar_init(&B.q_full, 1);
-        for (int s = 0; s < NST; ++s) {
+        for (int s = 0; s < NSK; ++s) {
             mbar_init(&B.k_full[s], 1);
+            mbar_init(&B.k_empty[s], 1);
+        }
+        for (int s = 0; s < NSV; ++s) {
             mbar_init(&B.v_full[s], 1);
-            mbar_init(&B.kv_empty[s], 1);
+            mbar_init(&B.v_empty[s], 1);
         }
         mbar_init(&B.s_full, 1);
         mbar_init(&B.s_empty, 8);
@@ -448,7 +457,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     if (warp == 8) {
         // ------------------------------------------------ TMA producer
         bool ok = true;
-        const int sA = ntiles % NST;  // stage of A_j^loc (K slot) and the carry (V slot)
+        const int sA = ntiles % NSK, sC = ntiles % NSV;  // slots of A_j^loc (K) and of the carry (V)
         if (lane == 0) {
             tma_prefetch_desc(&mq);
             tma_prefetch_desc(&mk);
@@ -456,31 +465,49 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             mbar_expect_tx(&B.q_full, C::QBYTES);
 #pragma unroll
             for (int b = 0; b < DK / 64; ++b) tma_load_3d(sm + b * 16384, &mq, &B.q_full, 64 * b, t0, bh);
-            const int nload = ntiles + (l2 ? 1 : 0);  // the last load is A_j^loc + carry
-            for (int n = 0; n < nload && ok; ++n) {
-                const int s = n % NST;
-                if (n >= NST) ok = mbar_wait(&B.kv_empty[s], ((n / NST) - 1) & 1);
-                if (!ok) break;
-                unsigned char *kd = sm + C::OFF_K + s * (C::KBYTES + C::VBYTES);
-                if (n < ntiles) {
-                    const int kt = kt0 + kBlk * (j_first + n);
-                    mbar_expect_tx(&B.k_full[s], C::KBYTES);
+            // A K slot is free once the S product of its previous tile has
+            // completed, a V slot once that tile's P V has.  K of tile n + 1 is
+            // requested before V of tile n, so each K tile lands well ahead of
+            // its S product.
+            auto kslot = [&](int n) { return sm + C::OFF_K + (n % NSK) * C::KBYTES; };
+            auto vslot = [&](int n) { return sm + C::OFF_V + (n % NSV) * C::VBYTES; };
+            auto load_k = [&](int n) -> bool {
+                const int s = n % NSK;
+                if (n >= NSK && !mbar_wait(&B.k_empty[s], ((n / NSK) - 1) & 1)) return false;
+                const int kt = kt0 + kBlk * (j_first + n);
+                mbar_expect_tx(&B.k_full[s], C::KBYTES);
 #pragma unroll
-                    for (int b = 0; b < DK / 64; ++b) tma_load_3d(kd + b * 16384, &mk, &B.k_full[s], 64 * b, kt, bh);
-                    mbar_expect_tx(&B.v_full[s], C::VBYTES);
+                for (int b = 0; b < DK / 64; ++b) tma_load_3d(kslot(n) + b * 16384, &mk, &B.k_full[s], 64 * b, kt, bh);
+                return true;
+            };
+            auto load_v = [&](int n) -> bool {
+                const int s = n % NSV;
+                if (n >= NSV && !mbar_wait(&B.v_empty[s], ((n / NSV) - 1) & 1)) return false;
+                const int kt = kt0 + kBlk * (j_first + n);
+                mbar_expect_tx(&B.v_full[s], C::VBYTES);
 #pragma unroll
-                    for (int b = 0; b < DV / 64; ++b)
-                        tma_load_3d(kd + C::KBYTES + b * 16384, &mv, &B.v_full[s], 64 * b, kt, bh);
-                } else {  // A_j^loc into the K slot, the segment carry into the V slot
-                    mbar_expect_tx(&B.k_full[s], 2 * DK * DV * 2);
+                for (int b = 0; b < DV / 64; ++b) tma_load_3d(vslot(n) + b * 16384, &mv, &B.v_full[s], 64 * b, kt, bh);
+                return true;
+            };
+            if (ntiles > 0) ok = load_k(0);
+            for (int n = 0; n < ntiles && ok; ++n) {
+                if (n + 1 < ntiles) ok = load_k(n + 1);
+                if (ok) ok = load_v(n);
+            }
+            if (ok && l2) {  // A_j^loc into K slot ntiles, the segment carry into V slot ntiles
+                const int n = ntiles;
+                if (n >= NSK) ok = mbar_wait(&B.k_empty[sA], ((n / NSK) - 1) & 1);
+                if (ok && n >= NSV) ok = mbar_wait(&B.v_empty[sC], ((n / NSV) - 1) & 1);
+                if (ok) {
+                    mbar_expect_tx(&B.k_full[sA], 2 * DK * DV * 2);
 #pragma unroll
                     for (int b = 0; b < DV / 64; ++b) {
-                        tma_load_3d(kd + b * (DK * 128), &ma, &B.k_full[s], 64 * b, 0, bh * nch + jq);
-                        tma_load_3d(kd + C::KBYTES + b * (DK * 128), &mc, &B.k_full[s], 64 * b, 0, bh * nseg + seg);
+                        tma_load_3d(kslot(n) + b * (DK * 128), &ma, &B.k_full[sA], 64 * b, 0, bh * nch + jq);
+                        tma_load_3d(vslot(n) + b * (DK * 128), &mc, &B.k_full[sA], 64 * b, 0, bh * nseg + seg);
                     }
                 }
             }
-            if (ok && l2) ok = mbar_wait(&B.k_full[sA], (ntiles / NST) & 1);
+            if (ok && l2) ok = mbar_wait(&B.k_full[sA], (ntiles / NSK) & 1);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok && l2) {
@@ -488,7 +515,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             // carry share one accumulator.
             const float c = powf(lam[h], (float)(kBlk * (jq - seg * L)));
             const __nv_bfloat162 c2 = __floats2bfloat162_rn(c, c);
-            const uint32_t base = sK0 + sA * (C::KBYTES + C::VBYTES) + C::KBYTES;
+            const uint32_t base = sQ + C::OFF_V + sC * C::VBYTES;
             for (int e = lane; e < DK * DV / 8; e += 32) {
                 uint32_t x[4];
                 ld_shared_v4(base + e * 16, x[0], x[1], x[2], x[3]);
@@ -514,25 +541,25 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             // Descriptors as a fixed upper half plus a lower half (address >> 4 |
             // leading offset), so each k step is one 32-bit add in the issue loop.
             constexpr uint32_t HI = sdesc_hi(1024);
-            constexpr uint32_t STG = (C::KBYTES + C::VBYTES) >> 4;  // one K/V stage, encoded
+            constexpr uint32_t KSTEP = C::KBYTES >> 4, VSTEP = C::VBYTES >> 4;  // one K / V slot, encoded
             const uint32_t q_lo = sdesc_lo(sQ, 16), k_lo = sdesc_lo(sK0, 16);
-            const uint32_t v_lo = sdesc_lo(sK0 + C::KBYTES, 16384), p_lo = sdesc_lo(sP0, 16);
+            const uint32_t v_lo = sdesc_lo(sQ + C::OFF_V, 16384), p_lo = sdesc_lo(sP0, 16);
             auto kofs = [](int k) { return (uint32_t)((k >> 2) * (16384 >> 4) + (k & 3) * 2); };  // K-major k step
             // P V products of processed tile n: per key half, O2 += P2 V' (tile 0)
             // then O_half += P V.
             auto pv = [&](int n) -> bool {
-                const int s = n % NST;
-                if (!mbar_wait(&B.v_full[s], (n / NST) & 1)) return false;
+                const int s = n % NSV;
+                if (!mbar_wait(&B.v_full[s], (n / NSV) & 1)) return false;
                 const int uses = (n == 0 && has_l2) ? 2 : 1;
                 for (int hh = 0; hh < 2; ++hh) {
                     for (int u = 0; u < uses; ++u) {
-                        const int slot = use[hh] & 1;
-                        if (!mbar_wait(&B.p_full[hh][slot], (use[hh] >> 1) & 1)) return false;
+                        const int slot = (int)(use[hh] % PS);
+                        if (!mbar_wait(&B.p_full[hh][slot], (use[hh] / PS) & 1)) return false;
                         tc_fence_after();
                         const bool l2 = (uses == 2 && u == 0);
                         const uint32_t dcol = l2 ? C::COL_O2 : (hh ? C::COL_O1 : C::COL_O0);
                         // V rows 64 hh + 16 k .. of stage s (MN-major B); P of key half hh, slot
-                        const uint32_t vb = v_lo + (uint32_t)s * STG + (uint32_t)hh * (8192 >> 4);
+                        const uint32_t vb = v_lo + (uint32_t)s * VSTEP + (uint32_t)hh * (8192 >> 4);
                         const uint32_t pb = p_lo + (uint32_t)(slot * 2 + hh) * (C::PHALF >> 4);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
@@ -543,32 +570,33 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                         ++use[hh];
                     }
                 }
-                mma_commit(&B.kv_empty[s]);
+                mma_commit(&B.v_empty[s]);
                 return true;
             };
             for (int n = 0; n < ntiles && ok; ++n) {
-                const int s = n % NST;
-                ok = mbar_wait(&B.k_full[s], (n / NST) & 1);
+                const int s = n % NSK;
+                ok = mbar_wait(&B.k_full[s], (n / NSK) & 1);
                 if (ok && n >= 1) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t kb = k_lo + (uint32_t)s * STG;
+                const uint32_t kb = k_lo + (uint32_t)s * KSTEP;
 #pragma unroll
                 for (int k = 0; k < DK / 16; ++k) mma_ss_h(tm, q_lo + kofs(k), HI, kb + kofs(k), HI, C::ID_S, k > 0 ? 1u : 0u);
                 mma_commit(&B.s_full);
+                mma_commit(&B.k_empty[s]);
                 if (n >= 1) ok = pv(n - 1);
             }
             if (ok) ok = pv(ntiles - 1);
             if (ok && !l2) mma_commit(&B.o_done);
             if (ok && l2) {  // q (A_j^loc + c A_{gL}) into the S columns
-                const int n = ntiles, s = n % NST;
-                ok = mbar_wait(&B.k_full[s], (n / NST) & 1);
+                const int n = ntiles, s = n % NSK;
+                ok = mbar_wait(&B.k_full[s], (n / NSK) & 1);
                 if (ok) ok = mbar_wait(&B.c_ready, 0);
                 if (ok) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
                 if (ok) {
                     tc_fence_after();
-                    const uint32_t aslot = sK0 + s * (C::KBYTES + C::VBYTES);
-                    const uint32_t a_lo = sdesc_lo(aslot, DK * 128), c_lo = sdesc_lo(aslot + C::KBYTES, DK * 128);
+                    const uint32_t a_lo = sdesc_lo(sK0 + s * C::KBYTES, DK * 128);
+                    const uint32_t c_lo = sdesc_lo(sQ + C::OFF_V + (n % NSV) * C::VBYTES, DK * 128);
 #pragma unroll
                     for (int k = 0; k < DK / 16; ++k)
                         mma_ss_h(tm, q_lo + kofs(k), HI, a_lo + k * (2048 >> 4), HI, C::ID_PV, k > 0 ? 1u : 0u);
@@ -598,7 +626,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         int last_o_use = -1;
         bool ok = true;
         auto wait_slot = [&](uint32_t u) -> bool {  // slot of use u is free again
-            return u < 2 || mbar_wait(&B.p_empty[half][u & 1], ((u - 2) >> 1) & 1);
+            return u < (uint32_t)PS || mbar_wait(&B.p_empty[half][u % PS], ((u / PS) - 1) & 1);
         };
         // 8 keys of row r into this half's P slot (128-byte-swizzle K-major).
         auto store8 = [&](uint32_t slot, int c, const float *p) {
@@ -650,10 +678,10 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                             p2[e] = (act && i >= lo && i <= r) ? B.pw[(r - i) & (kBlk - 1)] * s[32 * g + 8 * q + e]
                                                                : 0.f;
                         }
-                        store8(use & 1, 4 * g + q, p2);
+                        store8(use % PS, 4 * g + q, p2);
                     }
                 }
-                publish(use & 1);
+                publish(use % PS);
                 ++use;
             }
             // Softmax part: keys max(0, t-W+1) <= p <= t.  On edge tiles, 32-key
@@ -689,7 +717,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             if (__any_sync(0xffffffffu, grow) && last_o_use >= 0) {
                 // This half's O must hold every earlier P V product before it is rescaled.
                 const uint32_t u = (uint32_t)last_o_use;
-                ok = __all_sync(0xffffffffu, mbar_wait(&B.p_empty[half][u & 1], (u >> 1) & 1));
+                ok = __all_sync(0xffffffffu, mbar_wait(&B.p_empty[half][u % PS], (u / PS) & 1));
                 if (!ok) break;
                 tc_fence_after();
                 const float f = grow ? ex2(m - mx) : 1.f;
@@ -734,9 +762,9 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             ok = __all_sync(0xffffffffu, wait_slot(use));
             if (!ok) break;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) store8(use & 1, c, &s[8 * c]);
+            for (int c = 0; c < 8; ++c) store8(use % PS, c, &s[8 * c]);
             tc_fence_before();
-            publish(use & 1);
+            publish(use % PS);
             last_o_use = (int)use;
             ++use;
         }
