@@ -12,7 +12,8 @@
 //   dS <- dS - beta_t g k_t^T.
 //
 // One CTA per (batch, head); its d_v/8 warps each own 8 rows of S and of dS
-// in registers, a lane holding d_k/32 columns of each row, so every row
+// in registers, a lane holding d_k/32 columns of each row as pairs updated with
+// packed f32x2 FMAs (two FMAs per instruction), so every row
 // update is lane-local and every column sum over the warp's rows is too.  The
 // walk is sequential, so the time is the length of one warp's chain of
 // instructions per token: fewer rows per warp (more warps) shorten it.
@@ -28,9 +29,12 @@
 #include <math.h>
 
 #include "opam_internal.cuh"
+#include "sm100.cuh"
 
 namespace opam {
 namespace {
+
+using sm100::fma2;
 
 constexpr int kRows = 8;  // rows of S per warp
 
@@ -62,44 +66,60 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
                       T *__restrict__ dk, T *__restrict__ dv, float *__restrict__ dbeta, float *__restrict__ dS0,
                       unsigned int *__restrict__ status) {
     constexpr int CPL = DK / 32;          // columns per lane
+    constexpr int CP = (CPL + 1) / 2;     // column pairs per lane (packed f32x2 arithmetic)
     constexpr int NW = DV / kRows;        // warps
     __shared__ float red[2][NW][2 * DK + 1];
     const int tid = threadIdx.x, w = tid >> 5, lane = tid & 31, row = w * kRows + (lane & (kRows - 1));
     const int bh = blockIdx.x;
     const size_t tk = (size_t)bh * Tn * DK, tv = (size_t)bh * Tn * DV;
-    float S[kRows][CPL], dS[kRows][CPL];
+    // Columns of pair p: lane + 32 (2p) and lane + 32 (2p + 1); with an odd
+    // count the last pair's second half is a zero column that stays zero.
+    auto col = [&](int p, int h) { return lane + 32 * (2 * p + h); };
+    auto has = [&](int p, int h) { return 2 * p + h < CPL; };
+    float2 S[kRows][CP], dS[kRows][CP];
     // S stored key-major: S_{i,j} at [j * DV + i]
 #pragma unroll
     for (int i = 0; i < kRows; ++i)
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            const size_t at = (size_t)bh * DK * DV + (size_t)(lane + 32 * c) * DV + w * kRows + i;
-            S[i][c] = S0 ? S0[at] : 0.f;
-            dS[i][c] = dST ? dST[at] : 0.f;
+        for (int p = 0; p < CP; ++p) {
+            float sv[2], dv2[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const size_t at = (size_t)bh * DK * DV + (size_t)col(p, h) * DV + w * kRows + i;
+                sv[h] = (S0 && has(p, h)) ? S0[at] : 0.f;
+                dv2[h] = (dST && has(p, h)) ? dST[at] : 0.f;
+            }
+            S[i][p] = make_float2(sv[0], sv[1]);
+            dS[i][p] = make_float2(dv2[0], dv2[1]);
         }
+    auto load_pair = [&](const T *base, int p) {
+        return make_float2(Elem<T>::load(base + col(p, 0)), has(p, 1) ? Elem<T>::load(base + col(p, 1)) : 0.f);
+    };
     // ---- pass 1: forward, storing u_t.  The next token's inputs are loaded
     // while the current one is processed (the walk is sequential, so a load
     // issued at the top of its own step would expose the whole latency).
-    float kn[CPL], bn = 0.f, vn = 0.f;
+    float2 kn[CP];
+    float bn = 0.f, vn = 0.f;
     auto fetch1 = [&](int t) {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) kn[c] = Elem<T>::load(k + tk + (size_t)t * DK + lane + 32 * c);
+        for (int p = 0; p < CP; ++p) kn[p] = load_pair(k + tk + (size_t)t * DK, p);
         bn = beta[(size_t)bh * Tn + t];
         vn = Elem<T>::load(v + tv + (size_t)t * DV + row);
     };
     if (Tn > 0) fetch1(0);
     for (int t = 0; t < Tn; ++t) {
-        float kc[CPL], x[kRows];
+        float2 kc[CP];
+        float x[kRows];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) kc[c] = kn[c];
+        for (int p = 0; p < CP; ++p) kc[p] = kn[p];
         const float bt = bn, vr = vn;
         if (t + 1 < Tn) fetch1(t + 1);
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
-            float s = 0.f;
+            float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) s = fmaf(S[i][c], kc[c], s);
-            x[i] = s;
+            for (int p = 0; p < CP; ++p) s2 = fma2(S[i][p], kc[p], s2);
+            x[i] = s2.x + s2.y;
         }
         const float u = vr - transpose_reduce(x);
         if (lane < kRows && OPAM_BOUNDS(tv + (size_t)t * DV + row < (size_t)gridDim.x * Tn * DV, status))
@@ -107,17 +127,19 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             const float bu = bt * __shfl_sync(0xffffffffu, u, i);
+            const float2 bu2 = make_float2(bu, bu);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) S[i][c] = fmaf(bu, kc[c], S[i][c]);
+            for (int p = 0; p < CP; ++p) S[i][p] = fma2(bu2, kc[p], S[i][p]);
         }
     }
     // ---- pass 2: reverse (next token's inputs prefetched as in pass 1)
-    float qn[CPL], dn = 0.f, un = 0.f;
+    float2 qn[CP];
+    float dn = 0.f, un = 0.f;
     auto fetch2 = [&](int t) {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            qn[c] = Elem<T>::load(q + tk + (size_t)t * DK + lane + 32 * c);
-            kn[c] = Elem<T>::load(k + tk + (size_t)t * DK + lane + 32 * c);
+        for (int p = 0; p < CP; ++p) {
+            qn[p] = load_pair(q + tk + (size_t)t * DK, p);
+            kn[p] = load_pair(k + tk + (size_t)t * DK, p);
         }
         bn = beta[(size_t)bh * Tn + t];
         dn = Elem<T>::load(dy + tv + (size_t)t * DV + row);
@@ -126,13 +148,14 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
     __syncwarp();  // this lane's u stores of pass 1 precede its reloads
     if (Tn > 0) fetch2(Tn - 1);
     for (int t = Tn - 1; t >= 0; --t) {
-        float qc[CPL], kc[CPL], x[kRows], dqp[CPL], dkp[CPL];
+        float2 qc[CP], kc[CP], dqp[CP], dkp[CP];
+        float x[kRows];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            qc[c] = qn[c];
-            kc[c] = kn[c];
-            dqp[c] = 0.f;
-            dkp[c] = 0.f;
+        for (int p = 0; p < CP; ++p) {
+            qc[p] = qn[p];
+            kc[p] = kn[p];
+            dqp[p] = make_float2(0.f, 0.f);
+            dkp[p] = make_float2(0.f, 0.f);
         }
         const float bt = bn, dor = dn, ur = un;
         if (t > 0) fetch2(t - 1);
@@ -140,14 +163,15 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             const float di = __shfl_sync(0xffffffffu, dor, i);
-            float s = 0.f;
+            const float2 di2 = make_float2(di, di);
+            float2 s2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) {
-                dqp[c] = fmaf(S[i][c], di, dqp[c]);
-                dS[i][c] = fmaf(di, qc[c], dS[i][c]);
-                s = fmaf(dS[i][c], kc[c], s);
+            for (int p = 0; p < CP; ++p) {
+                dqp[p] = fma2(S[i][p], di2, dqp[p]);
+                dS[i][p] = fma2(di2, qc[p], dS[i][p]);
+                s2 = fma2(dS[i][p], kc[p], s2);
             }
-            x[i] = s;
+            x[i] = s2.x + s2.y;
         }
         const float g = transpose_reduce(x);
         const float du = bt * g;
@@ -161,18 +185,23 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
             const float ui = __shfl_sync(0xffffffffu, ur, i);
             const float dui = __shfl_sync(0xffffffffu, du, i);
             const float bu = bt * ui;
+            const float2 nbu2 = make_float2(-bu, -bu), bu2 = make_float2(bu, bu), ndu2 = make_float2(-dui, -dui);
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) {
-                S[i][c] = fmaf(-bu, kc[c], S[i][c]);
-                dkp[c] = fmaf(bu, dS[i][c], fmaf(-dui, S[i][c], dkp[c]));
-                dS[i][c] = fmaf(-dui, kc[c], dS[i][c]);
+            for (int p = 0; p < CP; ++p) {
+                S[i][p] = fma2(nbu2, kc[p], S[i][p]);
+                dkp[p] = fma2(bu2, dS[i][p], fma2(ndu2, S[i][p], dkp[p]));
+                dS[i][p] = fma2(ndu2, kc[p], dS[i][p]);
             }
         }
         float(*buf)[2 * DK + 1] = red[t & 1];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-            buf[w][lane + 32 * c] = dqp[c];
-            buf[w][DK + lane + 32 * c] = dkp[c];
+        for (int p = 0; p < CP; ++p) {
+            buf[w][col(p, 0)] = dqp[p].x;
+            buf[w][DK + col(p, 0)] = dkp[p].x;
+            if (has(p, 1)) {
+                buf[w][col(p, 1)] = dqp[p].y;
+                buf[w][DK + col(p, 1)] = dkp[p].y;
+            }
         }
         if (lane == 0) buf[w][2 * DK] = db;
         __syncthreads();
@@ -193,8 +222,10 @@ delta_backward_kernel(const T *__restrict__ q, const T *__restrict__ k, const T 
 #pragma unroll
         for (int i = 0; i < kRows; ++i)
 #pragma unroll
-            for (int c = 0; c < CPL; ++c)
-                dS0[(size_t)bh * DK * DV + (size_t)(lane + 32 * c) * DV + w * kRows + i] = dS[i][c];
+            for (int p = 0; p < CP; ++p) {
+                dS0[(size_t)bh * DK * DV + (size_t)col(p, 0) * DV + w * kRows + i] = dS[i][p].x;
+                if (has(p, 1)) dS0[(size_t)bh * DK * DV + (size_t)col(p, 1) * DV + w * kRows + i] = dS[i][p].y;
+            }
     }
     // nothing here waits on a barrier: the call's status words only need zeroing
     if (bh == 0 && tid < kStatusWords) status[tid] = 0u;
