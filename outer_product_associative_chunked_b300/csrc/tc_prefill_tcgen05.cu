@@ -378,22 +378,24 @@ struct FwdBars {
     uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];  // the K and V halves of a stage are freed apart
     uint64_t s_full, s_empty;
     uint64_t p_full[2][2], p_empty[2][2];  // [key half][slot], PS slots used
-    uint64_t c_ready, xe, o_done, drain;
+    uint64_t c_ready, xe, o_done, drain, drain_pv;  // o_done: one commit from each issuing thread
     uint32_t tbase;
     float pw[kBlk];      // eta lambda^d, d = 0..127
     float xm[2][kBlk];   // [key half][row] running maxima, exchanged once at the end
     float xl[2][kBlk];   // [key half][row] running sums
 };
 
-// 320 threads.  Warps 0-7 run the softmax: warp w owns rows 32 (w % 4) .. +31
+// 352 threads.  Warps 0-7 run the softmax: warp w owns rows 32 (w % 4) .. +31
 // (its TMEM lane quarter) and keys 64 (w / 4) .. +63 of every tile.  The two
 // key halves of a row keep separate running maxima, sums and P V accumulators
 // (O0, O1) and are merged once in the epilogue, so the softmax warps never
 // wait for each other inside the tile loop.  Warp 8 issues TMA loads and
-// scales the segment carry; warp 9 issues the MMAs and owns the TMEM
-// allocation.
+// scales the segment carry; warp 9 issues the S products (and the final
+// q A products) and owns the TMEM allocation; warp 10 issues the P V
+// products.  With two issuing threads the next tile's S does not queue
+// behind a P V that waits for the slowest softmax warp of the previous tile.
 template <int DK, int DV>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(352, 1)
 tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ma,
               const __grid_constant__ CUtensorMap mc, int T, int W, int H, int nch, int nseg, int L, int l2,
@@ -441,8 +443,9 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             }
         mbar_init(&B.c_ready, 1);
         mbar_init(&B.xe, 8);
-        mbar_init(&B.o_done, 1);
+        mbar_init(&B.o_done, 2);
         mbar_init(&B.drain, 1);
+        mbar_init(&B.drain_pv, 1);
         mbar_fence_init();
     }
     if (l2 && tid < kBlk) B.pw[tid] = eta[h] * powf(lam[h], (float)tid);
@@ -533,11 +536,10 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             atomicOr(status, kStFwdProducer);
         }
         __syncwarp();
-    } else if (warp == 9) {
-        // ------------------------------------------------ MMA issuer
+    } else if (warp == 9 || warp == 10) {
+        // ------------------------------------------------ MMA issue: S (warp 9), P V (warp 10)
         if (lane == 0) {
             bool ok = mbar_wait(&B.q_full, 0);
-            uint32_t use[2] = {0, 0};  // P-slot uses so far, per key half
             // Descriptors as a fixed upper half plus a lower half (address >> 4 |
             // leading offset), so each k step is one 32-bit add in the issue loop.
             constexpr uint32_t HI = sdesc_hi(1024);
@@ -545,71 +547,80 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             const uint32_t q_lo = sdesc_lo(sQ, 16), k_lo = sdesc_lo(sK0, 16);
             const uint32_t v_lo = sdesc_lo(sQ + C::OFF_V, 16384), p_lo = sdesc_lo(sP0, 16);
             auto kofs = [](int k) { return (uint32_t)((k >> 2) * (16384 >> 4) + (k & 3) * 2); };  // K-major k step
-            // P V products of processed tile n: per key half, O2 += P2 V' (tile 0)
-            // then O_half += P V.
-            auto pv = [&](int n) -> bool {
-                const int s = n % NSV;
-                if (!mbar_wait(&B.v_full[s], (n / NSV) & 1)) return false;
-                const int uses = (n == 0 && has_l2) ? 2 : 1;
-                for (int hh = 0; hh < 2; ++hh) {
-                    for (int u = 0; u < uses; ++u) {
-                        const int slot = (int)(use[hh] % PS);
-                        if (!mbar_wait(&B.p_full[hh][slot], (use[hh] / PS) & 1)) return false;
-                        tc_fence_after();
-                        const bool l2 = (uses == 2 && u == 0);
-                        const uint32_t dcol = l2 ? C::COL_O2 : (hh ? C::COL_O1 : C::COL_O0);
-                        // V rows 64 hh + 16 k .. of stage s (MN-major B); P of key half hh, slot
-                        const uint32_t vb = v_lo + (uint32_t)s * VSTEP + (uint32_t)hh * (8192 >> 4);
-                        const uint32_t pb = p_lo + (uint32_t)(slot * 2 + hh) * (C::PHALF >> 4);
+            if (warp == 10) {
+                // P V products of processed tile n: per key half, O2 += P2 V'
+                // (tile 0) then O_half += P V.
+                uint32_t use[2] = {0, 0};  // P-slot uses so far, per key half
+                for (int n = 0; n < ntiles && ok; ++n) {
+                    const int s = n % NSV;
+                    ok = mbar_wait(&B.v_full[s], (n / NSV) & 1);
+                    const int uses = (n == 0 && has_l2) ? 2 : 1;
+                    for (int hh = 0; hh < 2 && ok; ++hh) {
+                        for (int u = 0; u < uses && ok; ++u) {
+                            const int slot = (int)(use[hh] % PS);
+                            ok = mbar_wait(&B.p_full[hh][slot], (use[hh] / PS) & 1);
+                            if (!ok) break;
+                            tc_fence_after();
+                            const bool l2p = (uses == 2 && u == 0);
+                            const uint32_t dcol = l2p ? C::COL_O2 : (hh ? C::COL_O1 : C::COL_O0);
+                            // V rows 64 hh + 16 k .. of slot s (MN-major B); P of key half hh, slot
+                            const uint32_t vb = v_lo + (uint32_t)s * VSTEP + (uint32_t)hh * (8192 >> 4);
+                            const uint32_t pb = p_lo + (uint32_t)(slot * 2 + hh) * (C::PHALF >> 4);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const bool acc = l2 ? (hh > 0 || k > 0) : (n > 0 || k > 0);
-                            mma_ss_h(tm + dcol, pb + 2 * k, HI, vb + k * (2048 >> 4), HI, C::ID_PV, acc ? 1u : 0u);
+                            for (int k = 0; k < 4; ++k) {
+                                const bool acc = l2p ? (hh > 0 || k > 0) : (n > 0 || k > 0);
+                                mma_ss_h(tm + dcol, pb + 2 * k, HI, vb + k * (2048 >> 4), HI, C::ID_PV,
+                                         acc ? 1u : 0u);
+                            }
+                            mma_commit(&B.p_empty[hh][slot]);
+                            ++use[hh];
                         }
-                        mma_commit(&B.p_empty[hh][slot]);
-                        ++use[hh];
+                    }
+                    if (ok) mma_commit(&B.v_empty[s]);
+                }
+                if (ok) mma_commit(&B.o_done);
+                if (!ok) atomicOr(status, kStFwdMma);
+                // Every MMA issued by this thread has completed before TMEM is freed.
+                mma_commit(&B.drain_pv);
+                mbar_wait(&B.drain_pv, 0);
+            } else {
+                for (int n = 0; n < ntiles && ok; ++n) {
+                    const int s = n % NSK;
+                    ok = mbar_wait(&B.k_full[s], (n / NSK) & 1);
+                    if (ok && n >= 1) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t kb = k_lo + (uint32_t)s * KSTEP;
+#pragma unroll
+                    for (int k = 0; k < DK / 16; ++k)
+                        mma_ss_h(tm, q_lo + kofs(k), HI, kb + kofs(k), HI, C::ID_S, k > 0 ? 1u : 0u);
+                    mma_commit(&B.s_full);
+                    mma_commit(&B.k_empty[s]);
+                }
+                if (ok && !l2) mma_commit(&B.o_done);
+                if (ok && l2) {  // q (A_j^loc + c A_{gL}) into the S columns, once the last S has been read
+                    const int n = ntiles, s = n % NSK;
+                    ok = mbar_wait(&B.k_full[s], (n / NSK) & 1);
+                    if (ok) ok = mbar_wait(&B.c_ready, 0);
+                    if (ok) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
+                    if (ok) {
+                        tc_fence_after();
+                        const uint32_t a_lo = sdesc_lo(sK0 + s * C::KBYTES, DK * 128);
+                        const uint32_t c_lo = sdesc_lo(sQ + C::OFF_V + (n % NSV) * C::VBYTES, DK * 128);
+#pragma unroll
+                        for (int k = 0; k < DK / 16; ++k)
+                            mma_ss_h(tm, q_lo + kofs(k), HI, a_lo + k * (2048 >> 4), HI, C::ID_PV, k > 0 ? 1u : 0u);
+#pragma unroll
+                        for (int k = 0; k < DK / 16; ++k)
+                            mma_ss_h(tm, q_lo + kofs(k), HI, c_lo + k * (2048 >> 4), HI, C::ID_PV, 1u);
+                        mma_commit(&B.o_done);
                     }
                 }
-                mma_commit(&B.v_empty[s]);
-                return true;
-            };
-            for (int n = 0; n < ntiles && ok; ++n) {
-                const int s = n % NSK;
-                ok = mbar_wait(&B.k_full[s], (n / NSK) & 1);
-                if (ok && n >= 1) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
-                if (!ok) break;
-                tc_fence_after();
-                const uint32_t kb = k_lo + (uint32_t)s * KSTEP;
-#pragma unroll
-                for (int k = 0; k < DK / 16; ++k) mma_ss_h(tm, q_lo + kofs(k), HI, kb + kofs(k), HI, C::ID_S, k > 0 ? 1u : 0u);
-                mma_commit(&B.s_full);
-                mma_commit(&B.k_empty[s]);
-                if (n >= 1) ok = pv(n - 1);
+                if (!ok) atomicOr(status, kStFwdMma);
+                // Every MMA issued by this thread has completed before TMEM is freed.
+                mma_commit(&B.drain);
+                mbar_wait(&B.drain, 0);
             }
-            if (ok) ok = pv(ntiles - 1);
-            if (ok && !l2) mma_commit(&B.o_done);
-            if (ok && l2) {  // q (A_j^loc + c A_{gL}) into the S columns
-                const int n = ntiles, s = n % NSK;
-                ok = mbar_wait(&B.k_full[s], (n / NSK) & 1);
-                if (ok) ok = mbar_wait(&B.c_ready, 0);
-                if (ok) ok = mbar_wait(&B.s_empty, (n - 1) & 1);
-                if (ok) {
-                    tc_fence_after();
-                    const uint32_t a_lo = sdesc_lo(sK0 + s * C::KBYTES, DK * 128);
-                    const uint32_t c_lo = sdesc_lo(sQ + C::OFF_V + (n % NSV) * C::VBYTES, DK * 128);
-#pragma unroll
-                    for (int k = 0; k < DK / 16; ++k)
-                        mma_ss_h(tm, q_lo + kofs(k), HI, a_lo + k * (2048 >> 4), HI, C::ID_PV, k > 0 ? 1u : 0u);
-#pragma unroll
-                    for (int k = 0; k < DK / 16; ++k)
-                        mma_ss_h(tm, q_lo + kofs(k), HI, c_lo + k * (2048 >> 4), HI, C::ID_PV, 1u);
-                    mma_commit(&B.o_done);
-                }
-            }
-            if (!ok) atomicOr(status, kStFwdMma);
-            // Every MMA issued by this thread has completed before TMEM is freed.
-            mma_commit(&B.drain);
-            mbar_wait(&B.drain, 0);
         }
         __syncwarp();
     } else {
@@ -1409,7 +1420,7 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         const int smem = (int)(Cfg::OFF_BARS + sizeof(FwdBars));
         if (int rc_ = set_smem_limit((const void *)kern, smem, "tc_fwd smem attribute")) return rc_;
         prof_begin(st);
-        kern<<<dim3(g.nch, BH), 320, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, (int)l2, lam,
+        kern<<<dim3(g.nch, BH), 352, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, (int)l2, lam,
                                                   eta, gate, scale, (__nv_bfloat16 *)y, status + 1);
         rc = launched("tc_fwd");
         prof_end(st);
