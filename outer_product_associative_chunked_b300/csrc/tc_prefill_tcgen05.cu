@@ -351,24 +351,20 @@ struct Fwd {
     static constexpr uint32_t QBYTES = kBlk * DK * 2;
     static constexpr uint32_t KBYTES = kBlk * DK * 2;  // also holds A_j^loc (DK x DV bf16)
     static constexpr uint32_t VBYTES = kBlk * DV * 2;  // also holds the segment carry
-    static constexpr uint32_t PHALF = kBlk * 64 * 2;   // P of one key half: 128 rows x 64 keys
     static constexpr uint32_t kBudget = 227 * 1024 - 3072;  // 3 KB kept for the barriers block
-    // Three K slots and two V slots: a K slot is free once its S product has
-    // completed, so K tiles can be requested two softmax steps ahead; V is
-    // needed one step later than K.  P gets two slots per key half where they
-    // fit, else one (its writers compute the exponentials before they need it).
-    static constexpr int NSK = 3, NSV = 2;
-    static constexpr uint32_t KV_END = QBYTES + NSK * KBYTES + NSV * VBYTES;
-    static constexpr int PS = KV_END + 4 * PHALF <= kBudget ? 2 : 1;
-    static_assert(KV_END + 2 * PS * PHALF <= kBudget, "shared-memory budget");
+    // Three K slots and three V slots: a K slot is free once its S product
+    // has completed and a V slot once its P V has, so each tile is requested
+    // well before it is needed.  P lives in TMEM.
+    static constexpr int NSK = 3, NSV = 3;
     static constexpr uint32_t OFF_K = QBYTES;
     static constexpr uint32_t OFF_V = OFF_K + NSK * KBYTES;
-    static constexpr uint32_t OFF_P = KV_END;
-    static constexpr uint32_t OFF_BARS = OFF_P + 2 * PS * PHALF;
-    // TMEM columns: S [0,128); O of key half 0 / 1; O2 (the L2 term).  q A_j
-    // lands in the S columns after the last tile.
-    static constexpr uint32_t COL_O0 = 128, COL_O1 = 128 + DV, COL_O2 = 128 + 2 * DV;
-    static_assert(128 + 3 * DV <= 512, "TMEM columns");
+    static constexpr uint32_t OFF_BARS = OFF_V + NSV * VBYTES;
+    static_assert(OFF_BARS <= kBudget, "shared-memory budget");
+    // TMEM columns: S [0,128) (q A_j lands in [0,DV) after the last tile); O
+    // of key half 0 / 1; P of key half 0 / 1 (64 keys as packed bf16 pairs,
+    // 32 columns each), the A operand of O += P V.
+    static constexpr uint32_t COL_O0 = 128, COL_O1 = 128 + DV, COL_P = 128 + 2 * DV;
+    static_assert(COL_P + 64 <= 512, "TMEM columns");
     static constexpr uint32_t ID_S = idesc_bf16_f32(128, 128, false, false);
     static constexpr uint32_t ID_PV = idesc_bf16_f32(128, DV, false, true);
 };
@@ -377,7 +373,7 @@ struct FwdBars {
     uint64_t q_full;
     uint64_t k_full[4], v_full[4], k_empty[4], v_empty[4];  // the K and V halves of a stage are freed apart
     uint64_t s_full, s_empty;
-    uint64_t p_full[2][2], p_empty[2][2];  // [key half][slot], PS slots used
+    uint64_t p_full[2], p_empty[2];  // per key half
     uint64_t c_ready, xe, o_done, drain, drain_pv;  // o_done: one commit from each issuing thread
     uint32_t tbase;
     float pw[kBlk];      // eta lambda^d, d = 0..127
@@ -403,7 +399,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
               const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y,
               unsigned int *__restrict__ status) {
     using C = Fwd<DK, DV>;
-    constexpr int NSK = C::NSK, NSV = C::NSV, PS = C::PS;
+    constexpr int NSK = C::NSK, NSV = C::NSV;
     // All shared memory is dynamic: with no static shared memory its base is
     // 1024-byte aligned, as the 128-byte-swizzle tiles require (checked).
     extern __shared__ __align__(1024) unsigned char sm[];
@@ -422,6 +418,10 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const int ntiles = nt_total - j_first;
     // l2 == 0: window only (no L2 part, no state loads, no q A term).
     const bool has_l2 = l2 && (j_first == 0);
+    // Key tile j covers keys kt0 + 128 j ..; with an L2 part the tiles run
+    // 1, 2, .., nt-1 and the shifted chunk (j = 0) comes last, when the row's
+    // softmax statistics are final, so its L2 scores can join P scaled by them.
+    auto tile_j = [&](int n) { return has_l2 ? (n + 1 < ntiles ? n + 1 : 0) : j_first + n; };
 
     if (warp == 9) tmem_alloc(&B.tbase, 512);
     if (tid == 0) {
@@ -436,11 +436,10 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         }
         mbar_init(&B.s_full, 1);
         mbar_init(&B.s_empty, 8);
-        for (int hh = 0; hh < 2; ++hh)
-            for (int s = 0; s < 2; ++s) {
-                mbar_init(&B.p_full[hh][s], 4);
-                mbar_init(&B.p_empty[hh][s], 1);
-            }
+        for (int hh = 0; hh < 2; ++hh) {
+            mbar_init(&B.p_full[hh], 4);
+            mbar_init(&B.p_empty[hh], 1);
+        }
         mbar_init(&B.c_ready, 1);
         mbar_init(&B.xe, 8);
         mbar_init(&B.o_done, 2);
@@ -455,7 +454,6 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
     const uint32_t tm = B.tbase;
     const uint32_t sQ = smem_u32(sm);
     const uint32_t sK0 = sQ + C::OFF_K;
-    const uint32_t sP0 = sQ + C::OFF_P;
 
     if (warp == 8) {
         // ------------------------------------------------ TMA producer
@@ -477,7 +475,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             auto load_k = [&](int n) -> bool {
                 const int s = n % NSK;
                 if (n >= NSK && !mbar_wait(&B.k_empty[s], ((n / NSK) - 1) & 1)) return false;
-                const int kt = kt0 + kBlk * (j_first + n);
+                const int kt = kt0 + kBlk * tile_j(n);
                 mbar_expect_tx(&B.k_full[s], C::KBYTES);
 #pragma unroll
                 for (int b = 0; b < DK / 64; ++b) tma_load_3d(kslot(n) + b * 16384, &mk, &B.k_full[s], 64 * b, kt, bh);
@@ -486,7 +484,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             auto load_v = [&](int n) -> bool {
                 const int s = n % NSV;
                 if (n >= NSV && !mbar_wait(&B.v_empty[s], ((n / NSV) - 1) & 1)) return false;
-                const int kt = kt0 + kBlk * (j_first + n);
+                const int kt = kt0 + kBlk * tile_j(n);
                 mbar_expect_tx(&B.v_full[s], C::VBYTES);
 #pragma unroll
                 for (int b = 0; b < DV / 64; ++b) tma_load_3d(vslot(n) + b * 16384, &mv, &B.v_full[s], 64 * b, kt, bh);
@@ -545,36 +543,26 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             constexpr uint32_t HI = sdesc_hi(1024);
             constexpr uint32_t KSTEP = C::KBYTES >> 4, VSTEP = C::VBYTES >> 4;  // one K / V slot, encoded
             const uint32_t q_lo = sdesc_lo(sQ, 16), k_lo = sdesc_lo(sK0, 16);
-            const uint32_t v_lo = sdesc_lo(sQ + C::OFF_V, 16384), p_lo = sdesc_lo(sP0, 16);
+            const uint32_t v_lo = sdesc_lo(sQ + C::OFF_V, 16384);
             auto kofs = [](int k) { return (uint32_t)((k >> 2) * (16384 >> 4) + (k & 3) * 2); };  // K-major k step
             if (warp == 10) {
-                // P V products of processed tile n: per key half, O2 += P2 V'
-                // (tile 0) then O_half += P V.
-                uint32_t use[2] = {0, 0};  // P-slot uses so far, per key half
+                // O_half += P_half V of tile n, P_half (128 rows x 64 keys) from TMEM.
+                constexpr uint32_t ID_PVT = idesc_bf16_f32(128, DV, false, true);
                 for (int n = 0; n < ntiles && ok; ++n) {
                     const int s = n % NSV;
                     ok = mbar_wait(&B.v_full[s], (n / NSV) & 1);
-                    const int uses = (n == 0 && has_l2) ? 2 : 1;
                     for (int hh = 0; hh < 2 && ok; ++hh) {
-                        for (int u = 0; u < uses && ok; ++u) {
-                            const int slot = (int)(use[hh] % PS);
-                            ok = mbar_wait(&B.p_full[hh][slot], (use[hh] / PS) & 1);
-                            if (!ok) break;
-                            tc_fence_after();
-                            const bool l2p = (uses == 2 && u == 0);
-                            const uint32_t dcol = l2p ? C::COL_O2 : (hh ? C::COL_O1 : C::COL_O0);
-                            // V rows 64 hh + 16 k .. of slot s (MN-major B); P of key half hh, slot
-                            const uint32_t vb = v_lo + (uint32_t)s * VSTEP + (uint32_t)hh * (8192 >> 4);
-                            const uint32_t pb = p_lo + (uint32_t)(slot * 2 + hh) * (C::PHALF >> 4);
+                        ok = mbar_wait(&B.p_full[hh], n & 1);
+                        if (!ok) break;
+                        tc_fence_after();
+                        // V rows 64 hh + 16 k .. of slot s (MN-major B)
+                        const uint32_t vb = v_lo + (uint32_t)s * VSTEP + (uint32_t)hh * (8192 >> 4);
+                        const uint32_t pt = tm + C::COL_P + 32 * hh;
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                const bool acc = l2p ? (hh > 0 || k > 0) : (n > 0 || k > 0);
-                                mma_ss_h(tm + dcol, pb + 2 * k, HI, vb + k * (2048 >> 4), HI, C::ID_PV,
-                                         acc ? 1u : 0u);
-                            }
-                            mma_commit(&B.p_empty[hh][slot]);
-                            ++use[hh];
-                        }
+                        for (int k = 0; k < 4; ++k)
+                            mma_ts_h(tm + (hh ? C::COL_O1 : C::COL_O0), pt + 8 * k, vb + k * (2048 >> 4), HI, ID_PVT,
+                                     (n > 0 || k > 0) ? 1u : 0u);
+                        mma_commit(&B.p_empty[hh]);
                     }
                     if (ok) mma_commit(&B.v_empty[s]);
                 }
@@ -631,28 +619,33 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         const int c0 = half * 64;
         const uint32_t lrow = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t col_o = half ? C::COL_O1 : C::COL_O0;
+        const uint32_t col_p = C::COL_P + 32 * half;
         const float sc = scale * kLog2e;
+        const float sg = l2 ? 1.0f / (1.0f + expf(-gate[h])) : 0.f;
         float m = kNegBig, l = 0.f;
-        uint32_t use = 0;
-        int last_o_use = -1;
         bool ok = true;
-        auto wait_slot = [&](uint32_t u) -> bool {  // slot of use u is free again
-            return u < (uint32_t)PS || mbar_wait(&B.p_empty[half][u % PS], ((u / PS) - 1) & 1);
-        };
-        // 8 keys of row r into this half's P slot (128-byte-swizzle K-major).
-        auto store8 = [&](uint32_t slot, int c, const float *p) {
-            st_shared_v4(sP0 + (slot * 2 + half) * C::PHALF + sw128_off(r, c), pack_bf16(p[0], p[1]),
-                         pack_bf16(p[2], p[3]), pack_bf16(p[4], p[5]), pack_bf16(p[6], p[7]));
-        };
-        auto publish = [&](uint32_t slot) {
-            fence_async_smem();
+        // The row's merged statistics: each half leaves its maximum and sum
+        // in shared memory once (after its last softmax keys), then both read
+        // the other's.
+        auto exchange_stats = [&]() -> bool {
+            B.xm[half][r] = m;
+            B.xl[half][r] = l;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&B.p_full[half][slot]);
+            if (lane == 0) mbar_arrive(&B.xe);
+            return __all_sync(0xffffffffu, mbar_wait(&B.xe, 0));
+        };
+        // 32 keys (group g of this half) of row r into P as packed bf16.
+        auto store_p = [&](int g, const float *p) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) pk[e] = pack_bf16(p[2 * e], p[2 * e + 1]);
+            tmem_st16(tm + lrow + col_p + 16 * g, pk);
         };
         const int wrow_hi = (warp & 3) * 32 + 31;
         for (int n = 0; n < ntiles && ok; ++n) {
-            const int j = j_first + n;
+            const int j = tile_j(n);
             const int kt = kt0 + kBlk * j;
+            const bool shifted = has_l2 && j == 0;  // the last tile: its keys l <= r are the L2 part
             ok = __all_sync(0xffffffffu, mbar_wait(&B.s_full, n & 1));
             if (!ok) break;
             tc_fence_after();
@@ -667,33 +660,10 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 for (int i = 0; i < 32; ++i) s[32 + i] = v[i];
             }
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.s_empty);
-
-            if (has_l2 && j == 0) {  // L2 part of the shifted chunk: keys l <= r at positions >= 0
-                const int lo = max(0, -kt);
-                ok = __all_sync(0xffffffffu, wait_slot(use));
-                if (!ok) break;
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    // 32-key groups with no L2 key for any row of this warp are zeros.
-                    const int gk = c0 + 32 * g;
-                    const bool act = (gk <= wrow_hi) && (gk + 31 >= lo);
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float p2[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int i = gk + 8 * q + e;
-                            p2[e] = (act && i >= lo && i <= r) ? B.pw[(r - i) & (kBlk - 1)] * s[32 * g + 8 * q + e]
-                                                               : 0.f;
-                        }
-                        store8(use % PS, 4 * g + q, p2);
-                    }
-                }
-                publish(use % PS);
-                ++use;
+            if (!shifted) {  // the shifted chunk re-reads S for its L2 scores, so S is released later
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&B.s_empty);
             }
             // Softmax part: keys max(0, t-W+1) <= p <= t.  On edge tiles, 32-key
             // groups masked for every row of the warp skip the exponentials.
@@ -725,12 +695,11 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             const float mx = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
                                    fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * sc;
             const bool grow = mx > m + kRescale;
-            if (__any_sync(0xffffffffu, grow) && last_o_use >= 0) {
-                // This half's O must hold every earlier P V product before it is rescaled.
-                const uint32_t u = (uint32_t)last_o_use;
-                ok = __all_sync(0xffffffffu, mbar_wait(&B.p_empty[half][u % PS], (u / PS) & 1));
-                if (!ok) break;
-                tc_fence_after();
+            // P may be written (and O rescaled) once the previous P V of this half has completed.
+            ok = __all_sync(0xffffffffu, n == 0 || mbar_wait(&B.p_empty[half], (n - 1) & 1));
+            if (!ok) break;
+            tc_fence_after();
+            if (__any_sync(0xffffffffu, grow) && n > 0) {
                 const float f = grow ? ex2(m - mx) : 1.f;
 #pragma unroll 1
                 for (int cc = 0; cc < DV; cc += 32) {
@@ -741,7 +710,6 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                     for (int i = 0; i < 32; ++i) v[i] *= f;
                     tmem_st32(tm + lrow + col_o + cc, v);
                 }
-                tmem_wait_st();
             }
             if (grow) {
                 l *= ex2(m - mx);
@@ -770,23 +738,53 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 }
             }
             l += ((ps[0].x + ps[0].y) + (ps[1].x + ps[1].y)) + ((ps[2].x + ps[2].y) + (ps[3].x + ps[3].y));
-            ok = __all_sync(0xffffffffu, wait_slot(use));
-            if (!ok) break;
+            store_p(0, &s[0]);
+            store_p(1, &s[32]);
+            if (shifted) {
+                // The row's statistics are now final: merge them, then the L2
+                // scores eta lambda^(r-l) <q_r, k'_l> of keys l <= r (where the
+                // softmax P is zero) are added into P scaled by sigmoid(g) L /
+                // f_half, so that O_half f_half / L carries sigmoid(g) times
+                // their sum over V'.
+                ok = exchange_stats();
+                if (!ok) break;
+                const float mo = B.xm[half ^ 1][r], lo_ = B.xl[half ^ 1][r];
+                const float Mx = fmaxf(m, mo);
+                const float fs = ex2(m - Mx), fo = ex2(mo - Mx);
+                const float Lt = l * fs + lo_ * fo;
+                const float k2 = fs > 0.f ? sg * Lt / fs : 0.f;
+                const int lo2 = max(0, -kt);  // keys at positions >= 0
+                tmem_wait_st();
+#pragma unroll 1
+                for (int g = 0; g < 2; ++g) {
+                    const int gk = c0 + 32 * g;
+                    if (!((gk <= wrow_hi) && (gk + 31 >= lo2))) continue;  // no L2 key for any row of the warp
+                    float v[32];
+                    uint32_t pk[16];
+                    tmem_ld32(tm + lrow + c0 + 32 * g, v);  // S of this group again
+                    tmem_ld16u(tm + lrow + col_p + 16 * g, pk);
+                    tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < 8; ++c) store8(use % PS, c, &s[8 * c]);
+                    for (int e = 0; e < 32; e += 2) {
+                        const int i = gk + e;
+                        const float a = (i >= lo2 && i <= r) ? k2 * B.pw[(r - i) & (kBlk - 1)] * v[e] : 0.f;
+                        const float b = (i + 1 >= lo2 && i + 1 <= r) ? k2 * B.pw[(r - i - 1) & (kBlk - 1)] * v[e + 1] : 0.f;
+                        const float2 pv = unpack_bf16(pk[e >> 1]);
+                        pk[e >> 1] = pack_bf16(pv.x + a, pv.y + b);
+                    }
+                    tmem_st16(tm + lrow + col_p + 16 * g, pk);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&B.s_empty);  // S is read: the q A products may overwrite it
+            }
+            tmem_wait_st();
             tc_fence_before();
-            publish(use % PS);
-            last_o_use = (int)use;
-            ++use;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.p_full[half]);
         }
         // ------------------------------------------------ epilogue (DV/2 columns per half)
-        if (ok) {
-            B.xm[half][r] = m;
-            B.xl[half][r] = l;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.xe);
-            ok = __all_sync(0xffffffffu, mbar_wait(&B.xe, 0));
-        }
+        if (ok && !has_l2) ok = exchange_stats();
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&B.o_done, 0));
         if (ok) {
             tc_fence_after();
@@ -796,17 +794,15 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             const float lsum = B.xl[0][r] * f0 + B.xl[1][r] * f1;
             const float inv_l = lsum > 0.f ? 1.0f / lsum : 0.f;
             const float w0 = f0 * inv_l, w1 = f1 * inv_l;
-            const float sg = l2 ? 1.0f / (1.0f + expf(-gate[h])) : 0.f;
-            const float decay = l2 ? powf(lam[h], (float)(r + 1)) : 0.f;
+            const float cq = l2 ? sg * powf(lam[h], (float)(r + 1)) : 0.f;  // sigmoid(g) lambda^(i+1)
             __nv_bfloat16 *yr = y + ((size_t)bh * T + t) * DV;
 #pragma unroll 1
             for (int cc = 0; cc < DV / 2; cc += 16) {
                 const int col = half * (DV / 2) + cc;
-                float o0[16], o1[16], qa[16], o2[16];
+                float o0[16], o1[16], qa[16];
                 tmem_ld16(tm + lrow + C::COL_O0 + col, o0);
                 tmem_ld16(tm + lrow + C::COL_O1 + col, o1);
                 tmem_ld16(tm + lrow + col, qa);
-                if (has_l2) tmem_ld16(tm + lrow + C::COL_O2 + col, o2);
                 tmem_wait_ld();
                 if (t < T) {
                     uint32_t pk[8];
@@ -816,8 +812,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
                             const int e = 2 * i + u;
-                            const float mem = l2 ? fmaf(decay, qa[e], has_l2 ? o2[e] : 0.f) : 0.f;
-                            v2[u] = fmaf(o0[e], w0, fmaf(o1[e], w1, sg * mem));
+                            v2[u] = fmaf(o0[e], w0, fmaf(o1[e], w1, l2 ? cq * qa[e] : 0.f));
                         }
                         pk[i] = pack_bf16(v2[0], v2[1]);
                     }
