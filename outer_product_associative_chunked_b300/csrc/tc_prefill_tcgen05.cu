@@ -375,6 +375,7 @@ struct FwdBars {
     uint64_t s_full, s_empty;
     uint64_t p_full[2], p_empty[2];  // per key half
     uint64_t c_ready, xe, o_done, drain, drain_pv;  // o_done: one commit from each issuing thread
+    uint64_t y_ready;                               // the eight softmax warps have staged their y rows
     uint32_t tbase;
     float pw[kBlk];      // eta lambda^d, d = 0..127
     float xm[2][kBlk];   // [key half][row] running maxima, exchanged once at the end
@@ -394,9 +395,9 @@ template <int DK, int DV>
 __global__ void __launch_bounds__(352, 1)
 tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ma,
-              const __grid_constant__ CUtensorMap mc, int T, int W, int H, int nch, int nseg, int L, int l2,
-              const float *__restrict__ lam, const float *__restrict__ eta,
-              const float *__restrict__ gate, float scale, __nv_bfloat16 *__restrict__ y,
+              const __grid_constant__ CUtensorMap mc, const __grid_constant__ CUtensorMap my, int T, int W,
+              int H, int nch, int nseg, int L, int l2, const float *__restrict__ lam,
+              const float *__restrict__ eta, const float *__restrict__ gate, float scale,
               unsigned int *__restrict__ status) {
     using C = Fwd<DK, DV>;
     constexpr int NSK = C::NSK, NSV = C::NSV;
@@ -445,6 +446,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
         mbar_init(&B.o_done, 2);
         mbar_init(&B.drain, 1);
         mbar_init(&B.drain_pv, 1);
+        mbar_init(&B.y_ready, 8);
         mbar_fence_init();
     }
     if (l2 && tid < kBlk) B.pw[tid] = eta[h] * powf(lam[h], (float)tid);
@@ -463,6 +465,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             tma_prefetch_desc(&mq);
             tma_prefetch_desc(&mk);
             tma_prefetch_desc(&mv);
+            tma_prefetch_desc(&my);
             mbar_expect_tx(&B.q_full, C::QBYTES);
 #pragma unroll
             for (int b = 0; b < DK / 64; ++b) tma_load_3d(sm + b * 16384, &mq, &B.q_full, 64 * b, t0, bh);
@@ -764,11 +767,16 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                     tmem_ld32(tm + lrow + c0 + 32 * g, v);  // S of this group again
                     tmem_ld16u(tm + lrow + col_p + 16 * g, pk);
                     tmem_wait_ld();
+                    // The table is read unconditionally and the key range only
+                    // selects the factor: a load under a per-lane condition made
+                    // this loop about ten times slower.
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         const int i = gk + e;
-                        const float a = (i >= lo2 && i <= r) ? k2 * B.pw[(r - i) & (kBlk - 1)] * v[e] : 0.f;
-                        const float b = (i + 1 >= lo2 && i + 1 <= r) ? k2 * B.pw[(r - i - 1) & (kBlk - 1)] * v[e + 1] : 0.f;
+                        const float wa = B.pw[(r - i) & (kBlk - 1)], wb = B.pw[(r - i - 1) & (kBlk - 1)];
+                        const float ka = (i >= lo2 && i <= r) ? k2 : 0.f;
+                        const float kb = (i + 1 >= lo2 && i + 1 <= r) ? k2 : 0.f;
+                        const float a = ka * wa * v[e], b = kb * wb * v[e + 1];
                         const float2 pv = unpack_bf16(pk[e >> 1]);
                         pk[e >> 1] = pack_bf16(pv.x + a, pv.y + b);
                     }
@@ -784,6 +792,11 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             if (lane == 0) mbar_arrive(&B.p_full[half]);
         }
         // ------------------------------------------------ epilogue (DV/2 columns per half)
+        // y rows are staged from smem offset 0 (the spent Q tile, then K slot 0)
+        // with the tensor map's 128-byte swizzle, 64 columns per 16 KB box, and
+        // written by one TMA store per box; rows past T are clipped by the map.
+        // Every MMA has completed once o_done has, so nothing reads there.
+        static_assert(DV / 64 * 16384 <= C::OFF_V, "y staging fits in front of the V slots");
         if (ok && !has_l2) ok = exchange_stats();
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&B.o_done, 0));
         if (ok) {
@@ -795,7 +808,6 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
             const float inv_l = lsum > 0.f ? 1.0f / lsum : 0.f;
             const float w0 = f0 * inv_l, w1 = f1 * inv_l;
             const float cq = l2 ? sg * powf(lam[h], (float)(r + 1)) : 0.f;  // sigmoid(g) lambda^(i+1)
-            __nv_bfloat16 *yr = y + ((size_t)bh * T + t) * DV;
 #pragma unroll 1
             for (int cc = 0; cc < DV / 2; cc += 16) {
                 const int col = half * (DV / 2) + cc;
@@ -804,21 +816,32 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 tmem_ld16(tm + lrow + C::COL_O1 + col, o1);
                 tmem_ld16(tm + lrow + col, qa);
                 tmem_wait_ld();
-                if (t < T) {
-                    uint32_t pk[8];
+                uint32_t pk[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float v2[2];
+                for (int i = 0; i < 8; ++i) {
+                    float v2[2];
 #pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int e = 2 * i + u;
-                            v2[u] = fmaf(o0[e], w0, fmaf(o1[e], w1, l2 ? cq * qa[e] : 0.f));
-                        }
-                        pk[i] = pack_bf16(v2[0], v2[1]);
+                    for (int u = 0; u < 2; ++u) {
+                        const int e = 2 * i + u;
+                        v2[u] = fmaf(o0[e], w0, fmaf(o1[e], w1, l2 ? cq * qa[e] : 0.f));
                     }
-                    uint4 *dst = reinterpret_cast<uint4 *>(yr + col);
-                    dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    pk[i] = pack_bf16(v2[0], v2[1]);
+                }
+                const uint32_t box = sQ + (uint32_t)(col / 64) * 16384u, c16 = (uint32_t)((col % 64) / 8);
+                st_shared_v4(box + sw128_off(r, c16), pk[0], pk[1], pk[2], pk[3]);
+                st_shared_v4(box + sw128_off(r, c16 + 1), pk[4], pk[5], pk[6], pk[7]);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.y_ready);
+            if (tid == 0) {
+                if (mbar_wait(&B.y_ready, 0)) {
+#pragma unroll
+                    for (int b = 0; b < DV / 64; ++b) tma_store_3d(&my, sm + b * 16384, 64 * b, t0, bh);
+                    tma_store_commit();
+                    tma_store_wait_read();
+                } else {
+                    ok = false;
                 }
             }
         }
@@ -1414,9 +1437,11 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         static_assert(sizeof(FwdBars) <= 3072, "barriers block");
         const int smem = (int)(Cfg::OFF_BARS + sizeof(FwdBars));
         if (int rc_ = set_smem_limit((const void *)kern, smem, "tc_fwd smem attribute")) return rc_;
+        CUtensorMap my;
+        if ((rc = make_tmap_bf16_3d(&my, y, DV, T, BH, kBlk))) return rc;
         prof_begin(st);
-        kern<<<dim3(g.nch, BH), 352, smem, st>>>(mq, mk, mv, ma, mc, T, W, H, g.nch, g.nseg, g.L, (int)l2, lam,
-                                                  eta, gate, scale, (__nv_bfloat16 *)y, status + 1);
+        kern<<<dim3(g.nch, BH), 352, smem, st>>>(mq, mk, mv, ma, mc, my, T, W, H, g.nch, g.nseg, g.L, (int)l2,
+                                                  lam, eta, gate, scale, status + 1);
         rc = launched("tc_fwd");
         prof_end(st);
         return rc;
