@@ -664,7 +664,10 @@ delta_fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int i = 8 * ch + e;
-                        gv[e] = (i == j ? 1.f : (i > j ? Lb[lsw(i, j)] : 0.f)) * bt;
+                        // read unconditionally (every (i, j) lies in the tile), then select:
+                        // no per-lane branch around the load
+                        const float lv = Lb[lsw(i, j)];
+                        gv[e] = (i == j ? 1.f : (i > j ? lv : 0.f)) * bt;
                     }
                     st_shared_v4(gt + sw128_off(j, ch), pack_bf16(gv[0], gv[1]), pack_bf16(gv[2], gv[3]),
                                  pack_bf16(gv[4], gv[5]), pack_bf16(gv[6], gv[7]));

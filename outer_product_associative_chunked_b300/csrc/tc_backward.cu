@@ -313,7 +313,7 @@ tcb_window_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int r = ty + 16 * i, c = tx + 16 * j;
-                const float p = band(q0 + r, k0 + c) ? __expf(S[i][j] * scale - rf[r]) : 0.f;
+                const float p = __expf(band(q0 + r, k0 + c) ? S[i][j] * scale - rf[r] : -INFINITY);  // one path per warp
                 Ps[r * kLS + c] = p * (dP[i][j] - rD[r]);
             }
         __syncthreads();
@@ -377,7 +377,7 @@ tcb_window_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
             for (int j = 0; j < 4; ++j) {
                 const int s = k0 + ty + 16 * i, t = t0 + tx + 16 * j;
                 const bool ok = s <= t && s > t - W && t < Tn && s < Tn;
-                Pt[i][j] = ok ? __expf(St[i][j] * scale - rL[tx + 16 * j]) : 0.f;
+                Pt[i][j] = __expf(ok ? St[i][j] * scale - rL[tx + 16 * j] : -INFINITY);
                 Ps[(ty + 16 * i) * kLS + tx + 16 * j] = Pt[i][j];
             }
         __syncthreads();

@@ -1209,8 +1209,10 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
 #pragma unroll
                     for (int e = 0; e < 32; e += 2) {
                         float2 x = fma2(make_float2(v[e], v[e + 1]), sc2, nm2);
-                        x.x = ((bits >> e) & 1u) ? ex2(x.x) : 0.f;
-                        x.y = ((bits >> (e + 1)) & 1u) ? ex2(x.y) : 0.f;
+                        // masked keys select -inf (2^-inf = 0): the exponential itself is
+                        // unconditional, which keeps the warp on one path
+                        x.x = ex2(((bits >> e) & 1u) ? x.x : -INFINITY);
+                        x.y = ex2(((bits >> (e + 1)) & 1u) ? x.y : -INFINITY);
                         acc[(e >> 1) & 1] = add2(acc[(e >> 1) & 1], x);
                         pk[e >> 1] = pack_bf16(x.x, x.y);
                     }
@@ -1244,8 +1246,8 @@ tc_fwd_row_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant_
 #pragma unroll
                         for (int e = e0; e < e0 + 16; e += 2) {
                             float2 x = fma2(make_float2(v[e], v[e + 1]), sc2, nm2);
-                            x.x = ((bits >> e) & 1u) ? ex2(x.x) : 0.f;
-                            x.y = ((bits >> (e + 1)) & 1u) ? ex2(x.y) : 0.f;
+                            x.x = ex2(((bits >> e) & 1u) ? x.x : -INFINITY);
+                            x.y = ex2(((bits >> (e + 1)) & 1u) ? x.y : -INFINITY);
                             acc[(e >> 1) & 1] = add2(acc[(e >> 1) & 1], x);
                             ps[(e - e0) >> 1] = pack_bf16(x.x, x.y);
                             p2[(e - e0) >> 1] = pack_bf16(v[e] * pw[-e], v[e + 1] * pw[-e - 1]);
