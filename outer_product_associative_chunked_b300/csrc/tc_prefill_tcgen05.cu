@@ -27,10 +27,14 @@
 //                       segment's local final state (fp32);
 //   tc_l2_carry_kernel  per head: the segment start states A_{gL} (bf16) and
 //                       the final state after the whole sequence (fp32);
-//   tc_fwd_kernel       per (head, query block): flash-style online softmax
+//   tc_fwd_row_kernel   (d = 64) and tc_fwd_kernel (d = 128 and mixed sizes),
+//                       per (head, query block): flash-style online softmax
 //                       over the window tiles (S = Q K^T and O += P V on
-//                       tcgen05), the L2 term P2 V' and q (A_j^loc +
-//                       lambda^(C (j - gL)) A_{gL}), and the gate.
+//                       tcgen05, P in TMEM), the L2 term of the shifted chunk
+//                       (its own accumulator at d = 64; at d = 128 folded into
+//                       P, scaled by the row's final softmax statistics),
+//                       q (A_j^loc + lambda^(C (j - gL)) A_{gL}), and the gate;
+//                       y leaves through shared memory by TMA stores.
 //
 // Every wait inside these kernels is bounded; a wait that runs out records a
 // bit in the call's status word (the head of its workspace, read by
@@ -391,6 +395,10 @@ struct FwdBars {
 // q A products) and owns the TMEM allocation; warp 10 issues the P V
 // products.  With two issuing threads the next tile's S does not queue
 // behind a P V that waits for the slowest softmax warp of the previous tile.
+// The shifted chunk comes last: once its softmax keys are in P the two halves
+// exchange their statistics, and its L2 scores are added into P scaled by
+// sigmoid(g) L / f_half, so O_half f_half / L carries them with no extra
+// accumulator.  y is staged in the spent Q tile and stored by TMA.
 template <int DK, int DV>
 __global__ void __launch_bounds__(352, 1)
 tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -860,17 +868,17 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
 // +63 of every tile -- half a row per thread; the two halves of a row agree
 // on the row maximum (and, in the shifted chunk, on the row sum) through
 // shared memory.  One thread of warp 8 issues the TMA loads and the MMAs.
-// TMEM: S [0,128) (after the last tile q A_j^loc lands in columns [0,DV) and
-// q A_{gL} in [DV,2DV)), O [128, 128+DV), P [128+DV, 128+DV+64) -- P
-// is written by the softmax threads with tcgen05.st as packed bf16 and is
-// the A operand of O += P V, so it never touches shared memory.
+// TMEM: S [0,128), O [128, 128+DV), P [128+DV, 128+DV+64) -- P is written
+// by the softmax threads with tcgen05.st as packed bf16 and is the A operand
+// of O += P V, so it never touches shared memory.
 //
-// The L2 part of the block (keys of the shifted chunk with l <= i) is folded
-// into O: the shifted chunk is processed last, when the row's softmax sum L
-// is final, and its decayed scores enter P as L sigmoid(g) eta lambda^(i-l)
-// <q_i, k'_l>, next to its softmax probabilities (keys l > i).  Then
-// O / L = y_local + sigmoid(g) sum_l eta lambda^(i-l) <q_i,k'_l> v'_l and the
-// epilogue adds sigmoid(g) lambda^(i+1) q A_j with A_j = A_j^loc + c A_{gL}.
+// The L2 part of the block (keys l <= i of the shifted chunk, then the state)
+// has its own accumulators.  The shifted chunk is processed last: its
+// softmax keys (l > i) go to P as usual, and its decayed scores
+// eta lambda^(i-l) <q_i, k'_l> go to P2 over the spent S columns [0,64);
+// O2 = P2 V' accumulates into S columns [64,128).  After that q A_j^loc lands
+// in S columns [0,DV) and q A_{gL} in the P columns, and the epilogue forms
+// y = O / L + sigmoid(g) (O2 + lambda^(i+1) (q A_j^loc + c q A_{gL})).
 //
 // Stages: 3 K slots (the last also takes A_j^loc and A_{gL}) and 2 V slots.
 // The issuing thread learns that a slot is free from the softmax side: S(n)
