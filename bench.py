@@ -867,6 +867,54 @@ def cpu_baselines(synth):
     record("bdh_fp32_B2_H4_T2048_N16384_dv256", allv, dt,
            f"the first {Tp} of {d['T']} tokens of all {d['B']}x{d['H']} units (at most 8 threads busy)",
            one, dt1, "1 unit, 32 tokens")
+
+    # Tensor Cache backward: one whole sequence (8 heads x 4096 tokens), the
+    # same inputs and output gradient as the GPU line
+    import torch
+    w = synth.WORKLOADS["tc_bf16_B4_H8_T4096_d64_W512"]
+    d = w.dims
+    inp = synth.tc_inputs(d["B"], d["H"], d["T"], 64, 64, d["W"], dtype="bf16", seed=w.seed)
+    dy = torch.randn(inp.q.shape[:-1] + (64,), generator=torch.Generator().manual_seed(9)).to(inp.q.dtype)
+    a = [oracle.f64(x[:1]) for x in (inp.q, inp.k, inp.v, dy)]
+    s = [oracle.f64(x) for x in (inp.lam, inp.eta, inp.gate)]
+    allv, dt = _oracle_rate(oracle, lambda: oracle.tc_backward(a[0], a[1], a[2], s[0], s[1], s[2], d["W"], a[3]),
+                            d["T"], threads)
+    one, dt1 = _oracle_rate(oracle, lambda: oracle.tc_backward(a[0][:, :1], a[1][:, :1], a[2][:, :1], s[0][:1],
+                                                               s[1][:1], s[2][:1], d["W"], a[3][:, :1]),
+                            d["T"] / d["H"], 1)
+    record("tc_backward_bf16_B4_H8_T4096_d64_W512", allv, dt,
+           f"1 of {d['B']} sequences ({d['H']} heads x {d['T']} tokens), float64 reverse pass", one, dt1,
+           "1 head of it")
+
+    # delta-rule backward: the first 512 tokens of every unit
+    d = synth.WORKLOADS["delta_bf16_B8_H16_T8192_d128_C64"].dims
+    Tp = 512
+    inp = synth.delta_inputs(d["B"], d["H"], Tp, 128, 128, dtype="bf16", seed=2)
+    dy = torch.randn(inp.v.shape, generator=torch.Generator().manual_seed(10)).to(inp.v.dtype)
+    a = [oracle.f64(x) for x in (inp.q, inp.k, inp.v, inp.beta, dy)]
+    allv, dt = _oracle_rate(oracle, lambda: oracle.delta_backward(*a), d["B"] * Tp, threads)
+    one, dt1 = _oracle_rate(oracle, lambda: oracle.delta_backward(*[x[:1, :1] for x in a]), Tp / d["H"], 1)
+    record("delta_backward_bf16_B8_H16_T8192_d128", allv, dt,
+           f"the first {Tp} of {d['T']} tokens of all {d['B']}x{d['H']} units", one, dt1, f"1 unit, {Tp} tokens")
+
+    # BDH with generated keys: keys and queries by the oracle's max(0, x U - theta),
+    # then its attention, on the first 64 tokens of every unit
+    name = "bdh_keygen_B2_H4_T2048_R256_N16384_dv256"
+    d = synth.WORKLOADS[name].dims
+    Tp = 64
+    kg = synth.sparse_keygen_inputs(d["B"], d["H"], Tp, d["N"], d["d_v"], seed=synth.WORKLOADS[name].seed,
+                                    rank=d["R"])
+    xq, xk, U, vv = (oracle.f64(x) for x in (kg.xq, kg.xk, kg.U, kg.v))
+
+    def keygen_attn(b, h):
+        qk = oracle.bdh_keys(xq[:b, :h], U[:h], kg.theta)
+        kk = oracle.bdh_keys(xk[:b, :h], U[:h], kg.theta)
+        return oracle.sparse_linattn(qk, kk, vv[:b, :h])
+
+    allv, dt = _oracle_rate(oracle, lambda: keygen_attn(d["B"], d["H"]), d["B"] * Tp, threads)
+    one, dt1 = _oracle_rate(oracle, lambda: keygen_attn(1, 1), Tp / d["H"], 1)
+    record(name, allv, dt, f"the first {Tp} of {d['T']} tokens of all {d['B']}x{d['H']} units (keys generated "
+           f"by the oracle, then its attention)", one, dt1, f"1 unit, {Tp} tokens")
     oracle.set_threads(threads)
     return res
 
