@@ -231,7 +231,9 @@ int tc_decode_step(opam_tc_state *st, const void *q, const void *k, const void *
  *   S0     NULL (zero state) or [B][H][d_k][d_v] float32 key-major start state
  *   S_out  NULL or [B][H][d_k][d_v] float32 key-major final state (may equal S0)
  *   y      [B][H][T][d_v] dtype, output o_t
- * Supported: d_k, d_v in {32, 64, 128}. Errors as above. */
+ * Supported: d_k, d_v in {32, 64, 128}; bf16 with d_k, d_v in {64, 128} and
+ * chunk 64 runs on the tensor cores, every other case on the CUDA cores.
+ * Errors as above. */
 size_t delta_rule_forward_workspace_size(int B, int H, int T, int d_k, int d_v,
                                          int chunk, int dtype);
 int delta_rule_forward(const void *q, const void *k, const void *v,

@@ -434,7 +434,7 @@ int delta_rule_forward(const void *q, const void *k, const void *v, const float 
     cudaStream_t s = (cudaStream_t)stream;
     if (int rc = clear_status(workspace, s)) return rc;
     if (tc)
-        return delta_tcgen05(q, k, v, beta, B, H, T, d_k, S0, S_out, y, status_body(workspace),
+        return delta_tcgen05(q, k, v, beta, B, H, T, d_k, d_v, S0, S_out, y, status_body(workspace),
                              status_word(workspace), s);
     return delta_simt(q, k, v, beta, dtype, B, H, T, d_k, d_v, C, S0, S_out, y, status_body(workspace), s);
 }

@@ -44,7 +44,11 @@ using namespace sm100;
 namespace {
 
 constexpr int kC = 64;  // tokens per chunk
-constexpr int kDV = 128;
+// Every product whose rows are the value dimension runs with M = 128.  For
+// d_v = 64 both 64-row halves of M read the same v columns (the MN-major
+// operand's second block aliases the first), so TMEM lanes 64..127 carry an
+// exact copy of U^T, O^T and the state; only lanes below d_v read or write
+// global memory.
 
 // Bits recorded in the call's status word (the head of its workspace) when a
 // bounded wait runs out.
@@ -303,7 +307,7 @@ struct FusedBars {
     uint32_t tbase;
 };
 
-template <int DK>
+template <int DK, int DV>
 __global__ void __launch_bounds__(512, 1)
 delta_fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, const float *__restrict__ beta, int T, int nch,
@@ -350,9 +354,9 @@ delta_fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     auto qk_base = [&](int c) { return (uint32_t)(C::OFF_QK + (c % 3) * C::QK); };
     auto load_v = [&](int c) {
         uint64_t *bar = &B.v_full[c & 1];
-        mbar_expect_tx(bar, 16384);
+        mbar_expect_tx(bar, kC * DV * 2);
 #pragma unroll
-        for (int b = 0; b < 2; ++b) tma_load_3d(sm + C::OFF_V + b * 8192, &mv, bar, 64 * b, c * kC, bh);
+        for (int b = 0; b < DV / 64; ++b) tma_load_3d(sm + C::OFF_V + b * 8192, &mv, bar, 64 * b, c * kC, bh);
     };
 
     if (warp == 0) {
@@ -425,7 +429,7 @@ delta_fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 // V^T G^T: the state-free part of U^T, into the chunk's U buffer
 #pragma unroll
                 for (int k = 0; k < kC / 16; ++k)
-                    mma_ss(tm + C::COL_U + 64 * g, sdesc_sw128(s0 + C::OFF_V + k * 2048, 8192, 1024),
+                    mma_ss(tm + C::COL_U + 64 * g, sdesc_sw128(s0 + C::OFF_V + k * 2048, DV == 128 ? 8192 : 0, 1024),
                            sdesc_sw128(gt + k * 2048, 8192, 1024), ID_T, k > 0 ? 1u : 0u);
                 mma_commit(&B.w_full[g]);
                 mma_commit(&B.v_empty);
@@ -513,7 +517,7 @@ delta_fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
             for (int c0 = 0; c0 < DK; c0 += 32) {
                 float v[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) v[e] = has_s0 ? S0[((size_t)bh * DK + c0 + e) * kDV + i] : 0.f;
+                for (int e = 0; e < 32; ++e) v[e] = has_s0 ? S0[((size_t)bh * DK + c0 + e) * DV + (i & (DV - 1))] : 0.f;
                 if (has_s0) tmem_st32(tm + lrow + C::COL_S + c0, v);
                 put_s0(c0, v);
             }
@@ -558,11 +562,11 @@ delta_fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 if (c + 1 < nch) {
                     put_s0(c0, v0);
                     put_s0(c0 + 32, v1);
-                } else if (S_out) {
+                } else if (S_out && i < DV) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        S_out[((size_t)bh * DK + c0 + e) * kDV + i] = v0[e];
-                        S_out[((size_t)bh * DK + c0 + 32 + e) * kDV + i] = v1[e];
+                        S_out[((size_t)bh * DK + c0 + e) * DV + i] = v0[e];
+                        S_out[((size_t)bh * DK + c0 + 32 + e) * DV + i] = v1[e];
                     }
                 }
             }
@@ -572,7 +576,7 @@ delta_fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&B.s0_ready);
             }
-            {
+            if (q4 * 32 < DV) {
                 // O^T row i -> y[t0 + t][i], transposed through this warp's own
                 // 4 KB of the U tile (the rows of U^T that only this warp
                 // writes, free once the products have completed).
@@ -584,12 +588,12 @@ delta_fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
 #pragma unroll
                 for (int t = 0; t < kC; ++t) ys[t * 32 + lane] = __float2bfloat16_rn(t < 32 ? o0[t] : o1[t - 32]);
                 __syncwarp();
-                __nv_bfloat16 *yb = y + ((size_t)bh * T + t0) * kDV + q4 * 32;
+                __nv_bfloat16 *yb = y + ((size_t)bh * T + t0) * DV + q4 * 32;
 #pragma unroll
                 for (int e = lane; e < kC * 4; e += 32) {  // 64 rows x four 16-byte pieces
                     const int t = e >> 2, ch = e & 3;
                     if (t < n)
-                        reinterpret_cast<uint4 *>(yb + (size_t)t * kDV)[ch] =
+                        reinterpret_cast<uint4 *>(yb + (size_t)t * DV)[ch] =
                             reinterpret_cast<const uint4 *>(ys + t * 32)[ch];
                 }
                 __syncwarp();
@@ -710,7 +714,7 @@ delta_fused_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant
     if (warp == 1) tmem_dealloc(tm, C::TCOLS);
 }
 
-template <int DK>
+template <int DK, int DV>
 int run(const void *q, const void *k, const void *v, const float *beta, int BH, int T,
         const float *S0, float *S_out, void *y, unsigned int *status, cudaStream_t st) {
     const int nch = ceil_div(T, kC);
@@ -718,9 +722,9 @@ int run(const void *q, const void *k, const void *v, const float *beta, int BH, 
     int rc;
     if ((rc = make_tmap_bf16_3d(&mq, q, DK, T, BH, kC))) return rc;
     if ((rc = make_tmap_bf16_3d(&mk, k, DK, T, BH, kC))) return rc;
-    if ((rc = make_tmap_bf16_3d(&mv, v, kDV, T, BH, kC))) return rc;
+    if ((rc = make_tmap_bf16_3d(&mv, v, DV, T, BH, kC))) return rc;
     using Cfg = FusedCfg<DK>;
-    auto kern = delta_fused_kernel<DK>;
+    auto kern = delta_fused_kernel<DK, DV>;
     const int smem = (int)(Cfg::OFF_BARS + sizeof(FusedBars) + 16);
     if (int rc_ = set_smem_limit((const void *)kern, smem, "delta_fused smem attribute")) return rc_;
     prof_begin(st);
@@ -733,7 +737,7 @@ int run(const void *q, const void *k, const void *v, const float *beta, int BH, 
 }  // namespace
 
 bool delta_tcgen05_supported(int dtype, int dk, int dv, int chunk) {
-    return dtype == OPAM_BF16 && (dk == 64 || dk == 128) && dv == kDV && chunk == kC;
+    return dtype == OPAM_BF16 && (dk == 64 || dk == 128) && (dv == 64 || dv == 128) && chunk == kC;
 }
 
 size_t delta_tcgen05_workspace(int BH, int T, int dk) {
@@ -744,12 +748,14 @@ size_t delta_tcgen05_workspace(int BH, int T, int dk) {
 }
 
 int delta_tcgen05(const void *q, const void *k, const void *v, const float *beta, int B, int H, int T,
-                  int dk, const float *S0, float *S_out, void *y, void *ws, unsigned int *status,
+                  int dk, int dv, const float *S0, float *S_out, void *y, void *ws, unsigned int *status,
                   cudaStream_t s) {
     (void)ws;
-    if (dk == 64) return run<64>(q, k, v, beta, B * H, T, S0, S_out, y, status, s);
-    if (dk == 128) return run<128>(q, k, v, beta, B * H, T, S0, S_out, y, status, s);
-    set_error("tensor-core delta rule: d_k=%d unsupported", dk);
+    if (dk == 64 && dv == 128) return run<64, 128>(q, k, v, beta, B * H, T, S0, S_out, y, status, s);
+    if (dk == 128 && dv == 128) return run<128, 128>(q, k, v, beta, B * H, T, S0, S_out, y, status, s);
+    if (dk == 64 && dv == 64) return run<64, 64>(q, k, v, beta, B * H, T, S0, S_out, y, status, s);
+    if (dk == 128 && dv == 64) return run<128, 64>(q, k, v, beta, B * H, T, S0, S_out, y, status, s);
+    set_error("tensor-core delta rule: d_k=%d, d_v=%d unsupported", dk, dv);
     return OPAM_ERR_UNSUPPORTED;
 }
 

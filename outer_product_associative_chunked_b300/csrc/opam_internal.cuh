@@ -143,7 +143,7 @@ int delta_simt(const void *q, const void *k, const void *v, const float *beta, i
 bool delta_tcgen05_supported(int dtype, int dk, int dv, int chunk);
 size_t delta_tcgen05_workspace(int BH, int T, int dk);
 int delta_tcgen05(const void *q, const void *k, const void *v, const float *beta, int B, int H, int T,
-                  int dk, const float *S0, float *S_out, void *y, void *ws, unsigned int *status,
+                  int dk, int dv, const float *S0, float *S_out, void *y, void *ws, unsigned int *status,
                   cudaStream_t s);
 
 // DeltaNet backward (CUDA cores, per-token reverse recurrence).

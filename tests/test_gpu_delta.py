@@ -44,23 +44,28 @@ def test_small_parity(cuda_lib, oracle_mod, dtype, B, H, T, dk, dv, chunk, with_
     check_parity(to_np(S_out), ref["S"], dtype, "delta S")
 
 
-# Shapes served by the tensor-core path (bf16, d_v = 128, chunk 64): ragged
-# tails, a single token, exact chunk multiples, both key widths, start states.
-@pytest.mark.parametrize("B,H,T,dk,with_S0", [
-    (1, 1, 1, 128, False),
-    (1, 2, 63, 128, True),
-    (2, 1, 64, 128, False),
-    (1, 1, 65, 64, True),
-    (1, 3, 200, 128, True),
-    (2, 2, 333, 64, False),
-    (1, 1, 1024, 128, True),
+# Shapes served by the tensor-core path (bf16, chunk 64, d_v 64 or 128): ragged
+# tails, a single token, exact chunk multiples, both key and value widths,
+# start states (updated in place).
+@pytest.mark.parametrize("B,H,T,dk,dv,with_S0", [
+    (1, 1, 1, 128, 128, False),
+    (1, 2, 63, 128, 128, True),
+    (2, 1, 64, 128, 128, False),
+    (1, 1, 65, 64, 128, True),
+    (1, 3, 200, 128, 128, True),
+    (2, 2, 333, 64, 128, False),
+    (1, 1, 1024, 128, 128, True),
+    (1, 1, 1, 64, 64, False),
+    (1, 2, 63, 64, 64, True),
+    (2, 2, 333, 128, 64, True),
+    (1, 1, 1024, 64, 64, True),
 ])
-def test_tensor_core_shapes(cuda_lib, oracle_mod, B, H, T, dk, with_S0):
-    inp = synth.delta_inputs(B, H, T, dk, 128, dtype="bf16", seed=T + 7 * dk)
+def test_tensor_core_shapes(cuda_lib, oracle_mod, B, H, T, dk, dv, with_S0):
+    inp = synth.delta_inputs(B, H, T, dk, dv, dtype="bf16", seed=T + 7 * dk + dv)
     q, k, v, beta = _gpu(inp)
-    S0 = (torch.randn(B, H, dk, 128, generator=torch.Generator().manual_seed(9)) * 0.1) if with_S0 else None
+    S0 = (torch.randn(B, H, dk, dv, generator=torch.Generator().manual_seed(9)) * 0.1) if with_S0 else None
     S = None if S0 is None else S0.clone().cuda()
-    S_out = S if S is not None else torch.empty(B, H, dk, 128, device="cuda")  # in place when given
+    S_out = S if S is not None else torch.empty(B, H, dk, dv, device="cuda")  # in place when given
     y = cuda_lib.delta_rule_forward(q, k, v, beta, chunk=64, S0=S, S_out=S_out)
     torch.cuda.synchronize()
     cuda_lib.check_device_errors()
