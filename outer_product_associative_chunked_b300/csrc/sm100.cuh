@@ -110,6 +110,14 @@ __device__ __forceinline__ void tma_store_wait_read() {
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
+// Bring one box of a 3-D tensor map into L2 (no shared memory, no barrier):
+// warms the tiles that a CTA of a later wave will load first.
+__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
 
 // Order this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tcgen05.mma operands written with st.shared).

@@ -398,14 +398,17 @@ struct FwdBars {
 // The shifted chunk comes last: once its softmax keys are in P the two halves
 // exchange their statistics, and its L2 scores are added into P scaled by
 // sigmoid(g) L / f_half, so O_half f_half / L carries them with no extra
-// accumulator.  y is staged in the spent Q tile and stored by TMA.
+// accumulator.  y is staged in the spent Q tile and stored by TMA.  `wave`
+// is the number of CTAs resident at once (one per SM): the producer warms L2
+// with the first tiles of the CTA that many places later in launch order
+// (0 turns that off).
 template <int DK, int DV>
 __global__ void __launch_bounds__(352, 1)
 tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
               const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap ma,
               const __grid_constant__ CUtensorMap mc, const __grid_constant__ CUtensorMap my, int T, int W,
               int H, int nch, int nseg, int L, int l2, const float *__restrict__ lam,
-              const float *__restrict__ eta, const float *__restrict__ gate, float scale,
+              const float *__restrict__ eta, const float *__restrict__ gate, float scale, int wave,
               unsigned int *__restrict__ status) {
     using C = Fwd<DK, DV>;
     constexpr int NSK = C::NSK, NSV = C::NSV;
@@ -502,6 +505,26 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CU
                 return true;
             };
             if (ntiles > 0) ok = load_k(0);
+            {   // L2 prefetch for the CTA one wave later in launch order (grid x = query
+                // block, y = head): its Q tile and first K and V tiles
+                const int nl = (int)(blockIdx.y * gridDim.x + blockIdx.x) + wave;
+                if (wave > 0 && nl < (int)(gridDim.x * gridDim.y)) {
+                    const int njq = nl % (int)gridDim.x, nbh = nl / (int)gridDim.x;
+                    const int nt0 = njq * kBlk, nkt0 = nt0 - W;
+                    const int nj_first = (-nkt0 - (kBlk - 1) > 0) ? (-nkt0) / kBlk : 0;
+                    const int nnt = nt_total - nj_first;
+                    const bool nl2 = l2 && nj_first == 0;
+#pragma unroll
+                    for (int b = 0; b < DK / 64; ++b) tma_prefetch_l2_3d(&mq, 64 * b, nt0, nbh);
+                    for (int n = 0; n < 2 && n < nnt; ++n) {
+                        const int kt = nkt0 + kBlk * (nl2 ? (n + 1 < nnt ? n + 1 : 0) : nj_first + n);
+                        if (kt < 0) continue;
+                        for (int b = 0; b < DK / 64; ++b) tma_prefetch_l2_3d(&mk, 64 * b, kt, nbh);
+                        if (n == 0)
+                            for (int b = 0; b < DV / 64; ++b) tma_prefetch_l2_3d(&mv, 64 * b, kt, nbh);
+                    }
+                }
+            }
             for (int n = 0; n < ntiles && ok; ++n) {
                 if (n + 1 < ntiles) ok = load_k(n + 1);
                 if (ok) ok = load_v(n);
@@ -1451,7 +1474,7 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         if ((rc = make_tmap_bf16_3d(&my, y, DV, T, BH, kBlk))) return rc;
         prof_begin(st);
         kern<<<dim3(g.nch, BH), 352, smem, st>>>(mq, mk, mv, ma, mc, my, T, W, H, g.nch, g.nseg, g.L, (int)l2,
-                                                  lam, eta, gate, scale, status + 1);
+                                                  lam, eta, gate, scale, num_sms(), status + 1);
         rc = launched("tc_fwd");
         prof_end(st);
         return rc;
