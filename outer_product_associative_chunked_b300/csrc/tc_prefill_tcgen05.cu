@@ -66,15 +66,20 @@ enum : unsigned int {
     kStFwdAlign = kStatusTcPrefill << 6,
 };
 
-// Chunks per segment of the state recurrence: enough segments that the state
-// kernel fills the GPU (two CTAs per SM), at most one segment per chunk.
+// Chunks per segment of the state recurrence, at most one segment per chunk.
+// For d = 64 the state pass runs one CTA per SM (padded to kStateSoloSmem so
+// that two never share an SM), with twice as many chunks per segment as two
+// per SM would give: on the B4 H8 T4096 W512 step this measured 62.4 against
+// 64.0 us.  For the larger sizes two state CTAs per SM fill the GPU.
 struct Segments {
     int nch, nseg, L;
 };
-Segments segments(int BH, int T, int dv, int num_sms) {
+constexpr uint32_t kStateSoloSmem = 116 * 1024;  // above half an SM's shared memory
+Segments segments(int BH, int T, int dk, int dv, int num_sms) {
     const int nch = ceil_div(T, kBlk);
     const int units = BH * (dv / 64);
-    int want = (2 * num_sms) / units;
+    const int per_sm = (dk == 64 && dv == 64) ? 1 : 2;
+    int want = (per_sm * num_sms) / units;
     if (want < 1) want = 1;
     if (want > nch) want = nch;
     const int L = ceil_div(nch, want);
@@ -295,8 +300,12 @@ tc_l2_state_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant
 
 // --------------------------------------------------------------------- segment carries
 // A_{0} = 0, A_{(g+1)L} = lambda^{tokens of segment g} A_{gL} + local final of g.
-// Each thread owns 4 adjacent state elements of one head.
-__global__ void __launch_bounds__(128)
+// Each thread owns two groups of 4 adjacent state elements of one head (the
+// second blockDim.x groups after the first).  Few CTAs and at most 48
+// registers a thread, so that all of them are resident as soon as they are
+// launched: the forward grid, their programmatic dependent, launches only
+// once every carry CTA is.
+__global__ void __launch_bounds__(128, 10)
 tc_l2_carry_kernel(const float *__restrict__ Lfin, int nseg, int L, int T, int dkdv, int H,
                    const float *__restrict__ lam, __nv_bfloat16 *__restrict__ Cbf,
                    float *__restrict__ A_final, const unsigned int *__restrict__ cta_status, int n_cta,
@@ -314,39 +323,53 @@ tc_l2_carry_kernel(const float *__restrict__ Lfin, int nseg, int L, int T, int d
         if (threadIdx.x == 0) status[0] = st;
     }
     const int bh = blockIdx.y;
-    const int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
-    if (e >= dkdv) return;
+    const int e0 = (blockIdx.x * 2 * blockDim.x + threadIdx.x) * 4, estep = 4 * blockDim.x;
     const float lm = lam[bh % H];
     const float f = powf(lm, (float)(L * kBlk));  // decay across a full segment
-    const float *src = Lfin + (size_t)bh * nseg * dkdv + e;
-    __nv_bfloat16 *dst = Cbf + (size_t)bh * nseg * dkdv + e;
-    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-    // Segment finals are read eight at a time so their loads overlap; the
-    // recurrence itself is a chain of FMAs.
-    constexpr int kBatch = 8;
+    const float *src = Lfin + (size_t)bh * nseg * dkdv;
+    __nv_bfloat16 *dst = Cbf + (size_t)bh * nseg * dkdv;
+    float4 A[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    // Segment finals are read two at a time for both groups, so that four
+    // loads overlap; the recurrence itself is a chain of FMAs.
+    constexpr int kBatch = 2;
     for (int g0 = 0; g0 < nseg; g0 += kBatch) {
-        float4 d[kBatch];
+        float4 d[2][kBatch];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-            d[u] = g0 + u < nseg ? *reinterpret_cast<const float4 *>(src + (size_t)(g0 + u) * dkdv)
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int h = 0; h < 2; ++h) {
+            const int e = e0 + h * estep;
+#pragma unroll
+            for (int u = 0; u < kBatch; ++u)
+                d[h][u] = (e + 4 <= dkdv && g0 + u < nseg)
+                              ? *reinterpret_cast<const float4 *>(src + (size_t)(g0 + u) * dkdv + e)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
             const int g = g0 + u;
             if (g >= nseg) break;
-            uint2 o;
-            o.x = pack_bf16(A.x, A.y);
-            o.y = pack_bf16(A.z, A.w);
-            if (OPAM_BOUNDS(e + 4 <= dkdv, status)) *reinterpret_cast<uint2 *>(dst + (size_t)g * dkdv) = o;
             // the last segment may be shorter: its decay only matters for A_final
             const float fg = (g + 1) * L * kBlk <= T ? f : powf(lm, (float)(T - g * L * kBlk));
-            A.x = fmaf(fg, A.x, d[u].x);
-            A.y = fmaf(fg, A.y, d[u].y);
-            A.z = fmaf(fg, A.z, d[u].z);
-            A.w = fmaf(fg, A.w, d[u].w);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int e = e0 + h * estep;
+                if (e + 4 <= dkdv) {
+                    uint2 o;
+                    o.x = pack_bf16(A[h].x, A[h].y);
+                    o.y = pack_bf16(A[h].z, A[h].w);
+                    *reinterpret_cast<uint2 *>(dst + (size_t)g * dkdv + e) = o;
+                }
+                A[h].x = fmaf(fg, A[h].x, d[h][u].x);
+                A[h].y = fmaf(fg, A[h].y, d[h][u].y);
+                A[h].z = fmaf(fg, A[h].z, d[h][u].z);
+                A[h].w = fmaf(fg, A[h].w, d[h][u].w);
+            }
         }
     }
-    if (A_final && OPAM_BOUNDS(e + 4 <= dkdv, status)) *reinterpret_cast<float4 *>(A_final + (size_t)bh * dkdv + e) = A;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int e = e0 + h * estep;
+        if (A_final && e + 4 <= dkdv) *reinterpret_cast<float4 *>(A_final + (size_t)bh * dkdv + e) = A[h];
+    }
 }
 
 // --------------------------------------------------------------------- fused forward
@@ -1401,7 +1424,7 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         const float *eta, const float *gate, float scale, void *y, float *A_final, void *ws,
         unsigned int *status, cudaStream_t st, bool l2) {
     const int BH = B_ * H;
-    const Segments g = segments(BH, T, DV, num_sms());
+    const Segments g = segments(BH, T, DK, DV, num_sms());
     if (DK == 64 && DV == 64 && g.nch > 65535) {  // query blocks are the grid's y extent
         set_error("tc_layer_forward: T=%d above %d tokens on this path", T, 65535 * kBlk);
         return OPAM_ERR_UNSUPPORTED;
@@ -1424,14 +1447,16 @@ int run(const void *q, const void *k, const void *v, int B_, int H, int T, int W
         {
             using SC = StateCfg<DK>;
             auto kern = tc_l2_state_kernel<DK, DV>;
-            if (int rc_ = set_smem_limit((const void *)kern, (int)SC::SMEM, "tc_l2_state smem attribute")) return rc_;
-            kern<<<dim3(DV / 64, g.nseg, BH), 192, SC::SMEM, st>>>(mk, mv, T, W, H, lam, eta, g.nch, g.L, w.Aloc,
+            const uint32_t ssm = (DK == 64 && DV == 64) ? (SC::SMEM > kStateSoloSmem ? SC::SMEM : kStateSoloSmem)
+                                                        : SC::SMEM;
+            if (int rc_ = set_smem_limit((const void *)kern, (int)ssm, "tc_l2_state smem attribute")) return rc_;
+            kern<<<dim3(DV / 64, g.nseg, BH), 192, ssm, st>>>(mk, mv, T, W, H, lam, eta, g.nch, g.L, w.Aloc,
                                                                   w.Lfin, w.cta_status, status);
             if ((rc = launched("tc_l2_state"))) return rc;
         }
         {
             cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(ceil_div(DK * DV / 4, 128), BH);
+            cfg.gridDim = dim3(ceil_div(DK * DV / 4, 2 * 128), BH);  // two groups of 4 per thread
             cfg.blockDim = dim3(128);
             cfg.stream = st;
             cfg.attrs = pdl;
@@ -1488,7 +1513,7 @@ bool tc_prefill_tcgen05_supported(int dtype, int dk, int dv) {
 }
 
 size_t tc_prefill_tcgen05_workspace(int BH, int T, int dk, int dv) {
-    return ws_bytes(BH, segments(BH, T, dv, num_sms()), dk, dv);
+    return ws_bytes(BH, segments(BH, T, dk, dv, num_sms()), dk, dv);
 }
 
 int tc_prefill_tcgen05(const void *q, const void *k, const void *v, int B, int H, int T, int dk,

@@ -139,14 +139,15 @@ def test_cuda_graph_replay_matches_eager(cuda_lib):
 
 def test_multi_chunk_segments_full_tensor(cuda_lib, oracle_mod):
     """Every output element of a batch whose state recurrence is split into
-    segments of several chunks: 64 (batch, head) units leave about four
-    segments per head on a 148-SM GPU, so T = 2048 (16 chunks of 128) gives
-    segments of four chunks, and the carry lambda^(C (j - gL)) A_{gL} and the
-    local states A_j^loc are both exercised at every chunk."""
+    segments of several chunks: at d = 64 the library sizes the state pass to
+    one CTA per SM, so 64 (batch, head) units leave two segments per head on a
+    148-SM GPU and T = 2048 (16 chunks of 128) gives segments of eight chunks;
+    the carry lambda^(C (j - gL)) A_{gL} and the local states A_j^loc are both
+    exercised at every chunk."""
     B, H, T, d, W = 8, 8, 2048, 64, 256
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     nch = -(-T // 128)
-    want = max(1, min(nch, (2 * sms) // (B * H)))
+    want = max(1, min(nch, sms // (B * H)))
     chunks_per_segment = -(-nch // want)
     assert chunks_per_segment > 1 and -(-nch // chunks_per_segment) < nch
     inp = synth.tc_inputs(B, H, T, d, d, W, dtype="bf16", seed=55)
