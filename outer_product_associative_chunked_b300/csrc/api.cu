@@ -349,11 +349,11 @@ int tc_layer_backward(const void *q, const void *k, const void *v, int dtype, in
         return OPAM_ERR_WORKSPACE;
     }
     OPAM_CHECK_PTR(workspace);
-    // No kernel of the backward waits on a barrier; its last kernel zeroes
-    // the status words.
+    cudaStream_t s = (cudaStream_t)stream;
+    if (int rc = clear_status(workspace, s)) return rc;
     return tc_backward(q, k, v, dtype, B, H, T, d_k, d_v, W, lambda, eta, gate,
                        resolve_scale(softmax_scale, d_k), dy, dq, dk, dv, dlambda, deta, dgate,
-                       status_body(workspace), status_word(workspace), (cudaStream_t)stream);
+                       status_body(workspace), status_word(workspace), s);
 }
 
 size_t tc_decode_step_workspace_size(const opam_tc_state *st) {

@@ -67,6 +67,7 @@ __device__ __forceinline__ float warp_max(float x) {
 // opam_check_device_error reads them.
 constexpr unsigned int kStatusTcPrefill = 1u << 0;   // 7 bits: Tensor Cache prefill kernels
 constexpr unsigned int kStatusDelta = 1u << 8;       // 5 bits: DeltaNet tensor-core kernels
+constexpr unsigned int kStatusTcBackward = 1u << 13;  // 3 bits: Tensor Cache backward tensor-core kernel
 constexpr unsigned int kStatusSelfTest = 1u << 16;   // the bounded-wait self-test
 constexpr unsigned int kStatusKeygen = 1u << 20;     // 3 bits: BDH key generation
 constexpr unsigned int kStatusBounds = 1u << 24;     // an index check failed (debug-bounds builds)
@@ -123,6 +124,12 @@ int bounded_wait_selftest(int arrive, long long limit, unsigned int *status, cud
 int bounds_selftest(int n, unsigned int *status, cudaStream_t s);
 
 // Tensor Cache layer backward (CUDA cores; bf16 or fp32 inputs).
+// Window part of the Tensor Cache backward's dK and dV on the tensor cores
+// (bf16, d_k = d_v = 64); LSE and D rows at stride lstride (a multiple of 128).
+bool tcb_window_dkdv_tcgen05_supported(int dtype, int dk, int dv);
+int tcb_window_dkdv_tcgen05(const void *q, const void *k, const void *v, const void *dy, int BH, int Tn, int W,
+                            float scale, const float *lse, const float *D, int lstride, float *dK, float *dV,
+                            unsigned int *status, cudaStream_t st);
 size_t tc_backward_workspace(int BH, int T, int dk, int dv);
 int tc_backward(const void *q, const void *k, const void *v, int dtype, int B, int H, int T, int dk, int dv, int W,
                 const float *lam, const float *eta, const float *gate, float scale, const void *dy, void *dq,

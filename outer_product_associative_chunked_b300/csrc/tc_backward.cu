@@ -49,6 +49,8 @@
 // 256 threads as a 16 x 16 grid, each owning a 4 x (N/16) block).
 #include <math.h>
 
+#include <type_traits>
+
 #include "opam_internal.cuh"
 
 namespace opam {
@@ -198,7 +200,8 @@ template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThr)
 tcb_window_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                      const T *__restrict__ dy, int Tn, int W, float scale, float *__restrict__ lse_g,
-                     float *__restrict__ D_g, float *__restrict__ dQacc, unsigned int *__restrict__ status) {
+                     float *__restrict__ D_g, int lstride, float *__restrict__ dQacc,
+                     unsigned int *__restrict__ status) {
     using C = WinCfg<DK, DV>;
     constexpr int LQ = C::LQ, LV = C::LV, TNV = DV / 16, TNK = DK / 16;
     extern __shared__ float sm[];
@@ -287,8 +290,8 @@ tcb_window_dq_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *
             const float ls = l > 0.f ? rm[r] + __logf(l) : 0.f;
             rD[r] = d;
             rf[r] = ls;
-            const size_t at = (size_t)bh * Tn + q0 + r;
-            if (q0 + r < Tn && OPAM_BOUNDS(at < (size_t)gridDim.y * Tn, status)) {
+            const size_t at = (size_t)bh * lstride + q0 + r;
+            if (q0 + r < Tn && OPAM_BOUNDS(at < (size_t)gridDim.y * lstride, status)) {
                 lse_g[at] = ls;
                 D_g[at] = d;
             }
@@ -336,8 +339,8 @@ template <typename T, int DK, int DV>
 __global__ void __launch_bounds__(kThr)
 tcb_window_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                        const T *__restrict__ dy, int Tn, int W, float scale, const float *__restrict__ lse_g,
-                       const float *__restrict__ D_g, float *__restrict__ dKacc, float *__restrict__ dVacc,
-                       unsigned int *__restrict__ status) {
+                       const float *__restrict__ D_g, int lstride, float *__restrict__ dKacc,
+                       float *__restrict__ dVacc, unsigned int *__restrict__ status) {
     using C = WinCfg<DK, DV>;
     constexpr int LQ = C::LQ, LV = C::LV, TNV = DV / 16, TNK = DK / 16;
     extern __shared__ float sm[];
@@ -361,8 +364,8 @@ tcb_window_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
         load_rows<T, DV>(dYs, LV, dyh, DV, t0, 0, Tn, 0);
         if (tid < kR) {
             const bool ok = t0 + tid < Tn;
-            rL[tid] = ok ? lse_g[(size_t)bh * Tn + t0 + tid] : 0.f;
-            rD[tid] = ok ? D_g[(size_t)bh * Tn + t0 + tid] : 0.f;
+            rL[tid] = ok ? lse_g[(size_t)bh * lstride + t0 + tid] : 0.f;
+            rD[tid] = ok ? D_g[(size_t)bh * lstride + t0 + tid] : 0.f;
         }
         __syncthreads();
         // rows = keys (m), columns = queries (n)
@@ -692,7 +695,6 @@ tcb_finalize_kernel(const float *__restrict__ dQacc, const float *__restrict__ d
                     const float *__restrict__ part_r, const float *__restrict__ gate, float *__restrict__ dlam,
                     float *__restrict__ deta, float *__restrict__ dgate, unsigned int *__restrict__ status) {
     __shared__ float red[kThr / 32];
-    if (blockIdx.x == 0 && threadIdx.x < kStatusWords) status[threadIdx.x] = 0u;
     if ((int)blockIdx.x < nconv) {
         const size_t stride = (size_t)nconv * blockDim.x;
         for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < nqk; i += stride) {
@@ -730,6 +732,10 @@ tcb_finalize_kernel(const float *__restrict__ dQacc, const float *__restrict__ d
 }
 
 // ------------------------------------------------------------------ host
+// LSE and D rows are padded to a multiple of 128 entries, so that the
+// tensor-core dK/dV kernel copies each 128-query tile of them whole.
+int lse_stride(int T) { return ceil_div(T, 128) * 128; }
+
 struct BwdWs {
     float *lse, *D, *dQ, *dK, *dV, *part, *part_f, *part_r;
 };
@@ -743,8 +749,9 @@ BwdWs carve_bwd(void *ws, int BH, int T, int dk, int dv) {
         p += align_up(floats * sizeof(float), 256);
         return r;
     };
-    w.lse = take((size_t)BH * T);
-    w.D = take((size_t)BH * T);
+    const size_t ls = (size_t)BH * lse_stride(T);
+    w.lse = take(ls);
+    w.D = take(ls);
     w.dQ = take((size_t)BH * T * dk);
     w.dK = take((size_t)BH * T * dk);
     w.dV = take((size_t)BH * T * dv);
@@ -767,14 +774,20 @@ int run_bwd(const void *q, const void *k, const void *v, int B, int H, int Tn, i
         const int smem = (int)WinCfg<DK, DV>::SMEM;
         if ((rc = set_smem_limit((const void *)kern, smem, "tcb_window_dq smem attribute"))) return rc;
         prof_begin(s);
-        kern<<<dim3(nch, BH), kThr, smem, s>>>(Q, K, V, dY, Tn, W, scale, w.lse, w.D, w.dQ, status);
+        kern<<<dim3(nch, BH), kThr, smem, s>>>(Q, K, V, dY, Tn, W, scale, w.lse, w.D, lse_stride(Tn), w.dQ,
+                                               status);
         if ((rc = launched("tcb_window_dq"))) return rc;
     }
-    {
+    if (tcb_window_dkdv_tcgen05_supported(std::is_same<T, __nv_bfloat16>::value ? OPAM_BF16 : OPAM_F32, DK, DV)) {
+        if ((rc = tcb_window_dkdv_tcgen05(Q, K, V, dY, BH, Tn, W, scale, w.lse, w.D, lse_stride(Tn), w.dK, w.dV,
+                                          status, s)))
+            return rc;
+    } else {
         auto kern = tcb_window_dkdv_kernel<T, DK, DV>;
         const int smem = (int)WinCfg<DK, DV>::SMEM;
         if ((rc = set_smem_limit((const void *)kern, smem, "tcb_window_dkdv smem attribute"))) return rc;
-        kern<<<dim3(nch, BH), kThr, smem, s>>>(Q, K, V, dY, Tn, W, scale, w.lse, w.D, w.dK, w.dV, status);
+        kern<<<dim3(nch, BH), kThr, smem, s>>>(Q, K, V, dY, Tn, W, scale, w.lse, w.D, lse_stride(Tn), w.dK, w.dV,
+                                               status);
         if ((rc = launched("tcb_window_dkdv"))) return rc;
     }
     {
@@ -836,7 +849,7 @@ int bwd_dk(int dkk, int dvv, const void *q, const void *k, const void *v, int B,
 size_t tc_backward_workspace(int BH, int T, int dk, int dv) {
     const int nch = ceil_div(T, kR), nsl = dv / kSW;
     auto f = [](size_t floats) { return align_up(floats * sizeof(float), 256); };
-    return 2 * f((size_t)BH * T) + 2 * f((size_t)BH * T * dk) + f((size_t)BH * T * dv) + f((size_t)BH * nch * 4) +
+    return 2 * f((size_t)BH * lse_stride(T)) + 2 * f((size_t)BH * T * dk) + f((size_t)BH * T * dv) + f((size_t)BH * nch * 4) +
            f((size_t)BH * nsl * 2) + f((size_t)BH * nsl);
 }
 

@@ -53,6 +53,11 @@ TC_CASES = [
     ("bf16", 2, 1, 500, 128, 128, 100, None, None),
     ("bf16", 1, 1, 777, 64, 128, 300, None, None),
     ("bf16", 3, 1, 129, 128, 64, 64, None, None),
+    # bf16 d = 64 takes the tensor-core dK/dV kernel: W a multiple of the
+    # 128-key tile with a ragged tail, a single token, and W > T
+    ("bf16", 2, 1, 300, 64, 64, 128, None, None),
+    ("bf16", 1, 1, 1, 64, 64, 1, None, None),
+    ("bf16", 1, 2, 200, 64, 64, 256, None, None),
 ]
 
 
