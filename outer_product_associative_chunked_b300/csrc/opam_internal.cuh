@@ -127,6 +127,11 @@ int bounds_selftest(int n, unsigned int *status, cudaStream_t s);
 // Window part of the Tensor Cache backward's dK and dV on the tensor cores
 // (bf16, d_k = d_v = 64); LSE and D rows at stride lstride (a multiple of 128).
 bool tcb_window_dkdv_tcgen05_supported(int dtype, int dk, int dv);
+// Window dQ with the softmax statistics it writes (LSE, D at stride lstride),
+// on the tensor cores for the same sizes.
+int tcb_window_dq_tcgen05(const void *q, const void *k, const void *v, const void *dy, int BH, int Tn, int W,
+                          float scale, float *lse, float *D, int lstride, float *dQ, unsigned int *status,
+                          cudaStream_t st);
 int tcb_window_dkdv_tcgen05(const void *q, const void *k, const void *v, const void *dy, int BH, int Tn, int W,
                             float scale, const float *lse, const float *D, int lstride, float *dK, float *dV,
                             unsigned int *status, cudaStream_t st);

@@ -769,16 +769,22 @@ int run_bwd(const void *q, const void *k, const void *v, int B, int H, int Tn, i
     const BwdWs w = carve_bwd(ws, BH, Tn, DK, DV);
     const T *Q = (const T *)q, *K = (const T *)k, *V = (const T *)v, *dY = (const T *)dy;
     int rc;
-    {
+    const bool tc = tcb_window_dkdv_tcgen05_supported(std::is_same<T, __nv_bfloat16>::value ? OPAM_BF16 : OPAM_F32,
+                                                      DK, DV);
+    prof_begin(s);
+    if (tc) {
+        if ((rc = tcb_window_dq_tcgen05(Q, K, V, dY, BH, Tn, W, scale, w.lse, w.D, lse_stride(Tn), w.dQ, status,
+                                        s)))
+            return rc;
+    } else {
         auto kern = tcb_window_dq_kernel<T, DK, DV>;
         const int smem = (int)WinCfg<DK, DV>::SMEM;
         if ((rc = set_smem_limit((const void *)kern, smem, "tcb_window_dq smem attribute"))) return rc;
-        prof_begin(s);
         kern<<<dim3(nch, BH), kThr, smem, s>>>(Q, K, V, dY, Tn, W, scale, w.lse, w.D, lse_stride(Tn), w.dQ,
                                                status);
         if ((rc = launched("tcb_window_dq"))) return rc;
     }
-    if (tcb_window_dkdv_tcgen05_supported(std::is_same<T, __nv_bfloat16>::value ? OPAM_BF16 : OPAM_F32, DK, DV)) {
+    if (tc) {
         if ((rc = tcb_window_dkdv_tcgen05(Q, K, V, dY, BH, Tn, W, scale, w.lse, w.D, lse_stride(Tn), w.dK, w.dV,
                                           status, s)))
             return rc;
