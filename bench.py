@@ -98,19 +98,38 @@ def delta_decode_work(S, H, d_k, d_v, elem):
     return flops, bytes_
 
 
-def tc_backward_work(B, H, T, d_k, d_v, W, elem):
+def tc_backward_work(B, H, T, d_k, d_v, W, elem, split=False):
     """Backward of the prefill: the window part recomputes S = QK^T and the
     statistics (2 d_k per pair), y_loc (2 d_v), then dP = dy V^T (2 d_v),
     dQ, dK (2 d_k each) and dV (2 d_v) per (query, key) pair in the window;
     the L2 part is four d_k x d_v contractions per evicted token (dq, dk',
     dv', and the state write it replays), plus the same for the lambda
-    derivative.  Bytes: q, k, v, dy read once; dq, dk, dv written once."""
+    derivative.  Bytes: q, k, v, dy read once; dq, dk, dv written once.
+    With split=True the flops come back as (window, L2) separately."""
     BH = B * H
     pairs = tc_pairs(T, W) * BH
-    flops = pairs * (2 * d_k + 2 * d_v + 2 * d_v + 2 * d_k + 2 * d_k + 2 * d_v)
-    flops += 10 * d_k * d_v * max(0, T - W) * BH
-    bytes_ = BH * T * (3 * d_k + 3 * d_v) * elem + BH * T * 0
-    return flops, bytes_
+    window = pairs * (2 * d_k + 2 * d_v + 2 * d_v + 2 * d_k + 2 * d_k + 2 * d_v)
+    l2 = 10 * d_k * d_v * max(0, T - W) * BH
+    bytes_ = BH * T * (3 * d_k + 3 * d_v) * elem
+    if split:
+        return window, l2, bytes_
+    return window + l2, bytes_
+
+
+def mixed_roofline(fl_tc, fl_alu, bytes_, seconds, peaks, scope):
+    """Roofline of work split between the tensor cores (fl_tc at the bf16
+    burst peak) and the CUDA cores (fl_alu at the FP32 FMA rate): the ideal
+    time is the sum of the two, and the peak reported is the effective rate
+    (all flops over that time), so frac = ideal time / measured time."""
+    t_tc = fl_tc / (peaks["bf16_tflops"] * 1e12)
+    t_alu = fl_alu / (peaks["fp32_tflops"] * 1e12)
+    fl = fl_tc + fl_alu
+    ach = fl / seconds / 1e12
+    peak = fl / (t_tc + t_alu) / 1e12
+    return {"bound": "alu" if t_alu >= t_tc else "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+            "frac": ach / peak, "traffic": None, "algorithmic_bytes": bytes_, "algorithmic_flops": fl,
+            "scope": scope, "peak_kind": "mixed: bf16_tflops for the window products, fp32_tflops for the L2 part",
+            "ideal_us": {"tensor": t_tc * 1e6, "alu": t_alu * 1e6}}
 
 
 def delta_backward_work(B, H, T, d_k, d_v, elem):
@@ -654,9 +673,15 @@ def bench_extras(args, torch, binding, synth, peaks, flush):
     for _ in range(Wm):
         step()
     ms, dom = timed_steps(step, K, flush, torch, prof=True, binding=binding)
-    fl, by = tc_backward_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], 2)
-    summarize(name, d["B"] * d["T"], ms, fl, by, "fp32", "tcb_window_dq .. tcb_finalize (all five)", dom)
-    out[name]["note"] = "value = tokens/s of the backward pass; fp32 arithmetic on the CUDA cores"
+    fl_w, fl_l2, by = tc_backward_work(d["B"], d["H"], d["T"], d["d_k"], d["d_v"], d["W"], 2, split=True)
+    summarize(name, d["B"] * d["T"], ms, fl_w + fl_l2, by, "fp32", "tcb_window_dq_tc .. tcb_finalize (all five)",
+              dom)
+    out[name]["roofline"] = mixed_roofline(fl_w, fl_l2, by, statistics.mean(ms) / 1e3, peaks, "step")
+    if dom:
+        out[name]["dominant_roofline"] = mixed_roofline(fl_w, fl_l2, by, statistics.mean(dom) / 1e3, peaks,
+                                                        "kernel")
+    out[name]["note"] = ("value = tokens/s of the backward pass; the window products on the tensor cores (bf16 "
+                         "operands, fp32 accumulation), the L2 part in fp32 on the CUDA cores")
     del q, k, v, dy, outs, ws
 
     # Backward of the delta rule at the DeltaNet workload's shape.
