@@ -27,7 +27,7 @@ def _gpu(inp):
 
 
 def test_two_calls_match_workspace_entry_point(cuda_lib, oracle_mod):
-    # The headline shape needs about 14.7 MB of scratch on a 148-SM GPU (the
+    # The headline shape needs about 11.5 MB of scratch on a 148-SM GPU (the
     # segment count, and with it the size, follows the SM count).
     B, H, T, d, W = 4, 8, 4096, 64, 512
     need = cuda_lib.tc_layer_forward_workspace_size(B, H, T, d, d, W, torch.bfloat16)
