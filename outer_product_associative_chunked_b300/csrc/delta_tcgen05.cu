@@ -72,14 +72,10 @@ __device__ __forceinline__ float4 ld4(const float *S, int i, int q) { return *re
 __device__ __forceinline__ void st4(float *S, int i, int q, float4 v) { *reinterpret_cast<float4 *>(S + lsw4(i, q)) = v; }
 
 // ---- warp-level products for the solve: mma.sync m16n8k8 with tf32
-// operands and fp32 accumulation, each operand split into a tf32 head and
-// a tf32 remainder (x = hi + lo) and the three significant cross products
-// accumulated, which keeps the products at fp32 accuracy.
-__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
-    const float r = x - __uint_as_float(hi);
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
-}
+// operands (rounded to nearest) and fp32 accumulation.  Splitting each
+// operand into a tf32 head and remainder (three products instead of one)
+// left the layer's output error unchanged -- it is set by the bf16 operands
+// of the state products -- and cost 10% of the forward, so one product it is.
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
     asm volatile(
         "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
@@ -99,13 +95,11 @@ __device__ __forceinline__ void warp_tile_mma(float (&d)[4], int lane, FA fa, FB
     for (int k0 = 0; k0 < K; k0 += 8) {
         const float av[4] = {fa(g, k0 + t), fa(g + 8, k0 + t), fa(g, k0 + t + 4), fa(g + 8, k0 + t + 4)};
         const float bv[2] = {fb(k0 + t, g), fb(k0 + t + 4, g)};
-        uint32_t ah[4], al[4], bh[2], bl[2];
+        uint32_t ah[4], bh[2];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split_tf32(av[e], ah[e], al[e]);
+        for (int e = 0; e < 4; ++e) asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(ah[e]) : "f"(av[e]));
 #pragma unroll
-        for (int e = 0; e < 2; ++e) split_tf32(bv[e], bh[e], bl[e]);
-        mma_tf32(d, al, bh);
-        mma_tf32(d, ah, bl);
+        for (int e = 0; e < 2; ++e) asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(bh[e]) : "f"(bv[e]));
         mma_tf32(d, ah, bh);
     }
 }
@@ -119,18 +113,13 @@ __device__ __forceinline__ void warp_tile_mma2(float (&d0)[4], float (&d1)[4], i
     for (int k0 = 0; k0 < K; k0 += 8) {
         const float av[4] = {fa(g, k0 + t), fa(g + 8, k0 + t), fa(g, k0 + t + 4), fa(g + 8, k0 + t + 4)};
         const float bv[4] = {fb(k0 + t, g), fb(k0 + t + 4, g), fb(k0 + t, 8 + g), fb(k0 + t + 4, 8 + g)};
-        uint32_t ah[4], al[4], bh[4], bl[4];
+        uint32_t ah[4], bh[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            split_tf32(av[e], ah[e], al[e]);
-            split_tf32(bv[e], bh[e], bl[e]);
+            asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(ah[e]) : "f"(av[e]));
+            asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(bh[e]) : "f"(bv[e]));
         }
-        const uint32_t bh0[2] = {bh[0], bh[1]}, bl0[2] = {bl[0], bl[1]};
-        const uint32_t bh1[2] = {bh[2], bh[3]}, bl1[2] = {bl[2], bl[3]};
-        mma_tf32(d0, al, bh0);
-        mma_tf32(d1, al, bh1);
-        mma_tf32(d0, ah, bl0);
-        mma_tf32(d1, ah, bl1);
+        const uint32_t bh0[2] = {bh[0], bh[1]}, bh1[2] = {bh[2], bh[3]};
         mma_tf32(d0, ah, bh0);
         mma_tf32(d1, ah, bh1);
     }
