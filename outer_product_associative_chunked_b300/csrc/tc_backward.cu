@@ -81,6 +81,27 @@ __device__ __forceinline__ void mm_tile(float (&acc)[TM][TN], const float *A, in
     }
 }
 
+// Two single-column products that share A, in one pass over it:
+// acc0[i] += sum_k A(m_i, k) B0(k, tx), acc1[i] += sum_k A(m_i, k) B1(k, tx)
+// (the same order of operations per accumulator as two mm_tile<TM, 1> calls).
+template <int TM>
+__device__ __forceinline__ void mm_tile_2(float (&acc0)[TM][1], float (&acc1)[TM][1], const float *A, int am, int ak,
+                                          const float *B0, const float *B1, int bk, int bn, int K) {
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float a[TM];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) a[i] = A[(ty + 16 * i) * am + k * ak];
+        const float b0 = B0[k * bk + tx * bn], b1 = B1[k * bk + tx * bn];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            acc0[i][0] = fmaf(a[i], b0, acc0[i][0]);
+            acc1[i][0] = fmaf(a[i], b1, acc1[i][0]);
+        }
+    }
+}
+
 template <int TM, int TN>
 __device__ __forceinline__ void zero(float (&acc)[TM][TN]) {
 #pragma unroll
@@ -593,8 +614,7 @@ tcb_l2_scan_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
             zero(X);
             zero(Xp);
             zero(dq);
-            mm_tile<4, 1>(X, Qs, LQ, 1, St, LW, 1, DK);
-            mm_tile<4, 1>(Xp, Qs, LQ, 1, St2, LW, 1, DK);
+            mm_tile_2<4>(X, Xp, Qs, LQ, 1, St, St2, LW, 1, DK);
             mm_tile<4, TNK>(dq, dMs, LW, 1, St, 1, LW, kSW);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -621,8 +641,7 @@ tcb_l2_scan_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
             float a1[TMK][1], a2[TMK][1];
             zero(a1);
             zero(a2);
-            mm_tile<TMK, 1>(a1, Kp, 1, LQ, Vw, LW, 1, kR);
-            mm_tile<TMK, 1>(a2, Kp, 1, LQ, Vw2, LW, 1, kR);
+            mm_tile_2<TMK>(a1, a2, Kp, 1, LQ, Vw, Vw2, LW, 1, kR);
             const float ln = pw[n], dln = dpw[n];
 #pragma unroll
             for (int i = 0; i < TMK; ++i) {
