@@ -20,7 +20,8 @@
 //   warps 0-7        epilogue: warps w and w + 4 share TMEM lane quarter w and
 //                    take 64 columns each; a thread first counts the entries
 //                    above theta in its 64 values, the two halves exchange
-//                    counts, then each writes its entries in place.
+//                    counts, then each writes its entries in place
+//                    (coordinate lists: through a shared-memory stage).
 // Two output forms:
 //   row lists (ROWS): D = x U (M = tokens), thread = token row: a = acc -
 //     theta; if a > 0 append (n, a) to the row's list (the per-row format the
@@ -45,6 +46,10 @@ namespace {
 
 constexpr int kM = 128;   // token rows per CTA
 constexpr int kNT = 128;  // columns of U_h per tile
+// Coordinate lists: a tile's entries (one contiguous range of the block's
+// lists) are staged in shared memory when at most this many, then written
+// out with coalesced stores.
+constexpr int kStage = 4096;
 
 enum : unsigned int {
     kStKgProducer = kStatusKeygen << 0,
@@ -57,7 +62,8 @@ struct KgCfg {
     static constexpr uint32_t ABYTES = kM * R * 2;      // x tile, R/64 K-major blocks of 16 KB
     static constexpr uint32_t BBYTES = R * kNT * 2;     // U tile, two MN-major blocks of R x 64
     static constexpr uint32_t OFF_B = ABYTES;
-    static constexpr uint32_t SMEM = ABYTES + 2 * BBYTES + 1024;  // + alignment slack
+    static constexpr uint32_t OFF_S = ABYTES + 2 * BBYTES;  // staged values (fp32), then tokens (u8)
+    static constexpr uint32_t SMEM = OFF_S + kStage * 5 + 1024;  // + alignment slack
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -192,6 +198,8 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
         const size_t row = (size_t)bh * T + blk * kM + r;                               // list row (ROWS)
         int *oi = (is_q ? qidx : kidx) + row * (size_t)N;
         float *ov = (is_q ? qval : kval) + row * (size_t)N;
+        float *scv = (float *)(sm + C::OFF_S);
+        uint8_t *sct = sm + C::OFF_S + kStage * 4;
         int base = 0;  // ROWS: entries of row r so far; otherwise entries of the block so far
         bool ok = true;
         for (int i = 0; i < ntile && ok; ++i) {
@@ -206,17 +214,20 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&B.acc_empty[s]);
-            // a value counts when it is above theta and its token is in the sequence
+            // a value counts when it is above theta and its token is in the
+            // sequence: values of tokens past T become -inf first
+            if (ROWS ? !row_live : nlive < kM) {
+#pragma unroll
+                for (int c = 0; c < 64; ++c)
+                    if (ROWS || 64 * hf + c >= nlive) a[c] = -INFINITY;
+            }
             int n = 0;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const bool live = ROWS ? row_live : (64 * hf + c < nlive);
-                n += (live && a[c] - theta > 0.f) ? 1 : 0;
-            }
+            for (int c = 0; c < 64; ++c) n += (a[c] - theta > 0.f) ? 1 : 0;
             hcnt[s][hf][r] = n;
             epi_barrier();
             const int lo = hcnt[s][0][r];
-            int p;
+            int p, b0 = base, ttot = 0;  // !ROWS: the tile's range [b0, b0 + ttot)
             if constexpr (ROWS) {
                 p = base + (hf ? lo : 0);
                 base += lo + hcnt[s][1][r];
@@ -235,19 +246,23 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
                 for (int w = 0; w < qd; ++w) start += wtot[s][w];
                 if (hf == 0 && OPAM_BOUNDS(i * kNT + r < N, status)) off[i * kNT + r] = start;
                 p = start + (hf ? lo : 0);
-                base += wtot[s][0] + wtot[s][1] + wtot[s][2] + wtot[s][3];
+                ttot = wtot[s][0] + wtot[s][1] + wtot[s][2] + wtot[s][3];
+                base += ttot;
             }
+            const bool staged = !ROWS && ttot <= kStage;  // the same in every epilogue thread
             const int c0 = i * kNT + 64 * hf;  // ROWS: first coordinate of these columns
 #pragma unroll
             for (int c = 0; c < 64; ++c) {
-                const bool live = ROWS ? row_live : (64 * hf + c < nlive);
                 const float x = a[c] - theta;
-                if (live && x > 0.f) {
+                if (x > 0.f) {
                     if constexpr (ROWS) {
                         if (OPAM_BOUNDS(p < N, status)) {
                             oi[p] = c0 + c;
                             ov[p] = x;
                         }
+                    } else if (staged) {
+                        scv[p - b0] = x;
+                        sct[p - b0] = (uint8_t)(64 * hf + c);
                     } else {
                         if (OPAM_BOUNDS(p < kM * N, status)) {
                             et[p] = (uint8_t)(64 * hf + c);
@@ -255,6 +270,15 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
                         }
                     }
                     ++p;
+                }
+            }
+            if (staged) {
+                epi_barrier();
+                for (int j = tid; j < ttot; j += 256) {
+                    if (OPAM_BOUNDS(b0 + j < kM * N, status)) {
+                        et[b0 + j] = sct[j];
+                        ev[b0 + j] = scv[j];
+                    }
                 }
             }
         }

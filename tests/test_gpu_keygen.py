@@ -32,6 +32,7 @@ CASES = [
     (1, 2, 300, 256, 4096, 256, None),
     (1, 1, 257, 256, 2048, 128, None),
     (1, 1, 70, 64, 256, 32, -0.5),     # most entries kept: lists near their capacity
+    (1, 2, 350, 128, 1024, 64, 0.6745),  # a quarter kept: 128 x 128 tiles of about 4096 entries, some more
     (1, 1, 50, 64, 128, 64, 40.0),     # no entry passes: y = 0
 ]
 
