@@ -47,9 +47,9 @@ namespace {
 constexpr int kM = 128;   // token rows per CTA
 constexpr int kNT = 128;  // columns of U_h per tile
 // Coordinate lists: a tile's entries (one contiguous range of the block's
-// lists) are staged in shared memory when at most this many, then written
-// out with coalesced stores.
-constexpr int kStage = 4096;
+// lists) are staged in shared memory as 8-byte (value, token) pairs when at
+// most this many, then written out with coalesced stores.
+constexpr int kStage = 3584;
 
 enum : unsigned int {
     kStKgProducer = kStatusKeygen << 0,
@@ -62,8 +62,8 @@ struct KgCfg {
     static constexpr uint32_t ABYTES = kM * R * 2;      // x tile, R/64 K-major blocks of 16 KB
     static constexpr uint32_t BBYTES = R * kNT * 2;     // U tile, two MN-major blocks of R x 64
     static constexpr uint32_t OFF_B = ABYTES;
-    static constexpr uint32_t OFF_S = ABYTES + 2 * BBYTES;  // staged values (fp32), then tokens (u8)
-    static constexpr uint32_t SMEM = OFF_S + kStage * 5 + 1024;  // + alignment slack
+    static constexpr uint32_t OFF_S = ABYTES + 2 * BBYTES;  // the stage: kStage (value, token) pairs
+    static constexpr uint32_t SMEM = OFF_S + kStage * 8 + 1024;  // + alignment slack
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -76,6 +76,19 @@ struct KgBars {
 // also returns whether `ok` holds in every one of them, so that all eight
 // leave their loop together.
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Appends (x, t) at shared address sa, and advances sa, when x > 0 -- as
+// predicated instructions, with no branch per value; then t += 1.
+__device__ __forceinline__ void stage_put(uint32_t &sa, uint32_t &t, float x) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.gt.f32 q, %2, 0f00000000;\n\t"
+        "@q st.shared.v2.b32 [%0], {%2, %1};\n\t"
+        "@q add.u32 %0, %0, 8;\n\t"
+        "add.u32 %1, %1, 1;\n\t}"
+        : "+r"(sa), "+r"(t)
+        : "f"(x)
+        : "memory");
+}
 __device__ __forceinline__ bool epi_all(bool ok) {
     uint32_t r;
     asm volatile(
@@ -198,8 +211,7 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
         const size_t row = (size_t)bh * T + blk * kM + r;                               // list row (ROWS)
         int *oi = (is_q ? qidx : kidx) + row * (size_t)N;
         float *ov = (is_q ? qval : kval) + row * (size_t)N;
-        float *scv = (float *)(sm + C::OFF_S);
-        uint8_t *sct = sm + C::OFF_S + kStage * 4;
+        const uint2 *stage = reinterpret_cast<const uint2 *>(sm + C::OFF_S);
         int base = 0;  // ROWS: entries of row r so far; otherwise entries of the block so far
         bool ok = true;
         for (int i = 0; i < ntile && ok; ++i) {
@@ -211,19 +223,18 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
             tmem_ld32(tm + tcol + s * kNT + 64 * hf, *reinterpret_cast<float(*)[32]>(a));
             tmem_ld32(tm + tcol + s * kNT + 64 * hf + 32, *reinterpret_cast<float(*)[32]>(a + 32));
             tmem_wait_ld();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&B.acc_empty[s]);
             // a value counts when it is above theta and its token is in the
-            // sequence: values of tokens past T become -inf first
-            if (ROWS ? !row_live : nlive < kM) {
+            // sequence (tokens past T are dead columns)
+            const bool tail = ROWS ? !row_live : nlive < kM;
+            auto dead = [&](int c) { return ROWS || 64 * hf + c >= nlive; };
+            if (tail) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
-                    if (ROWS || 64 * hf + c >= nlive) a[c] = -INFINITY;
+                    if (dead(c)) a[c] = -INFINITY;
             }
             int n = 0;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) n += (a[c] - theta > 0.f) ? 1 : 0;
+            for (int c = 0; c < 64; ++c) n += a[c] - theta > 0.f ? 1 : 0;
             hcnt[s][hf][r] = n;
             epi_barrier();
             const int lo = hcnt[s][0][r];
@@ -249,35 +260,56 @@ bdh_keygen_kernel(const __grid_constant__ CUtensorMap mxk, const __grid_constant
                 ttot = wtot[s][0] + wtot[s][1] + wtot[s][2] + wtot[s][3];
                 base += ttot;
             }
+            // The values are read from TMEM again, 32 columns at a time (fewer
+            // live registers than holding all 64); the accumulator is released
+            // after that, which is still well before the MMAs of tile i + 2.
             const bool staged = !ROWS && ttot <= kStage;  // the same in every epilogue thread
-            const int c0 = i * kNT + 64 * hf;  // ROWS: first coordinate of these columns
+            uint32_t sa = smem_u32(stage + (p - b0)), tok = 64 * hf;  // staged: this thread's entries
+#pragma unroll 1
+            for (int h2 = 0; h2 < 2; ++h2) {
+                float b[32];
+                tmem_ld32(tm + tcol + s * kNT + 64 * hf + 32 * h2, b);
+                tmem_wait_ld();
+                if (tail) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const float x = a[c] - theta;
-                if (x > 0.f) {
-                    if constexpr (ROWS) {
-                        if (OPAM_BOUNDS(p < N, status)) {
-                            oi[p] = c0 + c;
-                            ov[p] = x;
-                        }
-                    } else if (staged) {
-                        scv[p - b0] = x;
-                        sct[p - b0] = (uint8_t)(64 * hf + c);
-                    } else {
-                        if (OPAM_BOUNDS(p < kM * N, status)) {
-                            et[p] = (uint8_t)(64 * hf + c);
-                            ev[p] = x;
+                    for (int c = 0; c < 32; ++c)
+                        if (dead(32 * h2 + c)) b[c] = -INFINITY;
+                }
+                if (staged) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) stage_put(sa, tok, b[c] - theta);
+                } else {
+                    const int c0 = i * kNT + 64 * hf + 32 * h2;  // ROWS: first coordinate of these columns
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const float x = b[c] - theta;
+                        if (x > 0.f) {
+                            if constexpr (ROWS) {
+                                if (OPAM_BOUNDS(p < N, status)) {
+                                    oi[p] = c0 + c;
+                                    ov[p] = x;
+                                }
+                            } else {
+                                if (OPAM_BOUNDS(p < kM * N, status)) {
+                                    et[p] = (uint8_t)(64 * hf + 32 * h2 + c);
+                                    ev[p] = x;
+                                }
+                            }
+                            ++p;
                         }
                     }
-                    ++p;
                 }
             }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&B.acc_empty[s]);
             if (staged) {
                 epi_barrier();
                 for (int j = tid; j < ttot; j += 256) {
                     if (OPAM_BOUNDS(b0 + j < kM * N, status)) {
-                        et[b0 + j] = sct[j];
-                        ev[b0 + j] = scv[j];
+                        const uint2 e = stage[j];
+                        et[b0 + j] = (uint8_t)e.y;
+                        ev[b0 + j] = __uint_as_float(e.x);
                     }
                 }
             }
