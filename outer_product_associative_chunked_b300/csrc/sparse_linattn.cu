@@ -396,9 +396,9 @@ constexpr int kCap = 2048;  // list entries per window buffered in shared memory
 
 struct PairSmem {
     float Z[kTB * (kTB + 1)];
-    float qv[kCap], kv[kCap];
+    uint2 qe[kCap], ke[kCap];  // the window's list entries: (value bits, token)
+    uint32_t qk[kCap];         // per query entry: its coordinate's key entries, first | count << 16
     int qo[kJW + 1], ko[kJW + 1];
-    uint8_t qt[kCap], kt[kCap], qj[kCap];
 };
 
 template <int DV>
@@ -479,14 +479,8 @@ pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8
 #pragma unroll
             for (int u = 0; u < EPT; ++u) {
                 const int i = tid + 256 * u;
-                if (i < nq_) {
-                    P.qt[i] = (uint8_t)pqt[u];
-                    P.qv[i] = pqv[u];
-                }
-                if (i < nk_) {
-                    P.kt[i] = (uint8_t)pkt[u];
-                    P.kv[i] = pkv[u];
-                }
+                if (i < nq_) P.qe[i] = make_uint2(__float_as_uint(pqv[u]), pqt[u]);
+                if (i < nk_) P.ke[i] = make_uint2(__float_as_uint(pkv[u]), pkt[u]);
             }
         }
     };
@@ -507,18 +501,32 @@ pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8
         fetch_window(w + 1, cq_b, cq_e, ck_b, ck_e);
         fetch_bounds(w + 2, nb_qb, nb_qe, nb_kb, nb_ke);
         if (fits) {
-            for (int jl = tid; jl < nw; jl += 256)  // tag each query entry with its coordinate
-                for (int e = P.qo[jl] - qb; e < P.qo[jl + 1] - qb; ++e) P.qj[e] = (uint8_t)jl;
+            // tag each query entry with the key entries of its coordinate
+            for (int jl = tid; jl < nw; jl += 256) {
+                const int k0 = P.ko[jl];
+                const uint32_t tag = (uint32_t)(k0 - kb) | (uint32_t)(P.ko[jl + 1] - k0) << 16;
+                for (int e = P.qo[jl] - qb; e < P.qo[jl + 1] - qb; ++e) P.qk[e] = tag;
+            }
             __syncthreads();
             for (int e = tid; e < nq; e += 256) {
-                const int jl = P.qj[e], t = P.qt[e];
-                const float x = P.qv[e];
-                const int b0 = P.ko[jl] - kb, b1 = P.ko[jl + 1] - kb;
+                const uint2 q = P.qe[e];
+                const uint32_t tag = P.qk[e];
+                const int t = (int)q.y, b0 = (int)(tag & 0xffffu), n = (int)(tag >> 16);
+                const float x = __uint_as_float(q.x);
                 const int smax = diag ? t : kTB - 1;  // causal inside the diagonal block
                 float *zrow = Zs + t * ZS;
-                for (int b = b0; b < b1; ++b) {
-                    const int s = P.kt[b];
-                    if (s <= smax && OPAM_BOUNDS(t < kTB && s < kTB, status)) red_add_shared(zrow + s, x * P.kv[b]);
+                // four key entries' loads in flight before their reductions
+                for (int u0 = 0; u0 < n; u0 += 4) {
+                    uint2 k[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        if (u0 + u < n) k[u] = P.ke[b0 + u0 + u];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int s_ = (int)k[u].y;
+                        if (u0 + u < n && s_ <= smax && OPAM_BOUNDS(t < kTB && s_ < kTB, status))
+                            red_add_shared(zrow + s_, x * __uint_as_float(k[u].x));
+                    }
                 }
             }
         } else {
