@@ -394,11 +394,16 @@ __device__ __forceinline__ void red_add_shared(float *p, float x) {
 constexpr int kJW = 256;    // coordinates per window
 constexpr int kCap = 2048;  // list entries per window buffered in shared memory
 
+constexpr int kBins = 32;   // query entries sorted by their key-list length: 1 .. 30, then >= 31
+
 struct PairSmem {
     float Z[kTB * (kTB + 1)];
     uint2 qe[kCap], ke[kCap];  // the window's list entries: (value bits, token)
-    uint32_t qk[kCap];         // per query entry: its coordinate's key entries, first | count << 16
+    uint32_t stag[kCap];       // sorted query entry k: its coordinate's key entries, first | count << 16
     int qo[kJW + 1], ko[kJW + 1];
+    uint16_t sidx[kCap];       // sorted query entry k: its index in qe
+    int bin[kBins];            // entries per key-list length, then the running start of each length
+    int nsort;                 // query entries with at least one key entry
 };
 
 template <int DV>
@@ -492,6 +497,7 @@ pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8
         const int w0 = w * kJW, nw = min(kJW, N - w0);
         __syncthreads();  // the previous window's buffers are no longer read (and Z is zeroed)
         store_window(w, cq_b, cq_e, ck_b, ck_e);
+        if (tid < kBins) P.bin[tid] = 0;
         const int qb = cq_b, kb = ck_b;
         const int nq = cq_e - cq_b, nk = ck_e - ck_b;
         const bool fits = nq <= kCap && nk <= kCap;
@@ -501,16 +507,43 @@ pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8
         fetch_window(w + 1, cq_b, cq_e, ck_b, ck_e);
         fetch_bounds(w + 2, nb_qb, nb_qe, nb_kb, nb_ke);
         if (fits) {
-            // tag each query entry with the key entries of its coordinate
+            // Query entries are sorted by the length of their coordinate's key
+            // list (a counting sort over kBins lengths), so that the lanes of a
+            // warp walk lists of one length; entries with no key entry drop out.
             for (int jl = tid; jl < nw; jl += 256) {
-                const int k0 = P.ko[jl];
-                const uint32_t tag = (uint32_t)(k0 - kb) | (uint32_t)(P.ko[jl + 1] - k0) << 16;
-                for (int e = P.qo[jl] - qb; e < P.qo[jl + 1] - qb; ++e) P.qk[e] = tag;
+                const int nqj = P.qo[jl + 1] - P.qo[jl], nkj = P.ko[jl + 1] - P.ko[jl];
+                if (nqj > 0 && nkj > 0) atomicAdd(&P.bin[min(nkj, kBins) - 1], nqj);
             }
             __syncthreads();
-            for (int e = tid; e < nq; e += 256) {
-                const uint2 q = P.qe[e];
-                const uint32_t tag = P.qk[e];
+            if (warp == 0) {  // exclusive scan of the bins
+                const int c = P.bin[lane];
+                int incl = c;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d) incl += y;
+                }
+                P.bin[lane] = incl - c;
+                if (lane == 31) P.nsort = incl;
+            }
+            __syncthreads();
+            for (int jl = tid; jl < nw; jl += 256) {
+                const int q0 = P.qo[jl] - qb, k0 = P.ko[jl];
+                const int nqj = P.qo[jl + 1] - qb - q0, nkj = P.ko[jl + 1] - k0;
+                if (nqj > 0 && nkj > 0) {
+                    const int pos = atomicAdd(&P.bin[min(nkj, kBins) - 1], nqj);
+                    const uint32_t tag = (uint32_t)(k0 - kb) | (uint32_t)nkj << 16;
+                    for (int a = 0; a < nqj; ++a) {
+                        P.sidx[pos + a] = (uint16_t)(q0 + a);
+                        P.stag[pos + a] = tag;
+                    }
+                }
+            }
+            __syncthreads();
+            const int ns = P.nsort;
+            for (int k = tid; k < ns; k += 256) {
+                const uint2 q = P.qe[P.sidx[k]];
+                const uint32_t tag = P.stag[k];
                 const int t = (int)q.y, b0 = (int)(tag & 0xffffu), n = (int)(tag >> 16);
                 const float x = __uint_as_float(q.x);
                 const int smax = diag ? t : kTB - 1;  // causal inside the diagonal block
