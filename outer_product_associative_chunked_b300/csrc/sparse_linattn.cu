@@ -591,44 +591,37 @@ pair_tile_kernel(int T, int N, int nb, const int *__restrict__ coff, const uint8
     constexpr int DVP = DV < 64 ? DV : 64;  // output columns per pass
     constexpr int CG = DVP / 8;             // column groups of 8
     constexpr int RPT = kTB / (256 / CG);   // rows per thread
+    constexpr int C4 = DVP / 4;             // float4 per staged V row
+    static_assert(sizeof(P.qe) + sizeof(P.ke) >= sizeof(float) * kTB * DVP, "V slice buffer");
+    // the pass's V slice [cols rows][DVP columns] is staged in the (now free)
+    // window buffers, so every thread's reads of it come from shared memory
+    float4 *Vs = reinterpret_cast<float4 *>(P.qe);
     const int cg = tid % CG, rg = tid / CG;
     const float *vb = v + ((size_t)bh * T + sb * kTB) * DV;
     float *yb = y + ((size_t)bh * T + tb * kTB) * DV;
 #pragma unroll 1
     for (int c0 = 0; c0 < DV; c0 += DVP) {
+        if (c0 > 0) __syncthreads();  // the previous slice is no longer read
+        for (int i = tid; i < cols * C4; i += 256) {
+            const int r = i / C4, c = i % C4;
+            Vs[i] = reinterpret_cast<const float4 *>(vb + (size_t)r * DV + c0)[c];
+        }
+        __syncthreads();
         float acc[RPT][8];
 #pragma unroll
         for (int i = 0; i < RPT; ++i)
 #pragma unroll
             for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
         const int col = c0 + 8 * cg;
-        // V rows are read from L2: keep kLook rows of loads in flight
-        constexpr int kLook = 4;
-        float4 va[kLook][2];
-        auto vload = [&](int s, float4 (&dst)[2]) {
-            if (s < cols) {
-                const float4 *vr = reinterpret_cast<const float4 *>(vb + (size_t)s * DV + col);
-                dst[0] = vr[0];
-                dst[1] = vr[1];
-            }
-        };
+#pragma unroll 4
+        for (int s_ = 0; s_ < cols; ++s_) {
+            const float4 va = Vs[s_ * C4 + 2 * cg], vc = Vs[s_ * C4 + 2 * cg + 1];
+            const float vv[8] = {va.x, va.y, va.z, va.w, vc.x, vc.y, vc.z, vc.w};
 #pragma unroll
-        for (int u = 0; u < kLook; ++u) vload(u, va[u]);
-        for (int s0 = 0; s0 < cols; s0 += kLook) {
+            for (int i = 0; i < RPT; ++i) {
+                const float z = Zs[(rg * RPT + i) * ZS + s_];
 #pragma unroll
-            for (int u = 0; u < kLook; ++u) {
-                const int s = s0 + u;
-                if (s < cols) {
-                    const float vv[8] = {va[u][0].x, va[u][0].y, va[u][0].z, va[u][0].w,
-                                         va[u][1].x, va[u][1].y, va[u][1].z, va[u][1].w};
-                    vload(s + kLook, va[u]);
-#pragma unroll
-                    for (int i = 0; i < RPT; ++i) {
-                        const float z = Zs[(rg * RPT + i) * ZS + s];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(z, vv[e], acc[i][e]);
-                    }
-                }
+                for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(z, vv[e], acc[i][e]);
             }
         }
 #pragma unroll
