@@ -290,15 +290,34 @@ csc_build_kernel(int T, int N, int nb, const int *__restrict__ kidx, const float
 // shared memory ([128 rows][128 columns]); thread c scans column c over half
 // of the rows, a scan over the tile's 128 columns places the lists, and each
 // coordinate's entries come out in ascending token order.  The next tile's
-// loads are issued before the current tile is scanned.
-constexpr int kCT = 128;  // columns per tile
+// loads are issued before the current tile is scanned.  A tile's entries (one
+// contiguous range of the block's lists) are staged in shared memory as
+// (value, token) pairs when they fit, then written out with coalesced stores.
+constexpr int kCT = 128;      // columns per tile
+constexpr int kCStage = 2048;  // staged entries per tile, at most
+
+// Appends (x, t) at shared address sa, and advances sa, when x != 0 (NaN
+// included, as for the C comparison) -- as predicated instructions, with no
+// branch per value; then t += 1.
+__device__ __forceinline__ void stage_nonzero(uint32_t &sa, uint32_t &t, float x) {
+    asm volatile(
+        "{\n\t.reg .pred q;\n\t"
+        "setp.neu.f32 q, %2, 0f00000000;\n\t"
+        "@q st.shared.v2.b32 [%0], {%2, %1};\n\t"
+        "@q add.u32 %0, %0, 8;\n\t"
+        "add.u32 %1, %1, 1;\n\t}"
+        : "+r"(sa), "+r"(t)
+        : "f"(x)
+        : "memory");
+}
 
 __global__ void __launch_bounds__(256)
 dense_csc_kernel(const float *__restrict__ q, const float *__restrict__ k, int T, int N, int nb,
                  int *__restrict__ coff, uint8_t *__restrict__ ct, float *__restrict__ cv,
                  unsigned int *__restrict__ status) {
     constexpr int LD = kCT + 4;  // padded row stride (float4-aligned)
-    extern __shared__ float tilef[];  // [kTB][LD]
+    extern __shared__ float tilef[];  // [kTB][LD], then the stage: kCStage (value, token) pairs
+    uint2 *stage = reinterpret_cast<uint2 *>(tilef + kTB * LD);
     __shared__ int cnt2[2][kCT];   // non-zeros of column c in the lower / upper 64 rows
     __shared__ int start[kCT];     // first entry of column c
     __shared__ int wtot[4];
@@ -358,17 +377,32 @@ dense_csc_kernel(const float *__restrict__ q, const float *__restrict__ k, int T
         }
         __syncthreads();
         int p = start[c] + (half ? cnt2[0][c] : 0);  // the upper rows follow the lower rows' entries
-        for (int r = 64 * half; r < 64 * half + 64; ++r) {
-            const float val = tilef[r * LD + c];
-            if (val != 0.f) {
-                if (OPAM_BOUNDS(p < kTB * N, status)) {
-                    et[p] = (uint8_t)r;
-                    ev[p] = val;
+        const int ttot = wtot[0] + wtot[1] + wtot[2] + wtot[3];  // the tile's range [base, base + ttot)
+        if (ttot <= kCStage) {
+            uint32_t sa = (uint32_t)__cvta_generic_to_shared(stage + (p - base)), tok = 64 * half;
+#pragma unroll 16
+            for (int r = 64 * half; r < 64 * half + 64; ++r) stage_nonzero(sa, tok, tilef[r * LD + c]);
+            __syncthreads();
+            for (int j = tid; j < ttot; j += 256) {
+                if (OPAM_BOUNDS(base + j < kTB * N, status)) {
+                    const uint2 e = stage[j];
+                    et[base + j] = (uint8_t)e.y;
+                    ev[base + j] = __uint_as_float(e.x);
                 }
-                ++p;
+            }
+        } else {
+            for (int r = 64 * half; r < 64 * half + 64; ++r) {
+                const float val = tilef[r * LD + c];
+                if (val != 0.f) {
+                    if (OPAM_BOUNDS(p < kTB * N, status)) {
+                        et[p] = (uint8_t)r;
+                        ev[p] = val;
+                    }
+                    ++p;
+                }
             }
         }
-        base += wtot[0] + wtot[1] + wtot[2] + wtot[3];
+        base += ttot;
     }
     if (tid == 0) off[N] = base;
 }
@@ -748,7 +782,7 @@ int launch(const float *q, const float *k, const float *v, int BH, int T, int N,
     if (S0 == nullptr && S_out == nullptr && N % kCT == 0) {
         // pairwise form: coordinate lists straight from the dense rows
         const int nb = ceil_div(T, kTB);
-        const int smem = (int)(sizeof(float) * kTB * (kCT + 4));
+        const int smem = (int)(sizeof(float) * kTB * (kCT + 4) + sizeof(uint2) * kCStage);
         if (int rc_ = set_smem_limit((const void *)dense_csc_kernel, smem, "dense_csc smem attribute")) return rc_;
         dense_csc_kernel<<<dim3(nb, BH, 2), 256, smem, s>>>(q, k, T, N, nb, l.coff, l.ct, l.cv, status);
         if (int rc = launched("dense_csc")) return rc;

@@ -79,6 +79,21 @@ def test_pairwise_form_overflowing_key_lists(cuda_lib, oracle_mod):
     check_parity(to_np(y), ref["y"], "f32", "pairwise overflowing key lists")
 
 
+def test_pairwise_form_dense_tiles_from_dense_rows(cuda_lib, oracle_mod):
+    # N a multiple of 128: the coordinate lists come straight from the dense
+    # rows, 128 x 128 tiles at a time.  A block of fully dense keys gives
+    # tiles with more entries than the shared-memory stage (written in
+    # place); the sparse block and a few dense queries are staged.
+    inp = synth.sparse_inputs(1, 1, 250, 384, 64, seed=29)
+    q, k = inp.q.clone(), inp.k.clone()
+    k[0, 0, :128] = torch.rand(128, 384, generator=torch.Generator().manual_seed(4))
+    q[0, 0, 130:135] = torch.rand(5, 384, generator=torch.Generator().manual_seed(5))
+    y = cuda_lib.sparse_linattn_forward(q.cuda(), k.cuda(), inp.v.cuda())
+    torch.cuda.synchronize()
+    ref = oracle_mod.sparse_linattn(q, k, inp.v)
+    check_parity(to_np(y), ref["y"], "f32", "pairwise dense tiles from dense rows")
+
+
 def test_dense_and_empty_rows_in_place_state(cuda_lib, oracle_mod):
     inp = synth.sparse_inputs(1, 2, 70, 300, 32, seed=9)
     q, k = inp.q.clone(), inp.k.clone()
