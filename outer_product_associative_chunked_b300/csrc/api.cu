@@ -154,6 +154,8 @@ const char *status_names(unsigned int bits) {
         const char *name;
     } parts[] = {{0x7Fu * kStatusTcPrefill, "Tensor Cache prefill "},
                  {0x1Fu * kStatusDelta, "DeltaNet tensor-core "},
+                 {0x7u * kStatusTcBackward, "Tensor Cache backward tensor-core "},
+                 {0x3u * kStatusSparse, "BDH lists from the dense rows "},
                  {0x7u * kStatusKeygen, "BDH key generation "},
                  {kStatusSelfTest, "bounded-wait self-test "},
                  {kStatusBounds, "(index check of a debug-bounds build) "}};

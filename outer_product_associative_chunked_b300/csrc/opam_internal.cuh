@@ -69,6 +69,7 @@ constexpr unsigned int kStatusTcPrefill = 1u << 0;   // 7 bits: Tensor Cache pre
 constexpr unsigned int kStatusDelta = 1u << 8;       // 5 bits: DeltaNet tensor-core kernels
 constexpr unsigned int kStatusTcBackward = 1u << 13;  // 3 bits: Tensor Cache backward tensor-core kernel
 constexpr unsigned int kStatusSelfTest = 1u << 16;   // the bounded-wait self-test
+constexpr unsigned int kStatusSparse = 1u << 17;     // 2 bits: BDH lists from the dense rows
 constexpr unsigned int kStatusKeygen = 1u << 20;     // 3 bits: BDH key generation
 constexpr unsigned int kStatusBounds = 1u << 24;     // an index check failed (debug-bounds builds)
 constexpr int kStatusWords = 4;

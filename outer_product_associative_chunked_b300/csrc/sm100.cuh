@@ -409,5 +409,9 @@ __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) {
 // (n0 innermost) with a {64, box1, 1} box and 128-byte swizzle.
 int make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t n0, uint64_t n1, uint64_t n2,
                       uint32_t box1);
+// Host: a 3-D float32 tensor map over a [n2][n1][n0] row-major array with a
+// {box0, box1, 1} box, no swizzle (the box lands row-major in shared memory).
+int make_tmap_f32_3d(CUtensorMap *map, const void *base, uint64_t n0, uint64_t n1, uint64_t n2,
+                     uint32_t box0, uint32_t box1);
 
 }  // namespace opam

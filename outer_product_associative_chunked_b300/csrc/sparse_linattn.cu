@@ -26,9 +26,12 @@
 // added into o (pair_tile_kernel).  The state's traffic (every token gathering
 // and scattering ~5% of the N rows) is replaced by one pass over the lists.
 #include "opam_internal.cuh"
+#include "sm100.cuh"
 
 namespace opam {
 namespace {
+
+using namespace sm100;
 
 constexpr int kC = 64;
 constexpr int kThreads = 256;
@@ -284,17 +287,47 @@ csc_build_kernel(int T, int N, int nb, const int *__restrict__ kidx, const float
 }
 
 // Pairwise form straight from the dense rows: one CTA per (token block,
-// head, q or k) reads the block's 128 rows once, in column tiles of 128, and
-// writes the coordinate-major lists of the block (the output of
-// csc_build_kernel) without per-row lists in between.  A tile goes through
-// shared memory ([128 rows][128 columns]); thread c scans column c over half
-// of the rows, a scan over the tile's 128 columns places the lists, and each
-// coordinate's entries come out in ascending token order.  The next tile's
-// loads are issued before the current tile is scanned.  A tile's entries (one
-// contiguous range of the block's lists) are staged in shared memory as
-// (value, token) pairs when they fit, then written out with coalesced stores.
-constexpr int kCT = 128;      // columns per tile
-constexpr int kCStage = 2048;  // staged entries per tile, at most
+// head, q or k) streams the block's 128 rows through shared memory in
+// 128 x 128 fp32 tiles and writes the coordinate-major lists of the block
+// (the output of csc_build_kernel) without per-row lists in between.
+//   warp 16 (lane 0)  TMA: the tiles, kCsStages in flight (rows past T read
+//                     as zero);
+//   warps 0-15        thread (row quarter rq, column c) counts the non-zeros
+//                     of column c in rows [32 rq, 32 rq + 32); a scan over
+//                     the tile's 128 columns places the lists, so each
+//                     coordinate's entries come out in ascending token order.
+// A tile's entries (one contiguous range of the block's lists) are staged in
+// shared memory as (value, token) pairs when they fit, then written out with
+// coalesced stores.  Every wait is bounded; one that runs out sets a bit in
+// the call's status word and the CTA winds down.
+constexpr int kCT = 128;        // columns per tile
+constexpr int kCStage = 2048;   // staged entries per tile, at most
+constexpr int kCsStages = 3;    // tiles in flight
+constexpr int kCsWarps = 16;    // consumer warps: 4 row quarters x 4 column groups of 32
+constexpr int kCsThreads = (kCsWarps + 1) * 32;
+constexpr uint32_t kCsTileBytes = kTB * kCT * sizeof(float);
+constexpr int kCsSmem = kCsStages * kCsTileBytes + kCStage * sizeof(uint2) + 128;  // + alignment slack
+
+enum : unsigned int {
+    kStCsProducer = kStatusSparse << 0,
+    kStCsConsumer = kStatusSparse << 1,
+};
+
+// Named barrier 1 over the consumer warps; the second form also returns
+// whether `ok` holds in all of them.
+__device__ __forceinline__ void cs_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(kCsWarps * 32) : "memory"); }
+__device__ __forceinline__ bool cs_all(bool ok) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)ok), "n"(kCsWarps * 32)
+        : "memory");
+    return r != 0;
+}
 
 // Appends (x, t) at shared address sa, and advances sa, when x != 0 (NaN
 // included, as for the C comparison) -- as predicated instructions, with no
@@ -311,88 +344,96 @@ __device__ __forceinline__ void stage_nonzero(uint32_t &sa, uint32_t &t, float x
         : "memory");
 }
 
-__global__ void __launch_bounds__(256)
-dense_csc_kernel(const float *__restrict__ q, const float *__restrict__ k, int T, int N, int nb,
+__global__ void __launch_bounds__(kCsThreads, 1)
+dense_csc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__ CUtensorMap mq, int N, int nb,
                  int *__restrict__ coff, uint8_t *__restrict__ ct, float *__restrict__ cv,
                  unsigned int *__restrict__ status) {
-    constexpr int LD = kCT + 4;  // padded row stride (float4-aligned)
-    extern __shared__ float tilef[];  // [kTB][LD], then the stage: kCStage (value, token) pairs
-    uint2 *stage = reinterpret_cast<uint2 *>(tilef + kTB * LD);
-    __shared__ int cnt2[2][kCT];   // non-zeros of column c in the lower / upper 64 rows
-    __shared__ int start[kCT];     // first entry of column c
+    extern __shared__ unsigned char csraw[];
+    float *tiles = reinterpret_cast<float *>(((uintptr_t)csraw + 127) & ~(uintptr_t)127);  // [stage][kTB][kCT]
+    uint2 *stage = reinterpret_cast<uint2 *>(tiles + kCsStages * kTB * kCT);
+    __shared__ uint64_t full[kCsStages], empty[kCsStages];
+    __shared__ int cnt4[4][kCT];  // non-zeros of column c in row quarter q
     __shared__ int wtot[4];
     const int b = blockIdx.x, bh = blockIdx.y, which = blockIdx.z;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float *x = which ? q : k;
-    const int t0 = b * kTB, nrows = min(kTB, T - t0);
+    const int ntile = N / kCT;
+    if (tid == 0) {
+        for (int i = 0; i < kCsStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kCsWarps);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (warp == kCsWarps) {
+        if (lane == 0) {
+            const CUtensorMap *m = which ? &mq : &mk;
+            bool ok = true;
+            int issued = 0;
+            for (int i = 0; i < ntile && ok; ++i) {
+                const int st = i % kCsStages;
+                if (i >= kCsStages) ok = mbar_wait(&empty[st], (i / kCsStages - 1) & 1);
+                if (!ok) break;
+                mbar_expect_tx(&full[st], kCsTileBytes);
+                tma_load_3d(tiles + st * kTB * kCT, m, &full[st], i * kCT, b * kTB, bh);
+                ++issued;
+            }
+            if (!ok) atomicOr(status, kStCsProducer);
+            // wait for this thread's copies still in flight before the CTA exits
+            bool dok = true;
+            for (int i = max(0, issued - kCsStages); i < issued && dok; ++i)
+                dok = mbar_wait(&full[i % kCsStages], (i / kCsStages) & 1);
+        }
+        __syncwarp();
+        return;
+    }
+    const int c = tid & (kCT - 1), rq = tid >> 7, wq = warp & 3;  // column, row quarter, column group
     const size_t blk = ((size_t)which * gridDim.y + bh) * nb + b;
     int *off = coff + blk * (size_t)(N + 1);
     uint8_t *et = ct + blk * (size_t)kTB * N;
     float *ev = cv + blk * (size_t)kTB * N;
-    const float *src = x + ((size_t)bh * T + t0) * N;
-    // loads: warp w reads rows w, w + 8, ..; a lane reads one float4 of the row's tile segment
-    constexpr int RPW = kTB / 8;
-    float4 buf[RPW];
-    auto fetch = [&](int n0) {
-#pragma unroll
-        for (int i = 0; i < RPW; ++i) {
-            const int r = warp + 8 * i;
-            buf[i] = r < nrows ? ldg_stream4(reinterpret_cast<const float4 *>(src + (size_t)r * N + n0) + lane)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-    const int c = tid & (kCT - 1), half = tid >> 7;
-    int base = 0;
-    fetch(0);
-    for (int n0 = 0; n0 < N; n0 += kCT) {
-        __syncthreads();  // the previous tile is no longer read
-#pragma unroll
-        for (int i = 0; i < RPW; ++i)
-            *reinterpret_cast<float4 *>(tilef + (warp + 8 * i) * LD + 4 * lane) = buf[i];
-        __syncthreads();
-        if (n0 + kCT < N) fetch(n0 + kCT);
-        // count column c over rows [64 half, 64 half + 64)
+    int base = 0;  // entries of the block so far
+    bool ok = true;
+    for (int i = 0; i < ntile && ok; ++i) {
+        const int st = i % kCsStages;
+        ok = cs_all(mbar_wait(&full[st], (i / kCsStages) & 1));
+        if (!ok) break;
+        const float *tile = tiles + st * kTB * kCT;
         int n = 0;
-        for (int r = 64 * half; r < 64 * half + 64; ++r) n += tilef[r * LD + c] != 0.f;
-        cnt2[half][c] = n;
-        __syncthreads();
-        // exclusive scan of the column totals (threads 0..127 = warps 0..3)
-        int excl = 0;
-        if (half == 0) {
-            const int tot = cnt2[0][c] + cnt2[1][c];
-            int incl = tot;
+#pragma unroll 8
+        for (int r = 32 * rq; r < 32 * rq + 32; ++r) n += tile[r * kCT + c] != 0.f ? 1 : 0;
+        cnt4[rq][c] = n;
+        cs_barrier();
+        // entries of column c in the row quarters before rq, and in all four
+        int before = 0, tot = 0;
 #pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, incl, d);
-                if (lane >= d) incl += y;
-            }
-            if (lane == 31) wtot[warp] = incl;
-            excl = incl - tot;
+        for (int q = 0; q < 4; ++q) {
+            const int v = cnt4[q][c];
+            before += q < rq ? v : 0;
+            tot += v;
         }
-        __syncthreads();
-        if (half == 0) {
-            for (int w = 0; w < warp; ++w) excl += wtot[w];
-            off[n0 + c] = base + excl;
-            start[c] = base + excl;
+        // inclusive scan of the column totals over this warp's 32 columns
+        int incl = tot;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, d);
+            if (lane >= d) incl += y;
         }
-        __syncthreads();
-        int p = start[c] + (half ? cnt2[0][c] : 0);  // the upper rows follow the lower rows' entries
+        if (rq == 0 && lane == 31) wtot[wq] = incl;
+        cs_barrier();
+        int start = base + incl - tot;
+        for (int w = 0; w < wq; ++w) start += wtot[w];
+        if (rq == 0) off[i * kCT + c] = start;
         const int ttot = wtot[0] + wtot[1] + wtot[2] + wtot[3];  // the tile's range [base, base + ttot)
-        if (ttot <= kCStage) {
-            uint32_t sa = (uint32_t)__cvta_generic_to_shared(stage + (p - base)), tok = 64 * half;
-#pragma unroll 16
-            for (int r = 64 * half; r < 64 * half + 64; ++r) stage_nonzero(sa, tok, tilef[r * LD + c]);
-            __syncthreads();
-            for (int j = tid; j < ttot; j += 256) {
-                if (OPAM_BOUNDS(base + j < kTB * N, status)) {
-                    const uint2 e = stage[j];
-                    et[base + j] = (uint8_t)e.y;
-                    ev[base + j] = __uint_as_float(e.x);
-                }
-            }
+        int p = start + before;
+        const bool staged = ttot <= kCStage;  // the same in every consumer thread
+        if (staged) {
+            uint32_t sa = (uint32_t)__cvta_generic_to_shared(stage + (p - base)), tok = 32 * rq;
+#pragma unroll 8
+            for (int r = 32 * rq; r < 32 * rq + 32; ++r) stage_nonzero(sa, tok, tile[r * kCT + c]);
         } else {
-            for (int r = 64 * half; r < 64 * half + 64; ++r) {
-                const float val = tilef[r * LD + c];
+            for (int r = 32 * rq; r < 32 * rq + 32; ++r) {
+                const float val = tile[r * kCT + c];
                 if (val != 0.f) {
                     if (OPAM_BOUNDS(p < kTB * N, status)) {
                         et[p] = (uint8_t)r;
@@ -402,9 +443,22 @@ dense_csc_kernel(const float *__restrict__ q, const float *__restrict__ k, int T
                 }
             }
         }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);  // the tile is no longer read
+        cs_barrier();
+        if (staged) {
+            for (int j = tid; j < ttot; j += kCsWarps * 32) {
+                if (OPAM_BOUNDS(base + j < kTB * N, status)) {
+                    const uint2 e = stage[j];
+                    et[base + j] = (uint8_t)e.y;
+                    ev[base + j] = __uint_as_float(e.x);
+                }
+            }
+        }
         base += ttot;
     }
-    if (tid == 0) off[N] = base;
+    if (!ok && lane == 0) atomicOr(status, kStCsConsumer);
+    if (ok && tid == 0) off[N] = base;
 }
 
 // One CTA per (pair of token blocks tb >= sb, head):
@@ -782,9 +836,11 @@ int launch(const float *q, const float *k, const float *v, int BH, int T, int N,
     if (S0 == nullptr && S_out == nullptr && N % kCT == 0) {
         // pairwise form: coordinate lists straight from the dense rows
         const int nb = ceil_div(T, kTB);
-        const int smem = (int)(sizeof(float) * kTB * (kCT + 4) + sizeof(uint2) * kCStage);
-        if (int rc_ = set_smem_limit((const void *)dense_csc_kernel, smem, "dense_csc smem attribute")) return rc_;
-        dense_csc_kernel<<<dim3(nb, BH, 2), 256, smem, s>>>(q, k, T, N, nb, l.coff, l.ct, l.cv, status);
+        CUtensorMap mk, mq;
+        if (int rc_ = make_tmap_f32_3d(&mk, k, N, T, BH, kCT, kTB)) return rc_;
+        if (int rc_ = make_tmap_f32_3d(&mq, q, N, T, BH, kCT, kTB)) return rc_;
+        if (int rc_ = set_smem_limit((const void *)dense_csc_kernel, kCsSmem, "dense_csc smem attribute")) return rc_;
+        dense_csc_kernel<<<dim3(nb, BH, 2), kCsThreads, kCsSmem, s>>>(mk, mq, N, nb, l.coff, l.ct, l.cv, status);
         if (int rc = launched("dense_csc")) return rc;
         return pairs<DV>(l, v, BH, T, N, y, status, s);
     }
