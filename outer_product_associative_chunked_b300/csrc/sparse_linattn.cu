@@ -399,9 +399,15 @@ dense_csc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
         ok = cs_all(mbar_wait(&full[st], (i / kCsStages) & 1));
         if (!ok) break;
         const float *tile = tiles + st * kTB * kCT;
+        // this thread's 32 values of column c stay in registers for the count and the placement
+        float a[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) a[r] = tile[(32 * rq + r) * kCT + c];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);  // the tile is no longer read
         int n = 0;
-#pragma unroll 8
-        for (int r = 32 * rq; r < 32 * rq + 32; ++r) n += tile[r * kCT + c] != 0.f ? 1 : 0;
+#pragma unroll
+        for (int r = 0; r < 32; ++r) n += a[r] != 0.f ? 1 : 0;
         cnt4[rq][c] = n;
         cs_barrier();
         // entries of column c in the row quarters before rq, and in all four
@@ -429,22 +435,20 @@ dense_csc_kernel(const __grid_constant__ CUtensorMap mk, const __grid_constant__
         const bool staged = ttot <= kCStage;  // the same in every consumer thread
         if (staged) {
             uint32_t sa = (uint32_t)__cvta_generic_to_shared(stage + (p - base)), tok = 32 * rq;
-#pragma unroll 8
-            for (int r = 32 * rq; r < 32 * rq + 32; ++r) stage_nonzero(sa, tok, tile[r * kCT + c]);
+#pragma unroll
+            for (int r = 0; r < 32; ++r) stage_nonzero(sa, tok, a[r]);
         } else {
-            for (int r = 32 * rq; r < 32 * rq + 32; ++r) {
-                const float val = tile[r * kCT + c];
-                if (val != 0.f) {
+#pragma unroll
+            for (int r = 0; r < 32; ++r) {
+                if (a[r] != 0.f) {
                     if (OPAM_BOUNDS(p < kTB * N, status)) {
-                        et[p] = (uint8_t)r;
-                        ev[p] = val;
+                        et[p] = (uint8_t)(32 * rq + r);
+                        ev[p] = a[r];
                     }
                     ++p;
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);  // the tile is no longer read
         cs_barrier();
         if (staged) {
             for (int j = tid; j < ttot; j += kCsWarps * 32) {
