@@ -299,7 +299,10 @@ int delta_decode_step(float *S, const void *q, const void *k, const void *v,
  *   S0     NULL or [B][H][N][d_v] float32 key-major start state
  *   S_out  NULL or [B][H][N][d_v] float32 key-major final state (may equal S0)
  *   y      [B][H][T][d_v] float32, output
- * Supported: 1 <= N <= 49152, d_v in {32, 64, 128, 256}. Errors as above. */
+ * Supported: 1 <= N <= 49152, d_v in {32, 64, 128, 256}. Errors as above.
+ * Without S0 and S_out, and with N a multiple of 128, the dense rows are
+ * streamed by TMA through bounded waits: one that runs out is reported by
+ * opam_check_device_error (the other paths have no such wait). */
 size_t sparse_linattn_forward_workspace_size(int B, int H, int T, int N, int d_v);
 int sparse_linattn_forward(const float *q, const float *k, const float *v,
                            int B, int H, int T, int N, int d_v,
