@@ -63,31 +63,89 @@ constexpr int kLS = kR + 1;    // padded stride of a 64 x 64 score tile
 
 // acc[i][j] += sum_k A(m_i, k) B(k, n_j) with m_i = ty + 16 i, n_j = tx + 16 j;
 // A(m, k) = A[m * am + k * ak], B(k, n) = B[k * bk + n * bn] (shared memory).
-template <int TM, int TN>
+// AV / BV: A (B) is contiguous along k (ak = 1, bk = 1) with 16-byte aligned
+// rows (am, bn and the base a multiple of 4 floats), and K a multiple of 4:
+// four k steps of it come in one 16-byte load.  The FMAs run in the same
+// order either way, so the results are identical.
+template <int TM, int TN, bool AV = false, bool BV = false>
 __device__ __forceinline__ void mm_tile(float (&acc)[TM][TN], const float *A, int am, int ak, const float *B,
                                         int bk, int bn, int K) {
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    if constexpr (AV || BV) {
+#pragma unroll 2
+        for (int k0 = 0; k0 < K; k0 += 4) {
+            float a[TM][4], b[TN][4];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                if constexpr (AV) {
+                    const float4 x = *reinterpret_cast<const float4 *>(A + (ty + 16 * i) * am + k0);
+                    a[i][0] = x.x; a[i][1] = x.y; a[i][2] = x.z; a[i][3] = x.w;
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) a[i][kk] = A[(ty + 16 * i) * am + (k0 + kk) * ak];
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                if constexpr (BV) {
+                    const float4 x = *reinterpret_cast<const float4 *>(B + k0 + (tx + 16 * j) * bn);
+                    b[j][0] = x.x; b[j][1] = x.y; b[j][2] = x.z; b[j][3] = x.w;
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) b[j][kk] = B[(k0 + kk) * bk + (tx + 16 * j) * bn];
+                }
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i][kk], b[j][kk], acc[i][j]);
+        }
+    } else {
 #pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        float a[TM], b[TN];
+        for (int k = 0; k < K; ++k) {
+            float a[TM], b[TN];
 #pragma unroll
-        for (int i = 0; i < TM; ++i) a[i] = A[(ty + 16 * i) * am + k * ak];
+            for (int i = 0; i < TM; ++i) a[i] = A[(ty + 16 * i) * am + k * ak];
 #pragma unroll
-        for (int j = 0; j < TN; ++j) b[j] = B[k * bk + (tx + 16 * j) * bn];
+            for (int j = 0; j < TN; ++j) b[j] = B[k * bk + (tx + 16 * j) * bn];
 #pragma unroll
-        for (int i = 0; i < TM; ++i)
+            for (int i = 0; i < TM; ++i)
 #pragma unroll
-            for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+                for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+        }
     }
 }
 
 // Two single-column products that share A, in one pass over it:
 // acc0[i] += sum_k A(m_i, k) B0(k, tx), acc1[i] += sum_k A(m_i, k) B1(k, tx)
 // (the same order of operations per accumulator as two mm_tile<TM, 1> calls).
-template <int TM>
+template <int TM, bool AV = false>
 __device__ __forceinline__ void mm_tile_2(float (&acc0)[TM][1], float (&acc1)[TM][1], const float *A, int am, int ak,
                                           const float *B0, const float *B1, int bk, int bn, int K) {
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    if constexpr (AV) {  // A contiguous along k, as for mm_tile
+#pragma unroll 2
+        for (int k0 = 0; k0 < K; k0 += 4) {
+            float a[TM][4];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                const float4 x = *reinterpret_cast<const float4 *>(A + (ty + 16 * i) * am + k0);
+                a[i][0] = x.x; a[i][1] = x.y; a[i][2] = x.z; a[i][3] = x.w;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const float b0 = B0[(k0 + kk) * bk + tx * bn], b1 = B1[(k0 + kk) * bk + tx * bn];
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+                    acc0[i][0] = fmaf(a[i][kk], b0, acc0[i][0]);
+                    acc1[i][0] = fmaf(a[i][kk], b1, acc1[i][0]);
+                }
+            }
+        }
+        return;
+    }
 #pragma unroll 4
     for (int k = 0; k < K; ++k) {
         float a[TM];
@@ -435,7 +493,10 @@ tcb_window_dkdv_kernel(const T *__restrict__ q, const T *__restrict__ k, const T
 // ------------------------------------------------------------------ L2: intra-chunk
 template <int DK, int DV>
 struct IntraCfg {
-    static constexpr int LQ = DK + 1, LV = DV + 1;
+    // row strides padded to a multiple of 4 floats: 16-byte aligned rows for
+    // the k-vectorised products
+    static constexpr int LQ = DK + 4, LV = DV + 4;
+    static_assert(LQ % 4 == 0 && LV % 4 == 0 && DK % 4 == 0 && DV % 4 == 0, "16-byte aligned rows");
     static constexpr int FLOATS = 2 * kR * LQ + 2 * kR * LV + kR * kLS + 2 * (kR + 1) + 32;
     static constexpr size_t SMEM = sizeof(float) * FLOATS;
 };
@@ -475,8 +536,8 @@ tcb_l2_intra_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
     float S1[4][4], S2[4][4];
     zero(S1);
     zero(S2);
-    mm_tile<4, 4>(S1, Qs, LQ, 1, Kp, 1, LQ, DK);
-    mm_tile<4, 4>(S2, dMs, LV, 1, Vp, 1, LV, DV);
+    mm_tile<4, 4, true, true>(S1, Qs, LQ, 1, Kp, 1, LQ, DK);
+    mm_tile<4, 4, true, true>(S2, dMs, LV, 1, Vp, 1, LV, DV);
     float g_eta = 0.f, g_lam = 0.f;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -559,7 +620,10 @@ tcb_l2_intra_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
 // ------------------------------------------------------------------ L2: chunk-state scans
 template <int DK>
 struct ScanCfg {
-    static constexpr int LQ = DK + 1, LW = kSW + 1;
+    // row strides padded to a multiple of 4 floats: 16-byte aligned rows for
+    // the k-vectorised products
+    static constexpr int LQ = DK + 4, LW = kSW + 4;
+    static_assert(LQ % 4 == 0 && LW % 4 == 0 && DK % 4 == 0 && kSW % 4 == 0, "16-byte aligned rows");
     static constexpr int FLOATS = 2 * kR * LQ + 4 * kR * LW + 2 * DK * LW + 2 * (kR + 1) + 32;
     static constexpr size_t SMEM = sizeof(float) * FLOATS;
 };
@@ -614,8 +678,8 @@ tcb_l2_scan_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
             zero(X);
             zero(Xp);
             zero(dq);
-            mm_tile_2<4>(X, Xp, Qs, LQ, 1, St, St2, LW, 1, DK);
-            mm_tile<4, TNK>(dq, dMs, LW, 1, St, 1, LW, kSW);
+            mm_tile_2<4, true>(X, Xp, Qs, LQ, 1, St, St2, LW, 1, DK);
+            mm_tile<4, TNK, true, true>(dq, dMs, LW, 1, St, 1, LW, kSW);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int r = ty + 16 * i, u = u0 + r;
@@ -655,8 +719,8 @@ tcb_l2_scan_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
             float dk[4][TNK], dvv[4][1];
             zero(dk);
             zero(dvv);
-            mm_tile<4, TNK>(dk, Vp, LW, 1, St, 1, LW, kSW);
-            mm_tile<4, 1>(dvv, Kp, LQ, 1, St, LW, 1, DK);
+            mm_tile<4, TNK, true, true>(dk, Vp, LW, 1, St, 1, LW, kSW);
+            mm_tile<4, 1, true, false>(dvv, Kp, LQ, 1, St, LW, 1, DK);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const int j = ty + 16 * i, u = u0 + j;
