@@ -144,13 +144,60 @@ __device__ __forceinline__ void mm_tile_2(float (&acc0)[TM][1], float (&acc1)[TM
                 }
             }
         }
-        return;
+    } else {
+#pragma unroll 4
+        for (int k = 0; k < K; ++k) {
+            float a[TM];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) a[i] = A[(ty + 16 * i) * am + k * ak];
+            const float b0 = B0[k * bk + tx * bn], b1 = B1[k * bk + tx * bn];
+#pragma unroll
+            for (int i = 0; i < TM; ++i) {
+                acc0[i][0] = fmaf(a[i], b0, acc0[i][0]);
+                acc1[i][0] = fmaf(a[i], b1, acc1[i][0]);
+            }
+        }
     }
+}
+
+// Single-column products whose A is contiguous along m (A(m, k) = A[m + k ak],
+// ak a multiple of 4, 16-byte aligned base): thread ty owns rows
+// mrow4(i) = 64 (i / 4) + 4 ty + i % 4, four of them per 16-byte load.
+__device__ __forceinline__ int mrow4(int i) { return 64 * (i >> 2) + 4 * (threadIdx.x >> 4) + (i & 3); }
+
+template <int TM>
+__device__ __forceinline__ void mm_tile_m4(float (&acc)[TM][1], const float *A, int ak, const float *B, int bk,
+                                           int bn, int K) {
+    static_assert(TM % 4 == 0, "rows in groups of four");
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
 #pragma unroll 4
     for (int k = 0; k < K; ++k) {
         float a[TM];
 #pragma unroll
-        for (int i = 0; i < TM; ++i) a[i] = A[(ty + 16 * i) * am + k * ak];
+        for (int g = 0; g < TM / 4; ++g) {
+            const float4 x = *reinterpret_cast<const float4 *>(A + 64 * g + 4 * ty + k * ak);
+            a[4 * g] = x.x; a[4 * g + 1] = x.y; a[4 * g + 2] = x.z; a[4 * g + 3] = x.w;
+        }
+        const float b = B[k * bk + tx * bn];
+#pragma unroll
+        for (int i = 0; i < TM; ++i) acc[i][0] = fmaf(a[i], b, acc[i][0]);
+    }
+}
+
+// The same with two B operands sharing A (as mm_tile_2).
+template <int TM>
+__device__ __forceinline__ void mm_tile_2_m4(float (&acc0)[TM][1], float (&acc1)[TM][1], const float *A, int ak,
+                                             const float *B0, const float *B1, int bk, int bn, int K) {
+    static_assert(TM % 4 == 0, "rows in groups of four");
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float a[TM];
+#pragma unroll
+        for (int g = 0; g < TM / 4; ++g) {
+            const float4 x = *reinterpret_cast<const float4 *>(A + 64 * g + 4 * ty + k * ak);
+            a[4 * g] = x.x; a[4 * g + 1] = x.y; a[4 * g + 2] = x.z; a[4 * g + 3] = x.w;
+        }
         const float b0 = B0[k * bk + tx * bn], b1 = B1[k * bk + tx * bn];
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
@@ -637,6 +684,7 @@ tcb_l2_scan_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
                    float *__restrict__ part_r, unsigned int *__restrict__ status) {
     using C = ScanCfg<DK>;
     constexpr int LQ = C::LQ, LW = C::LW, TNK = DK / 16, TMK = DK / 16;
+    constexpr bool M4 = TMK % 4 == 0;  // state rows four per 16-byte load (d_k >= 64)
     constexpr int NSL = DV / kSW;
     extern __shared__ float sm[];
     float *Qs = sm, *Kp = Qs + kR * LQ, *dMs = Kp + kR * LQ, *Vp = dMs + kR * LW, *Vw = Vp + kR * LW,
@@ -705,11 +753,14 @@ tcb_l2_scan_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
             float a1[TMK][1], a2[TMK][1];
             zero(a1);
             zero(a2);
-            mm_tile_2<TMK>(a1, a2, Kp, 1, LQ, Vw, Vw2, LW, 1, kR);
+            if constexpr (M4)
+                mm_tile_2_m4<TMK>(a1, a2, Kp, LQ, Vw, Vw2, LW, 1, kR);
+            else
+                mm_tile_2<TMK>(a1, a2, Kp, 1, LQ, Vw, Vw2, LW, 1, kR);
             const float ln = pw[n], dln = dpw[n];
 #pragma unroll
             for (int i = 0; i < TMK; ++i) {
-                const int a = ty + 16 * i;
+                const int a = M4 ? mrow4(i) : ty + 16 * i;
                 const float A0 = St[a * LW + tx], A1 = St2[a * LW + tx];
                 St[a * LW + tx] = fmaf(ln, A0, a1[i][0]);
                 St2[a * LW + tx] = fmaf(dln, A0, fmaf(ln, A1, a2[i][0]));
@@ -743,11 +794,14 @@ tcb_l2_scan_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
             __syncthreads();
             float r1[TMK][1];
             zero(r1);
-            mm_tile<TMK, 1>(r1, Qs, 1, LQ, Vw, LW, 1, kR);
+            if constexpr (M4)
+                mm_tile_m4<TMK>(r1, Qs, LQ, Vw, LW, 1, kR);
+            else
+                mm_tile<TMK, 1>(r1, Qs, 1, LQ, Vw, LW, 1, kR);
             const float ln = pw[n];
 #pragma unroll
             for (int i = 0; i < TMK; ++i) {
-                const int a = ty + 16 * i;
+                const int a = M4 ? mrow4(i) : ty + 16 * i;
                 St[a * LW + tx] = fmaf(ln, St[a * LW + tx], r1[i][0]);
             }
         }
