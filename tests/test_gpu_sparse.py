@@ -43,6 +43,7 @@ def test_small_parity(cuda_lib, oracle_mod, B, H, T, N, dv, with_S0):
     (1, 1, 257, 512, 256),
     (1, 3, 150, 2048, 32),
     (1, 1, 640, 4096, 256),
+    (1, 2, 200, 320, 64),     # N a multiple of 64 but not of 128
 ])
 def test_pairwise_form_parity(cuda_lib, oracle_mod, B, H, T, N, dv):
     inp = synth.sparse_inputs(B, H, T, N, dv, seed=3 * T + N)
